@@ -1,0 +1,153 @@
+"""GB300-native FP8 linear + normalization for recommendation models.
+
+The compute path is the CUDA library ``libloka.so`` (C ABI in
+``include/loka.h``; ctypes binding in ``_loka``).  The helpers below only
+allocate device memory with torch and marshal tensors into the C calls:
+
+  quantize_fp8(x, mode)                       -> (q, scales)
+  fp8_linear_norm(layers)                     -> [y, ...]   (grouped launch)
+  quant_error(x, w, bias, mode)               -> dict of error statistics
+  dispatch_select(table, problem, policy)     -> variant id
+
+Sources: "LoKA: Low-precision Kernel Applications for Recommendation Models
+at Scale" (sections II-C, III-A, III-B, III-C) and the MXFP8 scaling of the
+GEM Training page ("Low Precision Flash Attention").
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import List, Optional, Sequence
+
+from . import _loka
+from ._loka import (LOKA_BF16, LOKA_NORM_LAYER, LOKA_NORM_NONE, LOKA_NORM_RMS, LOKA_SCALE_MX32,  # noqa: F401
+                    LOKA_SCALE_ROW, LOKA_SCALE_TENSOR, DispatchEntry, LinearDesc, LokaError, Policy, Problem)
+
+__all__ = ["quantize_fp8", "fp8_linear_norm", "quant_error", "dispatch_select", "Layer", "Workspace"]
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def scales_shape(rows: int, cols: int, mode: int):
+    if mode == LOKA_SCALE_TENSOR:
+        return (1,), "float32"
+    if mode == LOKA_SCALE_ROW:
+        return (rows,), "float32"
+    if mode == LOKA_SCALE_MX32:
+        return (rows, cols // 32), "uint8"
+    raise ValueError(f"mode {mode} has no FP8 scales")
+
+
+class Workspace:
+    """A growable device byte buffer handed to calls that need scratch space."""
+
+    def __init__(self, device=None):
+        self.buf = None
+        self.device = device
+
+    def get(self, nbytes: int):
+        torch = _torch()
+        if nbytes == 0:
+            return None, 0
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.empty(nbytes, dtype=torch.uint8, device=self.device or "cuda")
+        return self.buf, self.buf.numel()
+
+
+_default_ws = {}
+
+
+def _ws(device) -> Workspace:
+    key = str(device)
+    if key not in _default_ws:
+        _default_ws[key] = Workspace(device)
+    return _default_ws[key]
+
+
+def quantize_fp8(x, mode: int, workspace: Optional[Workspace] = None, stream=None):
+    """E4M3 cast of a bf16 CUDA tensor [rows, cols]; returns (q uint8, scales)."""
+    torch = _torch()
+    assert x.dtype == torch.bfloat16 and x.is_cuda and x.is_contiguous() and x.dim() == 2
+    rows, cols = x.shape
+    q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    shp, dt = scales_shape(rows, cols, mode)
+    scales = torch.empty(shp, dtype=getattr(torch, dt), device=x.device)
+    need = _loka.loka_quantize_fp8_workspace_size(rows, cols, mode)
+    ws, nbytes = (workspace or _ws(x.device)).get(need)
+    _loka.loka_quantize_fp8(x, rows, cols, mode, q, scales, ws, nbytes, stream)
+    return q, scales
+
+
+@dataclasses.dataclass
+class Layer:
+    """One FP8 linear + norm problem (CUDA tensors)."""
+
+    x: object                      # bf16 [M,K] or uint8 E4M3 [M,K]
+    w: object                      # bf16 [N,K] or uint8 E4M3 [N,K]
+    mode: int
+    norm: int
+    eps: float
+    bias: object = None
+    gamma: object = None
+    beta: object = None
+    x_scales: object = None        # when x is E4M3
+    w_scales: object = None        # when w is E4M3
+    y: object = None               # bf16 [M,N] output (allocated if None)
+
+    def desc(self) -> LinearDesc:
+        torch = _torch()
+        M, K = self.x.shape
+        N = self.w.shape[0]
+        if self.y is None:
+            self.y = torch.empty((M, N), dtype=torch.bfloat16, device=self.x.device)
+        d = LinearDesc()
+        d.M, d.N, d.K = M, N, K
+        d.mode, d.norm, d.eps = self.mode, self.norm, self.eps
+        d.x_is_fp8 = int(self.x.dtype == torch.uint8)
+        d.w_is_fp8 = int(self.w.dtype == torch.uint8)
+        d.x, d.w, d.y = self.x.data_ptr(), self.w.data_ptr(), self.y.data_ptr()
+        d.x_scales = self.x_scales.data_ptr() if self.x_scales is not None else None
+        d.w_scales = self.w_scales.data_ptr() if self.w_scales is not None else None
+        d.bias = self.bias.data_ptr() if self.bias is not None else None
+        d.gamma = self.gamma.data_ptr() if self.gamma is not None else None
+        d.beta = self.beta.data_ptr() if self.beta is not None else None
+        return d
+
+
+def fp8_linear_norm(layers: Sequence[Layer], workspace: Optional[Workspace] = None, stream=None) -> List[object]:
+    """Runs all layers in one grouped call; returns their bf16 outputs."""
+    descs = [l.desc() for l in layers]
+    need = _loka.loka_fp8_linear_norm_workspace_size(descs)
+    ws, nbytes = (workspace or _ws(layers[0].x.device)).get(need)
+    _loka.loka_fp8_linear_norm(descs, ws, nbytes, stream)
+    return [l.y for l in layers]
+
+
+def quant_error(x, w, bias, mode: int, workspace: Optional[Workspace] = None, stream=None) -> dict:
+    """Probe: FP8 (mode) vs high-precision pre-norm outputs of one layer."""
+    layer = Layer(x=x, w=w, bias=bias, mode=mode, norm=LOKA_NORM_NONE, eps=0.0, y=x.new_empty((0,)))
+    d = layer.desc()
+    d.y = None
+    need = _loka.loka_quant_error_workspace_size(d)
+    ws, nbytes = (workspace or _ws(x.device)).get(need)
+    st = _loka.loka_quant_error(d, ws, nbytes, stream)
+    return {"mere": st.mere, "rel_err_fro": st.rel_err_fro, "max_abs": st.max_abs,
+            "zero_ref_count": st.zero_ref_count, "count": st.count}
+
+
+def dispatch_select(table, M: int, N: int, K: int, norm: int, outlier_frac: float,
+                    max_rel_err: float = 1e-2, max_mere: float = 0.2, min_speedup: float = -1.0) -> int:
+    """table: iterable of (M, N, K, norm, outlier_frac, variant, time_us, rel_err, mere)."""
+    rows = []
+    for (m, n, k, nm, o, v, t, r, me) in table:
+        e = DispatchEntry()
+        e.p.M, e.p.N, e.p.K, e.p.norm, e.p.outlier_frac = m, n, k, nm, o
+        e.variant, e.time_us, e.rel_err, e.mere = v, t, r, me
+        rows.append(e)
+    p = Problem()
+    p.M, p.N, p.K, p.norm, p.outlier_frac = M, N, K, norm, outlier_frac
+    pol = Policy()
+    pol.max_rel_err, pol.max_mere, pol.min_speedup = max_rel_err, max_mere, min_speedup
+    return _loka.loka_dispatch_select(rows, p, pol)

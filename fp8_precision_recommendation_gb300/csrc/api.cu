@@ -1,0 +1,510 @@
+// C ABI of the library (declared in include/loka.h): argument validation,
+// workspace layout, TMA descriptor encoding and launch sequencing.  Every
+// step of the computation runs in the kernels of quantize.cu, gemm_norm.cu
+// and probe.cu; this file does host bookkeeping only and has no fallback.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "loka.h"
+#include "loka_internal.h"
+
+namespace loka {
+namespace {
+
+// Device status word: kernels OR an error code into it when a wait gives up.
+__device__ unsigned g_status_word;
+
+thread_local std::string t_last_error;
+
+loka_status fail(loka_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return s;
+}
+
+loka_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(LOKA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
+
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0;
+  unsigned* status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+
+loka_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(LOKA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3)
+      return fail(LOKA_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only", dev, major, minor);
+    e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_status_word);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+    d.status = static_cast<unsigned*>(p);
+    d.ready = true;
+  }
+  *out = &d;
+  return LOKA_OK;
+}
+
+// ------------------------------------------------------------ tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D row-major tensor [outer, inner] with a 128-byte-wide, 128B-swizzled box.
+loka_status encode_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base, uint64_t inner,
+                      uint64_t outer, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return fail(LOKA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * static_cast<uint64_t>(elem_bytes)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elem_bytes), box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(LOKA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return LOKA_OK;
+}
+
+// ------------------------------------------------------------- workspace
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+size_t scale_bytes(int mode, int64_t rows, int64_t cols) {
+  if (mode == kScaleTensor) return sizeof(float);
+  if (mode == kScaleRow) return static_cast<size_t>(rows) * sizeof(float);
+  if (mode == kScaleMx32) return static_cast<size_t>(rows) * static_cast<size_t>(cols / 32);
+  return 0;
+}
+
+struct OperandSlots {   // workspace offsets of one group's quantized operands
+  size_t xq, sx, wq, sw, amax;
+};
+
+// Lays out the quantized operands of every group; returns the total bytes.
+size_t layout_operands(const loka_linear_desc* d, int n, std::vector<OperandSlots>* slots) {
+  size_t off = 0;
+  if (slots) slots->assign(n, OperandSlots{0, 0, 0, 0, 0});
+  for (int i = 0; i < n; ++i) {
+    OperandSlots s{0, 0, 0, 0, 0};
+    if (d[i].mode != kBf16) {
+      if (!d[i].x_is_fp8) {
+        s.xq = off;
+        off = align_up(off + static_cast<size_t>(d[i].M) * d[i].K);
+        s.sx = off;
+        off = align_up(off + scale_bytes(d[i].mode, d[i].M, d[i].K));
+      }
+      if (!d[i].w_is_fp8) {
+        s.wq = off;
+        off = align_up(off + static_cast<size_t>(d[i].N) * d[i].K);
+        s.sw = off;
+        off = align_up(off + scale_bytes(d[i].mode, d[i].N, d[i].K));
+      }
+      if (d[i].mode == kScaleTensor) {
+        s.amax = off;
+        off = align_up(off + 2 * sizeof(unsigned));
+      }
+    }
+    if (slots) (*slots)[i] = s;
+  }
+  return off;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+loka_status validate(const loka_linear_desc* d, int n, bool probe) {
+  if (d == nullptr) return fail(LOKA_ERR_INVALID_ARG, "descs is NULL");
+  if (n < 1 || n > kMaxGroups) return fail(LOKA_ERR_INVALID_ARG, "num_groups %d not in [1, %d]", n, kMaxGroups);
+  const loka_linear_desc& a = d[0];
+  if (!(a.eps >= 0.0f) || !std::isfinite(a.eps)) return fail(LOKA_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  for (int i = 0; i < n; ++i) {
+    const loka_linear_desc& g = d[i];
+    if (g.N != a.N || g.K != a.K || g.mode != a.mode || g.norm != a.norm || g.eps != a.eps ||
+        g.x_is_fp8 != a.x_is_fp8 || g.w_is_fp8 != a.w_is_fp8)
+      return fail(LOKA_ERR_UNSUPPORTED, "group %d differs from group 0 in N, K, mode, norm, eps or operand kind", i);
+    if (g.M < 0) return fail(LOKA_ERR_INVALID_ARG, "group %d: M = %lld < 0", i, static_cast<long long>(g.M));
+    if (g.M > (int64_t(1) << 31)) return fail(LOKA_ERR_UNSUPPORTED, "group %d: M too large", i);
+  }
+  if (a.mode < 0 || a.mode > kBf16) return fail(LOKA_ERR_INVALID_ARG, "mode %d is not a LOKA_SCALE_* value", a.mode);
+  if (a.norm < 0 || a.norm > kNormRms) return fail(LOKA_ERR_INVALID_ARG, "norm %d is not a LOKA_NORM_* value", a.norm);
+  if (a.K < 128 || a.K % 128 != 0)
+    return fail(LOKA_ERR_UNSUPPORTED, "K = %lld: K must be a positive multiple of 128", static_cast<long long>(a.K));
+  if (a.K > (int64_t(1) << 20)) return fail(LOKA_ERR_UNSUPPORTED, "K too large");
+  if (!(a.N == 64 || a.N == 128 || a.N == 192 || a.N == 256 || a.N == 512))
+    return fail(LOKA_ERR_UNSUPPORTED, "N = %lld: supported N are 64, 128, 192, 256, 512", static_cast<long long>(a.N));
+  if (a.mode == kScaleMx32) return fail(LOKA_ERR_UNSUPPORTED, "MX 1x32 GEMM is not available in this build");
+  if (a.mode == kBf16 && (a.x_is_fp8 || a.w_is_fp8))
+    return fail(LOKA_ERR_INVALID_ARG, "LOKA_BF16 takes bf16 operands (x_is_fp8 = w_is_fp8 = 0)");
+  if (probe && (a.x_is_fp8 || a.w_is_fp8))
+    return fail(LOKA_ERR_INVALID_ARG, "the error probe needs bf16 x and w (it runs the high-precision reference too)");
+  for (int i = 0; i < n; ++i) {
+    const loka_linear_desc& g = d[i];
+    if (g.M == 0) continue;
+    if (g.x == nullptr || g.w == nullptr || (!probe && g.y == nullptr))
+      return fail(LOKA_ERR_INVALID_ARG, "group %d: x, w and y must not be NULL", i);
+    if (!aligned16(g.x) || !aligned16(g.w) || (!probe && !aligned16(g.y)))
+      return fail(LOKA_ERR_INVALID_ARG, "group %d: x, w and y must be 16-byte aligned", i);
+    if (g.x_is_fp8 && g.x_scales == nullptr) return fail(LOKA_ERR_INVALID_ARG, "group %d: x_scales is NULL", i);
+    if (g.w_is_fp8 && g.w_scales == nullptr) return fail(LOKA_ERR_INVALID_ARG, "group %d: w_scales is NULL", i);
+  }
+  return LOKA_OK;
+}
+
+// Builds the GEMM launch parameters for the groups; `slots` gives the
+// workspace locations of operands quantized by this call (bf16 inputs).
+loka_status build_gemm(const loka_linear_desc* d, int n, const std::vector<OperandSlots>& slots, uint8_t* ws,
+                       bool bf16_operands, OutKind out, void* const* y_override, int norm, DeviceInfo* dev,
+                       GemmParams* p) {
+  std::memset(p, 0, sizeof(*p));
+  const int mode = d[0].mode;
+  int tiles = 0;
+  for (int i = 0; i < n; ++i) {
+    const loka_linear_desc& g = d[i];
+    GemmGroup& G = p->g[i];
+    G.M = g.M;
+    G.tile_begin = tiles;
+    tiles += static_cast<int>((g.M + 127) / 128);
+    const uint16_t* bias = static_cast<const uint16_t*>(g.bias);
+    G.bias = bias;
+    G.gamma = static_cast<const uint16_t*>(g.gamma);
+    G.beta = static_cast<const uint16_t*>(g.beta);
+    void* y = y_override ? y_override[i] : g.y;
+    if (g.M == 0) continue;
+    loka_status s;
+    if (bf16_operands) {
+      if ((s = encode_2d(&G.tm_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.x, g.K, g.M, 128)) != LOKA_OK) return s;
+      if ((s = encode_2d(&G.tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.w, g.K, g.N, g.N > 256 ? 256 : g.N)) != LOKA_OK) return s;
+    } else {
+      const void* xq = g.x_is_fp8 ? g.x : ws + slots[i].xq;
+      const void* wq = g.w_is_fp8 ? g.w : ws + slots[i].wq;
+      const void* sx = g.x_is_fp8 ? g.x_scales : ws + slots[i].sx;
+      const void* sw = g.w_is_fp8 ? g.w_scales : ws + slots[i].sw;
+      if ((s = encode_2d(&G.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xq, g.K, g.M, 128)) != LOKA_OK) return s;
+      if ((s = encode_2d(&G.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wq, g.K, g.N, g.N > 256 ? 256 : g.N)) != LOKA_OK) return s;
+      G.sx = static_cast<const float*>(sx);
+      G.sw = static_cast<const float*>(sw);
+      G.sx_per_row = mode == kScaleRow;
+      G.sw_per_row = mode == kScaleRow;
+    }
+    if (out == OutKind::kBf16)
+      s = encode_2d(&G.tm_y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y, g.N, g.M, 128);
+    else
+      s = encode_2d(&G.tm_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, y, g.N, g.M, 128);
+    if (s != LOKA_OK) return s;
+  }
+  p->num_groups = n;
+  p->total_tiles = tiles;
+  p->K = static_cast<int32_t>(d[0].K);
+  p->norm = norm;
+  p->eps = d[0].eps;
+  p->status = dev->status;
+  p->wait_limit_ns = kDefaultWaitLimitNs;
+  return LOKA_OK;
+}
+
+// Quantizes every bf16 operand of the groups into the workspace (one launch
+// for X and W of all groups; tensorwise scaling takes an amax launch first).
+loka_status quantize_operands(const loka_linear_desc* d, int n, const std::vector<OperandSlots>& slots, uint8_t* ws,
+                              DeviceInfo* dev, cudaStream_t stream) {
+  QuantJobs jobs;
+  std::memset(&jobs, 0, sizeof(jobs));
+  int64_t rows = 0;
+  for (int i = 0; i < n; ++i) {
+    const loka_linear_desc& g = d[i];
+    if (!g.x_is_fp8 && g.M > 0) {
+      QuantJob& j = jobs.j[jobs.n++];
+      j.x = g.x;
+      j.q = ws + slots[i].xq;
+      j.scales = ws + slots[i].sx;
+      j.amax_slot = reinterpret_cast<unsigned*>(ws + slots[i].amax);
+      j.rows = g.M;
+      j.cols = g.K;
+      j.row_begin = rows;
+      rows += g.M;
+    }
+    if (!g.w_is_fp8) {
+      QuantJob& j = jobs.j[jobs.n++];
+      j.x = g.w;
+      j.q = ws + slots[i].wq;
+      j.scales = ws + slots[i].sw;
+      j.amax_slot = reinterpret_cast<unsigned*>(ws + slots[i].amax) + 1;
+      j.rows = g.N;
+      j.cols = g.K;
+      j.row_begin = rows;
+      rows += g.N;
+    }
+  }
+  jobs.total_rows = rows;
+  cudaError_t e = launch_quantize(jobs, d[0].mode, dev->sms, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+  return LOKA_OK;
+}
+
+}  // namespace
+}  // namespace loka
+
+using namespace loka;
+
+extern "C" {
+
+int32_t loka_version(void) { return (0 << 16) | 1; }
+
+const char* loka_last_error(void) { return t_last_error.c_str(); }
+
+loka_status loka_device_status(void* stream) {
+  DeviceInfo* dev = nullptr;
+  loka_status s = device_info(&dev);
+  if (s != LOKA_OK) return s;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned word = 0;
+  e = cudaMemcpy(&word, dev->status, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+  if (word != 0) {
+    const unsigned zero = 0;
+    e = cudaMemcpy(dev->status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the device status word");
+    return fail(LOKA_ERR_TIMEOUT, "a kernel wait ran out of time (status bits 0x%x)", word);
+  }
+  return LOKA_OK;
+}
+
+loka_status loka_selftest_watchdog(uint64_t limit_ns, void* stream) {
+  DeviceInfo* dev = nullptr;
+  loka_status s = device_info(&dev);
+  if (s != LOKA_OK) return s;
+  if (limit_ns == 0 || limit_ns > 10000000000ull) return fail(LOKA_ERR_INVALID_ARG, "limit_ns must be in (0, 1e10]");
+  cudaError_t e = launch_watchdog_selftest(dev->status, limit_ns, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "watchdog self-test launch");
+  return LOKA_OK;
+}
+
+size_t loka_quantize_fp8_workspace_size(int64_t, int64_t, int32_t mode) {
+  return mode == LOKA_SCALE_TENSOR ? kAlign : 0;
+}
+
+loka_status loka_quantize_fp8(const void* x, int64_t rows, int64_t cols, int32_t mode, void* q, void* scales,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  if (mode != LOKA_SCALE_TENSOR && mode != LOKA_SCALE_ROW && mode != LOKA_SCALE_MX32)
+    return fail(LOKA_ERR_INVALID_ARG, "mode %d is not an FP8 scaling mode", mode);
+  if (rows < 0 || cols < 0) return fail(LOKA_ERR_INVALID_ARG, "negative size");
+  if (cols % 32 != 0) return fail(LOKA_ERR_INVALID_ARG, "cols = %lld is not a multiple of 32", static_cast<long long>(cols));
+  if (rows == 0 || cols == 0) {
+    if (mode == LOKA_SCALE_TENSOR && scales != nullptr) {
+      const float one = 1.0f;
+      cudaError_t e = cudaMemcpyAsync(scales, &one, sizeof(one), cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream));
+      if (e != cudaSuccess) return cuda_fail(e, "writing the unit scale");
+    }
+    return LOKA_OK;
+  }
+  if (x == nullptr || q == nullptr || scales == nullptr) return fail(LOKA_ERR_INVALID_ARG, "x, q and scales must not be NULL");
+  if (!aligned16(x) || !aligned16(q)) return fail(LOKA_ERR_INVALID_ARG, "x and q must be 16-byte aligned");
+  if (mode != LOKA_SCALE_MX32 && (reinterpret_cast<uintptr_t>(scales) & 3u))
+    return fail(LOKA_ERR_INVALID_ARG, "scales must be 4-byte aligned");
+  const size_t need = loka_quantize_fp8_workspace_size(rows, cols, mode);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+    return fail(LOKA_ERR_WORKSPACE, "workspace must be >= %zu bytes, 256-byte aligned", need);
+  DeviceInfo* dev = nullptr;
+  loka_status s = device_info(&dev);
+  if (s != LOKA_OK) return s;
+  QuantJobs jobs;
+  std::memset(&jobs, 0, sizeof(jobs));
+  jobs.n = 1;
+  jobs.j[0].x = x;
+  jobs.j[0].q = static_cast<uint8_t*>(q);
+  jobs.j[0].scales = scales;
+  jobs.j[0].amax_slot = static_cast<unsigned*>(workspace);
+  jobs.j[0].rows = rows;
+  jobs.j[0].cols = cols;
+  jobs.total_rows = rows;
+  cudaError_t e = launch_quantize(jobs, mode, dev->sms, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+  return LOKA_OK;
+}
+
+size_t loka_fp8_linear_norm_workspace_size(const loka_linear_desc* descs, int32_t num_groups) {
+  if (descs == nullptr || num_groups < 1 || num_groups > kMaxGroups) return 0;
+  return layout_operands(descs, num_groups, nullptr);
+}
+
+loka_status loka_fp8_linear_norm(const loka_linear_desc* descs, int32_t num_groups, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  loka_status s = validate(descs, num_groups, false);
+  if (s != LOKA_OK) return s;
+  std::vector<OperandSlots> slots;
+  const size_t need = layout_operands(descs, num_groups, &slots);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+    return fail(LOKA_ERR_WORKSPACE, "workspace must be >= %zu bytes, 256-byte aligned", need);
+  int64_t total_m = 0;
+  for (int i = 0; i < num_groups; ++i) total_m += descs[i].M;
+  if (total_m == 0) return LOKA_OK;
+  DeviceInfo* dev = nullptr;
+  if ((s = device_info(&dev)) != LOKA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const bool bf16 = descs[0].mode == kBf16;
+  if (!bf16 && (!descs[0].x_is_fp8 || !descs[0].w_is_fp8)) {
+    if ((s = quantize_operands(descs, num_groups, slots, ws, dev, st)) != LOKA_OK) return s;
+  }
+  static thread_local GemmParams p;
+  if ((s = build_gemm(descs, num_groups, slots, ws, bf16, OutKind::kBf16, nullptr, descs[0].norm, dev, &p)) != LOKA_OK)
+    return s;
+  cudaError_t e = launch_gemm_norm(p, static_cast<int>(descs[0].N), bf16 ? OperandKind::kBf16 : OperandKind::kE4M3,
+                                   OutKind::kBf16, dev->sms, st);
+  if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
+  return LOKA_OK;
+}
+
+size_t loka_quant_error_workspace_size(const loka_linear_desc* desc) {
+  if (desc == nullptr) return 0;
+  size_t off = layout_operands(desc, 1, nullptr);
+  const size_t mn = static_cast<size_t>(desc->M) * static_cast<size_t>(desc->N) * sizeof(float);
+  return off + 2 * align_up(mn) + kAlign;
+}
+
+loka_status loka_quant_error(const loka_linear_desc* desc, void* workspace, size_t workspace_bytes,
+                             loka_error_stats* stats, void* stream) {
+  loka_status s = validate(desc, 1, true);
+  if (s != LOKA_OK) return s;
+  if (stats == nullptr) return fail(LOKA_ERR_INVALID_ARG, "stats is NULL");
+  const size_t need = loka_quant_error_workspace_size(desc);
+  if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(LOKA_ERR_WORKSPACE, "workspace must be >= %zu bytes, 256-byte aligned", need);
+  std::memset(stats, 0, sizeof(*stats));
+  stats->count = desc->M * desc->N;
+  if (desc->M == 0) return LOKA_OK;
+  DeviceInfo* dev = nullptr;
+  if ((s = device_info(&dev)) != LOKA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  std::vector<OperandSlots> slots;
+  const size_t ops = layout_operands(desc, 1, &slots);
+  const size_t mn = static_cast<size_t>(desc->M) * static_cast<size_t>(desc->N) * sizeof(float);
+  float* out = reinterpret_cast<float*>(ws + ops);
+  float* ref = reinterpret_cast<float*>(ws + ops + align_up(mn));
+  double* acc = reinterpret_cast<double*>(ws + ops + 2 * align_up(mn));
+  const bool bf16 = desc->mode == kBf16;
+  static thread_local GemmParams p;
+  cudaError_t e;
+  if (!bf16) {
+    if ((s = quantize_operands(desc, 1, slots, ws, dev, st)) != LOKA_OK) return s;
+  }
+  void* y_out[1] = {out};
+  if ((s = build_gemm(desc, 1, slots, ws, bf16, OutKind::kF32, y_out, kNormNone, dev, &p)) != LOKA_OK) return s;
+  e = launch_gemm_norm(p, static_cast<int>(desc->N), bf16 ? OperandKind::kBf16 : OperandKind::kE4M3, OutKind::kF32,
+                       dev->sms, st);
+  if (e != cudaSuccess) return cuda_fail(e, "probe GEMM launch");
+  void* y_ref[1] = {ref};
+  if ((s = build_gemm(desc, 1, slots, ws, true, OutKind::kF32, y_ref, kNormNone, dev, &p)) != LOKA_OK) return s;
+  e = launch_gemm_norm(p, static_cast<int>(desc->N), OperandKind::kBf16, OutKind::kF32, dev->sms, st);
+  if (e != cudaSuccess) return cuda_fail(e, "reference GEMM launch");
+  e = launch_error_reduce(out, ref, desc->M * desc->N, acc, dev->sms, st);
+  if (e != cudaSuccess) return cuda_fail(e, "probe reduction launch");
+  double host[5];
+  e = cudaMemcpyAsync(host, acc, sizeof(host), cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return cuda_fail(e, "reading probe statistics");
+  if ((s = loka_device_status(stream)) != LOKA_OK) return s;
+  stats->mere = host[1] > 0 ? host[0] / host[1] : 0.0;
+  stats->rel_err_fro = host[3] > 0 ? std::sqrt(host[2]) / std::sqrt(host[3]) : 0.0;
+  stats->max_abs = host[4];
+  stats->zero_ref_count = desc->M * desc->N - static_cast<int64_t>(host[1]);
+  return LOKA_OK;
+}
+
+loka_status loka_dispatch_select(const loka_dispatch_entry* table, int64_t n, const loka_problem* p,
+                                 const loka_policy* policy, int32_t* choice) {
+  if (p == nullptr || policy == nullptr || choice == nullptr) return fail(LOKA_ERR_INVALID_ARG, "NULL argument");
+  if (n < 0 || (n > 0 && table == nullptr)) return fail(LOKA_ERR_INVALID_ARG, "bad table");
+  if (p->M <= 0) return fail(LOKA_ERR_INVALID_ARG, "problem M must be positive");
+  *choice = LOKA_BF16;
+  // candidate rows: same N, K, norm; nearest log2(M) (ties: larger M);
+  // nearest outlier fraction (ties: larger)
+  double best_dm = INFINITY;
+  int64_t best_m = -1;
+  for (int64_t i = 0; i < n; ++i) {
+    const loka_problem& q = table[i].p;
+    if (q.N != p->N || q.K != p->K || q.norm != p->norm || q.M <= 0) continue;
+    const double dm = std::fabs(std::log2(static_cast<double>(q.M)) - std::log2(static_cast<double>(p->M)));
+    if (dm < best_dm || (dm == best_dm && q.M > best_m)) {
+      best_dm = dm;
+      best_m = q.M;
+    }
+  }
+  if (best_m < 0) return LOKA_OK;
+  double best_do = INFINITY, best_o = -INFINITY;
+  for (int64_t i = 0; i < n; ++i) {
+    const loka_problem& q = table[i].p;
+    if (q.N != p->N || q.K != p->K || q.norm != p->norm || q.M != best_m) continue;
+    const double d_o = std::fabs(q.outlier_frac - p->outlier_frac);
+    if (d_o < best_do || (d_o == best_do && q.outlier_frac > best_o)) {
+      best_do = d_o;
+      best_o = q.outlier_frac;
+    }
+  }
+  auto is_cand = [&](const loka_dispatch_entry& e) {
+    return e.p.N == p->N && e.p.K == p->K && e.p.norm == p->norm && e.p.M == best_m && e.p.outlier_frac == best_o;
+  };
+  double t_ref = INFINITY;
+  bool have_ref = false;
+  for (int64_t i = 0; i < n; ++i)
+    if (is_cand(table[i]) && table[i].variant == LOKA_BF16) {
+      have_ref = true;
+      t_ref = std::fmin(t_ref, table[i].time_us);
+    }
+  const loka_dispatch_entry* best = nullptr;
+  for (int64_t i = 0; i < n; ++i) {
+    const loka_dispatch_entry& e = table[i];
+    if (!is_cand(e)) continue;
+    if (!(e.rel_err <= policy->max_rel_err)) continue;
+    if (policy->max_mere >= 0 && !(e.mere < policy->max_mere)) continue;
+    if (policy->min_speedup >= 0 && e.variant != LOKA_BF16) {
+      if (!have_ref || !(t_ref / e.time_us > policy->min_speedup)) continue;
+    }
+    if (best == nullptr || e.time_us < best->time_us ||
+        (e.time_us == best->time_us && (e.rel_err < best->rel_err ||
+                                        (e.rel_err == best->rel_err && e.variant < best->variant))))
+      best = &e;
+  }
+  if (best != nullptr) *choice = best->variant;
+  return LOKA_OK;
+}
+
+}  // extern "C"

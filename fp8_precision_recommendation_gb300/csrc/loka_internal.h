@@ -1,0 +1,91 @@
+// Internal declarations shared by the library's translation units (not part
+// of the C ABI; see include/loka.h for that).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace loka {
+
+constexpr int kScaleTensor = 0;
+constexpr int kScaleRow = 1;
+constexpr int kScaleMx32 = 2;
+constexpr int kBf16 = 3;
+
+constexpr int kNormNone = 0;
+constexpr int kNormLayer = 1;
+constexpr int kNormRms = 2;
+
+constexpr int kMaxGroups = 16;
+constexpr int kMaxQuantJobs = 2 * kMaxGroups;
+
+// One tensor to quantize: x bf16 [rows, cols] -> q E4M3 [rows, cols] +
+// scales (fp32 [1] / fp32 [rows] / E8M0 [rows, cols/32]).
+struct QuantJob {
+  const void* x;
+  uint8_t* q;
+  void* scales;
+  unsigned* amax_slot;   // tensorwise only: 4-byte accumulator, zeroed by the launcher
+  int64_t rows;
+  int64_t cols;
+  int64_t row_begin;     // first row of this job in the launch's joint row space
+};
+
+struct QuantJobs {
+  QuantJob j[kMaxQuantJobs];
+  int n;
+  int64_t total_rows;
+};
+
+cudaError_t launch_quantize(const QuantJobs& jobs, int mode, int sms, cudaStream_t stream);
+
+// ------------------------------------------------------------------ GEMM
+// Per-group arguments of the fused GEMM + normalization kernel.
+struct GemmGroup {
+  CUtensorMap tm_a;      // A [M,K] (E4M3 or bf16), box {128 bytes of K, 128 rows}
+  CUtensorMap tm_b;      // B [N,K], box {128 bytes of K, min(N,256) rows}
+  CUtensorMap tm_y;      // Y [M,N] (bf16 or fp32), box {128 bytes of N, 128 rows}
+  CUtensorMap tm_sfa;    // MX only: A scales, see gemm_norm.cu
+  CUtensorMap tm_sfb;    // MX only: B scales
+  const float* sx;       // per-row [M] / per-tensor [1] activation scale, or null (=1)
+  const float* sw;       // per-row [N] / per-tensor [1] weight scale, or null (=1)
+  const uint16_t* bias;  // bf16 [N] or null
+  const uint16_t* gamma; // bf16 [N] or null
+  const uint16_t* beta;  // bf16 [N] or null
+  int64_t M;
+  int32_t tile_begin;    // first tile of this group in the launch's tile space
+  int32_t sx_per_row;    // 1: sx has M entries, 0: one entry
+  int32_t sw_per_row;
+  int32_t pad;
+};
+
+struct GemmParams {
+  GemmGroup g[kMaxGroups];
+  int32_t num_groups;
+  int32_t total_tiles;
+  int32_t K;
+  int32_t norm;
+  float eps;
+  int32_t pad;
+  unsigned* status;      // device status word
+  uint64_t wait_limit_ns;
+};
+
+enum class OperandKind : int { kE4M3 = 0, kBf16 = 1, kMxE4M3 = 2 };
+enum class OutKind : int { kBf16 = 0, kF32 = 1 };
+
+// Launches the persistent GEMM + epilogue kernel for N columns.
+cudaError_t launch_gemm_norm(const GemmParams& p, int N, OperandKind op, OutKind out, int sms, cudaStream_t stream);
+
+// Shared-memory bytes the kernel needs (host side, for validation).
+size_t gemm_smem_bytes(int N, OperandKind op);
+
+// Probe reduction: accumulates MERE / Frobenius / max statistics of out vs ref.
+cudaError_t launch_error_reduce(const float* out, const float* ref, int64_t n, double* acc, int sms, cudaStream_t stream);
+
+// Watchdog self-test: waits on a barrier that nothing completes.
+cudaError_t launch_watchdog_selftest(unsigned* status, uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace loka

@@ -1,0 +1,262 @@
+// amax -> scale -> E4M3 cast kernels (tensorwise, rowwise, MX 1x32).
+//
+// Defined by "LoKA: Low-precision Kernel Applications for Recommendation
+// Models at Scale", section II-C (FP8 recipes with tensorwise / rowwise /
+// blockwise scaling, whose quantization cost is over 30% of GEMM latency) and
+// by the MXFP8 block scaling on the GEM Training page ("Low Precision Flash
+// Attention": scale factors along each GEMM's K dimension).
+//
+// These are HBM-bound streaming kernels: every thread moves 16-byte vectors
+// (8 bf16 in, 8 E4M3 codes out), a warp covers 512 contiguous input bytes per
+// load, and the row amax is a warp-shuffle reduction, so the data are read
+// from HBM exactly once.  Several tensors (the X and W of every group of a
+// grouped layer) are handled by one launch through a job table.
+#include "loka_internal.h"
+#include "ptx.cuh"
+
+namespace loka {
+
+namespace {
+
+constexpr float kE4M3Max = 448.0f;
+
+__device__ __forceinline__ float abs_max8(const uint4& v, float m) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    m = fmaxf(m, fabsf(bf16lo(w[i])));
+    m = fmaxf(m, fabsf(bf16hi(w[i])));
+  }
+  return m;
+}
+
+// 8 bf16 * mul -> 8 E4M3 codes; the multiply is one fp32 round-to-nearest.
+__device__ __forceinline__ uint2 cast8(const uint4& v, float mul) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t out[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint16_t a = cvt_e4m3x2(__fmul_rn(bf16lo(w[2 * i]), mul), __fmul_rn(bf16hi(w[2 * i]), mul));
+    const uint16_t b = cvt_e4m3x2(__fmul_rn(bf16lo(w[2 * i + 1]), mul), __fmul_rn(bf16hi(w[2 * i + 1]), mul));
+    out[i] = static_cast<uint32_t>(a) | (static_cast<uint32_t>(b) << 16);
+  }
+  return make_uint2(out[0], out[1]);
+}
+
+__device__ __forceinline__ float warp_max(float m) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  return m;
+}
+
+// inv = 448/amax and scale = amax/448, one IEEE division each; amax 0 -> 1.
+__device__ __forceinline__ void row_scales(float amax, float& inv, float& scale) {
+  if (amax == 0.0f) {
+    inv = 1.0f;
+    scale = 1.0f;
+  } else {
+    inv = __fdiv_rn(kE4M3Max, amax);
+    scale = __fdiv_rn(amax, kE4M3Max);
+  }
+}
+
+// E8M0 exponent of a block from the fp32 exponent field of its amax:
+// e = clamp(floor(log2 amax) - 8, -127, 127).  A subnormal or zero amax has
+// field 0, which lands below -127 and clamps; Inf/NaN have field 255.
+__device__ __forceinline__ int mx_exponent(float amax) {
+  const int field = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+  int e = field - 127 - 8;
+  e = e < -127 ? -127 : e;
+  e = e > 127 ? 127 : e;
+  return e;
+}
+
+// 2^-e as an fp32 (exact: e is in [-127, 120], so 127 - e is in [7, 254]).
+__device__ __forceinline__ float pow2_neg(int e) { return __uint_as_float(static_cast<uint32_t>(127 - e) << 23); }
+
+__device__ __forceinline__ int find_job(const QuantJobs& jobs, int64_t gr) {
+  int j = 0;
+  while (j + 1 < jobs.n && jobs.j[j + 1].row_begin <= gr) ++j;
+  return j;
+}
+
+// One warp per row.  V = 16-byte vectors per lane kept in registers
+// (cols <= 256 * V).  MODE 1 = rowwise, MODE 2 = MX 1x32.
+template <int MODE, int V>
+__global__ void __launch_bounds__(256) quant_rows_kernel(const __grid_constant__ QuantJobs jobs) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t gr = warp0; gr < jobs.total_rows; gr += nwarps) {
+    const QuantJob& job = jobs.j[find_job(jobs, gr)];
+    const int64_t row = gr - job.row_begin;
+    const int nvec = static_cast<int>(job.cols >> 3);
+    const uint4* src = reinterpret_cast<const uint4*>(job.x) + row * nvec;
+    uint2* dst = reinterpret_cast<uint2*>(job.q + row * job.cols);
+    uint4 v[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int idx = i * 32 + lane;
+      v[i] = idx < nvec ? __ldcs(src + idx) : make_uint4(0, 0, 0, 0);
+    }
+    if (MODE == kScaleRow) {
+      float m = 0.0f;
+#pragma unroll
+      for (int i = 0; i < V; ++i) m = abs_max8(v[i], m);
+      m = warp_max(m);
+      float inv, scale;
+      row_scales(m, inv, scale);
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        const int idx = i * 32 + lane;
+        if (idx < nvec) dst[idx] = cast8(v[i], inv);
+      }
+      if (lane == 0) reinterpret_cast<float*>(job.scales)[row] = scale;
+    } else {
+      uint8_t* sc = reinterpret_cast<uint8_t*>(job.scales) + row * (job.cols >> 5);
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        const int idx = i * 32 + lane;
+        float m = abs_max8(v[i], 0.0f);
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        const int e = mx_exponent(m);
+        if (idx < nvec) {
+          dst[idx] = cast8(v[i], pow2_neg(e));
+          if ((lane & 3) == 0) sc[idx >> 2] = static_cast<uint8_t>(e + 127);
+        }
+      }
+    }
+  }
+}
+
+// Rows longer than 2048 elements: amax pass, then a cast pass that re-reads
+// the row (it is still in L1/L2).  Same arithmetic as above.
+template <int MODE>
+__global__ void __launch_bounds__(256) quant_rows_long_kernel(const __grid_constant__ QuantJobs jobs) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t gr = warp0; gr < jobs.total_rows; gr += nwarps) {
+    const QuantJob& job = jobs.j[find_job(jobs, gr)];
+    const int64_t row = gr - job.row_begin;
+    const int nvec = static_cast<int>(job.cols >> 3);
+    const uint4* src = reinterpret_cast<const uint4*>(job.x) + row * nvec;
+    uint2* dst = reinterpret_cast<uint2*>(job.q + row * job.cols);
+    if (MODE == kScaleRow) {
+      float m = 0.0f;
+      for (int idx = lane; idx < nvec; idx += 32) m = abs_max8(__ldg(src + idx), m);
+      m = warp_max(m);
+      float inv, scale;
+      row_scales(m, inv, scale);
+      for (int idx = lane; idx < nvec; idx += 32) dst[idx] = cast8(__ldg(src + idx), inv);
+      if (lane == 0) reinterpret_cast<float*>(job.scales)[row] = scale;
+    } else {
+      uint8_t* sc = reinterpret_cast<uint8_t*>(job.scales) + row * (job.cols >> 5);
+      for (int base = 0; base < nvec; base += 32) {   // nvec % 4 == 0: whole blocks per step
+        const int idx = base + lane;
+        const uint4 v = idx < nvec ? __ldcs(src + idx) : make_uint4(0, 0, 0, 0);
+        float m = abs_max8(v, 0.0f);
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        const int e = mx_exponent(m);
+        if (idx < nvec) {
+          dst[idx] = cast8(v, pow2_neg(e));
+          if ((lane & 3) == 0) sc[idx >> 2] = static_cast<uint8_t>(e + 127);
+        }
+      }
+    }
+  }
+}
+
+// Tensorwise pass 1: amax of each job into its slot (fp32 bits; the slot must
+// be zero beforehand).  blockIdx.y = job.
+__global__ void __launch_bounds__(256) amax_tensor_kernel(const __grid_constant__ QuantJobs jobs) {
+  const QuantJob& job = jobs.j[blockIdx.y];
+  const int64_t nvec = (job.rows * job.cols) >> 3;
+  const uint4* src = reinterpret_cast<const uint4*>(job.x);
+  float m = 0.0f;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    m = abs_max8(__ldg(src + i), m);
+  m = warp_max(m);
+  __shared__ float red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    m = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
+    m = warp_max(m);
+    // non-negative floats order like their bit patterns
+    if (threadIdx.x == 0 && !(m != m)) atomicMax(job.amax_slot, __float_as_uint(m));
+  }
+}
+
+// Tensorwise pass 2: cast with the tensor's scale; block (0, job) writes it.
+__global__ void __launch_bounds__(256) cast_tensor_kernel(const __grid_constant__ QuantJobs jobs) {
+  const QuantJob& job = jobs.j[blockIdx.y];
+  const float amax = __uint_as_float(*reinterpret_cast<volatile unsigned*>(job.amax_slot));
+  float inv, scale;
+  row_scales(amax, inv, scale);
+  if (blockIdx.x == 0 && threadIdx.x == 0) reinterpret_cast<float*>(job.scales)[0] = scale;
+  const int64_t nvec = (job.rows * job.cols) >> 3;
+  const uint4* src = reinterpret_cast<const uint4*>(job.x);
+  uint2* dst = reinterpret_cast<uint2*>(job.q);
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    dst[i] = cast8(__ldcs(src + i), inv);
+}
+
+template <int MODE>
+cudaError_t launch_rows(const QuantJobs& jobs, int max_cols, int sms, cudaStream_t stream) {
+  const int threads = 256;
+  const int64_t warps_needed = jobs.total_rows;
+  int64_t blocks = (warps_needed + 7) / 8;
+  const int64_t cap = static_cast<int64_t>(sms) * 8;   // 8 resident 256-thread blocks per SM
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  const dim3 grid(static_cast<unsigned>(blocks));
+  if (max_cols <= 256)
+    quant_rows_kernel<MODE, 1><<<grid, threads, 0, stream>>>(jobs);
+  else if (max_cols <= 512)
+    quant_rows_kernel<MODE, 2><<<grid, threads, 0, stream>>>(jobs);
+  else if (max_cols <= 1024)
+    quant_rows_kernel<MODE, 4><<<grid, threads, 0, stream>>>(jobs);
+  else if (max_cols <= 2048)
+    quant_rows_kernel<MODE, 8><<<grid, threads, 0, stream>>>(jobs);
+  else
+    quant_rows_long_kernel<MODE><<<grid, threads, 0, stream>>>(jobs);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(const QuantJobs& jobs, int mode, int sms, cudaStream_t stream) {
+  if (jobs.n == 0 || jobs.total_rows == 0) return cudaSuccess;
+  int max_cols = 0;
+  int64_t max_elems = 0;
+  for (int i = 0; i < jobs.n; ++i) {
+    if (jobs.j[i].cols > max_cols) max_cols = static_cast<int>(jobs.j[i].cols);
+    if (jobs.j[i].rows * jobs.j[i].cols > max_elems) max_elems = jobs.j[i].rows * jobs.j[i].cols;
+  }
+  if (mode == kScaleRow) return launch_rows<kScaleRow>(jobs, max_cols, sms, stream);
+  if (mode == kScaleMx32) return launch_rows<kScaleMx32>(jobs, max_cols, sms, stream);
+  if (mode == kScaleTensor) {
+    for (int i = 0; i < jobs.n; ++i) {
+      cudaError_t e = cudaMemsetAsync(jobs.j[i].amax_slot, 0, sizeof(unsigned), stream);
+      if (e != cudaSuccess) return e;
+    }
+    int64_t per_job = (max_elems / 8 + 255) / 256;
+    const int64_t cap = (static_cast<int64_t>(sms) * 8 + jobs.n - 1) / jobs.n;
+    if (per_job > cap) per_job = cap;
+    if (per_job < 1) per_job = 1;
+    const dim3 grid(static_cast<unsigned>(per_job), static_cast<unsigned>(jobs.n));
+    amax_tensor_kernel<<<grid, 256, 0, stream>>>(jobs);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    cast_tensor_kernel<<<grid, 256, 0, stream>>>(jobs);
+    return cudaGetLastError();
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace loka

@@ -1,0 +1,228 @@
+/*
+ * loka.h -- C ABI of the GB300 (sm_103a) FP8 linear + normalization library.
+ *
+ * The operation is the FP8 linear layer of a large recommendation model: a
+ * small GEMM followed immediately by a normalization, whose quantization
+ * overhead can cancel the FP8 gain ("LoKA: Low-precision Kernel Applications
+ * for Recommendation Models at Scale", section I and section II-C "Key
+ * findings").  The library computes, on one GPU:
+ *
+ *   amax -> scale -> E4M3 cast of activations X[M,K] and weights W[N,K]
+ *   -> FP8 GEMM with fp32 accumulation (tcgen05 tensor cores, TMEM)
+ *   -> epilogue: dequantize, add bias, LayerNorm or RMSNorm over N, bf16 store
+ *
+ * plus a per-layer quantization-error probe (LoKA section III-A, MERE of
+ * FP8(Wx+b) against a high-precision Wx+b) and a variant selector (LoKA
+ * section III-C, Dispatch).
+ *
+ * Conventions for every call:
+ *   - Pointers named as device pointers must be device memory of the current
+ *     CUDA device; the caller owns all memory.  No call allocates device
+ *     memory; calls that need temporary space take a caller-provided
+ *     workspace, whose size the matching *_workspace_size() call returns.
+ *   - Work is enqueued on `stream` (a cudaStream_t, NULL = legacy default
+ *     stream) and is asynchronous, except where a call says it synchronizes.
+ *   - Argument errors are found on the host before anything is launched; the
+ *     call then returns a non-zero loka_status and loka_last_error() gives a
+ *     message.  Launch failures return LOKA_ERR_CUDA.
+ *   - Kernels never spin forever: every wait inside a kernel has a time
+ *     limit; a kernel that gives up sets a device status flag and returns.
+ *     loka_device_status() (or the next synchronizing call) reports it as
+ *     LOKA_ERR_TIMEOUT.
+ *   - Tensors are row-major.  X is [M,K] (K contiguous), W is [N,K] (the
+ *     nn.Linear layout; the GEMM is Y = X W^T), Y is [M,N].
+ *   - Not thread-safe per stream; calls on different streams may overlap.
+ */
+#ifndef LOKA_H_
+#define LOKA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t loka_status;
+#define LOKA_OK 0
+#define LOKA_ERR_INVALID_ARG 1   /* bad pointer, size, alignment or enum   */
+#define LOKA_ERR_UNSUPPORTED 2   /* valid but not implemented (e.g. N)    */
+#define LOKA_ERR_WORKSPACE 3     /* workspace missing or too small         */
+#define LOKA_ERR_TIMEOUT 4       /* a kernel wait ran out of time          */
+#define LOKA_ERR_CUDA 5          /* a CUDA runtime/driver call failed      */
+
+/* Scaling granularity of the E4M3 cast (LoKA section II-C / Table VI name
+ * tensorwise, rowwise and blockwise recipes; the GEM Training page, "Low
+ * Precision Flash Attention", places MXFP8 scale factors along K). */
+#define LOKA_SCALE_TENSOR 0      /* one fp32 scale for the whole tensor    */
+#define LOKA_SCALE_ROW 1         /* one fp32 scale per row                 */
+#define LOKA_SCALE_MX32 2        /* one E8M0 scale per 1x32 block along K  */
+#define LOKA_BF16 3              /* no quantization: bf16 GEMM (fallback)  */
+
+/* Normalization applied to each output row (LoKA section III-B). */
+#define LOKA_NORM_NONE 0
+#define LOKA_NORM_LAYER 1        /* (v-mean)/sqrt(var+eps)*gamma+beta      */
+#define LOKA_NORM_RMS 2          /* v/sqrt(mean(v^2)+eps)*gamma            */
+
+/* Library version, (major << 16) | minor. */
+int32_t loka_version(void);
+
+/* Message for the last non-OK status returned on this host thread. */
+const char* loka_last_error(void);
+
+/* Synchronizes `stream`, then reads and clears the device status flag that
+ * kernels set when a wait runs out of time.  Returns LOKA_OK,
+ * LOKA_ERR_TIMEOUT or LOKA_ERR_CUDA. */
+loka_status loka_device_status(void* stream);
+
+/* Diagnostic: launches one kernel whose only wait can never complete (an
+ * mbarrier that nothing arrives at).  Its bounded wait gives up after
+ * limit_ns nanoseconds (0 < limit_ns <= 1e10), sets the device status flag
+ * and returns, so the next loka_device_status() reports LOKA_ERR_TIMEOUT and
+ * the GPU context stays usable.  Exists to test the timeout path without
+ * ever hanging or faulting a GPU.  Asynchronous. */
+loka_status loka_selftest_watchdog(uint64_t limit_ns, void* stream);
+
+/* ------------------------------------------------------------------------
+ * loka_quantize_fp8 -- amax, scale selection and E4M3 cast of one tensor.
+ *
+ * Defined by LoKA section II-C (FP8 recipes: tensorwise, rowwise, blockwise)
+ * and the MX block scaling the GEM Training page uses (scale factors along
+ * K).  For x of shape [rows, cols] (bf16, device, row-major, 16-byte
+ * aligned, cols % 32 == 0):
+ *   LOKA_SCALE_TENSOR: amax = max|x|;  inv = fl32(448/amax); q = E4M3(fl32(x*inv));
+ *                      scales[0] = fl32(amax/448)  (fp32, 1 element)
+ *   LOKA_SCALE_ROW:    the same per row; scales is fp32 [rows]
+ *   LOKA_SCALE_MX32:   per block of 32 along cols: e = clamp(floor(log2 amax)-8,
+ *                      -127, 127); q = E4M3(x * 2^-e); scales is uint8 E8M0
+ *                      [rows, cols/32] holding e + 127
+ * amax == 0 gives scale 1 (tensor/row) or E8M0 code 0 (MX).  E4M3 rounding
+ * is to nearest, ties to even, saturating at +-448; NaN stays NaN.
+ * q: uint8 [rows, cols] device (16-byte aligned).  workspace: device, at
+ * least loka_quantize_fp8_workspace_size() bytes (0 for ROW and MX32; NULL
+ * allowed then).  Asynchronous.
+ * ---------------------------------------------------------------------- */
+size_t loka_quantize_fp8_workspace_size(int64_t rows, int64_t cols, int32_t mode);
+loka_status loka_quantize_fp8(const void* x, int64_t rows, int64_t cols, int32_t mode,
+                              void* q, void* scales, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/* ------------------------------------------------------------------------
+ * loka_fp8_linear_norm -- Y = Norm(dequant(E4M3(X) E4M3(W)^T) + b), bf16.
+ *
+ * Defined by LoKA section II-C (the FP8 linear y = Wx + b), section III-B
+ * "Block-wise Normalization" (the normalization fused into the GEMM
+ * epilogue while the output row is still on chip; case 1, a whole output row
+ * per thread block) and section I (wide ensembles of small GEMMs: a grouped
+ * call runs several independent layers in one launch).
+ *
+ * One descriptor per independent layer (group).  All groups of one call must
+ * share N, K, mode, norm and eps and the *_is_fp8 flags; M may differ.
+ *   M >= 0; K % 128 == 0; N in {64, 128, 192, 256, 512}.
+ *   x: bf16 [M,K] (x_is_fp8 = 0) or E4M3 [M,K] with x_scales as produced by
+ *      loka_quantize_fp8 (x_is_fp8 = 1).  Same for w / w_scales / w_is_fp8.
+ *   mode: LOKA_SCALE_* (LOKA_BF16 runs the bf16 GEMM; *_is_fp8 must be 0).
+ *   bias, gamma, beta: bf16 [N] or NULL (0, 1, 0).  y: bf16 [M,N].
+ *   eps: added to the variance (LayerNorm) or mean square (RMSNorm).
+ * Accumulation is fp32 in tensor memory; the epilogue works in fp32.
+ * workspace: device, loka_fp8_linear_norm_workspace_size() bytes (holds the
+ * quantized operands and scales of bf16 inputs).  Asynchronous.
+ * num_groups in [1, 16].  `descs` is a host array.
+ * ---------------------------------------------------------------------- */
+typedef struct loka_linear_desc {
+  int64_t M, N, K;
+  int32_t mode;          /* LOKA_SCALE_* or LOKA_BF16 */
+  int32_t norm;          /* LOKA_NORM_* */
+  float eps;
+  int32_t x_is_fp8;
+  int32_t w_is_fp8;
+  int32_t reserved;
+  const void* x;         /* device */
+  const void* x_scales;  /* device, used when x_is_fp8 */
+  const void* w;         /* device */
+  const void* w_scales;  /* device, used when w_is_fp8 */
+  const void* bias;      /* device bf16 [N] or NULL */
+  const void* gamma;     /* device bf16 [N] or NULL */
+  const void* beta;      /* device bf16 [N] or NULL */
+  void* y;               /* device bf16 [M,N] */
+} loka_linear_desc;
+
+size_t loka_fp8_linear_norm_workspace_size(const loka_linear_desc* descs, int32_t num_groups);
+loka_status loka_fp8_linear_norm(const loka_linear_desc* descs, int32_t num_groups,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * loka_quant_error -- quantization-error probe of one layer.
+ *
+ * Defined by LoKA section II-C "Error Analysis" (MERE: the mean element-wise
+ * relative error |out-ref|/|ref| of a low-precision output against a
+ * high-precision one) and section III-A "Offline Error Quantification"
+ * (loss = MERE(FP8(Wx+b), high-precision(Wx+b)) per layer, Fig. 5).
+ * out = the FP8 linear output before normalization in fp32 (desc->mode);
+ * ref = the bf16-input linear with fp32 accumulation.  desc->norm, gamma,
+ * beta and y are ignored.  Reports, over all M*N elements:
+ *   mere        mean of |out-ref|/|ref| over elements with ref != 0
+ *   rel_err_fro ||out-ref||_F / ||ref||_F
+ *   max_abs     max |out-ref|
+ *   zero_ref_count, count
+ * workspace: loka_quant_error_workspace_size() bytes.  SYNCHRONIZES the
+ * stream; `stats` is a host pointer.
+ * ---------------------------------------------------------------------- */
+typedef struct loka_error_stats {
+  double mere;
+  double rel_err_fro;
+  double max_abs;
+  int64_t zero_ref_count;
+  int64_t count;
+} loka_error_stats;
+
+size_t loka_quant_error_workspace_size(const loka_linear_desc* desc);
+loka_status loka_quant_error(const loka_linear_desc* desc, void* workspace, size_t workspace_bytes,
+                             loka_error_stats* stats, void* stream);
+
+/* ------------------------------------------------------------------------
+ * loka_dispatch_select -- choose a variant for one layer (host only).
+ *
+ * Defined by LoKA section III-C "Library and Recipe Selection": filter the
+ * candidates by expected error (MERE below a threshold, typically 0.2) and by
+ * speedup over the high-precision path (typically > 1.05x), then take the one
+ * with the highest measured throughput; section VI "Limitations": a layer
+ * with no qualifying candidate runs in high precision (LOKA_BF16).
+ * table: host array of n measured rows.  A query matches rows with equal N,
+ * K and norm; among them the rows nearest in log2(M) (ties: larger M) and in
+ * outlier fraction (ties: larger) are the candidates.  Filters: rel_err <=
+ * max_rel_err; mere < max_mere when max_mere >= 0; t_bf16/t > min_speedup
+ * when min_speedup >= 0 (needs a LOKA_BF16 row).  Smallest time wins; ties
+ * go to smaller rel_err, then the smaller variant id.  *choice (host) gets a
+ * LOKA_SCALE_* / LOKA_BF16 value.  Pure host code, no GPU work.
+ * ---------------------------------------------------------------------- */
+typedef struct loka_problem {
+  int64_t M, N, K;
+  int32_t norm;
+  int32_t reserved;
+  double outlier_frac;
+} loka_problem;
+
+typedef struct loka_dispatch_entry {
+  loka_problem p;
+  int32_t variant;
+  int32_t reserved;
+  double time_us;
+  double rel_err;
+  double mere;
+} loka_dispatch_entry;
+
+typedef struct loka_policy {
+  double max_rel_err;   /* e.g. 1e-2 */
+  double max_mere;      /* e.g. 0.2; < 0 disables */
+  double min_speedup;   /* e.g. 1.05; < 0 disables */
+} loka_policy;
+
+loka_status loka_dispatch_select(const loka_dispatch_entry* table, int64_t n, const loka_problem* p,
+                                 const loka_policy* policy, int32_t* choice);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LOKA_H_ */

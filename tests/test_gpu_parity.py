@@ -1,0 +1,277 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the CPU oracle
+on the same seeded inputs.  Quantized bytes and scales must be bit-exact;
+bf16 outputs must meet the rule in tests/parity.py."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import formats as F
+from oracle import linear as OL
+from oracle import probe as OP
+from oracle import quantize as OQ
+from parity import check_bf16_output
+
+import fp8_precision_recommendation_gb300 as loka
+from fp8_precision_recommendation_gb300 import _loka
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _gpu(t):
+    return t.to(DEV) if t is not None else None
+
+
+def _oracle_quant(x, mode):
+    q, s = OQ.quantize(x, mode)
+    return q, np.asarray(s)
+
+
+def _check_quant(x_cpu, mode, rows=None):
+    q, s = loka.quantize_fp8(x_cpu.to(DEV), mode)
+    torch.cuda.synchronize()
+    q = q.cpu().numpy()
+    s = s.cpu().numpy()
+    if rows is not None:
+        xq = x_cpu[torch.as_tensor(rows)]
+        q = q[rows]
+        s = s[rows] if mode != W.SCALE_TENSOR else s
+    else:
+        xq = x_cpu
+    oq, os_ = _oracle_quant(xq, mode)
+    if mode == W.SCALE_TENSOR:
+        assert s.shape == (1,)
+        assert np.float32(s[0]).tobytes() == np.float32(os_).tobytes()
+    elif mode == W.SCALE_ROW:
+        assert np.array_equal(s.view(np.uint32), os_.astype(np.float32).view(np.uint32))
+    else:
+        assert np.array_equal(s, os_)
+    if not np.array_equal(q, oq):
+        bad = np.argwhere(q != oq)[:8]
+        raise AssertionError(f"{int((q != oq).sum())} codes differ; first {[(tuple(b), q[tuple(b)], oq[tuple(b)]) for b in bad]}")
+
+
+# ------------------------------------------------------------ quantization
+@pytest.mark.parametrize("mode", [W.SCALE_TENSOR, W.SCALE_ROW, W.SCALE_MX32])
+def test_quantize_every_finite_bf16_pattern(lib, mode):
+    v = W.all_bf16_patterns()
+    fin = torch.isfinite(v.float())
+    v = v[fin]
+    v = v[: (v.numel() // 64) * 64].reshape(-1, 64)
+    _check_quant(v, mode)
+
+
+@pytest.mark.parametrize("mode", [W.SCALE_TENSOR, W.SCALE_ROW, W.SCALE_MX32])
+def test_quantize_every_bf16_pattern_at_unit_scale(lib, mode):
+    # rows whose amax is 448 (tensor/row) so that x * inv == x exactly, or MX
+    # blocks whose scale is 2^0, put every bf16 value through the cast itself
+    v = W.all_bf16_patterns().float()
+    fin = torch.isfinite(v) & (v.abs() <= 448)
+    v = v[fin]
+    n = (v.numel() // 31) * 31
+    body = v[:n].reshape(-1, 31)
+    anchor = torch.full((body.shape[0], 1), 448.0 if mode != W.SCALE_MX32 else 256.0)
+    x = torch.cat([anchor, body], dim=1).to(torch.bfloat16)
+    x = torch.cat([x, x], dim=1)      # 64 columns (two MX blocks)
+    _check_quant(x, mode)
+
+
+@pytest.mark.parametrize("mode", [W.SCALE_ROW, W.SCALE_MX32])
+@pytest.mark.parametrize("cols", [32, 96, 128, 256, 512, 1024, 2048, 2080, 4096])
+def test_quantize_shapes_and_ragged_widths(lib, mode, cols):
+    x = W.random_bf16((37, cols), seed=cols, dist="laplace", outlier_frac=0.01)
+    _check_quant(x, mode)
+
+
+def test_quantize_zero_and_extreme_rows(lib):
+    x = torch.zeros((6, 64), dtype=torch.bfloat16)
+    x[1, 3] = 1e-38
+    x[2, 5] = -3.0e38
+    x[3, :] = -0.0
+    x[4, 7] = 1e-40          # bf16 subnormal
+    x[5, 0] = 3.0e38
+    x[5, 1] = 1.0
+    for mode in (W.SCALE_TENSOR, W.SCALE_ROW, W.SCALE_MX32):
+        _check_quant(x, mode)
+
+
+def test_quantize_infinite_inputs(lib):
+    # amax = inf: rowwise gives inv = 0, so finite elements become signed
+    # zeros and the infinity becomes a NaN code (sign unspecified); MX gives
+    # the block exponent of 2^128 and the infinity saturates to 448.
+    x = torch.ones((2, 64), dtype=torch.bfloat16)
+    x[0, 3] = float("inf")
+    x[1, 5] = -float("inf")
+    x[1, 6] = -2.0
+    q, s = loka.quantize_fp8(x.to(DEV), W.SCALE_ROW)
+    q = q.cpu().numpy()
+    assert np.isinf(s.cpu().numpy()).all()
+    assert q[0, 3] & 0x7F == 0x7F and q[1, 5] & 0x7F == 0x7F
+    assert q[0, 0] == 0x00 and q[1, 6] == 0x80
+    q, s = loka.quantize_fp8(x.to(DEV), W.SCALE_MX32)
+    q, s = q.cpu().numpy(), s.cpu().numpy()
+    assert q[0, 3] == 0x7E and q[1, 5] == 0xFE
+    oq, os_ = OQ.quantize_mx(x)
+    assert np.array_equal(q, oq) and np.array_equal(s, os_)
+
+
+@pytest.mark.parametrize("mode", [W.SCALE_TENSOR, W.SCALE_ROW, W.SCALE_MX32])
+def test_quantize_single_config_bit_exact(lib, mode):
+    inp = W.single()
+    _check_quant(inp.x, mode)
+    _check_quant(inp.w, mode)
+
+
+def test_quantize_rec_mlp_full_size_rowwise(lib):
+    inp = W.rec_mlp()
+    _check_quant(inp.x, W.SCALE_ROW)
+    _check_quant(inp.w, W.SCALE_ROW)
+
+
+def test_quantize_mxfp8_layer_sampled_rows(lib):
+    inp = W.mxfp8()
+    rng = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([np.arange(128), rng.integers(0, inp.M, 2048), np.arange(inp.M - 128, inp.M)]))
+    _check_quant(inp.x, W.SCALE_MX32, rows=rows)
+    _check_quant(inp.w, W.SCALE_MX32)
+
+
+def test_quantize_empty(lib):
+    q = torch.empty((0, 64), dtype=torch.uint8, device=DEV)
+    s = torch.zeros((1,), dtype=torch.float32, device=DEV)
+    x = torch.empty((0, 64), dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(256, dtype=torch.uint8, device=DEV)
+    _loka.loka_quantize_fp8(x, 0, 64, W.SCALE_TENSOR, q, s, ws, 256)
+    torch.cuda.synchronize()
+    assert s.item() == 1.0
+
+
+# ------------------------------------------------------- linear + norm
+def _layer(inp, y=None):
+    return loka.Layer(x=_gpu(inp.x), w=_gpu(inp.w), bias=_gpu(inp.bias), gamma=_gpu(inp.gamma),
+                      beta=_gpu(inp.beta), mode=inp.mode, norm=inp.norm, eps=inp.eps, y=y)
+
+
+def _run(inps):
+    ys = loka.fp8_linear_norm([_layer(i) for i in inps])
+    torch.cuda.synchronize()
+    assert loka._loka.loka_device_status() == 0
+    return [y.cpu() for y in ys]
+
+
+def _check_layer(inp, y_gpu, rows=None, what=""):
+    y, _, _ = OL.linear_norm_inputs(inp, rows=rows)
+    g = y_gpu if rows is None else y_gpu[torch.as_tensor(rows)]
+    return check_bf16_output(g, y, normalized=inp.norm != W.NORM_NONE, what=what)
+
+
+def test_single_config_per_tensor_layernorm(lib):
+    inp = W.single()
+    (y,) = _run([inp])
+    _check_layer(inp, y, what="single")
+
+
+@pytest.mark.parametrize("mode", [W.SCALE_TENSOR, W.SCALE_ROW, W.SCALE_BF16])
+@pytest.mark.parametrize("norm", [W.NORM_NONE, W.NORM_LAYER, W.NORM_RMS])
+@pytest.mark.parametrize("N", [64, 128, 192, 256, 512])
+def test_small_shapes_all_variants(lib, mode, norm, N):
+    # M spans several 128-row tiles and ends in a ragged tail
+    inp = W.make_layer(389, 256, N, mode=mode, norm=norm, seed=N + 7 * norm + 31 * mode,
+                       outlier_frac=0.01, bias_var=0.02, gamma_uniform=True)
+    inp.beta = W.random_bf16((N,), seed=5, var=0.1)
+    (y,) = _run([inp])
+    _check_layer(inp, y, what=f"mode{mode} norm{norm} N{N}")
+
+
+@pytest.mark.parametrize("M", [1, 127, 128, 129, 1000])
+@pytest.mark.parametrize("K", [128, 384, 2048])
+def test_ragged_m_and_k(lib, M, K):
+    inp = W.make_layer(M, K, 256, mode=W.SCALE_ROW, norm=W.NORM_LAYER, seed=M + K, bias_var=0.02)
+    (y,) = _run([inp])
+    _check_layer(inp, y, what=f"M{M} K{K}")
+
+
+def test_m_zero_is_a_no_op(lib):
+    inp = W.make_layer(0, 128, 128, mode=W.SCALE_ROW, norm=W.NORM_LAYER)
+    (y,) = _run([inp])
+    assert y.shape == (0, 128)
+
+
+def test_rec_mlp_full_size(lib):
+    inp = W.rec_mlp()
+    (y,) = _run([inp])
+    rng = np.random.default_rng(1)
+    rows = np.unique(np.concatenate([np.arange(256), rng.integers(0, inp.M, 4096), np.arange(inp.M - 256, inp.M)]))
+    err = _check_layer(inp, y, rows=rows, what="rec_mlp")
+    assert err < 1e-2
+    # properties of every row: LayerNorm output has mean ~0 and mean square ~1
+    yf = y.float()
+    assert yf.mean(dim=1).abs().max().item() < 2e-2
+    assert (yf.pow(2).mean(dim=1) - 1).abs().max().item() < 2e-2
+
+
+def test_ensemble_grouped_launch(lib):
+    inps = W.ensemble()
+    ys = _run(inps)
+    rng = np.random.default_rng(2)
+    for g, (inp, y) in enumerate(zip(inps, ys)):
+        rows = np.unique(np.concatenate([np.arange(128), rng.integers(0, inp.M, 512), np.arange(inp.M - 128, inp.M)]))
+        _check_layer(inp, y, rows=rows, what=f"group{g}")
+
+
+def test_grouped_with_ragged_and_empty_groups(lib):
+    inps = [W.make_layer(m, 256, 256, mode=W.SCALE_ROW, norm=W.NORM_RMS, seed=m, gamma_uniform=True, eps=1e-6)
+            for m in (300, 0, 129, 1)]
+    ys = _run(inps)
+    for inp, y in zip(inps, ys):
+        if inp.M:
+            _check_layer(inp, y, what=f"M{inp.M}")
+
+
+def test_prequantized_inputs_match_bf16_inputs(lib):
+    inp = W.make_layer(500, 512, 256, mode=W.SCALE_ROW, norm=W.NORM_LAYER, seed=3, bias_var=0.02, outlier_frac=0.01)
+    (y_ref,) = _run([inp])
+    x, w = _gpu(inp.x), _gpu(inp.w)
+    qx, sx = loka.quantize_fp8(x, W.SCALE_ROW)
+    qw, sw = loka.quantize_fp8(w, W.SCALE_ROW)
+    layer = loka.Layer(x=qx, w=qw, x_scales=sx, w_scales=sw, bias=_gpu(inp.bias), mode=W.SCALE_ROW,
+                       norm=W.NORM_LAYER, eps=inp.eps)
+    (y,) = loka.fp8_linear_norm([layer])
+    torch.cuda.synchronize()
+    assert torch.equal(y.cpu(), y_ref)
+
+
+def test_deterministic(lib):
+    inp = W.make_layer(1000, 512, 256, mode=W.SCALE_ROW, norm=W.NORM_LAYER, seed=4, bias_var=0.02)
+    (a,) = _run([inp])
+    (b,) = _run([inp])
+    assert torch.equal(a, b)
+
+
+# ----------------------------------------------------------------- probe
+@pytest.mark.parametrize("mode", [W.SCALE_TENSOR, W.SCALE_ROW, W.SCALE_BF16])
+def test_quant_error_probe_matches_oracle(lib, mode):
+    inp = W.make_layer(1000, 512, 256, mode=mode, norm=W.NORM_NONE, seed=6, bias_var=0.02, outlier_frac=0.01)
+    st = loka.quant_error(_gpu(inp.x), _gpu(inp.w), _gpu(inp.bias), mode)
+    want = OP.quant_error(inp.x, inp.w, inp.bias, mode)
+    assert st["count"] == want["count"]
+    assert st["zero_ref_count"] == want["zero_ref_count"]
+    if mode == W.SCALE_BF16:
+        assert st["rel_err_fro"] < 1e-6 and st["mere"] < 1e-5
+    else:
+        assert abs(st["rel_err_fro"] - want["rel_err_fro"]) <= 1e-3 * want["rel_err_fro"]
+        assert abs(st["mere"] - want["mere"]) <= 1e-2 * want["mere"]
+        assert abs(st["max_abs"] - want["max_abs"]) <= 1e-3 * want["max_abs"] + 1e-6
+
+
+# -------------------------------------------------------------- watchdog
+def test_watchdog_turns_a_stuck_wait_into_a_status(lib):
+    assert _loka.loka_device_status() == _loka.LOKA_OK
+    _loka.loka_selftest_watchdog(2_000_000)          # 2 ms
+    assert _loka.loka_device_status() == _loka.LOKA_ERR_TIMEOUT
+    assert _loka.loka_device_status() == _loka.LOKA_OK   # cleared, context still usable
+    inp = W.single()
+    (y,) = _run([inp])
+    _check_layer(inp, y, what="after watchdog")

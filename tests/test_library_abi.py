@@ -1,0 +1,156 @@
+"""CPU checks of the C-ABI library: it builds, loads, exports every symbol the
+header declares, rejects bad arguments on the host before any launch, and its
+host-only dispatch selector agrees with the oracle's reading of the rule."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import dispatch as D
+from fp8_precision_recommendation_gb300 import _loka
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "loka.h")
+
+
+@pytest.fixture(scope="module")
+def cpu_lib():
+    if not os.path.exists(_loka.LIB_PATH):
+        from fp8_precision_recommendation_gb300 import build
+        build.build()
+    return _loka.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(loka_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_four_calls():
+    names = declared_functions()
+    for n in ["loka_quantize_fp8", "loka_fp8_linear_norm", "loka_quant_error", "loka_dispatch_select"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(cpu_lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(cpu_lib, n), n
+        assert n in _loka.SIGNATURES, n
+
+
+def test_struct_layouts_match_header():
+    # sizes of the C structs (x86-64 / aarch64 LP64 ABI)
+    assert ctypes.sizeof(_loka.LinearDesc) == 3 * 8 + 6 * 4 + 8 * 8
+    assert ctypes.sizeof(_loka.ErrorStats) == 5 * 8
+    assert ctypes.sizeof(_loka.Problem) == 3 * 8 + 2 * 4 + 8
+    assert ctypes.sizeof(_loka.DispatchEntry) == 40 + 8 + 3 * 8
+
+
+def test_version(cpu_lib):
+    assert _loka.loka_version() >= 1
+
+
+def _desc(**kw):
+    d = _loka.LinearDesc()
+    d.M, d.N, d.K, d.mode, d.norm, d.eps = 256, 256, 512, 1, 1, 1e-5
+    d.x = d.w = d.y = 1 << 20
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({"N": 100}, _loka.LOKA_ERR_UNSUPPORTED),
+    ({"K": 96}, _loka.LOKA_ERR_UNSUPPORTED),
+    ({"M": -1}, _loka.LOKA_ERR_INVALID_ARG),
+    ({"mode": 7}, _loka.LOKA_ERR_INVALID_ARG),
+    ({"norm": 9}, _loka.LOKA_ERR_INVALID_ARG),
+    ({"eps": float("nan")}, _loka.LOKA_ERR_INVALID_ARG),
+    ({"x": None}, _loka.LOKA_ERR_INVALID_ARG),
+    ({"y": (1 << 20) + 8}, _loka.LOKA_ERR_INVALID_ARG),         # misaligned
+    ({"mode": 3, "x_is_fp8": 1, "x_scales": 64}, _loka.LOKA_ERR_INVALID_ARG),
+    ({"x_is_fp8": 1}, _loka.LOKA_ERR_INVALID_ARG),                # no x_scales
+])
+def test_linear_norm_rejects_bad_arguments_on_host(cpu_lib, kw, status):
+    arr = _loka.make_descs([_desc(**kw)])
+    assert cpu_lib.loka_fp8_linear_norm(arr, 1, None, 0, None) == status
+    assert len(cpu_lib.loka_last_error()) > 0
+
+
+def test_linear_norm_rejects_group_count_and_mismatch(cpu_lib):
+    arr = _loka.make_descs([_desc()])
+    assert cpu_lib.loka_fp8_linear_norm(arr, 0, None, 0, None) == _loka.LOKA_ERR_INVALID_ARG
+    assert cpu_lib.loka_fp8_linear_norm(arr, 17, None, 0, None) == _loka.LOKA_ERR_INVALID_ARG
+    arr2 = _loka.make_descs([_desc(), _desc(K=256)])
+    assert cpu_lib.loka_fp8_linear_norm(arr2, 2, None, 0, None) == _loka.LOKA_ERR_UNSUPPORTED
+
+
+def test_linear_norm_workspace_is_required_and_sized(cpu_lib):
+    d = _desc()
+    need = _loka.loka_fp8_linear_norm_workspace_size([d])
+    # X E4M3 + row scales + W E4M3 + row scales, each 256-byte aligned
+    al = lambda n: (n + 255) // 256 * 256
+    assert need == al(256 * 512) + al(256 * 4) + al(256 * 512) + al(256 * 4)
+    arr = _loka.make_descs([d])
+    assert cpu_lib.loka_fp8_linear_norm(arr, 1, None, 0, None) == _loka.LOKA_ERR_WORKSPACE
+    assert _loka.loka_fp8_linear_norm_workspace_size([_desc(mode=3)]) == 0
+
+
+def test_quantize_rejects_bad_arguments_on_host(cpu_lib):
+    f = cpu_lib.loka_quantize_fp8
+    assert f(1 << 20, 4, 48, 1, 1 << 20, 1 << 20, None, 0, None) == _loka.LOKA_ERR_INVALID_ARG   # cols % 32
+    assert f(1 << 20, 4, 64, 5, 1 << 20, 1 << 20, None, 0, None) == _loka.LOKA_ERR_INVALID_ARG   # mode
+    assert f(None, 4, 64, 1, 1 << 20, 1 << 20, None, 0, None) == _loka.LOKA_ERR_INVALID_ARG
+    assert f((1 << 20) + 2, 4, 64, 1, 1 << 20, 1 << 20, None, 0, None) == _loka.LOKA_ERR_INVALID_ARG
+    assert f(1 << 20, 4, 64, 0, 1 << 20, 1 << 20, None, 0, None) == _loka.LOKA_ERR_WORKSPACE
+    assert _loka.loka_quantize_fp8_workspace_size(4, 64, 0) > 0
+    assert _loka.loka_quantize_fp8_workspace_size(4, 64, 1) == 0
+
+
+def _c_table(rows):
+    out = []
+    for e in rows:
+        d = _loka.DispatchEntry()
+        d.p.M, d.p.N, d.p.K, d.p.norm, d.p.outlier_frac = e.M, e.N, e.K, e.norm, e.outlier_frac
+        d.variant, d.time_us, d.rel_err, d.mere = e.variant, e.time_us, e.rel_err, e.mere
+        out.append(d)
+    return out
+
+
+def _c_select(rows, M, N, K, norm, o, pol):
+    p = _loka.Problem()
+    p.M, p.N, p.K, p.norm, p.outlier_frac = M, N, K, norm, o
+    c = _loka.Policy()
+    c.max_rel_err, c.max_mere, c.min_speedup = pol.max_rel_err, pol.max_mere, pol.min_speedup
+    return _loka.loka_dispatch_select(_c_table(rows), p, c)
+
+
+def test_dispatch_select_agrees_with_oracle_on_random_tables(cpu_lib):
+    rng = np.random.default_rng(3)
+    Ms = [4096, 16384, 65536]
+    for trial in range(300):
+        rows = []
+        for m in Ms:
+            for o in (0.0, 0.01):
+                for v in range(4):
+                    if rng.random() < 0.85:
+                        rows.append(D.Entry(m, 256, 512, 1, o, v, float(rng.integers(1, 6)),
+                                            float(rng.choice([1e-3, 5e-3, 2e-2])), float(rng.choice([0.05, 0.1, 0.3]))))
+        pol = D.Policy(max_rel_err=float(rng.choice([1e-2, 1e-1])), max_mere=float(rng.choice([0.2, -1.0])),
+                       min_speedup=float(rng.choice([1.05, -1.0])))
+        M = int(rng.choice([3000, 8192, 30000, 65536, 100000]))
+        o = float(rng.choice([0.0, 0.004, 0.02]))
+        assert _c_select(rows, M, 256, 512, 1, o, pol) == D.select(rows, M, 256, 512, 1, o, pol)
+
+
+def test_dispatch_select_empty_table_is_bf16(cpu_lib):
+    p = _loka.Problem()
+    p.M, p.N, p.K, p.norm = 1024, 256, 512, 1
+    pol = _loka.Policy()
+    pol.max_rel_err, pol.max_mere, pol.min_speedup = 1e-2, 0.2, 1.05
+    assert _loka.loka_dispatch_select([], p, pol) == _loka.LOKA_BF16
