@@ -42,6 +42,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-compare", action="store_true")
+    ap.add_argument("--M", type=int, default=65536, help="rows of X (65536 is the headline workload)")
     return ap.parse_args()
 
 
@@ -115,9 +116,9 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------- workload
-def workload(rank: int):
+def workload(rank: int, M: int = 65536):
     import workloads as W
-    return W.rec_mlp(seed=rank)
+    return W.rec_mlp(seed=rank, M=M)
 
 
 def algorithmic_bytes_step(M, K, N):
@@ -209,7 +210,7 @@ def max_over_ranks(world, value: float, device=None) -> float:
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    inp = workload(0)
+    inp = workload(0, args.M)
     M, K, N = inp.M, inp.K, inp.N
     for _ in range(args.warmup):
         oracle_throughput(inp, 0.0, rows_per_call=512)
@@ -244,7 +245,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     _loka.load()
-    inp = workload(rank)
+    inp = workload(rank, args.M)
     M, K, N = inp.M, inp.K, inp.N
     flops = 2.0 * M * N * K
     x_bytes = 2 * M * K

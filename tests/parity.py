@@ -1,7 +1,9 @@
 """Acceptance rules shared by the GPU parity tests.
 
-bf16 outputs: per element |gpu - oracle| <= 2 bf16 ulps of max(|exact|, floor)
-and, after normalization, max |gpu - exact| <= 1e-2.  The floor (2^-6 for
+bf16 outputs: per element |gpu - exact| <= 2 bf16 ulps of max(|exact|, floor)
+and, after normalization, |gpu - exact| <= 1e-2 beyond the unavoidable bf16
+output rounding (half an ulp of the exact value): a LayerNorm row with one
+dominant element reaches |y| ~ sqrt(N), where one bf16 ulp alone exceeds 1e-2.  The floor (2^-6 for
 normalized outputs, 2^-6 times the row RMS for un-normalized ones) keeps the
 ulp criterion meaningful for outputs that cancel to nearly zero, where any
 fp32 accumulator carries an absolute, not a relative, error.
@@ -38,5 +40,6 @@ def check_bf16_output(gpu, y_exact, normalized: bool, what: str = ""):
         raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} elements beyond {ULPS} bf16 ulps; "
                              f"first {[(tuple(k), g[tuple(k)], y[tuple(k)]) for k in i]}")
     if normalized:
-        assert err.max() <= MAX_ABS_POST_NORM, f"{what}: max abs error {err.max()}"
+        excess = err - bf16_ulp(y) / 2
+        assert excess.max() <= MAX_ABS_POST_NORM, f"{what}: error beyond bf16 rounding {excess.max()}"
     return float(err.max()) if err.size else 0.0
