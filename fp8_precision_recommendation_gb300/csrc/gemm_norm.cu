@@ -9,19 +9,20 @@
 // section I (LRMs are wide ensembles of small GEMMs: several independent
 // layers share one launch here).
 //
-// Design (one CTA per SM, persistent, warp-specialized, 192 threads):
+// Design (one CTA per SM, persistent, warp-specialized, 320 threads):
 //   warp 0      TMA producer: A and B tiles of 128-byte K slices into a
 //               shared-memory ring, 128B-swizzled, one mbarrier per stage.
 //   warp 1      allocates tensor memory and issues tcgen05.mma (one thread);
 //               the fp32 accumulator of a 128 x N tile lives in TMEM, double
 //               buffered when 2N <= 512 columns so the epilogue of tile i
 //               overlaps the MMAs of tile i+1.
-//   warps 2..5  epilogue: thread t owns output row t of the tile (TMEM lane
-//               t); it reads its row with tcgen05.ld, applies the dequant
-//               scales and bias, computes the row statistics in fp32 (chunked
-//               Chan/Welford merge for LayerNorm, sum of squares for RMSNorm),
-//               normalizes, packs bf16 into a swizzled staging tile and one
-//               thread TMA-stores 128-byte-wide column slabs to HBM.
+//   warps 2..9  epilogue: two threads per output row (TMEM lane), each owning
+//               half of the row's 32-column chunks; they read the row with
+//               tcgen05.ld, apply the dequant scales and bias, compute the row
+//               statistics in fp32 (Chan/Welford merge of 32-column chunks for
+//               LayerNorm, sum of squares for RMSNorm), merge the two halves
+//               through shared memory, normalize, pack bf16 into a swizzled
+//               staging slab, and one thread TMA-stores each 64-column slab.
 // The output makes no extra HBM round trip: Y is written once.
 #include <cudaTypedefs.h>
 
@@ -39,8 +40,8 @@ constexpr int kSliceBytes = 128;         // bytes of K per stage per row
 constexpr uint32_t kABytes = kBM * kSliceBytes;
 constexpr uint32_t kStagingBytes = kBM * 128;   // one 128-byte-wide output slab
 constexpr int kTmemCols = 512;
-constexpr int kThreads = 192;
-constexpr int kEpiThreads = 128;
+constexpr int kThreads = 320;
+constexpr int kEpiThreads = 256;
 constexpr int kEpiBar = 1;               // named barrier id for the epilogue warps
 constexpr size_t kSmemBudget = 225 * 1024;
 
@@ -51,7 +52,8 @@ struct Cfg {
   static constexpr uint32_t B_BYTES = static_cast<uint32_t>(N) * kSliceBytes;
   static constexpr uint32_t STAGE = kABytes + B_BYTES;
   static constexpr int NBUF = (2 * N <= kTmemCols) ? 2 : 1;
-  static constexpr size_t FIXED = 1024 /*align*/ + 2 * kStagingBytes + 4 * N * sizeof(float) + 512 /*barriers*/;
+  static constexpr size_t FIXED = 1024 /*align*/ + 2 * kStagingBytes + 4 * N * sizeof(float) +
+                               2 * kBM * sizeof(float2) /*row statistics*/ + 512 /*barriers*/;
   static constexpr int STAGES_RAW = static_cast<int>((kSmemBudget - FIXED) / STAGE);
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   static_assert(STAGES >= 2, "not enough shared memory for two stages");
@@ -86,7 +88,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
   float* vec_b = vec_sw + N;
   float* vec_g = vec_b + N;
   float* vec_be = vec_g + N;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(vec_be + N);
+  float2* stat_part = reinterpret_cast<float2*>(vec_be + N);   // [2][128] partial row statistics
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stat_part + 2 * kBM);
   uint64_t* full = bars;
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
@@ -216,19 +219,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int ep = threadIdx.x - 64;         // 0..127
+    // Eight warps: two per TMEM lane quadrant.  Warp pair (q, q+4) shares
+    // rows 32q..32q+31; half h = 0/1 takes the interleaved 32-column chunks
+    // c = 2i + h, so each 64-column output slab is written by both halves.
+    const int et = threadIdx.x - 64;         // 0..255
+    const int half = et >> 7;                // column half
     const int quad = warp & 3;               // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;        // row of the tile owned by this thread
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+    constexpr int NCHUNK = N / 32;           // 32-column chunks, NCHUNK / 2 per half
     int cur_group = -1;
     int local = 0;
-    int slab = 0;
+    int step_count = 0;
     for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x, ++local) {
       const int g = group_of(p, tile);
       const GemmGroup& G = p.g[g];
       if (g != cur_group) {
         named_bar_sync(kEpiBar, kEpiThreads);
-        for (int n = ep; n < N; n += kEpiThreads) {
+        for (int n = et; n < N; n += kEpiThreads) {
           vec_sw[n] = G.sw == nullptr ? 1.0f : (G.sw_per_row ? G.sw[n] : G.sw[0]);
           vec_b[n] = G.bias == nullptr ? 0.0f : bf16_to_f(G.bias[n]);
           vec_g[n] = G.gamma == nullptr ? 1.0f : bf16_to_f(G.gamma[n]);
@@ -251,46 +259,66 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
       if (G.sx != nullptr) sxm = G.sx_per_row ? (m < G.M ? G.sx[m] : 0.0f) : G.sx[0];
       const uint32_t t_row = tmem_base + lane_addr + static_cast<uint32_t>(buf * N);
 
-      // pass 1: row statistics
+      // pass 1: statistics of this half's N/2 columns, 32-column chunks
+      // merged with Chan et al.'s pairwise update; then the two halves merge
       float mean = 0.0f, m2 = 0.0f;
       if (p.norm != kNormNone) {
-        for (int c0 = 0; c0 < N; c0 += 64) {
-          uint32_t r0[32], r1[32];
-          tmem_ld_32x32b_x32(t_row + c0, r0);
-          tmem_ld_32x32b_x32(t_row + c0 + 32, r1);
+#pragma unroll 1
+        for (int i = 0; i < NCHUNK / 2; ++i) {
+          const int c0 = (2 * i + half) * 32;
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_row + c0, r);
           tmem_ld_wait();
-          float v[64];
+          float v[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            v[j] = fmaf(__uint_as_float(r0[j]) * sxm, vec_sw[c0 + j], vec_b[c0 + j]);
-            v[32 + j] = fmaf(__uint_as_float(r1[j]) * sxm, vec_sw[c0 + 32 + j], vec_b[c0 + 32 + j]);
+          for (int j = 0; j < 32; j += 4) {
+            const float4 sw4 = *reinterpret_cast<const float4*>(vec_sw + c0 + j);
+            const float4 b4 = *reinterpret_cast<const float4*>(vec_b + c0 + j);
+            v[j + 0] = fmaf(__uint_as_float(r[j + 0]) * sxm, sw4.x, b4.x);
+            v[j + 1] = fmaf(__uint_as_float(r[j + 1]) * sxm, sw4.y, b4.y);
+            v[j + 2] = fmaf(__uint_as_float(r[j + 2]) * sxm, sw4.z, b4.z);
+            v[j + 3] = fmaf(__uint_as_float(r[j + 3]) * sxm, sw4.w, b4.w);
           }
           if (p.norm == kNormRms) {
             float s = 0.0f;
 #pragma unroll
-            for (int j = 0; j < 64; ++j) s = fmaf(v[j], v[j], s);
+            for (int j = 0; j < 32; ++j) s = fmaf(v[j], v[j], s);
             m2 += s;
           } else {
             float s = 0.0f;
 #pragma unroll
-            for (int j = 0; j < 64; ++j) s += v[j];
-            const float cm = s * (1.0f / 64.0f);
+            for (int j = 0; j < 32; ++j) s += v[j];
+            const float cm = s * (1.0f / 32.0f);
             float cq = 0.0f;
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
+            for (int j = 0; j < 32; ++j) {
               const float d = v[j] - cm;
               cq = fmaf(d, d, cq);
             }
-            if (c0 == 0) {
+            if (i == 0) {
               mean = cm;
               m2 = cq;
-            } else {   // Chan et al. merge of (c0, mean, m2) with (64, cm, cq)
-              const float nt = static_cast<float>(c0 + 64);
+            } else {   // merge (32 i, mean, m2) with (32, cm, cq)
+              const float na = static_cast<float>(32 * i);
+              const float nt = na + 32.0f;
               const float delta = cm - mean;
-              mean = fmaf(delta, 64.0f / nt, mean);
-              m2 += cq + delta * delta * (static_cast<float>(c0) * 64.0f / nt);
+              mean = fmaf(delta, 32.0f / nt, mean);
+              m2 += cq + delta * delta * (na * 32.0f / nt);
             }
           }
+        }
+        stat_part[half * kBM + row] = make_float2(mean, m2);
+        named_bar_sync(kEpiBar, kEpiThreads);
+        // both threads of the row evaluate the same expression in the same
+        // order, so they agree bit for bit
+        const float2 lo = stat_part[row];
+        const float2 hi = stat_part[kBM + row];
+        if (p.norm == kNormRms) {
+          m2 = lo.y + hi.y;
+        } else {   // two halves of N/2 elements each
+          const float delta = hi.x - lo.x;
+          m2 = (lo.y + hi.y) + delta * delta * (0.25f * static_cast<float>(N));
+          mean = 0.5f * (lo.x + hi.x);
         }
       }
       float rstd = 1.0f;
@@ -299,65 +327,87 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
         rstd = rsqrtf(m2 / static_cast<float>(N) + p.eps);
         mean = 0.0f;
       }
+      const float shift = p.norm == kNormNone ? 0.0f : mean;
+      const bool use_beta = p.norm == kNormLayer;
+      const bool normed = p.norm != kNormNone;
 
-      // pass 2: normalize, pack, stage, TMA-store 128-byte-wide slabs
-      for (int c0 = 0; c0 < N; c0 += OUT_COLS) {
-        uint32_t r0[32], r1[32];
-        tmem_ld_32x32b_x32(t_row + c0, r0);
-        if (OUT_COLS == 64) tmem_ld_32x32b_x32(t_row + c0 + 32, r1);
+      // pass 2: normalize, pack, stage and TMA-store.  Step i covers columns
+      // [64 i, 64 i + 64): this half writes chunk 2 i + half of it.
+#pragma unroll 1
+      for (int i = 0; i < NCHUNK / 2; ++i) {
+        const int c0 = (2 * i + half) * 32;
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_row + c0, r);
         tmem_ld_wait();
-        if (c0 + OUT_COLS >= N) {   // last read of this accumulator: hand it back to the MMA warp
+        if (i == NCHUNK / 2 - 1) {   // last read of this accumulator: hand it back to the MMA warp
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));
         }
-        const int sb = slab & 1;
-        if (slab >= 2) {
-          if (ep == 0) bulk_wait_read<1>();
-          named_bar_sync(kEpiBar, kEpiThreads);
-        }
-        uint8_t* srow = staging + sb * kStagingBytes + row * 128;
+        float y[32];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {   // eight 16-byte units of the 128-byte row slab
-          uint4 pk;
-          if (OUT == static_cast<int>(OutKind::kBf16)) {
-            uint32_t w[4];
+        for (int j = 0; j < 32; j += 4) {
+          const float4 sw4 = *reinterpret_cast<const float4*>(vec_sw + c0 + j);
+          const float4 b4 = *reinterpret_cast<const float4*>(vec_b + c0 + j);
+          const float4 g4 = *reinterpret_cast<const float4*>(vec_g + c0 + j);
+          const float4 be4 = *reinterpret_cast<const float4*>(vec_be + c0 + j);
+          const float swv[4] = {sw4.x, sw4.y, sw4.z, sw4.w};
+          const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
+          const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+          const float bev[4] = {be4.x, be4.y, be4.z, be4.w};
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              float y2[2];
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int j = u * 8 + h * 2 + e;
-                const int n = c0 + j;
-                const float v = fmaf(__uint_as_float(j < 32 ? r0[j] : r1[j & 31]) * sxm, vec_sw[n], vec_b[n]);
-                y2[e] = p.norm == kNormNone ? v : fmaf((v - mean) * rstd, vec_g[n], p.norm == kNormLayer ? vec_be[n] : 0.0f);
-              }
-              w[h] = pack_bf16x2(y2[0], y2[1]);
-            }
-            pk = make_uint4(w[0], w[1], w[2], w[3]);
-          } else {
-            float y4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int j = u * 4 + e;
-              const int n = c0 + j;
-              const float v = fmaf(__uint_as_float(j < 32 ? r0[j] : r1[j & 31]) * sxm, vec_sw[n], vec_b[n]);
-              y4[e] = p.norm == kNormNone ? v : fmaf((v - mean) * rstd, vec_g[n], p.norm == kNormLayer ? vec_be[n] : 0.0f);
-            }
-            pk = make_uint4(__float_as_uint(y4[0]), __float_as_uint(y4[1]), __float_as_uint(y4[2]), __float_as_uint(y4[3]));
+          for (int e = 0; e < 4; ++e) {
+            const float v = fmaf(__uint_as_float(r[j + e]) * sxm, swv[e], bv[e]);
+            y[j + e] = normed ? fmaf((v - shift) * rstd, gv[e], use_beta ? bev[e] : 0.0f) : v;
           }
-          *reinterpret_cast<uint4*>(srow + ((u ^ (row & 7)) << 4)) = pk;
+        }
+        // staging: bf16 -> one 64-column slab per step (double-buffered);
+        // fp32 -> two 32-column slabs per step (single buffer)
+        constexpr bool kBf16Out = OUT == static_cast<int>(OutKind::kBf16);
+        uint8_t* buf_base;
+        if (kBf16Out) {
+          buf_base = staging + (step_count & 1) * kStagingBytes;
+          if (step_count >= 2) {
+            if (et == 0) bulk_wait_read<1>();
+            named_bar_sync(kEpiBar, kEpiThreads);
+          }
+          uint8_t* srow = buf_base + row * 128;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {   // 4 units of 8 bf16; this half owns units 4h..4h+3
+            const uint4 pk = make_uint4(pack_bf16x2(y[8 * u + 0], y[8 * u + 1]), pack_bf16x2(y[8 * u + 2], y[8 * u + 3]),
+                                        pack_bf16x2(y[8 * u + 4], y[8 * u + 5]), pack_bf16x2(y[8 * u + 6], y[8 * u + 7]));
+            const int unit = half * 4 + u;
+            *reinterpret_cast<uint4*>(srow + ((unit ^ (row & 7)) << 4)) = pk;
+          }
+        } else {
+          buf_base = staging;
+          if (step_count >= 1) {
+            if (et == 0) bulk_wait_read<0>();
+            named_bar_sync(kEpiBar, kEpiThreads);
+          }
+          uint8_t* srow = buf_base + half * kStagingBytes + row * 128;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {   // 8 units of 4 floats: the whole 128-byte row of this half's slab
+            const uint4 pk = make_uint4(__float_as_uint(y[4 * u + 0]), __float_as_uint(y[4 * u + 1]),
+                                        __float_as_uint(y[4 * u + 2]), __float_as_uint(y[4 * u + 3]));
+            *reinterpret_cast<uint4*>(srow + ((u ^ (row & 7)) << 4)) = pk;
+          }
         }
         fence_proxy_async_smem();
         named_bar_sync(kEpiBar, kEpiThreads);
-        if (ep == 0) {
-          tma_store_2d(&G.tm_y, smem_u32(staging + sb * kStagingBytes), c0, m0);
+        if (et == 0) {
+          if (kBf16Out) {
+            tma_store_2d(&G.tm_y, smem_u32(buf_base), 64 * i, m0);
+          } else {
+            tma_store_2d(&G.tm_y, smem_u32(buf_base), 64 * i, m0);
+            tma_store_2d(&G.tm_y, smem_u32(buf_base + kStagingBytes), 64 * i + 32, m0);
+          }
           bulk_commit();
         }
-        ++slab;
+        ++step_count;
       }
     }
-    if (ep == 0) bulk_wait<0>();
+    if (et == 0) bulk_wait<0>();
   }
 
   tc_fence_before();
