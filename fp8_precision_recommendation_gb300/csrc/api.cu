@@ -171,6 +171,10 @@ loka_status validate(const loka_linear_desc* d, int n, bool probe) {
   if (!(a.N == 64 || a.N == 128 || a.N == 192 || a.N == 256 || a.N == 512))
     return fail(LOKA_ERR_UNSUPPORTED, "N = %lld: supported N are 64, 128, 192, 256, 512", static_cast<long long>(a.N));
   if (a.mode == kScaleMx32) return fail(LOKA_ERR_UNSUPPORTED, "MX 1x32 GEMM is not available in this build");
+  if (!gemm_supported(static_cast<int>(a.N), static_cast<int>(a.K), a.mode == kBf16 ? OperandKind::kBf16 : OperandKind::kE4M3) ||
+      (probe && !gemm_supported(static_cast<int>(a.N), static_cast<int>(a.K), OperandKind::kBf16)))
+    return fail(LOKA_ERR_UNSUPPORTED, "no shared-memory plan for N = %lld, K = %lld", static_cast<long long>(a.N),
+                static_cast<long long>(a.K));
   if (a.mode == kBf16 && (a.x_is_fp8 || a.w_is_fp8))
     return fail(LOKA_ERR_INVALID_ARG, "LOKA_BF16 takes bf16 operands (x_is_fp8 = w_is_fp8 = 0)");
   if (probe && (a.x_is_fp8 || a.w_is_fp8))
@@ -207,6 +211,7 @@ loka_status build_gemm(const loka_linear_desc* d, int n, const std::vector<Opera
     G.gamma = static_cast<const uint16_t*>(g.gamma);
     G.beta = static_cast<const uint16_t*>(g.beta);
     void* y = y_override ? y_override[i] : g.y;
+    G.y = y;
     if (g.M == 0) continue;
     loka_status s;
     if (bf16_operands) {

@@ -10,19 +10,26 @@
 // layers share one launch here).
 //
 // Design (one CTA per SM, persistent, warp-specialized, 320 threads):
-//   warp 0      TMA producer: A and B tiles of 128-byte K slices into a
-//               shared-memory ring, 128B-swizzled, one mbarrier per stage.
+//   warp 0      TMA producer: 128-byte K slices of A (and of B when W does
+//               not stay resident) into a shared-memory ring, 128B-swizzled,
+//               one mbarrier per stage.  When N x K of the weights fits in
+//               128 KB, W is loaded once per CTA (per group) and stays in
+//               shared memory, so each tile streams only its activations.
 //   warp 1      allocates tensor memory and issues tcgen05.mma (one thread);
 //               the fp32 accumulator of a 128 x N tile lives in TMEM, double
 //               buffered when 2N <= 512 columns so the epilogue of tile i
 //               overlaps the MMAs of tile i+1.
-//   warps 2..9  epilogue: two threads per output row (TMEM lane), each owning
-//               half of the row's 32-column chunks; they read the row with
-//               tcgen05.ld, apply the dequant scales and bias, compute the row
-//               statistics in fp32 (Chan/Welford merge of 32-column chunks for
-//               LayerNorm, sum of squares for RMSNorm), merge the two halves
-//               through shared memory, normalize, pack bf16 into a swizzled
-//               staging slab, and one thread TMA-stores each 64-column slab.
+//   warps 2..9  epilogue: two warps per TMEM lane quadrant, each taking
+//               every other 32-column chunk; tcgen05.ld.16x256b gives every
+//               thread 4 rows x 8 columns of a chunk, so a per-column value
+//               (scale, bias, gamma, beta) read from shared memory serves 4
+//               rows, and the math runs on packed fp32 pairs (fma/mul/add
+//               .f32x2); TMEM reads are pipelined one chunk ahead.
+//               Row statistics are fp32 Chan/Welford merges (LayerNorm) or sums
+//               of squares (RMSNorm) across chunks, lanes (shuffles) and the
+//               two parts (shared memory); the normalized bf16 row is
+//               packed into swizzled staging slabs and one thread TMA-stores
+//               each 64-column slab.
 // The output makes no extra HBM round trip: Y is written once.
 #include <cudaTypedefs.h>
 
@@ -43,22 +50,35 @@ constexpr int kTmemCols = 512;
 constexpr int kThreads = 320;
 constexpr int kEpiThreads = 256;
 constexpr int kEpiBar = 1;               // named barrier id for the epilogue warps
-constexpr size_t kSmemBudget = 225 * 1024;
+constexpr int kMaxStages = 8;
+constexpr size_t kSmemLimit = 227 * 1024;
+constexpr size_t kResidentWLimit = 128 * 1024;
 
-template <int N>
-struct Cfg {
-  static constexpr int N_MMA = N > 256 ? 256 : N;
-  static constexpr int N_SPLIT = N / N_MMA;
-  static constexpr uint32_t B_BYTES = static_cast<uint32_t>(N) * kSliceBytes;
-  static constexpr uint32_t STAGE = kABytes + B_BYTES;
-  static constexpr int NBUF = (2 * N <= kTmemCols) ? 2 : 1;
-  static constexpr size_t FIXED = 1024 /*align*/ + 2 * kStagingBytes + 4 * N * sizeof(float) +
-                               2 * kBM * sizeof(float2) /*row statistics*/ + 512 /*barriers*/;
-  static constexpr int STAGES_RAW = static_cast<int>((kSmemBudget - FIXED) / STAGE);
-  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
-  static_assert(STAGES >= 2, "not enough shared memory for two stages");
-  static constexpr size_t SMEM = FIXED + static_cast<size_t>(STAGES) * STAGE;
+// Shared-memory carve-up (all offsets from a 1024-byte-aligned base):
+//   ring     stages x (A slice [| B slice])
+//   w        resident W: K/KE slices of N rows x 128 bytes (when resident)
+//   staging  2 x 16 KB output slabs
+//   vectors  4 x N fp32 (weight scale, bias, gamma, beta)
+//   stats    4 x 128 float2 partial row statistics
+//   barriers
+struct Layout {
+  uint32_t stage_bytes, ring, w, staging, vec, stats, bars, total;
 };
+
+__host__ __device__ inline Layout make_layout(int N, int K, int elem_bytes, bool resident, int stages) {
+  Layout L;
+  const uint32_t b_slice = static_cast<uint32_t>(N) * kSliceBytes;
+  L.stage_bytes = kABytes + (resident ? 0u : b_slice);
+  L.ring = 0;
+  L.w = L.ring + static_cast<uint32_t>(stages) * L.stage_bytes;
+  const uint32_t w_bytes = resident ? static_cast<uint32_t>(N) * static_cast<uint32_t>(K) * elem_bytes : 0u;
+  L.staging = L.w + w_bytes;
+  L.vec = L.staging + 2 * kStagingBytes;
+  L.stats = L.vec + 4u * N * sizeof(float);
+  L.bars = L.stats + 4u * kBM * sizeof(float2);
+  L.total = L.bars + 256;
+  return L;
+}
 
 __device__ __forceinline__ int group_of(const GemmParams& p, int tile) {
   int g = 0;
@@ -68,41 +88,56 @@ __device__ __forceinline__ int group_of(const GemmParams& p, int tile) {
 
 __device__ __forceinline__ float bf16_to_f(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
 
-template <int N, int OP, int OUT>
-__global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_constant__ GemmParams p) {
-  using C = Cfg<N>;
-  constexpr int STAGES = C::STAGES;
-  constexpr int NBUF = C::NBUF;
-  // K elements per 128-byte slice and per MMA instruction (32 bytes each)
-  constexpr int KE = OP == static_cast<int>(OperandKind::kBf16) ? 64 : 128;
-  constexpr uint32_t IDESC = OP == static_cast<int>(OperandKind::kBf16)
-                                 ? idesc_dense(1, 1, kBM, C::N_MMA)    // bf16 x bf16 -> f32
-                                 : idesc_dense(0, 0, kBM, C::N_MMA);   // e4m3 x e4m3 -> f32
-  constexpr int OUT_COLS = OUT == static_cast<int>(OutKind::kBf16) ? 64 : 32;   // columns per 128-byte slab
+__device__ __forceinline__ float2 dup2(float a) { return make_float2(a, a); }
 
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* ring = smem;                                         // STAGES x (A | B)
-  uint8_t* staging = ring + static_cast<size_t>(STAGES) * C::STAGE;   // 2 x 16 KB
-  float* vec_sw = reinterpret_cast<float*>(staging + 2 * kStagingBytes);
+template <int N, int OP, int OUT, bool RESIDENT>
+__global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_constant__ GemmParams p) {
+  constexpr int NBUF = (2 * N <= kTmemCols) ? 2 : 1;
+  constexpr int N_MMA = N > 256 ? 256 : N;
+  constexpr int N_SPLIT = N / N_MMA;
+  constexpr bool kBf16Op = OP == static_cast<int>(OperandKind::kBf16);
+  constexpr int EB = kBf16Op ? 2 : 1;               // operand element bytes
+  constexpr int KE = kSliceBytes / EB;              // K elements per 128-byte slice
+  constexpr uint32_t IDESC = kBf16Op ? idesc_dense(1, 1, kBM, N_MMA)    // bf16 x bf16 -> f32
+                                     : idesc_dense(0, 0, kBM, N_MMA);   // e4m3 x e4m3 -> f32
+  constexpr uint32_t B_SLICE = static_cast<uint32_t>(N) * kSliceBytes;
+
+  const int stages = p.stages;
+  const int num_kb = p.K / KE;
+  const Layout L = make_layout(N, p.K, EB, RESIDENT, stages);
+
+  // Pointers are derived from the __shared__ array by plain offsets, so the
+  // compiler keeps them in the shared address space (LDS/STS, not generic
+  // loads).  The 128B-swizzled TMA/UMMA tiles need the 1024-byte alignment.
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(p.status, kErrMisaligned);
+    return;
+  }
+  uint8_t* ring = smem + L.ring;
+  uint8_t* wres = smem + L.w;
+  uint8_t* staging = smem + L.staging;
+  float* vec_sw = reinterpret_cast<float*>(smem + L.vec);
   float* vec_b = vec_sw + N;
   float* vec_g = vec_b + N;
   float* vec_be = vec_g + N;
-  float2* stat_part = reinterpret_cast<float2*>(vec_be + N);   // [2][128] partial row statistics
-  uint64_t* bars = reinterpret_cast<uint64_t*>(stat_part + 2 * kBM);
+  float2* stat_part = reinterpret_cast<float2*>(smem + L.stats);   // [4][128] partial row statistics
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* full = bars;
-  uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;
-  uint64_t* tempty = tfull + NBUF;
-  uint64_t* mma_done = tempty + NBUF;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* tfull = empty + kMaxStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* mma_done = tempty + 2;
+  uint64_t* w_full = mma_done + 1;
+  uint64_t* w_free = w_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(w_free + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < stages; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
     }
@@ -111,6 +146,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
       mbar_init(smem_u32(&tempty[b]), kEpiThreads / 32);
     }
     mbar_init(smem_u32(mma_done), 1);
+    mbar_init(smem_u32(w_full), 1);
+    mbar_init(smem_u32(w_free), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -131,7 +168,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const Watchdog wd{abort_flag, p.status, p.wait_limit_ns};
-  const int num_kb = p.K / KE;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -139,26 +175,45 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, last_parity = 0;
+      int cur_group = -1, w_loads = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
         const int g = group_of(p, tile);
         const int m0 = (tile - p.g[g].tile_begin) * kBM;
+        if (RESIDENT && g != cur_group) {
+          // reload the resident weights once the MMAs of the previous group are done with them
+          if (w_loads > 0 && !wait_parity(wd, smem_u32(w_free), (w_loads - 1) & 1, kErrProducerWait)) {
+            ok = false;
+            break;
+          }
+          const uint32_t wb = smem_u32(w_full);
+          mbar_arrive_expect_tx(wb, static_cast<uint32_t>(num_kb) * B_SLICE);
+          for (int kb = 0; kb < num_kb; ++kb) {
+#pragma unroll
+            for (int s = 0; s < N_SPLIT; ++s)
+              tma_load_2d(smem_u32(wres + kb * B_SLICE + s * N_MMA * kSliceBytes), &p.g[g].tm_b, wb, kb * KE, s * N_MMA);
+          }
+          ++w_loads;
+          cur_group = g;
+        }
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!wait_parity(wd, smem_u32(&empty[stage]), phase ^ 1u, kErrProducerWait)) {
             ok = false;
             break;
           }
-          uint8_t* a_dst = ring + static_cast<size_t>(stage) * C::STAGE;
-          uint8_t* b_dst = a_dst + kABytes;
+          uint8_t* a_dst = ring + static_cast<size_t>(stage) * L.stage_bytes;
           const uint32_t fb = smem_u32(&full[stage]);
-          mbar_arrive_expect_tx(fb, C::STAGE);
+          mbar_arrive_expect_tx(fb, L.stage_bytes);
           tma_load_2d(smem_u32(a_dst), &p.g[g].tm_a, fb, kb * KE, m0);
+          if (!RESIDENT) {
+            uint8_t* b_dst = a_dst + kABytes;
 #pragma unroll
-          for (int s = 0; s < C::N_SPLIT; ++s)
-            tma_load_2d(smem_u32(b_dst + s * C::N_MMA * kSliceBytes), &p.g[g].tm_b, fb, kb * KE, s * C::N_MMA);
+            for (int s = 0; s < N_SPLIT; ++s)
+              tma_load_2d(smem_u32(b_dst + s * N_MMA * kSliceBytes), &p.g[g].tm_b, fb, kb * KE, s * N_MMA);
+          }
           issued |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) {
+          if (++stage == stages) {
             stage = 0;
             phase ^= 1u;
           }
@@ -166,8 +221,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
       }
       if (!ok) {
         // let the copies already in flight land before the CTA exits
-        for (int s = 0; s < STAGES; ++s)
+        for (int s = 0; s < stages; ++s)
           if (issued & (1u << s)) wait_parity_drain(wd, smem_u32(&full[s]), (last_parity >> s) & 1u);
+        if (RESIDENT && w_loads > 0) wait_parity_drain(wd, smem_u32(w_full), (w_loads - 1) & 1);
       }
     }
   } else if (warp == 1) {
@@ -176,8 +232,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
+      int cur_group = -1, w_uses = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x, ++local) {
+        if (RESIDENT) {
+          const int g = group_of(p, tile);
+          if (g != cur_group) {
+            if (w_uses > 0) mma_commit(smem_u32(w_free));   // previous weights free once these MMAs finish
+            if (!wait_parity(wd, smem_u32(w_full), w_uses & 1, kErrMmaWait)) break;
+            ++w_uses;
+            cur_group = g;
+          }
+        }
         const int buf = NBUF == 2 ? (local & 1) : 0;
         const uint32_t use = NBUF == 2 ? (local >> 1) : local;
         if (!wait_parity(wd, smem_u32(&tempty[buf]), (use & 1u) ^ 1u, kErrMmaWait)) break;
@@ -189,23 +255,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(ring + static_cast<size_t>(stage) * C::STAGE);
-          const uint32_t b_addr = a_addr + kABytes;
+          const uint32_t a_addr = smem_u32(ring + static_cast<size_t>(stage) * L.stage_bytes);
+          const uint32_t b_addr = RESIDENT ? smem_u32(wres + kb * B_SLICE) : a_addr + kABytes;
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint64_t adesc = sdesc_k128_sw128(a_addr + k * 32);
 #pragma unroll
-            for (int s = 0; s < C::N_SPLIT; ++s) {
-              const uint64_t bdesc = sdesc_k128_sw128(b_addr + s * C::N_MMA * kSliceBytes + k * 32);
+            for (int s = 0; s < N_SPLIT; ++s) {
+              const uint64_t bdesc = sdesc_k128_sw128(b_addr + s * N_MMA * kSliceBytes + k * 32);
               const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
-              if (OP == static_cast<int>(OperandKind::kBf16))
-                mma_f16(d_tmem + s * C::N_MMA, adesc, bdesc, IDESC, acc);
+              if (kBf16Op)
+                mma_f16(d_tmem + s * N_MMA, adesc, bdesc, IDESC, acc);
               else
-                mma_f8f6f4(d_tmem + s * C::N_MMA, adesc, bdesc, IDESC, acc);
+                mma_f8f6f4(d_tmem + s * N_MMA, adesc, bdesc, IDESC, acc);
             }
           }
           mma_commit(smem_u32(&empty[stage]));   // frees the slot once these MMAs finish
-          if (++stage == STAGES) {
+          if (++stage == stages) {
             stage = 0;
             phase ^= 1u;
           }
@@ -219,31 +285,107 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // Eight warps: two per TMEM lane quadrant.  Warp pair (q, q+4) shares
-    // rows 32q..32q+31; half h = 0/1 takes the interleaved 32-column chunks
-    // c = 2i + h, so each 64-column output slab is written by both halves.
+    // Eight warps, two per TMEM lane quadrant: warp (quad q, part w) covers
+    // rows 32q..32q+31 and the 32-column chunks c = w + 2s.  The 16x256b
+    // load shape gives thread t rows t/4 + {0, 8, 16, 24} and column pairs
+    // 8i + 2(t%4) of each chunk.  Chunk reads are pipelined one ahead.
     const int et = threadIdx.x - 64;         // 0..255
-    const int half = et >> 7;                // column half
     const int quad = warp & 3;               // TMEM lane quadrant this warp may access
-    const int row = quad * 32 + lane;        // row of the tile owned by this thread
+    constexpr int NPART = kEpiThreads / 128; // warps per lane quadrant
+    const int part = (warp - 2) >> 2;        // which half of the chunks
+    const int g4 = lane >> 2;                // row within each 8-row group
+    const int cp = lane & 3;                 // column pair within each 8-column group
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
-    constexpr int NCHUNK = N / 32;           // 32-column chunks, NCHUNK / 2 per half
+    constexpr int NCHUNK = N / 32;
+    static_assert(NCHUNK % NPART == 0, "chunks split evenly between the parts");
+    constexpr int CH = NCHUNK / NPART;       // chunks per warp
+    constexpr bool kBf16Out = OUT == static_cast<int>(OutKind::kBf16);
+    const int norm = p.norm;
+    const float eps = p.eps;
+    int rowk[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) rowk[k] = quad * 32 + g4 + 8 * k;
+
+    // activation scales of a tile's four rows of this thread (per-tensor
+    // weight scales fold in); loaded one tile ahead to hide the latency
+    auto row_scales = [&](int tile, float (&out)[4]) {
+      const int g = group_of(p, tile);
+      const GemmGroup& G = p.g[g];
+      const int m0 = (tile - G.tile_begin) * kBM;
+      const float swc = (G.sw != nullptr && !G.sw_per_row) ? G.sw[0] : 1.0f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int64_t m = static_cast<int64_t>(m0) + rowk[k];
+        float sx = 1.0f;
+        if (G.sx != nullptr) sx = G.sx_per_row ? (m < G.M ? G.sx[m] : 0.0f) : G.sx[0];
+        out[k] = sx * swc;
+      }
+    };
+    auto vec2 = [&](const float* vec, int c0, int i) {
+      return *reinterpret_cast<const float2*>(vec + c0 + 8 * i + 2 * cp);
+    };
+    auto acc2 = [&](const uint32_t (&ra)[16], const uint32_t (&rb)[16], int k, int i) {
+      const uint32_t* r = k < 2 ? ra : rb;
+      const int o = 4 * i + 2 * (k & 1);
+      return make_float2(__uint_as_float(r[o]), __uint_as_float(r[o + 1]));
+    };
+    // Runs fn(ra, rb, c) over this warp's chunks, the TMEM read of chunk
+    // s + 1 in flight while chunk s is processed.
+    auto for_chunks = [&](uint32_t t_base, auto&& fn) {
+      uint32_t ra[2][16], rb[2][16];
+      tmem_ld_16x256b_x4(t_base + part * 32, ra[0]);
+      tmem_ld_16x256b_x4(t_base + (16u << 16) + part * 32, rb[0]);
+      tmem_ld_wait();
+      reg_fence(ra[0]);
+      reg_fence(rb[0]);
+#pragma unroll
+      for (int s = 0; s < CH; ++s) {
+        const int c = part + NPART * s;
+        if (s + 1 < CH) {
+          tmem_ld_16x256b_x4(t_base + (c + NPART) * 32, ra[(s + 1) & 1]);
+          tmem_ld_16x256b_x4(t_base + (16u << 16) + (c + NPART) * 32, rb[(s + 1) & 1]);
+        }
+        fn(ra[s & 1], rb[s & 1], c);
+        if (s + 1 < CH) {
+          tmem_ld_wait();
+          reg_fence(ra[(s + 1) & 1]);
+          reg_fence(rb[(s + 1) & 1]);
+        }
+      }
+    };
+
     int cur_group = -1;
     int local = 0;
-    int step_count = 0;
+    float sx_next[4] = {1.f, 1.f, 1.f, 1.f};
+    if (static_cast<int>(blockIdx.x) < p.total_tiles) row_scales(blockIdx.x, sx_next);
     for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x, ++local) {
       const int g = group_of(p, tile);
       const GemmGroup& G = p.g[g];
       if (g != cur_group) {
         named_bar_sync(kEpiBar, kEpiThreads);
+        const bool normed = norm != kNormNone;
         for (int n = et; n < N; n += kEpiThreads) {
-          vec_sw[n] = G.sw == nullptr ? 1.0f : (G.sw_per_row ? G.sw[n] : G.sw[0]);
+          vec_sw[n] = (G.sw != nullptr && G.sw_per_row) ? G.sw[n] : 1.0f;
           vec_b[n] = G.bias == nullptr ? 0.0f : bf16_to_f(G.bias[n]);
-          vec_g[n] = G.gamma == nullptr ? 1.0f : bf16_to_f(G.gamma[n]);
-          vec_be[n] = G.beta == nullptr ? 0.0f : bf16_to_f(G.beta[n]);
+          vec_g[n] = (G.gamma == nullptr || !normed) ? 1.0f : bf16_to_f(G.gamma[n]);
+          vec_be[n] = (G.beta == nullptr || norm != kNormLayer) ? 0.0f : bf16_to_f(G.beta[n]);
         }
         named_bar_sync(kEpiBar, kEpiThreads);
         cur_group = g;
+      }
+      float sxr[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) sxr[k] = sx_next[k];
+      const int m0 = (tile - G.tile_begin) * kBM;
+      // output row addresses and validity, once per tile
+      const int64_t Mg = G.M;
+      uint8_t* rowp[4];
+      uint32_t ok[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int64_t m = static_cast<int64_t>(m0) + rowk[k];
+        ok[k] = m < Mg ? 1u : 0u;
+        rowp[k] = static_cast<uint8_t*>(G.y) + (m * N + 2 * cp) * (kBf16Out ? 2 : 4);
       }
       const int buf = NBUF == 2 ? (local & 1) : 0;
       const uint32_t use = NBUF == 2 ? (local >> 1) : local;
@@ -253,161 +395,135 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
       named_bar_sync(kEpiBar, kEpiThreads);
       if (*abort_flag) break;
       tc_fence_after();
-      const int m0 = (tile - G.tile_begin) * kBM;
-      const int64_t m = static_cast<int64_t>(m0) + row;
-      float sxm = 1.0f;
-      if (G.sx != nullptr) sxm = G.sx_per_row ? (m < G.M ? G.sx[m] : 0.0f) : G.sx[0];
-      const uint32_t t_row = tmem_base + lane_addr + static_cast<uint32_t>(buf * N);
+      if (tile + static_cast<int>(gridDim.x) < p.total_tiles) row_scales(tile + gridDim.x, sx_next);
+      const uint32_t t_base = tmem_base + lane_addr + static_cast<uint32_t>(buf * N);
 
-      // pass 1: statistics of this half's N/2 columns, 32-column chunks
-      // merged with Chan et al.'s pairwise update; then the two halves merge
-      float mean = 0.0f, m2 = 0.0f;
-      if (p.norm != kNormNone) {
-#pragma unroll 1
-        for (int i = 0; i < NCHUNK / 2; ++i) {
-          const int c0 = (2 * i + half) * 32;
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(t_row + c0, r);
-          tmem_ld_wait();
-          float v[32];
+      // pass 1: row statistics of v = acc * sx * sw + b
+      float mean[4] = {0.f, 0.f, 0.f, 0.f}, m2[4] = {0.f, 0.f, 0.f, 0.f};
+      if (norm == kNormLayer) {
+        // shifted sums: with K the mean of the row's first 8-value piece,
+        // s1 += v - K and s2 += (v - K)^2; no division, little cancellation
+        float shift[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+        for_chunks(t_base, [&](const uint32_t (&ra)[16], const uint32_t (&rb)[16], int c) {
+          const int c0 = c * 32;
+          float2 sw[4], b[4];
 #pragma unroll
-          for (int j = 0; j < 32; j += 4) {
-            const float4 sw4 = *reinterpret_cast<const float4*>(vec_sw + c0 + j);
-            const float4 b4 = *reinterpret_cast<const float4*>(vec_b + c0 + j);
-            v[j + 0] = fmaf(__uint_as_float(r[j + 0]) * sxm, sw4.x, b4.x);
-            v[j + 1] = fmaf(__uint_as_float(r[j + 1]) * sxm, sw4.y, b4.y);
-            v[j + 2] = fmaf(__uint_as_float(r[j + 2]) * sxm, sw4.z, b4.z);
-            v[j + 3] = fmaf(__uint_as_float(r[j + 3]) * sxm, sw4.w, b4.w);
+          for (int i = 0; i < 4; ++i) {
+            sw[i] = vec2(vec_sw, c0, i);
+            b[i] = vec2(vec_b, c0, i);
           }
-          if (p.norm == kNormRms) {
-            float s = 0.0f;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) s = fmaf(v[j], v[j], s);
-            m2 += s;
-          } else {
-            float s = 0.0f;
+          for (int k = 0; k < 4; ++k) {
+            float2 v[4];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) s += v[j];
-            const float cm = s * (1.0f / 32.0f);
-            float cq = 0.0f;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float d = v[j] - cm;
-              cq = fmaf(d, d, cq);
+            for (int i = 0; i < 4; ++i) v[i] = __ffma2_rn(__fmul2_rn(acc2(ra, rb, k, i), dup2(sxr[k])), sw[i], b[i]);
+            if (c == part) {
+              const float2 t = __fadd2_rn(__fadd2_rn(v[0], v[1]), __fadd2_rn(v[2], v[3]));
+              shift[k] = (t.x + t.y) * 0.125f;
             }
-            if (i == 0) {
-              mean = cm;
-              m2 = cq;
-            } else {   // merge (32 i, mean, m2) with (32, cm, cq)
-              const float na = static_cast<float>(32 * i);
-              const float nt = na + 32.0f;
-              const float delta = cm - mean;
-              mean = fmaf(delta, 32.0f / nt, mean);
-              m2 += cq + delta * delta * (na * 32.0f / nt);
+            const float2 nk = dup2(-shift[k]);
+            float2 a1 = make_float2(0.f, 0.f), a2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 d = __fadd2_rn(v[i], nk);
+              a1 = __fadd2_rn(a1, d);
+              a2 = __ffma2_rn(d, d, a2);
             }
+            s1[k] += a1.x + a1.y;
+            m2[k] += a2.x + a2.y;
+          }
+        });
+        constexpr float kInvMe = 1.0f / (8.0f * CH);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float d = s1[k] * kInvMe;
+          mean[k] = shift[k] + d;
+          m2[k] = fmaxf(m2[k] - s1[k] * d, 0.0f);
+        }
+      } else if (norm == kNormRms) {
+        for_chunks(t_base, [&](const uint32_t (&ra)[16], const uint32_t (&rb)[16], int c) {
+          const int c0 = c * 32;
+          float2 sw[4], b[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            sw[i] = vec2(vec_sw, c0, i);
+            b[i] = vec2(vec_b, c0, i);
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            float2 q = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 v = __ffma2_rn(__fmul2_rn(acc2(ra, rb, k, i), dup2(sxr[k])), sw[i], b[i]);
+              q = __ffma2_rn(v, v, q);
+            }
+            m2[k] += q.x + q.y;
+          }
+        });
+      }
+
+      float rstd[4] = {1.f, 1.f, 1.f, 1.f};
+      if (norm != kNormNone) {
+        // merge the 4 lanes of a row group (equal counts) with an ordered
+        // expression so all four end bit-identical
+#pragma unroll
+        for (int lvl = 0; lvl < 2; ++lvl) {
+          const int off = 1 << lvl;
+          const float half_n = 4.0f * CH * static_cast<float>(off);   // n_a n_b / (n_a + n_b)
+          const bool lo_side = (lane & off) == 0;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float om = __shfl_xor_sync(0xffffffffu, mean[k], off);
+            const float oq = __shfl_xor_sync(0xffffffffu, m2[k], off);
+            const float lm = lo_side ? mean[k] : om, hm = lo_side ? om : mean[k];
+            const float lq = lo_side ? m2[k] : oq, hq = lo_side ? oq : m2[k];
+            const float delta = hm - lm;
+            m2[k] = norm == kNormRms ? lq + hq : (lq + hq) + delta * delta * half_n;
+            mean[k] = norm == kNormRms ? 0.0f : 0.5f * (lm + hm);
           }
         }
-        stat_part[half * kBM + row] = make_float2(mean, m2);
+        if (cp == 0) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) stat_part[part * kBM + rowk[k]] = make_float2(mean[k], m2[k]);
+        }
         named_bar_sync(kEpiBar, kEpiThreads);
-        // both threads of the row evaluate the same expression in the same
-        // order, so they agree bit for bit
-        const float2 lo = stat_part[row];
-        const float2 hi = stat_part[kBM + row];
-        if (p.norm == kNormRms) {
-          m2 = lo.y + hi.y;
-        } else {   // two halves of N/2 elements each
+        // the two parts hold N/2 elements each
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 lo = stat_part[rowk[k]];
+          const float2 hi = stat_part[kBM + rowk[k]];
           const float delta = hi.x - lo.x;
-          m2 = (lo.y + hi.y) + delta * delta * (0.25f * static_cast<float>(N));
-          mean = 0.5f * (lo.x + hi.x);
+          const float q = norm == kNormRms ? lo.y + hi.y : (lo.y + hi.y) + delta * delta * (0.25f * N);
+          mean[k] = norm == kNormRms ? 0.0f : 0.5f * (lo.x + hi.x);
+          rstd[k] = rsqrtf(q * (1.0f / N) + eps);
         }
       }
-      float rstd = 1.0f;
-      if (p.norm == kNormLayer) rstd = rsqrtf(m2 / static_cast<float>(N) + p.eps);
-      if (p.norm == kNormRms) {
-        rstd = rsqrtf(m2 / static_cast<float>(N) + p.eps);
-        mean = 0.0f;
-      }
-      const float shift = p.norm == kNormNone ? 0.0f : mean;
-      const bool use_beta = p.norm == kNormLayer;
-      const bool normed = p.norm != kNormNone;
 
-      // pass 2: normalize, pack, stage and TMA-store.  Step i covers columns
-      // [64 i, 64 i + 64): this half writes chunk 2 i + half of it.
-#pragma unroll 1
-      for (int i = 0; i < NCHUNK / 2; ++i) {
-        const int c0 = (2 * i + half) * 32;
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(t_row + c0, r);
-        tmem_ld_wait();
-        if (i == NCHUNK / 2 - 1) {   // last read of this accumulator: hand it back to the MMA warp
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));
-        }
-        float y[32];
+      // pass 2: y = ((v - mean) * rstd) * gamma + beta, stored straight from
+      // registers (column pairs; the rows of a ragged last tile are masked)
+      for_chunks(t_base, [&](const uint32_t (&ra)[16], const uint32_t (&rb)[16], int c) {
+        const int c0 = c * 32;
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          const float4 sw4 = *reinterpret_cast<const float4*>(vec_sw + c0 + j);
-          const float4 b4 = *reinterpret_cast<const float4*>(vec_b + c0 + j);
-          const float4 g4 = *reinterpret_cast<const float4*>(vec_g + c0 + j);
-          const float4 be4 = *reinterpret_cast<const float4*>(vec_be + c0 + j);
-          const float swv[4] = {sw4.x, sw4.y, sw4.z, sw4.w};
-          const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
-          const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
-          const float bev[4] = {be4.x, be4.y, be4.z, be4.w};
+        for (int i = 0; i < 4; ++i) {
+          const float2 sw = vec2(vec_sw, c0, i), b = vec2(vec_b, c0, i);
+          const float2 gm = vec2(vec_g, c0, i), be = vec2(vec_be, c0, i);
+          const int col = c0 + 8 * i;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float v = fmaf(__uint_as_float(r[j + e]) * sxm, swv[e], bv[e]);
-            y[j + e] = normed ? fmaf((v - shift) * rstd, gv[e], use_beta ? bev[e] : 0.0f) : v;
+          for (int k = 0; k < 4; ++k) {
+            const float2 v = __ffma2_rn(__fmul2_rn(acc2(ra, rb, k, i), dup2(sxr[k])), sw, b);
+            const float2 y = __ffma2_rn(__fmul2_rn(__fadd2_rn(v, dup2(-mean[k])), dup2(rstd[k])), gm, be);
+            if (kBf16Out)
+              st_global_pred_b32(rowp[k] + col * 2, pack_bf16x2(y.x, y.y), ok[k]);
+            else
+              st_global_pred_v2f32(rowp[k] + col * 4, y, ok[k]);
           }
         }
-        // staging: bf16 -> one 64-column slab per step (double-buffered);
-        // fp32 -> two 32-column slabs per step (single buffer)
-        constexpr bool kBf16Out = OUT == static_cast<int>(OutKind::kBf16);
-        uint8_t* buf_base;
-        if (kBf16Out) {
-          buf_base = staging + (step_count & 1) * kStagingBytes;
-          if (step_count >= 2) {
-            if (et == 0) bulk_wait_read<1>();
-            named_bar_sync(kEpiBar, kEpiThreads);
-          }
-          uint8_t* srow = buf_base + row * 128;
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {   // 4 units of 8 bf16; this half owns units 4h..4h+3
-            const uint4 pk = make_uint4(pack_bf16x2(y[8 * u + 0], y[8 * u + 1]), pack_bf16x2(y[8 * u + 2], y[8 * u + 3]),
-                                        pack_bf16x2(y[8 * u + 4], y[8 * u + 5]), pack_bf16x2(y[8 * u + 6], y[8 * u + 7]));
-            const int unit = half * 4 + u;
-            *reinterpret_cast<uint4*>(srow + ((unit ^ (row & 7)) << 4)) = pk;
-          }
-        } else {
-          buf_base = staging;
-          if (step_count >= 1) {
-            if (et == 0) bulk_wait_read<0>();
-            named_bar_sync(kEpiBar, kEpiThreads);
-          }
-          uint8_t* srow = buf_base + half * kStagingBytes + row * 128;
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {   // 8 units of 4 floats: the whole 128-byte row of this half's slab
-            const uint4 pk = make_uint4(__float_as_uint(y[4 * u + 0]), __float_as_uint(y[4 * u + 1]),
-                                        __float_as_uint(y[4 * u + 2]), __float_as_uint(y[4 * u + 3]));
-            *reinterpret_cast<uint4*>(srow + ((u ^ (row & 7)) << 4)) = pk;
-          }
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(kEpiBar, kEpiThreads);
-        if (et == 0) {
-          if (kBf16Out) {
-            tma_store_2d(&G.tm_y, smem_u32(buf_base), 64 * i, m0);
-          } else {
-            tma_store_2d(&G.tm_y, smem_u32(buf_base), 64 * i, m0);
-            tma_store_2d(&G.tm_y, smem_u32(buf_base + kStagingBytes), 64 * i + 32, m0);
-          }
-          bulk_commit();
-        }
-        ++step_count;
-      }
+      });
+      // all reads of this accumulator are done: hand it back to the MMA warp
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));
     }
-    if (et == 0) bulk_wait<0>();
   }
 
   tc_fence_before();
@@ -416,10 +532,37 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
   if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
 
-template <int N, int OP, int OUT>
-cudaError_t launch_one(const GemmParams& p, int sms, cudaStream_t stream) {
-  constexpr size_t smem = Cfg<N>::SMEM;
-  auto kern = gemm_norm_kernel<N, OP, OUT>;
+// Picks resident W when it fits and leaves at least three A stages.
+struct Plan {
+  bool resident;
+  int stages;
+  size_t smem;
+};
+
+Plan plan_for(int N, int K, int elem_bytes) {
+  Plan pl{false, 0, 0};
+  const size_t w_bytes = static_cast<size_t>(N) * K * elem_bytes;
+  for (int pass = 0; pass < 2; ++pass) {
+    const bool resident = pass == 0;
+    if (resident && w_bytes > kResidentWLimit) continue;
+    const Layout base = make_layout(N, K, elem_bytes, resident, 0);
+    const size_t fixed = base.total;
+    const size_t per_stage = base.stage_bytes;
+    if (fixed + 2 * per_stage > kSmemLimit) continue;
+    int st = static_cast<int>((kSmemLimit - fixed) / per_stage);
+    if (st > kMaxStages) st = kMaxStages;
+    if (resident && st < 3) continue;
+    pl.resident = resident;
+    pl.stages = st;
+    pl.smem = fixed + static_cast<size_t>(st) * per_stage;
+    return pl;
+  }
+  return pl;
+}
+
+template <int N, int OP, int OUT, bool RES>
+cudaError_t launch_one(const GemmParams& p, size_t smem, int sms, cudaStream_t stream) {
+  auto kern = gemm_norm_kernel<N, OP, OUT, RES>;
   // the shared-memory opt-in is set once per device (it is not a stream
   // operation, so it also stays out of captured CUDA graphs)
   static std::atomic<uint64_t> configured{0};
@@ -428,7 +571,7 @@ cudaError_t launch_one(const GemmParams& p, int sms, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const uint64_t bit = uint64_t(1) << (dev & 63);
   if (!(configured.load() & bit)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemLimit));
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
@@ -438,29 +581,33 @@ cudaError_t launch_one(const GemmParams& p, int sms, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+template <int N, int OP, int OUT>
+cudaError_t launch_res(const GemmParams& p, const Plan& pl, int sms, cudaStream_t stream) {
+  return pl.resident ? launch_one<N, OP, OUT, true>(p, pl.smem, sms, stream)
+                     : launch_one<N, OP, OUT, false>(p, pl.smem, sms, stream);
+}
+
 template <int N>
-cudaError_t launch_n(const GemmParams& p, OperandKind op, OutKind out, int sms, cudaStream_t stream) {
-  if (op == OperandKind::kE4M3 && out == OutKind::kBf16) return launch_one<N, 0, 0>(p, sms, stream);
-  if (op == OperandKind::kE4M3 && out == OutKind::kF32) return launch_one<N, 0, 1>(p, sms, stream);
-  if (op == OperandKind::kBf16 && out == OutKind::kBf16) return launch_one<N, 1, 0>(p, sms, stream);
-  if (op == OperandKind::kBf16 && out == OutKind::kF32) return launch_one<N, 1, 1>(p, sms, stream);
+cudaError_t launch_n(GemmParams& p, OperandKind op, OutKind out, int sms, cudaStream_t stream) {
+  const int eb = op == OperandKind::kBf16 ? 2 : 1;
+  const Plan pl = plan_for(N, p.K, eb);
+  if (pl.stages == 0) return cudaErrorInvalidValue;
+  p.stages = pl.stages;
+  if (op == OperandKind::kE4M3 && out == OutKind::kBf16) return launch_res<N, 0, 0>(p, pl, sms, stream);
+  if (op == OperandKind::kE4M3 && out == OutKind::kF32) return launch_res<N, 0, 1>(p, pl, sms, stream);
+  if (op == OperandKind::kBf16 && out == OutKind::kBf16) return launch_res<N, 1, 0>(p, pl, sms, stream);
+  if (op == OperandKind::kBf16 && out == OutKind::kF32) return launch_res<N, 1, 1>(p, pl, sms, stream);
   return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-size_t gemm_smem_bytes(int N, OperandKind) {
-  switch (N) {
-    case 64: return Cfg<64>::SMEM;
-    case 128: return Cfg<128>::SMEM;
-    case 192: return Cfg<192>::SMEM;
-    case 256: return Cfg<256>::SMEM;
-    case 512: return Cfg<512>::SMEM;
-    default: return 0;
-  }
+bool gemm_supported(int N, int K, OperandKind op) {
+  if (!(N == 64 || N == 128 || N == 192 || N == 256 || N == 512)) return false;
+  return plan_for(N, K, op == OperandKind::kBf16 ? 2 : 1).stages > 0;
 }
 
-cudaError_t launch_gemm_norm(const GemmParams& p, int N, OperandKind op, OutKind out, int sms, cudaStream_t stream) {
+cudaError_t launch_gemm_norm(GemmParams& p, int N, OperandKind op, OutKind out, int sms, cudaStream_t stream) {
   if (op == OperandKind::kMxE4M3) return cudaErrorNotSupported;
   switch (N) {
     case 64: return launch_n<64>(p, op, out, sms, stream);

@@ -54,6 +54,7 @@ struct GemmGroup {
   const uint16_t* bias;  // bf16 [N] or null
   const uint16_t* gamma; // bf16 [N] or null
   const uint16_t* beta;  // bf16 [N] or null
+  void* y;               // output (the fp32 output is stored directly)
   int64_t M;
   int32_t tile_begin;    // first tile of this group in the launch's tile space
   int32_t sx_per_row;    // 1: sx has M entries, 0: one entry
@@ -68,7 +69,7 @@ struct GemmParams {
   int32_t K;
   int32_t norm;
   float eps;
-  int32_t pad;
+  int32_t stages;        // shared-memory ring depth (set by the launcher)
   unsigned* status;      // device status word
   uint64_t wait_limit_ns;
 };
@@ -76,11 +77,12 @@ struct GemmParams {
 enum class OperandKind : int { kE4M3 = 0, kBf16 = 1, kMxE4M3 = 2 };
 enum class OutKind : int { kBf16 = 0, kF32 = 1 };
 
-// Launches the persistent GEMM + epilogue kernel for N columns.
-cudaError_t launch_gemm_norm(const GemmParams& p, int N, OperandKind op, OutKind out, int sms, cudaStream_t stream);
+// Launches the persistent GEMM + epilogue kernel for N columns (fills in
+// p.stages).
+cudaError_t launch_gemm_norm(GemmParams& p, int N, OperandKind op, OutKind out, int sms, cudaStream_t stream);
 
-// Shared-memory bytes the kernel needs (host side, for validation).
-size_t gemm_smem_bytes(int N, OperandKind op);
+// Whether the kernel has a shared-memory plan for this N, K and operand type.
+bool gemm_supported(int N, int K, OperandKind op);
 
 // Probe reduction: accumulates MERE / Frobenius / max statistics of out vs ref.
 cudaError_t launch_error_reduce(const float* out, const float* ref, int64_t n, double* acc, int sms, cudaStream_t stream);

@@ -20,6 +20,7 @@ enum : unsigned {
   kErrEpilogueWait = 4u,
   kErrDrainWait = 8u,
   kErrSelftest = 16u,
+  kErrMisaligned = 32u,
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -49,14 +50,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
+// Suspending wait: the thread sleeps in hardware until the phase completes
+// or about kSuspendHintNs pass, so a waiting warp takes no issue slots from
+// the warps that are working.
+constexpr uint32_t kSuspendHintNs = 1000000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -202,7 +208,29 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
       : "memory");
 }
 
+// 16 lanes x 256 bits, repeated 4 times along columns (32 columns in all).
+// Thread t of the warp gets, for repetition i = 0..3 (columns 8i..8i+7):
+//   r[4i+0], r[4i+1] = lane (base + t/4),     columns 8i + 2(t%4) + {0, 1}
+//   r[4i+2], r[4i+3] = lane (base + 8 + t/4), columns 8i + 2(t%4) + {0, 1}
+__device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Makes every register of a tcgen05.ld destination appear redefined after
+// tcgen05.wait::ld, so no use of it can be scheduled before the wait.
+template <int NR>
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[NR]) {
+#pragma unroll
+  for (int i = 0; i < NR; ++i) asm volatile("" : "+r"(r[i])::"memory");
+}
 
 // Shared-memory matrix descriptor for a K-major operand tile whose rows are
 // 128 bytes, stored with the 128-byte swizzle (8-row atoms of 1024 bytes, as
@@ -225,6 +253,20 @@ __device__ __forceinline__ uint64_t sdesc_k128_sw128(uint32_t smem_addr) {
 // M >> 4 (24-28).
 __host__ __device__ constexpr uint32_t idesc_dense(uint32_t a_fmt, uint32_t b_fmt, uint32_t m, uint32_t n) {
   return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+// Predicated global stores (no branch around them).
+__device__ __forceinline__ void st_global_pred_b32(void* ptr, uint32_t v, uint32_t pred) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %2, 0;\n\t@p st.global.b32 [%0], %1;\n\t}" ::"l"(ptr), "r"(v), "r"(pred)
+      : "memory");
+}
+
+__device__ __forceinline__ void st_global_pred_v2f32(void* ptr, float2 v, uint32_t pred) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %3, 0;\n\t@p st.global.v2.f32 [%0], {%1, %2};\n\t}" ::"l"(ptr), "f"(v.x),
+      "f"(v.y), "r"(pred)
+      : "memory");
 }
 
 // -------------------------------------------------------------- conversions
