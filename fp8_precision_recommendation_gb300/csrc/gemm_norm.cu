@@ -25,11 +25,10 @@
 //               (scale, bias, gamma, beta) read from shared memory serves 4
 //               rows, and the math runs on packed fp32 pairs (fma/mul/add
 //               .f32x2); TMEM reads are pipelined one chunk ahead.
-//               Row statistics are fp32 Chan/Welford merges (LayerNorm) or sums
-//               of squares (RMSNorm) across chunks, lanes (shuffles) and the
-//               two parts (shared memory); the normalized bf16 row is
-//               packed into swizzled staging slabs and one thread TMA-stores
-//               each 64-column slab.
+//               Row statistics are fp32 shifted sums (LayerNorm) or sums of
+//               squares (RMSNorm) across chunks, merged across lanes
+//               (shuffles) and the two parts (shared memory); normalized
+//               column pairs go straight from registers to global memory.
 // The output makes no extra HBM round trip: Y is written once.
 #include <cudaTypedefs.h>
 
@@ -45,7 +44,6 @@ namespace {
 constexpr int kBM = 128;                 // rows per tile (= TMEM lanes)
 constexpr int kSliceBytes = 128;         // bytes of K per stage per row
 constexpr uint32_t kABytes = kBM * kSliceBytes;
-constexpr uint32_t kStagingBytes = kBM * 128;   // one 128-byte-wide output slab
 constexpr int kTmemCols = 512;
 constexpr int kThreads = 320;
 constexpr int kEpiThreads = 256;
@@ -57,12 +55,11 @@ constexpr size_t kResidentWLimit = 128 * 1024;
 // Shared-memory carve-up (all offsets from a 1024-byte-aligned base):
 //   ring     stages x (A slice [| B slice])
 //   w        resident W: K/KE slices of N rows x 128 bytes (when resident)
-//   staging  2 x 16 KB output slabs
 //   vectors  4 x N fp32 (weight scale, bias, gamma, beta)
 //   stats    4 x 128 float2 partial row statistics
 //   barriers
 struct Layout {
-  uint32_t stage_bytes, ring, w, staging, vec, stats, bars, total;
+  uint32_t stage_bytes, ring, w, vec, stats, bars, total;
 };
 
 __host__ __device__ inline Layout make_layout(int N, int K, int elem_bytes, bool resident, int stages) {
@@ -72,8 +69,7 @@ __host__ __device__ inline Layout make_layout(int N, int K, int elem_bytes, bool
   L.ring = 0;
   L.w = L.ring + static_cast<uint32_t>(stages) * L.stage_bytes;
   const uint32_t w_bytes = resident ? static_cast<uint32_t>(N) * static_cast<uint32_t>(K) * elem_bytes : 0u;
-  L.staging = L.w + w_bytes;
-  L.vec = L.staging + 2 * kStagingBytes;
+  L.vec = L.w + w_bytes;
   L.stats = L.vec + 4u * N * sizeof(float);
   L.bars = L.stats + 4u * kBM * sizeof(float2);
   L.total = L.bars + 256;
@@ -116,7 +112,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
   }
   uint8_t* ring = smem + L.ring;
   uint8_t* wres = smem + L.w;
-  uint8_t* staging = smem + L.staging;
   float* vec_sw = reinterpret_cast<float*>(smem + L.vec);
   float* vec_b = vec_sw + N;
   float* vec_g = vec_b + N;
