@@ -58,6 +58,7 @@ SIGNATURES = {
     "loka_quantize_fp8": (c_i32, [c_p, c_i64, c_i64, c_i32, c_p, c_p, c_p, c_sz, c_p]),
     "loka_fp8_linear_norm_workspace_size": (c_sz, [ctypes.POINTER(LinearDesc), c_i32]),
     "loka_fp8_linear_norm": (c_i32, [ctypes.POINTER(LinearDesc), c_i32, c_p, c_sz, c_p]),
+    "loka_fp8_linear_norm_static": (c_i32, [ctypes.POINTER(LinearDesc), c_i32, c_p]),
     "loka_quant_error_workspace_size": (c_sz, [ctypes.POINTER(LinearDesc)]),
     "loka_quant_error": (c_i32, [ctypes.POINTER(LinearDesc), c_p, c_sz, ctypes.POINTER(ErrorStats), c_p]),
     "loka_dispatch_select": (c_i32, [ctypes.POINTER(DispatchEntry), c_i64, ctypes.POINTER(Problem),
@@ -150,6 +151,13 @@ def loka_fp8_linear_norm_workspace_size(descs: Sequence[LinearDesc]) -> int:
 def loka_fp8_linear_norm(descs: Sequence[LinearDesc], workspace=None, workspace_bytes: int = 0, stream=None) -> None:
     arr = make_descs(descs)
     check(load().loka_fp8_linear_norm(arr, len(descs), _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def loka_fp8_linear_norm_static(descs: Sequence[LinearDesc], stream=None) -> None:
+    """loka_fp8_linear_norm with the library's built-in scratch (no workspace,
+    no allocation; for callers that cannot allocate device memory)."""
+    arr = make_descs(descs)
+    check(load().loka_fp8_linear_norm_static(arr, len(descs), _stream(stream)))
 
 
 def loka_quant_error_workspace_size(desc: LinearDesc) -> int:

@@ -75,6 +75,33 @@ loka_status device_info(DeviceInfo** out) {
   return LOKA_OK;
 }
 
+// Built-in scratch for loka_fp8_linear_norm_static, for callers that cannot
+// allocate device memory.  A file-scope __device__ array: every GPU that
+// loads this library holds these bytes until the process exits.
+constexpr size_t kStaticScratchBytes = size_t(4) << 20;   // 4 MiB
+__device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+void* g_static_scratch_addr[64];
+
+// Device address of the built-in scratch on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// once per device, with that device current, and cached.
+loka_status static_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(LOKA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_static_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+    g_static_scratch_addr[dev] = p;
+  }
+  *out = g_static_scratch_addr[dev];
+  return LOKA_OK;
+}
+
 // ------------------------------------------------------------ tensor maps
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -396,6 +423,20 @@ loka_status loka_fp8_linear_norm(const loka_linear_desc* descs, int32_t num_grou
                                    OutKind::kBf16, dev->sms, st);
   if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
   return LOKA_OK;
+}
+
+loka_status loka_fp8_linear_norm_static(const loka_linear_desc* descs, int32_t num_groups, void* stream) {
+  loka_status s = validate(descs, num_groups, false);
+  if (s != LOKA_OK) return s;
+  const size_t need = layout_operands(descs, num_groups, nullptr);
+  if (need > kStaticScratchBytes)
+    return fail(LOKA_ERR_WORKSPACE,
+                "this call needs %zu bytes of scratch; the built-in scratch of loka_fp8_linear_norm_static holds %zu "
+                "bytes (use loka_fp8_linear_norm with a caller workspace)",
+                need, kStaticScratchBytes);
+  void* scratch = nullptr;
+  if ((s = static_scratch(&scratch)) != LOKA_OK) return s;
+  return loka_fp8_linear_norm(descs, num_groups, scratch, kStaticScratchBytes, stream);
 }
 
 size_t loka_quant_error_workspace_size(const loka_linear_desc* desc) {

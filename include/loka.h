@@ -152,6 +152,31 @@ loka_status loka_fp8_linear_norm(const loka_linear_desc* descs, int32_t num_grou
                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * loka_fp8_linear_norm_static -- loka_fp8_linear_norm without any allocation.
+ *
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot allocate device memory: code running where no allocator is reachable
+ * (a plugin handed only input and output buffers by its host framework, or a
+ * runtime that forbids cudaMalloc on its path) and so cannot supply the
+ * workspace that loka_fp8_linear_norm needs for the quantized operands.
+ *
+ * Same arguments, semantics and results as loka_fp8_linear_norm, minus the
+ * workspace: the scratch is a built-in 4 MiB device array owned by the
+ * library (every GPU that loads the library holds it until the process
+ * exits).  Calls whose quantized operands and scales need more than 4 MiB
+ * (loka_fp8_linear_norm_workspace_size() > 4194304) fail with
+ * LOKA_ERR_WORKSPACE before anything is launched.  The call allocates
+ * nothing itself (no cudaMalloc, cudaFree or allocating library routine).
+ * The first call on a device looks up the array's device address (a host
+ * runtime query, done once per device); make that first call before any
+ * stream capture.  Every call shares the one array and leaves its contents
+ * behind; the call clears what must start at zero.  Calls that overlap on
+ * the GPU (different streams, or different host threads) race on the array:
+ * serialize them.
+ * ---------------------------------------------------------------------- */
+loka_status loka_fp8_linear_norm_static(const loka_linear_desc* descs, int32_t num_groups, void* stream);
+
+/* ------------------------------------------------------------------------
  * loka_quant_error -- quantization-error probe of one layer.
  *
  * Defined by LoKA section II-C "Error Analysis" (MERE: the mean element-wise
