@@ -144,14 +144,15 @@ size_t scale_bytes(int mode, int64_t rows, int64_t cols) {
 
 struct OperandSlots {   // workspace offsets of one group's quantized operands
   size_t xq, sx, wq, sw, amax;
+  size_t sx_tc, sw_tc;   // MX: scale codes in the tensor-memory copy layout
 };
 
 // Lays out the quantized operands of every group; returns the total bytes.
 size_t layout_operands(const loka_linear_desc* d, int n, std::vector<OperandSlots>* slots) {
   size_t off = 0;
-  if (slots) slots->assign(n, OperandSlots{0, 0, 0, 0, 0});
+  if (slots) slots->assign(n, OperandSlots{0, 0, 0, 0, 0, 0, 0});
   for (int i = 0; i < n; ++i) {
-    OperandSlots s{0, 0, 0, 0, 0};
+    OperandSlots s{0, 0, 0, 0, 0, 0, 0};
     if (d[i].mode != kBf16) {
       if (!d[i].x_is_fp8) {
         s.xq = off;
@@ -169,6 +170,12 @@ size_t layout_operands(const loka_linear_desc* d, int n, std::vector<OperandSlot
         s.amax = off;
         off = align_up(off + 2 * sizeof(unsigned));
       }
+      if (d[i].mode == kScaleMx32) {
+        s.sx_tc = off;
+        off = align_up(off + static_cast<size_t>(sf_tc_bytes(d[i].M, d[i].K)));
+        s.sw_tc = off;
+        off = align_up(off + static_cast<size_t>(sf_tc_bytes(d[i].N, d[i].K)));
+      }
     }
     if (slots) (*slots)[i] = s;
   }
@@ -176,6 +183,10 @@ size_t layout_operands(const loka_linear_desc* d, int n, std::vector<OperandSlot
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+OperandKind operand_kind(int mode) {
+  return mode == kBf16 ? OperandKind::kBf16 : (mode == kScaleMx32 ? OperandKind::kMxE4M3 : OperandKind::kE4M3);
+}
 
 loka_status validate(const loka_linear_desc* d, int n, bool probe) {
   if (d == nullptr) return fail(LOKA_ERR_INVALID_ARG, "descs is NULL");
@@ -197,8 +208,7 @@ loka_status validate(const loka_linear_desc* d, int n, bool probe) {
   if (a.K > (int64_t(1) << 20)) return fail(LOKA_ERR_UNSUPPORTED, "K too large");
   if (!(a.N == 64 || a.N == 128 || a.N == 192 || a.N == 256 || a.N == 512))
     return fail(LOKA_ERR_UNSUPPORTED, "N = %lld: supported N are 64, 128, 192, 256, 512", static_cast<long long>(a.N));
-  if (a.mode == kScaleMx32) return fail(LOKA_ERR_UNSUPPORTED, "MX 1x32 GEMM is not available in this build");
-  if (!gemm_supported(static_cast<int>(a.N), static_cast<int>(a.K), a.mode == kBf16 ? OperandKind::kBf16 : OperandKind::kE4M3) ||
+  if (!gemm_supported(static_cast<int>(a.N), static_cast<int>(a.K), operand_kind(a.mode)) ||
       (probe && !gemm_supported(static_cast<int>(a.N), static_cast<int>(a.K), OperandKind::kBf16)))
     return fail(LOKA_ERR_UNSUPPORTED, "no shared-memory plan for N = %lld, K = %lld", static_cast<long long>(a.N),
                 static_cast<long long>(a.K));
@@ -251,10 +261,15 @@ loka_status build_gemm(const loka_linear_desc* d, int n, const std::vector<Opera
       const void* sw = g.w_is_fp8 ? g.w_scales : ws + slots[i].sw;
       if ((s = encode_2d(&G.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xq, g.K, g.M, 128)) != LOKA_OK) return s;
       if ((s = encode_2d(&G.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wq, g.K, g.N, g.N > 256 ? 256 : g.N)) != LOKA_OK) return s;
-      G.sx = static_cast<const float*>(sx);
-      G.sw = static_cast<const float*>(sw);
-      G.sx_per_row = mode == kScaleRow;
-      G.sw_per_row = mode == kScaleRow;
+      if (mode == kScaleMx32) {   // the block scales are applied inside the MMA
+        G.sfa_tc = ws + slots[i].sx_tc;
+        G.sfb_tc = ws + slots[i].sw_tc;
+      } else {
+        G.sx = static_cast<const float*>(sx);
+        G.sw = static_cast<const float*>(sw);
+        G.sx_per_row = mode == kScaleRow;
+        G.sw_per_row = mode == kScaleRow;
+      }
     }
     if (out == OutKind::kBf16)
       s = encode_2d(&G.tm_y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y, g.N, g.M, 128);
@@ -287,6 +302,7 @@ loka_status quantize_operands(const loka_linear_desc* d, int n, const std::vecto
       j.q = ws + slots[i].xq;
       j.scales = ws + slots[i].sx;
       j.amax_slot = reinterpret_cast<unsigned*>(ws + slots[i].amax);
+      j.sf_tc = g.mode == kScaleMx32 ? ws + slots[i].sx_tc : nullptr;
       j.rows = g.M;
       j.cols = g.K;
       j.row_begin = rows;
@@ -298,6 +314,7 @@ loka_status quantize_operands(const loka_linear_desc* d, int n, const std::vecto
       j.q = ws + slots[i].wq;
       j.scales = ws + slots[i].sw;
       j.amax_slot = reinterpret_cast<unsigned*>(ws + slots[i].amax) + 1;
+      j.sf_tc = g.mode == kScaleMx32 ? ws + slots[i].sw_tc : nullptr;
       j.rows = g.N;
       j.cols = g.K;
       j.row_begin = rows;
@@ -416,11 +433,22 @@ loka_status loka_fp8_linear_norm(const loka_linear_desc* descs, int32_t num_grou
   if (!bf16 && (!descs[0].x_is_fp8 || !descs[0].w_is_fp8)) {
     if ((s = quantize_operands(descs, num_groups, slots, ws, dev, st)) != LOKA_OK) return s;
   }
+  if (descs[0].mode == kScaleMx32) {   // caller-quantized MX operands: scales into the copy layout
+    for (int i = 0; i < num_groups; ++i) {
+      const loka_linear_desc& g = descs[i];
+      cudaError_t e = cudaSuccess;
+      if (g.x_is_fp8 && g.M > 0)
+        e = launch_sf_permute(static_cast<const uint8_t*>(g.x_scales), ws + slots[i].sx_tc, g.M, g.K, dev->sms, st);
+      if (e == cudaSuccess && g.w_is_fp8)
+        e = launch_sf_permute(static_cast<const uint8_t*>(g.w_scales), ws + slots[i].sw_tc, g.N, g.K, dev->sms, st);
+      if (e != cudaSuccess) return cuda_fail(e, "scale permute launch");
+    }
+  }
   static thread_local GemmParams p;
   if ((s = build_gemm(descs, num_groups, slots, ws, bf16, OutKind::kBf16, nullptr, descs[0].norm, dev, &p)) != LOKA_OK)
     return s;
-  cudaError_t e = launch_gemm_norm(p, static_cast<int>(descs[0].N), bf16 ? OperandKind::kBf16 : OperandKind::kE4M3,
-                                   OutKind::kBf16, dev->sms, st);
+  cudaError_t e = launch_gemm_norm(p, static_cast<int>(descs[0].N), operand_kind(descs[0].mode), OutKind::kBf16,
+                                   dev->sms, st);
   if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
   return LOKA_OK;
 }
@@ -475,8 +503,7 @@ loka_status loka_quant_error(const loka_linear_desc* desc, void* workspace, size
   }
   void* y_out[1] = {out};
   if ((s = build_gemm(desc, 1, slots, ws, bf16, OutKind::kF32, y_out, kNormNone, dev, &p)) != LOKA_OK) return s;
-  e = launch_gemm_norm(p, static_cast<int>(desc->N), bf16 ? OperandKind::kBf16 : OperandKind::kE4M3, OutKind::kF32,
-                       dev->sms, st);
+  e = launch_gemm_norm(p, static_cast<int>(desc->N), operand_kind(desc->mode), OutKind::kF32, dev->sms, st);
   if (e != cudaSuccess) return cuda_fail(e, "probe GEMM launch");
   void* y_ref[1] = {ref};
   if ((s = build_gemm(desc, 1, slots, ws, true, OutKind::kF32, y_ref, kNormNone, dev, &p)) != LOKA_OK) return s;

@@ -62,13 +62,22 @@ struct Layout {
   uint32_t stage_bytes, ring, w, vec, stats, bars, total;
 };
 
-__host__ __device__ inline Layout make_layout(int N, int K, int elem_bytes, bool resident, int stages) {
+// MX scale blocks: 512 bytes per 128 rows per 128-element K slice.
+constexpr uint32_t kSfBlock = 512;
+__host__ __device__ constexpr int sfb_blocks(int N) { return (N + 127) / 128; }
+
+__host__ __device__ inline Layout make_layout(int N, int K, int elem_bytes, bool resident, int stages, bool mx) {
   Layout L;
   const uint32_t b_slice = static_cast<uint32_t>(N) * kSliceBytes;
-  L.stage_bytes = kABytes + (resident ? 0u : b_slice);
+  const uint32_t sfa = mx ? kSfBlock : 0u;
+  const uint32_t sfb = mx ? kSfBlock * sfb_blocks(N) : 0u;
+  // stage: [A slice][B slice, streamed W][A scales][B scales, streamed W]
+  L.stage_bytes = kABytes + (resident ? 0u : b_slice) + sfa + (resident ? 0u : sfb);
   L.ring = 0;
   L.w = L.ring + static_cast<uint32_t>(stages) * L.stage_bytes;
-  const uint32_t w_bytes = resident ? static_cast<uint32_t>(N) * static_cast<uint32_t>(K) * elem_bytes : 0u;
+  const int nkb = K * elem_bytes / kSliceBytes;
+  // resident W: [nkb B slices][nkb x B scale blocks]
+  const uint32_t w_bytes = resident ? static_cast<uint32_t>(nkb) * (b_slice + sfb) : 0u;
   L.vec = L.w + w_bytes;
   L.stats = L.vec + 4u * N * sizeof(float);
   L.bars = L.stats + 4u * kBM * sizeof(float2);
@@ -88,10 +97,16 @@ __device__ __forceinline__ float2 dup2(float a) { return make_float2(a, a); }
 
 template <int N, int OP, int OUT, bool RESIDENT>
 __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_constant__ GemmParams p) {
-  constexpr int NBUF = (2 * N <= kTmemCols) ? 2 : 1;
+  constexpr int SF_COLS_MAX = OP == static_cast<int>(OperandKind::kMxE4M3) ? kMaxStages * (4 + 4 * sfb_blocks(N)) : 0;
+  constexpr int NBUF = (2 * N + SF_COLS_MAX <= kTmemCols) ? 2 : 1;
+  static_assert(N + SF_COLS_MAX <= kTmemCols, "accumulator and scale factors must fit in tensor memory");
   constexpr int N_MMA = N > 256 ? 256 : N;
   constexpr int N_SPLIT = N / N_MMA;
   constexpr bool kBf16Op = OP == static_cast<int>(OperandKind::kBf16);
+  constexpr bool kMx = OP == static_cast<int>(OperandKind::kMxE4M3);
+  constexpr int NSFB = sfb_blocks(N);
+  constexpr uint32_t SFB_BYTES = kMx ? kSfBlock * NSFB : 0u;
+  constexpr uint32_t SF_COLS = kMx ? 4 + 4 * NSFB : 0;    // TMEM columns of one stage's scales
   constexpr int EB = kBf16Op ? 2 : 1;               // operand element bytes
   constexpr int KE = kSliceBytes / EB;              // K elements per 128-byte slice
   constexpr uint32_t IDESC = kBf16Op ? idesc_dense(1, 1, kBM, N_MMA)    // bf16 x bf16 -> f32
@@ -100,7 +115,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
 
   const int stages = p.stages;
   const int num_kb = p.K / KE;
-  const Layout L = make_layout(N, p.K, EB, RESIDENT, stages);
+  const Layout L = make_layout(N, p.K, EB, RESIDENT, stages, kMx);
 
   // Pointers are derived from the __shared__ array by plain offsets, so the
   // compiler keeps them in the shared address space (LDS/STS, not generic
@@ -182,11 +197,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
             break;
           }
           const uint32_t wb = smem_u32(w_full);
-          mbar_arrive_expect_tx(wb, static_cast<uint32_t>(num_kb) * B_SLICE);
+          mbar_arrive_expect_tx(wb, static_cast<uint32_t>(num_kb) * (B_SLICE + SFB_BYTES));
           for (int kb = 0; kb < num_kb; ++kb) {
 #pragma unroll
             for (int s = 0; s < N_SPLIT; ++s)
               tma_load_2d(smem_u32(wres + kb * B_SLICE + s * N_MMA * kSliceBytes), &p.g[g].tm_b, wb, kb * KE, s * N_MMA);
+            if (kMx) {
+#pragma unroll
+              for (int h = 0; h < NSFB; ++h)
+                bulk_load_1d(smem_u32(wres + num_kb * B_SLICE + (kb * NSFB + h) * kSfBlock),
+                             p.g[g].sfb_tc + (static_cast<int64_t>(h) * num_kb + kb) * kSfBlock, kSfBlock, wb);
+            }
           }
           ++w_loads;
           cur_group = g;
@@ -205,6 +226,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
 #pragma unroll
             for (int s = 0; s < N_SPLIT; ++s)
               tma_load_2d(smem_u32(b_dst + s * N_MMA * kSliceBytes), &p.g[g].tm_b, fb, kb * KE, s * N_MMA);
+          }
+          if (kMx) {
+            uint8_t* sf_dst = a_dst + kABytes + (RESIDENT ? 0u : B_SLICE);
+            bulk_load_1d(smem_u32(sf_dst), p.g[g].sfa_tc + (static_cast<int64_t>(m0 >> 7) * num_kb + kb) * kSfBlock,
+                         kSfBlock, fb);
+            if (!RESIDENT) {
+#pragma unroll
+              for (int h = 0; h < NSFB; ++h)
+                bulk_load_1d(smem_u32(sf_dst + kSfBlock + h * kSfBlock),
+                             p.g[g].sfb_tc + (static_cast<int64_t>(h) * num_kb + kb) * kSfBlock, kSfBlock, fb);
+            }
           }
           issued |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -252,6 +284,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
           tc_fence_after();
           const uint32_t a_addr = smem_u32(ring + static_cast<size_t>(stage) * L.stage_bytes);
           const uint32_t b_addr = RESIDENT ? smem_u32(wres + kb * B_SLICE) : a_addr + kABytes;
+          uint32_t sfa_tmem = 0, sfb_tmem = 0;
+          if (kMx) {
+            // E8M0 codes of this K slice into tensor memory: A's 128 rows to
+            // 4 columns, B's rows to 4 columns per 128 rows
+            const uint32_t sfa_smem = a_addr + kABytes + (RESIDENT ? 0u : B_SLICE);
+            const uint32_t sfb_smem = RESIDENT ? smem_u32(wres + num_kb * B_SLICE + kb * NSFB * kSfBlock)
+                                               : sfa_smem + kSfBlock;
+            sfa_tmem = tmem_base + static_cast<uint32_t>(NBUF * N + stage * SF_COLS);
+            sfb_tmem = sfa_tmem + 4;
+            tmem_cp_32x128b_warpx4(sfa_tmem, sdesc_rows16(sfa_smem));
+#pragma unroll
+            for (int h = 0; h < NSFB; ++h) tmem_cp_32x128b_warpx4(sfb_tmem + 4 * h, sdesc_rows16(sfb_smem + h * kSfBlock));
+          }
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint64_t adesc = sdesc_k128_sw128(a_addr + k * 32);
@@ -261,6 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
               const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
               if (kBf16Op)
                 mma_f16(d_tmem + s * N_MMA, adesc, bdesc, IDESC, acc);
+              else if (kMx)
+                mma_mxf8f6f4(d_tmem + s * N_MMA, adesc, bdesc, idesc_mx(kBM, N_MMA, k), sfa_tmem, sfb_tmem, acc);
               else
                 mma_f8f6f4(d_tmem + s * N_MMA, adesc, bdesc, IDESC, acc);
             }
@@ -534,13 +581,14 @@ struct Plan {
   size_t smem;
 };
 
-Plan plan_for(int N, int K, int elem_bytes) {
+Plan plan_for(int N, int K, int elem_bytes, bool mx) {
   Plan pl{false, 0, 0};
   const size_t w_bytes = static_cast<size_t>(N) * K * elem_bytes;
+  if (mx && N > 256) return pl;   // the accumulator would leave no tensor memory for the scales
   for (int pass = 0; pass < 2; ++pass) {
     const bool resident = pass == 0;
     if (resident && w_bytes > kResidentWLimit) continue;
-    const Layout base = make_layout(N, K, elem_bytes, resident, 0);
+    const Layout base = make_layout(N, K, elem_bytes, resident, 0, mx);
     const size_t fixed = base.total;
     const size_t per_stage = base.stage_bytes;
     if (fixed + 2 * per_stage > kSmemLimit) continue;
@@ -585,13 +633,17 @@ cudaError_t launch_res(const GemmParams& p, const Plan& pl, int sms, cudaStream_
 template <int N>
 cudaError_t launch_n(GemmParams& p, OperandKind op, OutKind out, int sms, cudaStream_t stream) {
   const int eb = op == OperandKind::kBf16 ? 2 : 1;
-  const Plan pl = plan_for(N, p.K, eb);
+  const Plan pl = plan_for(N, p.K, eb, op == OperandKind::kMxE4M3);
   if (pl.stages == 0) return cudaErrorInvalidValue;
   p.stages = pl.stages;
   if (op == OperandKind::kE4M3 && out == OutKind::kBf16) return launch_res<N, 0, 0>(p, pl, sms, stream);
   if (op == OperandKind::kE4M3 && out == OutKind::kF32) return launch_res<N, 0, 1>(p, pl, sms, stream);
   if (op == OperandKind::kBf16 && out == OutKind::kBf16) return launch_res<N, 1, 0>(p, pl, sms, stream);
   if (op == OperandKind::kBf16 && out == OutKind::kF32) return launch_res<N, 1, 1>(p, pl, sms, stream);
+  if constexpr (N <= 256) {
+    if (op == OperandKind::kMxE4M3 && out == OutKind::kBf16) return launch_res<N, 2, 0>(p, pl, sms, stream);
+    if (op == OperandKind::kMxE4M3 && out == OutKind::kF32) return launch_res<N, 2, 1>(p, pl, sms, stream);
+  }
   return cudaErrorInvalidValue;
 }
 
@@ -599,11 +651,10 @@ cudaError_t launch_n(GemmParams& p, OperandKind op, OutKind out, int sms, cudaSt
 
 bool gemm_supported(int N, int K, OperandKind op) {
   if (!(N == 64 || N == 128 || N == 192 || N == 256 || N == 512)) return false;
-  return plan_for(N, K, op == OperandKind::kBf16 ? 2 : 1).stages > 0;
+  return plan_for(N, K, op == OperandKind::kBf16 ? 2 : 1, op == OperandKind::kMxE4M3).stages > 0;
 }
 
 cudaError_t launch_gemm_norm(GemmParams& p, int N, OperandKind op, OutKind out, int sms, cudaStream_t stream) {
-  if (op == OperandKind::kMxE4M3) return cudaErrorNotSupported;
   switch (N) {
     case 64: return launch_n<64>(p, op, out, sms, stream);
     case 128: return launch_n<128>(p, op, out, sms, stream);

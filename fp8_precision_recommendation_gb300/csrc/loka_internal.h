@@ -28,6 +28,7 @@ struct QuantJob {
   uint8_t* q;
   void* scales;
   unsigned* amax_slot;   // tensorwise only: 4-byte accumulator, zeroed by the launcher
+  uint8_t* sf_tc;        // MX only, optional: E8M0 codes again in the tensor-memory copy layout
   int64_t rows;
   int64_t cols;
   int64_t row_begin;     // first row of this job in the launch's joint row space
@@ -41,6 +42,24 @@ struct QuantJobs {
 
 cudaError_t launch_quantize(const QuantJobs& jobs, int mode, int sms, cudaStream_t stream);
 
+// MX scale factors in the tensor-memory copy layout: for row block rb (128
+// rows) and K block kb (128 elements = 4 codes per row), a 512-byte block at
+// (rb * (K/128) + kb) * 512; inside it row m, code kk sits at byte
+// (m % 32) * 16 + ((m % 128) / 32) * 4 + kk.  tcgen05.cp.32x128b.warpx4 of
+// such a block puts the codes of row m in TMEM lane m, column (m % 128) / 32,
+// byte kk.
+__host__ __device__ inline int64_t sf_tc_offset(int64_t m, int64_t blk32, int64_t kb128_count) {
+  const int64_t rb = m >> 7, kb = blk32 >> 2, kk = blk32 & 3;
+  return (rb * kb128_count + kb) * 512 + (m & 31) * 16 + ((m & 127) >> 5) * 4 + kk;
+}
+__host__ __device__ inline int64_t sf_tc_bytes(int64_t rows, int64_t cols) {
+  return ((rows + 127) / 128) * (cols / 128) * 512;
+}
+
+// Rewrites logical [rows, cols/32] E8M0 codes into the tensor-memory copy layout.
+cudaError_t launch_sf_permute(const uint8_t* logical, uint8_t* tc, int64_t rows, int64_t cols, int sms,
+                              cudaStream_t stream);
+
 // ------------------------------------------------------------------ GEMM
 // Per-group arguments of the fused GEMM + normalization kernel.
 struct GemmGroup {
@@ -51,6 +70,8 @@ struct GemmGroup {
   CUtensorMap tm_sfb;    // MX only: B scales
   const float* sx;       // per-row [M] / per-tensor [1] activation scale, or null (=1)
   const float* sw;       // per-row [N] / per-tensor [1] weight scale, or null (=1)
+  const uint8_t* sfa_tc; // MX: A scale codes in the tensor-memory copy layout
+  const uint8_t* sfb_tc; // MX: B scale codes in the tensor-memory copy layout
   const uint16_t* bias;  // bf16 [N] or null
   const uint16_t* gamma; // bf16 [N] or null
   const uint16_t* beta;  // bf16 [N] or null

@@ -125,6 +125,14 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int
                : "memory");
 }
 
+// 1-D bulk copy global -> shared, completing on an mbarrier (16-byte aligned
+// addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 template <int N>
@@ -189,6 +197,13 @@ __device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t adesc, ui
       : "memory");
 }
 
+// Copies a 32-row x 16-byte shared-memory block into tensor memory, lanes
+// 0-31 of every lane quadrant (the same 16 bytes replicated 4 times),
+// columns [col, col + 4).
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
@@ -246,6 +261,26 @@ __device__ __forceinline__ uint64_t sdesc_k128_sw128(uint32_t smem_addr) {
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(2) << 61;
   return d;
+}
+
+// Shared-memory descriptor of an unswizzled block of 16-byte rows stored
+// contiguously (core matrices of 8 rows x 16 bytes, 128 bytes apart), as the
+// source of tcgen05.cp: stride byte offset 128, swizzle mode 0.
+__device__ __forceinline__ uint64_t sdesc_rows16(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFF) >> 4);
+  d |= static_cast<uint64_t>(128 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
+// Instruction descriptor for kind::mxf8f6f4 block scaling (E4M3 A and B,
+// fp32 D): B scale-factor byte id (bits 4-5), A/B formats 0 = E4M3, N >> 3
+// (17-22), scale type 1 = UE8M0 (23), M >> 4 (24-28), A scale-factor byte id
+// (29-30).  The byte id picks which of the four E8M0 codes packed in each
+// 32-bit tensor-memory word applies to this K-step of 32.
+__host__ __device__ constexpr uint32_t idesc_mx(uint32_t m, uint32_t n, uint32_t sf_id) {
+  return (sf_id << 4) | ((n >> 3) << 17) | (1u << 23) | ((m >> 4) << 24) | (sf_id << 29);
 }
 
 // Instruction descriptor for kind::f16 / kind::f8f6f4: D fp32 (bits 4-5 = 1),

@@ -123,7 +123,10 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const __grid_constant__
         const int e = mx_exponent(m);
         if (idx < nvec) {
           dst[idx] = cast8(v[i], pow2_neg(e));
-          if ((lane & 3) == 0) sc[idx >> 2] = static_cast<uint8_t>(e + 127);
+          if ((lane & 3) == 0) {
+            sc[idx >> 2] = static_cast<uint8_t>(e + 127);
+            if (job.sf_tc != nullptr) job.sf_tc[sf_tc_offset(row, idx >> 2, job.cols >> 7)] = static_cast<uint8_t>(e + 127);
+          }
         }
       }
     }
@@ -162,7 +165,10 @@ __global__ void __launch_bounds__(256) quant_rows_long_kernel(const __grid_const
         const int e = mx_exponent(m);
         if (idx < nvec) {
           dst[idx] = cast8(v, pow2_neg(e));
-          if ((lane & 3) == 0) sc[idx >> 2] = static_cast<uint8_t>(e + 127);
+          if ((lane & 3) == 0) {
+            sc[idx >> 2] = static_cast<uint8_t>(e + 127);
+            if (job.sf_tc != nullptr) job.sf_tc[sf_tc_offset(row, idx >> 2, job.cols >> 7)] = static_cast<uint8_t>(e + 127);
+          }
         }
       }
     }
@@ -206,6 +212,17 @@ __global__ void __launch_bounds__(256) cast_tensor_kernel(const __grid_constant_
     dst[i] = cast8(__ldcs(src + i), inv);
 }
 
+__global__ void __launch_bounds__(256) sf_permute_kernel(const uint8_t* __restrict__ logical, uint8_t* __restrict__ tc,
+                                                         int64_t rows, int64_t cols) {
+  const int64_t nb = cols >> 5;
+  const int64_t total = rows * nb;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t m = i / nb, b = i - m * nb;
+    tc[sf_tc_offset(m, b, cols >> 7)] = logical[i];
+  }
+}
+
 template <int MODE>
 cudaError_t launch_rows(const QuantJobs& jobs, int max_cols, int sms, cudaStream_t stream) {
   const int threads = 256;
@@ -229,6 +246,16 @@ cudaError_t launch_rows(const QuantJobs& jobs, int max_cols, int sms, cudaStream
 }
 
 }  // namespace
+
+cudaError_t launch_sf_permute(const uint8_t* logical, uint8_t* tc, int64_t rows, int64_t cols, int sms,
+                              cudaStream_t stream) {
+  const int64_t total = rows * (cols >> 5);
+  if (total == 0) return cudaSuccess;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > static_cast<int64_t>(sms) * 4) blocks = static_cast<int64_t>(sms) * 4;
+  sf_permute_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(logical, tc, rows, cols);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quantize(const QuantJobs& jobs, int mode, int sms, cudaStream_t stream) {
   if (jobs.n == 0 || jobs.total_rows == 0) return cudaSuccess;

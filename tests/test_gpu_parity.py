@@ -274,3 +274,55 @@ def test_watchdog_turns_a_stuck_wait_into_a_status(lib):
     inp = W.single()
     (y,) = _run([inp])
     _check_layer(inp, y, what="after watchdog")
+
+
+# -------------------------------------------------------------- MX 1x32
+@pytest.mark.parametrize("N", [64, 128, 192, 256])
+@pytest.mark.parametrize("norm", [W.NORM_NONE, W.NORM_LAYER, W.NORM_RMS])
+def test_mx_block_scaled_small_shapes(lib, N, norm):
+    inp = W.make_layer(389, 256, N, mode=W.SCALE_MX32, norm=norm, seed=N + 3 * norm, x_dist="laplace",
+                       outlier_frac=0.01, bias_var=0.02, gamma_uniform=True)
+    (y,) = _run([inp])
+    _check_layer(inp, y, what=f"MX norm{norm} N{N}")
+
+
+def test_mx_scales_vary_per_row_and_block(lib):
+    # rows and 32-element blocks with very different magnitudes, so that a
+    # scale code applied to the wrong row or block shows up at once
+    M, K, N = 256, 512, 128
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    x *= np.exp2(rng.integers(-12, 12, size=(M, K // 32))).repeat(32, axis=1).astype(np.float32)
+    w = (rng.standard_normal((N, K)) / np.sqrt(K)).astype(np.float32)
+    w *= np.exp2(rng.integers(-6, 6, size=(N, K // 32))).repeat(32, axis=1).astype(np.float32)
+    inp = W.LayerInputs(x=torch.from_numpy(x).to(torch.bfloat16), w=torch.from_numpy(w).to(torch.bfloat16),
+                        bias=None, gamma=None, beta=None, mode=W.SCALE_MX32, norm=W.NORM_NONE, eps=0.0)
+    (y,) = _run([inp])
+    _check_layer(inp, y, what="MX structured scales")
+
+
+def test_mx_long_k_layer(lib):
+    inp = W.make_layer(4096, 2048, 256, mode=W.SCALE_MX32, norm=W.NORM_LAYER, seed=5, x_dist="laplace")
+    (y,) = _run([inp])
+    rng = np.random.default_rng(3)
+    rows = np.unique(np.concatenate([np.arange(128), rng.integers(0, inp.M, 512), np.arange(inp.M - 128, inp.M)]))
+    _check_layer(inp, y, rows=rows, what="MX K=2048")
+
+
+def test_mx_prequantized_inputs_match_bf16_inputs(lib):
+    inp = W.make_layer(300, 256, 128, mode=W.SCALE_MX32, norm=W.NORM_RMS, seed=8, x_dist="laplace", eps=1e-6)
+    (y_ref,) = _run([inp])
+    qx, sx = loka.quantize_fp8(_gpu(inp.x), W.SCALE_MX32)
+    qw, sw = loka.quantize_fp8(_gpu(inp.w), W.SCALE_MX32)
+    layer = loka.Layer(x=qx, w=qw, x_scales=sx, w_scales=sw, mode=W.SCALE_MX32, norm=W.NORM_RMS, eps=inp.eps)
+    (y,) = loka.fp8_linear_norm([layer])
+    torch.cuda.synchronize()
+    assert torch.equal(y.cpu(), y_ref)
+
+
+def test_mx_probe_matches_oracle(lib):
+    inp = W.make_layer(1000, 512, 256, mode=W.SCALE_MX32, norm=W.NORM_NONE, seed=6, bias_var=0.02, x_dist="laplace")
+    st = loka.quant_error(_gpu(inp.x), _gpu(inp.w), _gpu(inp.bias), W.SCALE_MX32)
+    want = OP.quant_error(inp.x, inp.w, inp.bias, W.SCALE_MX32)
+    assert abs(st["rel_err_fro"] - want["rel_err_fro"]) <= 1e-3 * want["rel_err_fro"]
+    assert abs(st["mere"] - want["mere"]) <= 1e-2 * want["mere"]
