@@ -206,8 +206,9 @@ loka_status validate(const loka_linear_desc* d, int n, bool probe) {
   if (a.K < 128 || a.K % 128 != 0)
     return fail(LOKA_ERR_UNSUPPORTED, "K = %lld: K must be a positive multiple of 128", static_cast<long long>(a.K));
   if (a.K > (int64_t(1) << 20)) return fail(LOKA_ERR_UNSUPPORTED, "K too large");
-  if (!(a.N == 64 || a.N == 128 || a.N == 192 || a.N == 256 || a.N == 512))
-    return fail(LOKA_ERR_UNSUPPORTED, "N = %lld: supported N are 64, 128, 192, 256, 512", static_cast<long long>(a.N));
+  if (!(a.N == 64 || a.N == 128 || a.N == 192 || a.N == 256 || a.N == 512 || a.N == 1024 || a.N == 2048))
+    return fail(LOKA_ERR_UNSUPPORTED, "N = %lld: supported N are 64, 128, 192, 256, 512, 1024, 2048",
+                static_cast<long long>(a.N));
   if (!gemm_supported(static_cast<int>(a.N), static_cast<int>(a.K), operand_kind(a.mode)) ||
       (probe && !gemm_supported(static_cast<int>(a.N), static_cast<int>(a.K), OperandKind::kBf16)))
     return fail(LOKA_ERR_UNSUPPORTED, "no shared-memory plan for N = %lld, K = %lld", static_cast<long long>(a.N),

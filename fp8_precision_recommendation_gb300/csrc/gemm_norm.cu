@@ -66,7 +66,8 @@ struct Layout {
 constexpr uint32_t kSfBlock = 512;
 __host__ __device__ constexpr int sfb_blocks(int N) { return (N + 127) / 128; }
 
-__host__ __device__ inline Layout make_layout(int N, int K, int elem_bytes, bool resident, int stages, bool mx) {
+__host__ __device__ inline Layout make_layout(int N, int K, int elem_bytes, bool resident, int stages, bool mx,
+                                              int cl = 1) {
   Layout L;
   const uint32_t b_slice = static_cast<uint32_t>(N) * kSliceBytes;
   const uint32_t sfa = mx ? kSfBlock : 0u;
@@ -80,7 +81,9 @@ __host__ __device__ inline Layout make_layout(int N, int K, int elem_bytes, bool
   const uint32_t w_bytes = resident ? static_cast<uint32_t>(nkb) * (b_slice + sfb) : 0u;
   L.vec = L.w + w_bytes;
   L.stats = L.vec + 4u * N * sizeof(float);
-  L.bars = L.stats + 4u * kBM * sizeof(float2);
+  // [4][128] partial row statistics, then [2][cluster][128] row statistics of
+  // the cluster's CTAs (written remotely, double-buffered by tile parity)
+  L.bars = L.stats + 4u * kBM * sizeof(float2) + (cl > 1 ? 2u * cl * kBM * sizeof(float2) : 0u);
   L.total = L.bars + 256;
   return L;
 }
@@ -95,8 +98,15 @@ __device__ __forceinline__ float bf16_to_f(uint16_t h) { return __uint_as_float(
 
 __device__ __forceinline__ float2 dup2(float a) { return make_float2(a, a); }
 
-template <int N, int OP, int OUT, bool RESIDENT>
+// N = the columns this CTA owns (<= 256); CL = CTAs per cluster sharing each
+// 128-row tile (the layer's output has N * CL columns; CTA r owns columns
+// [r N, r N + N) and the CTAs of a cluster merge their row statistics
+// through distributed shared memory, so a row wider than one CTA's tensor
+// memory is still normalized in the epilogue).
+template <int N, int CL, int OP, int OUT, bool RESIDENT>
 __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_constant__ GemmParams p) {
+  static_assert(N <= 256, "one MMA per K step");
+  constexpr int NG = N * CL;                        // columns of the whole output row
   constexpr int SF_COLS_MAX = OP == static_cast<int>(OperandKind::kMxE4M3) ? kMaxStages * (4 + 4 * sfb_blocks(N)) : 0;
   constexpr int NBUF = (2 * N + SF_COLS_MAX <= kTmemCols) ? 2 : 1;
   static_assert(N + SF_COLS_MAX <= kTmemCols, "accumulator and scale factors must fit in tensor memory");
@@ -115,16 +125,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
 
   const int stages = p.stages;
   const int num_kb = p.K / KE;
-  const Layout L = make_layout(N, p.K, EB, RESIDENT, stages, kMx);
+  const Layout L = make_layout(N, p.K, EB, RESIDENT, stages, kMx, CL);
+  const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
+  const int col0 = static_cast<int>(rank) * N;      // first output column of this CTA
+  const int cid = static_cast<int>(blockIdx.x) / CL;
+  const int ncl = static_cast<int>(gridDim.x) / CL;
 
   // Pointers are derived from the __shared__ array by plain offsets, so the
   // compiler keeps them in the shared address space (LDS/STS, not generic
   // loads).  The 128B-swizzled TMA/UMMA tiles need the 1024-byte alignment.
   extern __shared__ __align__(1024) uint8_t smem[];
-  if (smem_u32(smem) & 1023u) {
-    if (threadIdx.x == 0) atomicOr(p.status, kErrMisaligned);
-    return;
-  }
+  // uniform over the CTA; a misaligned CTA skips all work but still takes
+  // part in the cluster barriers below
+  const bool misaligned = (smem_u32(smem) & 1023u) != 0;
   uint8_t* ring = smem + L.ring;
   uint8_t* wres = smem + L.w;
   float* vec_sw = reinterpret_cast<float*>(smem + L.vec);
@@ -132,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
   float* vec_g = vec_b + N;
   float* vec_be = vec_g + N;
   float2* stat_part = reinterpret_cast<float2*>(smem + L.stats);   // [4][128] partial row statistics
+  float2* cl_stats = stat_part + 4 * kBM;                           // [2][CL][128] cluster row statistics
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* full = bars;
   uint64_t* empty = full + kMaxStages;
@@ -140,7 +154,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
   uint64_t* mma_done = tempty + 2;
   uint64_t* w_full = mma_done + 1;
   uint64_t* w_free = w_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(w_free + 1);
+  uint64_t* cl_bar = w_free + 1;                                    // [2] cluster statistics arrivals
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cl_bar + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -158,7 +173,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
     mbar_init(smem_u32(mma_done), 1);
     mbar_init(smem_u32(w_full), 1);
     mbar_init(smem_u32(w_free), 1);
-    *abort_flag = 0;
+    // each of the cluster's CTAs sends its statistics from 4 warps x 8 lanes
+    mbar_init(smem_u32(&cl_bar[0]), 32 * CL);
+    mbar_init(smem_u32(&cl_bar[1]), 32 * CL);
+    *abort_flag = misaligned ? 1 : 0;
+    if (misaligned) atomicOr(p.status, kErrMisaligned);
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -176,10 +195,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // no CTA touches a partner's shared memory before the partner has set up
+  // its barriers
+  if (CL > 1) cluster_sync_all();
   const uint32_t tmem_base = *tmem_slot;
   const Watchdog wd{abort_flag, p.status, p.wait_limit_ns};
 
-  if (warp == 0) {
+  if (misaligned) {
+    // nothing to do: fall through to the teardown barriers
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int stage = 0;
@@ -187,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
       uint32_t issued = 0, last_parity = 0;
       int cur_group = -1, w_loads = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
+      for (int tile = cid; ok && tile < p.total_tiles; tile += ncl) {
         const int g = group_of(p, tile);
         const int m0 = (tile - p.g[g].tile_begin) * kBM;
         if (RESIDENT && g != cur_group) {
@@ -201,12 +225,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
           for (int kb = 0; kb < num_kb; ++kb) {
 #pragma unroll
             for (int s = 0; s < N_SPLIT; ++s)
-              tma_load_2d(smem_u32(wres + kb * B_SLICE + s * N_MMA * kSliceBytes), &p.g[g].tm_b, wb, kb * KE, s * N_MMA);
+              tma_load_2d(smem_u32(wres + kb * B_SLICE + s * N_MMA * kSliceBytes), &p.g[g].tm_b, wb, kb * KE,
+                          col0 + s * N_MMA);
             if (kMx) {
 #pragma unroll
               for (int h = 0; h < NSFB; ++h)
                 bulk_load_1d(smem_u32(wres + num_kb * B_SLICE + (kb * NSFB + h) * kSfBlock),
-                             p.g[g].sfb_tc + (static_cast<int64_t>(h) * num_kb + kb) * kSfBlock, kSfBlock, wb);
+                             p.g[g].sfb_tc + (static_cast<int64_t>(rank * NSFB + h) * num_kb + kb) * kSfBlock,
+                             kSfBlock, wb);
             }
           }
           ++w_loads;
@@ -225,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
             uint8_t* b_dst = a_dst + kABytes;
 #pragma unroll
             for (int s = 0; s < N_SPLIT; ++s)
-              tma_load_2d(smem_u32(b_dst + s * N_MMA * kSliceBytes), &p.g[g].tm_b, fb, kb * KE, s * N_MMA);
+              tma_load_2d(smem_u32(b_dst + s * N_MMA * kSliceBytes), &p.g[g].tm_b, fb, kb * KE, col0 + s * N_MMA);
           }
           if (kMx) {
             uint8_t* sf_dst = a_dst + kABytes + (RESIDENT ? 0u : B_SLICE);
@@ -235,7 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
 #pragma unroll
               for (int h = 0; h < NSFB; ++h)
                 bulk_load_1d(smem_u32(sf_dst + kSfBlock + h * kSfBlock),
-                             p.g[g].sfb_tc + (static_cast<int64_t>(h) * num_kb + kb) * kSfBlock, kSfBlock, fb);
+                             p.g[g].sfb_tc + (static_cast<int64_t>(rank * NSFB + h) * num_kb + kb) * kSfBlock,
+                             kSfBlock, fb);
             }
           }
           issued |= 1u << stage;
@@ -261,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
       int local = 0;
       int cur_group = -1, w_uses = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x, ++local) {
+      for (int tile = cid; ok && tile < p.total_tiles; tile += ncl, ++local) {
         if (RESIDENT) {
           const int g = group_of(p, tile);
           if (g != cur_group) {
@@ -399,18 +426,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
     int cur_group = -1;
     int local = 0;
     float sx_next[4] = {1.f, 1.f, 1.f, 1.f};
-    if (static_cast<int>(blockIdx.x) < p.total_tiles) row_scales(blockIdx.x, sx_next);
-    for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x, ++local) {
+    if (cid < p.total_tiles) row_scales(cid, sx_next);
+    for (int tile = cid; tile < p.total_tiles; tile += ncl, ++local) {
       const int g = group_of(p, tile);
       const GemmGroup& G = p.g[g];
       if (g != cur_group) {
         named_bar_sync(kEpiBar, kEpiThreads);
         const bool normed = norm != kNormNone;
         for (int n = et; n < N; n += kEpiThreads) {
-          vec_sw[n] = (G.sw != nullptr && G.sw_per_row) ? G.sw[n] : 1.0f;
-          vec_b[n] = G.bias == nullptr ? 0.0f : bf16_to_f(G.bias[n]);
-          vec_g[n] = (G.gamma == nullptr || !normed) ? 1.0f : bf16_to_f(G.gamma[n]);
-          vec_be[n] = (G.beta == nullptr || norm != kNormLayer) ? 0.0f : bf16_to_f(G.beta[n]);
+          const int gn = col0 + n;
+          vec_sw[n] = (G.sw != nullptr && G.sw_per_row) ? G.sw[gn] : 1.0f;
+          vec_b[n] = G.bias == nullptr ? 0.0f : bf16_to_f(G.bias[gn]);
+          vec_g[n] = (G.gamma == nullptr || !normed) ? 1.0f : bf16_to_f(G.gamma[gn]);
+          vec_be[n] = (G.beta == nullptr || norm != kNormLayer) ? 0.0f : bf16_to_f(G.beta[gn]);
         }
         named_bar_sync(kEpiBar, kEpiThreads);
         cur_group = g;
@@ -427,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
       for (int k = 0; k < 4; ++k) {
         const int64_t m = static_cast<int64_t>(m0) + rowk[k];
         ok[k] = m < Mg ? 1u : 0u;
-        rowp[k] = static_cast<uint8_t*>(G.y) + (m * N + 2 * cp) * (kBf16Out ? 2 : 4);
+        rowp[k] = static_cast<uint8_t*>(G.y) + (m * NG + col0 + 2 * cp) * (kBf16Out ? 2 : 4);
       }
       const int buf = NBUF == 2 ? (local & 1) : 0;
       const uint32_t use = NBUF == 2 ? (local >> 1) : local;
@@ -437,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
       named_bar_sync(kEpiBar, kEpiThreads);
       if (*abort_flag) break;
       tc_fence_after();
-      if (tile + static_cast<int>(gridDim.x) < p.total_tiles) row_scales(tile + gridDim.x, sx_next);
+      if (tile + ncl < p.total_tiles) row_scales(tile + ncl, sx_next);
       const uint32_t t_base = tmem_base + lane_addr + static_cast<uint32_t>(buf * N);
 
       // pass 1: row statistics of v = acc * sx * sw + b
@@ -530,15 +558,60 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
         }
         named_bar_sync(kEpiBar, kEpiThreads);
         // the two parts hold N/2 elements each
+        float qrow[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const float2 lo = stat_part[rowk[k]];
           const float2 hi = stat_part[kBM + rowk[k]];
           const float delta = hi.x - lo.x;
-          const float q = norm == kNormRms ? lo.y + hi.y : (lo.y + hi.y) + delta * delta * (0.25f * N);
+          qrow[k] = norm == kNormRms ? lo.y + hi.y : (lo.y + hi.y) + delta * delta * (0.25f * N);
           mean[k] = norm == kNormRms ? 0.0f : 0.5f * (lo.x + hi.x);
-          rstd[k] = rsqrtf(q * (1.0f / N) + eps);
         }
+        if constexpr (CL > 1) {
+          // exchange (mean, M2) of this CTA's N columns with the cluster:
+          // part-0 lanes with cp == 0 hold one row each and write it into
+          // every CTA's slot [buffer][rank][row], then arrive there
+          const int cb = local & 1;
+          if (part == 0 && cp == 0) {
+#pragma unroll
+            for (int j = 0; j < CL; ++j) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint32_t a = smem_u32(&cl_stats[(cb * CL + static_cast<int>(rank)) * kBM + rowk[k]]);
+                st_cluster_f32x2(mapa_shared(a, j), mean[k], qrow[k]);
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < CL; ++j) mbar_arrive_cluster(mapa_shared(smem_u32(&cl_bar[cb]), j));
+          }
+          wait_parity_cluster(wd, smem_u32(&cl_bar[cb]), (local >> 1) & 1, kErrClusterWait);
+          named_bar_sync(kEpiBar, kEpiThreads);
+          if (*abort_flag) break;
+          // merge the CTAs' statistics in rank order (N elements each)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            float mA = 0.f, qA = 0.f;
+#pragma unroll
+            for (int j = 0; j < CL; ++j) {
+              const float2 part_j = cl_stats[(cb * CL + j) * kBM + rowk[k]];
+              if (norm == kNormRms) {
+                qA += part_j.y;
+              } else if (j == 0) {
+                mA = part_j.x;
+                qA = part_j.y;
+              } else {
+                const float delta = part_j.x - mA;
+                const float w = 1.0f / static_cast<float>(j + 1);          // n_b / n_total
+                mA = fmaf(delta, w, mA);
+                qA += part_j.y + delta * delta * (static_cast<float>(N) * j * w);
+              }
+            }
+            mean[k] = norm == kNormRms ? 0.0f : mA;
+            qrow[k] = qA;
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) rstd[k] = rsqrtf(qrow[k] * (1.0f / NG) + eps);
       }
 
       // pass 2: y = ((v - mean) * rstd) * gamma + beta, stored straight from
@@ -572,6 +645,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+  // partners may still write statistics into this CTA's shared memory until
+  // they are done: leave together
+  if (CL > 1) cluster_sync_all();
 }
 
 // Picks resident W when it fits and leaves at least three A stages.
@@ -581,14 +657,13 @@ struct Plan {
   size_t smem;
 };
 
-Plan plan_for(int N, int K, int elem_bytes, bool mx) {
+Plan plan_for(int N, int K, int elem_bytes, bool mx, int cl) {
   Plan pl{false, 0, 0};
   const size_t w_bytes = static_cast<size_t>(N) * K * elem_bytes;
-  if (mx && N > 256) return pl;   // the accumulator would leave no tensor memory for the scales
   for (int pass = 0; pass < 2; ++pass) {
     const bool resident = pass == 0;
     if (resident && w_bytes > kResidentWLimit) continue;
-    const Layout base = make_layout(N, K, elem_bytes, resident, 0, mx);
+    const Layout base = make_layout(N, K, elem_bytes, resident, 0, mx, cl);
     const size_t fixed = base.total;
     const size_t per_stage = base.stage_bytes;
     if (fixed + 2 * per_stage > kSmemLimit) continue;
@@ -603,9 +678,9 @@ Plan plan_for(int N, int K, int elem_bytes, bool mx) {
   return pl;
 }
 
-template <int N, int OP, int OUT, bool RES>
+template <int N, int CL, int OP, int OUT, bool RES>
 cudaError_t launch_one(const GemmParams& p, size_t smem, int sms, cudaStream_t stream) {
-  auto kern = gemm_norm_kernel<N, OP, OUT, RES>;
+  auto kern = gemm_norm_kernel<N, CL, OP, OUT, RES>;
   // the shared-memory opt-in is set once per device (it is not a stream
   // operation, so it also stays out of captured CUDA graphs)
   static std::atomic<uint64_t> configured{0};
@@ -616,51 +691,82 @@ cudaError_t launch_one(const GemmParams& p, size_t smem, int sms, cudaStream_t s
   if (!(configured.load() & bit)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemLimit));
     if (e != cudaSuccess) return e;
+    if (CL > 1) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+      if (e != cudaSuccess) return e;
+    }
     configured.fetch_or(bit);
   }
-  int grid = p.total_tiles < sms ? p.total_tiles : sms;
-  if (grid < 1) return cudaSuccess;
-  kern<<<grid, kThreads, smem, stream>>>(p);
+  int clusters = sms / CL;
+  if (p.total_tiles < clusters) clusters = p.total_tiles;
+  if (clusters < 1) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * CL));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-template <int N, int OP, int OUT>
+template <int N, int CL, int OP, int OUT>
 cudaError_t launch_res(const GemmParams& p, const Plan& pl, int sms, cudaStream_t stream) {
-  return pl.resident ? launch_one<N, OP, OUT, true>(p, pl.smem, sms, stream)
-                     : launch_one<N, OP, OUT, false>(p, pl.smem, sms, stream);
+  return pl.resident ? launch_one<N, CL, OP, OUT, true>(p, pl.smem, sms, stream)
+                     : launch_one<N, CL, OP, OUT, false>(p, pl.smem, sms, stream);
 }
 
-template <int N>
+// N here is the width one CTA owns; CL CTAs of a cluster cover N * CL columns.
+template <int N, int CL>
 cudaError_t launch_n(GemmParams& p, OperandKind op, OutKind out, int sms, cudaStream_t stream) {
   const int eb = op == OperandKind::kBf16 ? 2 : 1;
-  const Plan pl = plan_for(N, p.K, eb, op == OperandKind::kMxE4M3);
+  const Plan pl = plan_for(N, p.K, eb, op == OperandKind::kMxE4M3, CL);
   if (pl.stages == 0) return cudaErrorInvalidValue;
   p.stages = pl.stages;
-  if (op == OperandKind::kE4M3 && out == OutKind::kBf16) return launch_res<N, 0, 0>(p, pl, sms, stream);
-  if (op == OperandKind::kE4M3 && out == OutKind::kF32) return launch_res<N, 0, 1>(p, pl, sms, stream);
-  if (op == OperandKind::kBf16 && out == OutKind::kBf16) return launch_res<N, 1, 0>(p, pl, sms, stream);
-  if (op == OperandKind::kBf16 && out == OutKind::kF32) return launch_res<N, 1, 1>(p, pl, sms, stream);
-  if constexpr (N <= 256) {
-    if (op == OperandKind::kMxE4M3 && out == OutKind::kBf16) return launch_res<N, 2, 0>(p, pl, sms, stream);
-    if (op == OperandKind::kMxE4M3 && out == OutKind::kF32) return launch_res<N, 2, 1>(p, pl, sms, stream);
-  }
+  if (op == OperandKind::kE4M3 && out == OutKind::kBf16) return launch_res<N, CL, 0, 0>(p, pl, sms, stream);
+  if (op == OperandKind::kE4M3 && out == OutKind::kF32) return launch_res<N, CL, 0, 1>(p, pl, sms, stream);
+  if (op == OperandKind::kBf16 && out == OutKind::kBf16) return launch_res<N, CL, 1, 0>(p, pl, sms, stream);
+  if (op == OperandKind::kBf16 && out == OutKind::kF32) return launch_res<N, CL, 1, 1>(p, pl, sms, stream);
+  if (op == OperandKind::kMxE4M3 && out == OutKind::kBf16) return launch_res<N, CL, 2, 0>(p, pl, sms, stream);
+  if (op == OperandKind::kMxE4M3 && out == OutKind::kF32) return launch_res<N, CL, 2, 1>(p, pl, sms, stream);
   return cudaErrorInvalidValue;
+}
+
+// (local width, cluster size) of an output row of N columns
+bool split_n(int N, int* local, int* cl) {
+  switch (N) {
+    case 64: case 128: case 192: case 256: *local = N; *cl = 1; return true;
+    case 512: *local = 256; *cl = 2; return true;
+    case 1024: *local = 256; *cl = 4; return true;
+    case 2048: *local = 256; *cl = 8; return true;
+    default: return false;
+  }
 }
 
 }  // namespace
 
 bool gemm_supported(int N, int K, OperandKind op) {
-  if (!(N == 64 || N == 128 || N == 192 || N == 256 || N == 512)) return false;
-  return plan_for(N, K, op == OperandKind::kBf16 ? 2 : 1, op == OperandKind::kMxE4M3).stages > 0;
+  int local = 0, cl = 0;
+  if (!split_n(N, &local, &cl)) return false;
+  return plan_for(local, K, op == OperandKind::kBf16 ? 2 : 1, op == OperandKind::kMxE4M3, cl).stages > 0;
 }
 
 cudaError_t launch_gemm_norm(GemmParams& p, int N, OperandKind op, OutKind out, int sms, cudaStream_t stream) {
   switch (N) {
-    case 64: return launch_n<64>(p, op, out, sms, stream);
-    case 128: return launch_n<128>(p, op, out, sms, stream);
-    case 192: return launch_n<192>(p, op, out, sms, stream);
-    case 256: return launch_n<256>(p, op, out, sms, stream);
-    case 512: return launch_n<512>(p, op, out, sms, stream);
+    case 64: return launch_n<64, 1>(p, op, out, sms, stream);
+    case 128: return launch_n<128, 1>(p, op, out, sms, stream);
+    case 192: return launch_n<192, 1>(p, op, out, sms, stream);
+    case 256: return launch_n<256, 1>(p, op, out, sms, stream);
+    case 512: return launch_n<256, 2>(p, op, out, sms, stream);
+    case 1024: return launch_n<256, 4>(p, op, out, sms, stream);
+    case 2048: return launch_n<256, 8>(p, op, out, sms, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -118,7 +118,9 @@ loka_status loka_quantize_fp8(const void* x, int64_t rows, int64_t cols, int32_t
  *
  * One descriptor per independent layer (group).  All groups of one call must
  * share N, K, mode, norm and eps and the *_is_fp8 flags; M may differ.
- *   M >= 0; K % 128 == 0; N in {64, 128, 192, 256, 512}.
+ *   M >= 0; K % 128 == 0; N in {64, 128, 192, 256, 512, 1024, 2048} (rows
+ *   wider than 256 are split over a thread-block cluster of N/256 CTAs that
+ *   merge their row statistics through distributed shared memory).
  *   x: bf16 [M,K] (x_is_fp8 = 0) or E4M3 [M,K] with x_scales as produced by
  *      loka_quantize_fp8 (x_is_fp8 = 1).  Same for w / w_scales / w_is_fp8.
  *   mode: LOKA_SCALE_* (LOKA_BF16 runs the bf16 GEMM; *_is_fp8 must be 0).

@@ -326,3 +326,34 @@ def test_mx_probe_matches_oracle(lib):
     want = OP.quant_error(inp.x, inp.w, inp.bias, W.SCALE_MX32)
     assert abs(st["rel_err_fro"] - want["rel_err_fro"]) <= 1e-3 * want["rel_err_fro"]
     assert abs(st["mere"] - want["mere"]) <= 1e-2 * want["mere"]
+
+
+# ------------------------------------------- rows wider than one CTA (clusters)
+@pytest.mark.parametrize("N", [512, 1024, 2048])
+@pytest.mark.parametrize("mode,norm", [(W.SCALE_ROW, W.NORM_LAYER), (W.SCALE_MX32, W.NORM_RMS),
+                                       (W.SCALE_TENSOR, W.NORM_NONE), (W.SCALE_MX32, W.NORM_LAYER)])
+def test_cluster_wide_rows(lib, N, mode, norm):
+    inp = W.make_layer(300, 256, N, mode=mode, norm=norm, seed=N + mode, x_dist="laplace",
+                       bias_var=0.02, gamma_uniform=True)
+    inp.beta = W.random_bf16((N,), seed=9, var=0.1)
+    (y,) = _run([inp])
+    _check_layer(inp, y, what=f"cluster N{N} mode{mode} norm{norm}")
+
+
+def test_cluster_grouped_ragged(lib):
+    inps = [W.make_layer(m, 256, 512, mode=W.SCALE_ROW, norm=W.NORM_LAYER, seed=m, bias_var=0.02) for m in (129, 0, 400)]
+    ys = _run(inps)
+    for inp, y in zip(inps, ys):
+        if inp.M:
+            _check_layer(inp, y, what=f"cluster group M{inp.M}")
+
+
+def test_mxfp8_layer_full_size(lib):
+    inp = W.mxfp8()
+    (y,) = _run([inp])
+    rng = np.random.default_rng(4)
+    rows = np.unique(np.concatenate([np.arange(128), rng.integers(0, inp.M, 1024), np.arange(inp.M - 128, inp.M)]))
+    _check_layer(inp, y, rows=rows, what="mxfp8 262144x2048x512")
+    yf = y.float()
+    assert yf.mean(dim=1).abs().max().item() < 2e-2
+    assert (yf.pow(2).mean(dim=1) - 1).abs().max().item() < 2e-2

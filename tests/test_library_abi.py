@@ -65,7 +65,7 @@ def _desc(**kw):
 
 
 @pytest.mark.parametrize("kw,status", [
-    ({"N": 100}, _loka.LOKA_ERR_UNSUPPORTED),
+    ({"N": 100}, _loka.LOKA_ERR_UNSUPPORTED), ({"N": 4096}, _loka.LOKA_ERR_UNSUPPORTED),
     ({"K": 96}, _loka.LOKA_ERR_UNSUPPORTED),
     ({"M": -1}, _loka.LOKA_ERR_INVALID_ARG),
     ({"mode": 7}, _loka.LOKA_ERR_INVALID_ARG),
