@@ -42,7 +42,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-compare", action="store_true")
-    ap.add_argument("--M", type=int, default=65536, help="rows of X (65536 is the headline workload)")
+    ap.add_argument("--M", type=int, default=None, help="rows of X per layer (default: the workload's own)")
+    ap.add_argument("--workload", default="rec_mlp", choices=["rec_mlp", "ensemble", "mxfp8", "single"])
     return ap.parse_args()
 
 
@@ -116,9 +117,9 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------- workload
-def workload(rank: int, M: int = 65536):
+def workload(rank: int, M=None):
     import workloads as W
-    return W.rec_mlp(seed=rank, M=M)
+    return W.rec_mlp(seed=rank, **({"M": M} if M else {}))
 
 
 def algorithmic_bytes_step(M, K, N):
@@ -157,15 +158,27 @@ def oracle_throughput(inp, budget_s: float, rows_per_call: int = 4096):
     import torch
     from oracle import linear as OL
     M, K, N = inp.M, inp.K, inp.N
+    if inp.mode == 0:   # per-tensor scaling is not row-local: time the whole (small) layer
+        t0 = time.perf_counter()
+        n = 0
+        while True:
+            OL.linear_norm_inputs(inp)
+            n += 1
+            if time.perf_counter() - t0 >= max(budget_s, 1e-3) or n >= 1000:
+                break
+        tt = time.perf_counter() - t0
+        return 2.0 * n * M * N * K / tt / 1e12, n * M, tt
     rng = np.random.default_rng(123)
     done, t_total = 0, 0.0
-    while t_total < budget_s and done < 64 * rows_per_call:
+    while True:   # at least one sample, then until the time budget is spent
         start = int(rng.integers(0, max(1, M - rows_per_call)))
         rows = np.arange(start, min(M, start + rows_per_call))
         t0 = time.perf_counter()
         OL.linear_norm_inputs(inp, rows=rows)
         t_total += time.perf_counter() - t0
         done += len(rows)
+        if t_total >= budget_s or done >= 64 * rows_per_call:
+            break
     return 2.0 * done * N * K / t_total / 1e12, done, t_total
 
 
@@ -210,7 +223,8 @@ def max_over_ranks(world, value: float, device=None) -> float:
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    inp = workload(0, args.M)
+    layers = workload_layers(args.workload, 0, args.M)
+    inp = layers[0]
     M, K, N = inp.M, inp.K, inp.N
     for _ in range(args.warmup):
         oracle_throughput(inp, 0.0, rows_per_call=512)
@@ -224,10 +238,11 @@ def run_reference(args, world, rank):
     value = 2.0 * rows_total * N * K / t / 1e12
     cores = oracle_threads()
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "impl": "reference", "metric": METRIC if args.workload == "rec_mlp" and not args.M else
+        f"FP8 linear+norm TFLOP/s ({args.workload} {len(layers)}x{M}x{K}x{N}) on 1 GB300", "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": f"rec_mlp M={M} K={K} N={N} per-row E4M3, LayerNorm",
+        "data": "synthetic", "config": {"workload": f"{args.workload} M={M} K={K} N={N} (group 0 of {len(layers)})",
                                         "sample": f"512 rows of X per step (rows are independent under per-row scaling)"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"{rows_total} rows in {args.steps} steps of 512 rows"},
@@ -237,6 +252,23 @@ def run_reference(args, world, rank):
 
 
 # ------------------------------------------------------------------ ours
+def workload_layers(name: str, rank: int, M):
+    import workloads as W
+    if name == "rec_mlp":
+        return [W.rec_mlp(seed=rank, **({"M": M} if M else {}))]
+    if name == "ensemble":
+        return W.ensemble(seed=rank, **({"M": M} if M else {}))
+    if name == "mxfp8":
+        return [W.mxfp8(seed=rank, **({"M": M} if M else {}))]
+    if name == "single":
+        return [W.single(seed=rank)]
+    raise ValueError(name)
+
+
+def scale_bytes(mode, rows, cols):
+    return {0: 4, 1: 4 * rows, 2: rows * cols // 32}.get(mode, 0)
+
+
 def run_ours(args, world, rank, local):
     import torch
     import fp8_precision_recommendation_gb300 as loka
@@ -245,23 +277,27 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     _loka.load()
-    inp = workload(rank, args.M)
-    M, K, N = inp.M, inp.K, inp.N
-    flops = 2.0 * M * N * K
-    x_bytes = 2 * M * K
-    nbuf = max(2, math.ceil(3 * L2_BYTES / (x_bytes + 2 * M * N)))
-    xs = [inp.x.to(dev) for _ in range(nbuf)]
-    ys = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(nbuf)]
-    w, bias = inp.w.to(dev), inp.bias.to(dev)
-    ws = loka.Workspace(dev)
+    layers = workload_layers(args.workload, rank, args.M)
+    mode, norm, eps = layers[0].mode, layers[0].norm, layers[0].eps
+    flops = sum(2.0 * l.M * l.N * l.K for l in layers)
+    x_bytes = sum(2 * l.M * l.K for l in layers)
+    y_bytes = sum(2 * l.M * l.N for l in layers)
+    nbuf = max(2, math.ceil(3 * L2_BYTES / (x_bytes + y_bytes)))
+    dv = lambda t: None if t is None else t.to(dev)
+    xs = [[l.x.to(dev) for l in layers] for _ in range(nbuf)]
+    ys = [[torch.empty((l.M, l.N), dtype=torch.bfloat16, device=dev) for l in layers] for _ in range(nbuf)]
+    ws_, bs_, gs_, bes_ = ([dv(getattr(l, a)) for l in layers] for a in ("w", "bias", "gamma", "beta"))
+    wsp = loka.Workspace(dev)
     stream = torch.cuda.Stream(device=dev)
+    s = stream.cuda_stream
 
-    def layer(i):
-        return loka.Layer(x=xs[i % nbuf], w=w, bias=bias, mode=inp.mode, norm=inp.norm, eps=inp.eps,
-                          y=ys[i % nbuf])
+    def mk(i, x_list=None, mode_=None, **kw):
+        return [loka.Layer(x=(x_list or xs[i % nbuf])[gi], w=ws_[gi], bias=bs_[gi], gamma=gs_[gi], beta=bes_[gi],
+                           mode=mode if mode_ is None else mode_, norm=norm, eps=eps, y=ys[i % nbuf][gi],
+                           **{k: v[gi] for k, v in kw.items()}) for gi in range(len(layers))]
 
     def step(i):
-        loka.fp8_linear_norm([layer(i)], workspace=ws, stream=stream.cuda_stream)
+        loka.fp8_linear_norm(mk(i), workspace=wsp, stream=s)
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -295,13 +331,6 @@ def run_ours(args, world, rank, local):
     value = world * flops * args.steps / t / 1e12
     clocks = clk.summary()
 
-    # ---- per-kernel timing (same launches, same stream) for the roofline
-    kern = {}
-    qx = torch.empty((M, K), dtype=torch.uint8, device=dev)
-    sx = torch.empty((M,), dtype=torch.float32, device=dev)
-    qw = torch.empty((N, K), dtype=torch.uint8, device=dev)
-    sw = torch.empty((N,), dtype=torch.float32, device=dev)
-
     def timed(fn, n):
         with torch.cuda.stream(stream):
             for i in range(3):
@@ -314,77 +343,111 @@ def run_ours(args, world, rank, local):
             b.synchronize()
         return a.elapsed_time(b) / 1e3 / n
 
-    s = stream.cuda_stream
-    kern["quantize_x"] = timed(lambda i: _loka.loka_quantize_fp8(xs[i % nbuf], M, K, 1, qx, sx, None, 0, s), args.steps)
-    _loka.loka_quantize_fp8(w, N, K, 1, qw, sw, None, 0, s)
-    gl = [loka.Layer(x=qx, w=qw, x_scales=sx, w_scales=sw, bias=bias, mode=inp.mode, norm=inp.norm, eps=inp.eps,
-                     y=ys[i]) for i in range(nbuf)]
-    kern["gemm_norm"] = timed(lambda i: loka.fp8_linear_norm([gl[i % nbuf]], workspace=ws, stream=s), args.steps)
+    # ---- per-kernel timing (same kernels, same stream) for the roofline
+    kern = {}
+    qx = [torch.empty((l.M, l.K), dtype=torch.uint8, device=dev) for l in layers]
+    qw = [torch.empty((l.N, l.K), dtype=torch.uint8, device=dev) for l in layers]
+    shp = [(loka.scales_shape(l.M, l.K, mode), loka.scales_shape(l.N, l.K, mode)) for l in layers]
+    sx = [torch.empty(a[0], dtype=getattr(torch, a[1]), device=dev) for a, _ in shp]
+    sw = [torch.empty(b[0], dtype=getattr(torch, b[1]), device=dev) for _, b in shp]
+    qws = torch.empty(max(256, _loka.loka_quantize_fp8_workspace_size(1, 32, mode)), dtype=torch.uint8, device=dev)
+
+    def quantize_x(i):
+        for gi, l in enumerate(layers):
+            _loka.loka_quantize_fp8(xs[i % nbuf][gi], l.M, l.K, mode, qx[gi], sx[gi], qws, qws.numel(), s)
+
+    kern["quantize_x"] = timed(quantize_x, args.steps)
+    for gi, l in enumerate(layers):
+        _loka.loka_quantize_fp8(ws_[gi], l.N, l.K, mode, qw[gi], sw[gi], qws, qws.numel(), s)
+    pre = [mk(i, x_list=qx, x_scales=sx, w_scales=sw) for i in range(nbuf)]
+    for lst in pre:
+        for gi, lay in enumerate(lst):
+            lay.w = qw[gi]
+    kern["gemm_norm"] = timed(lambda i: loka.fp8_linear_norm(pre[i % nbuf], workspace=wsp, stream=s), args.steps)
     torch.cuda.synchronize()
-    bytes_q = 2 * M * K + M * K + 4 * M
-    bytes_g = M * K + 4 * M + N * K + 4 * N + 3 * 2 * N + 2 * M * N
+    vec_bytes = lambda l: 2 * l.N * sum(v is not None for v in (l.bias, l.gamma, l.beta))
+    bytes_q = sum(3 * l.M * l.K + scale_bytes(mode, l.M, l.K) for l in layers)
+    bytes_g = sum(l.M * l.K + scale_bytes(mode, l.M, l.K) + l.N * l.K + scale_bytes(mode, l.N, l.K) + vec_bytes(l)
+                  + 2 * l.M * l.N for l in layers)
     P, src = peaks()
     bw = P["hbm_gbs"]
     dom = "gemm_norm" if kern["gemm_norm"] >= kern["quantize_x"] else "quantize_x"
     dom_bytes = bytes_g if dom == "gemm_norm" else bytes_q
     achieved = dom_bytes / kern[dom] / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": bw, "unit": "GB/s", "frac": achieved / bw,
-                "traffic": recorded_traffic(dom), "kernel": dom, "peak_source": f"{src} hbm_gbs",
+                "traffic": recorded_traffic(dom) if args.workload == "rec_mlp" and not args.M else None,
+                "kernel": dom, "peak_source": f"{src} hbm_gbs",
                 "algorithmic_bytes_per_launch": dom_bytes, "launch_us": kern[dom] * 1e6}
-    step_bytes = algorithmic_bytes_step(M, K, N)
+    step_bytes = sum(algorithmic_bytes_step(l.M, l.K, l.N) for l in layers)
     step_time = t / args.steps
     path_roofline = {"bytes_per_step": step_bytes, "floor_us": step_bytes / (bw * 1e9) * 1e6,
                      "frac_of_hbm_floor": (step_bytes / (bw * 1e9)) / step_time,
                      "achieved_gbs": step_bytes / step_time / 1e9}
 
-    # ---- comparators: our bf16 GEMM+norm and torch eager bf16 linear + layer_norm
+    # ---- comparators: our bf16 GEMM+norm and torch eager bf16 linear + norm
     compare = {}
     if not args.no_compare:
-        bl = [loka.Layer(x=xs[i], w=w, bias=bias, mode=3, norm=inp.norm, eps=inp.eps, y=ys[i]) for i in range(nbuf)]
-        compare["loka_bf16_fused_us"] = 1e6 * timed(lambda i: loka.fp8_linear_norm([bl[i % nbuf]], workspace=ws, stream=s), args.steps)
+        bl = [mk(i, mode_=3) for i in range(nbuf)]
+        compare["loka_bf16_fused_us"] = 1e6 * timed(lambda i: loka.fp8_linear_norm(bl[i % nbuf], workspace=wsp,
+                                                                                    stream=s), args.steps)
 
         def torch_bf16(i):
-            v = torch.nn.functional.linear(xs[i % nbuf], w, bias)
-            torch.nn.functional.layer_norm(v, (N,), eps=inp.eps)
-        compare["torch_bf16_linear_layernorm_us"] = 1e6 * timed(torch_bf16, args.steps)
+            for gi, l in enumerate(layers):
+                v = torch.nn.functional.linear(xs[i % nbuf][gi], ws_[gi], bs_[gi])
+                if norm == 1:
+                    torch.nn.functional.layer_norm(v, (l.N,), gs_[gi], bes_[gi], eps=eps)
+                elif norm == 2:
+                    torch.nn.functional.rms_norm(v, (l.N,), gs_[gi], eps=eps)
+        compare["torch_bf16_linear_norm_us"] = 1e6 * timed(torch_bf16, args.steps)
         compare["loka_fp8_step_us"] = 1e6 * step_time
 
     # ---- end to end through the public API with pinned host buffers
     e2e = None
     if not args.no_e2e:
-        hx = inp.x.pin_memory()
-        hy = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
-        dx = torch.empty_like(xs[0])
-        dy = torch.empty_like(ys[0])
-        el = loka.Layer(x=dx, w=w, bias=bias, mode=inp.mode, norm=inp.norm, eps=inp.eps, y=dy)
+        hx = [l.x.pin_memory() for l in layers]
+        hy = [torch.empty((l.M, l.N), dtype=torch.bfloat16).pin_memory() for l in layers]
+        dx = [torch.empty_like(x) for x in xs[0]]
+        dy = [torch.empty_like(y) for y in ys[0]]
+        el = mk(0, x_list=dx)
+        for gi, lay in enumerate(el):
+            lay.y = dy[gi]
 
         def e2e_step(i):
-            dx.copy_(hx, non_blocking=True)
-            loka.fp8_linear_norm([el], workspace=ws, stream=s)
-            hy.copy_(dy, non_blocking=True)
+            for a, b in zip(dx, hx):
+                a.copy_(b, non_blocking=True)
+            loka.fp8_linear_norm(el, workspace=wsp, stream=s)
+            for a, b in zip(hy, dy):
+                a.copy_(b, non_blocking=True)
 
         te = timed(e2e_step, max(3, args.steps // 2))
         te = max_over_ranks(world, te, dev)
         e2e = {"value": world * flops / te / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": x_bytes,
-               "d2h_bytes_per_step": 2 * M * N}
+               "d2h_bytes_per_step": y_bytes}
 
     cpu = None
     if rank == 0 and not args.no_cpu:
-        v, rows, tc = oracle_throughput(inp, 10.0)
+        v, rows, tc = oracle_throughput(layers[0], 10.0)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": oracle_threads(), "kind": "oracle",
-               "sample": f"{rows} rows of X (4096-row slices, per-row scaling is row-local), {tc:.1f} s"}
+               "sample": f"{rows} rows of X (4096-row slices, row-local scaling), {tc:.1f} s"}
 
     status = _loka.loka_device_status()
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
-    launches_per_step = 2   # one quantize launch (X and W), one GEMM+norm launch
+    launches_per_step = (3 if mode == 0 else 1) + 1   # quantize (amax + cast for per-tensor) + GEMM+norm
+    l0 = layers[0]
+    desc = {"rec_mlp": "rec-MLP X N(0,1)+1%x100 outliers, per-row E4M3, bias, LayerNorm",
+            "ensemble": "8-layer ensemble, per-row E4M3, RMSNorm, one grouped launch",
+            "mxfp8": "Laplace X, MX 1x32 E8M0 block scaling, LayerNorm",
+            "single": "per-tensor E4M3, LayerNorm"}[args.workload]
+    metric = METRIC if args.workload == "rec_mlp" and not args.M else \
+        f"FP8 linear+norm TFLOP/s ({args.workload} {len(layers)}x{l0.M}x{l0.K}x{l0.N}) on 1 GB300"
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * step_time, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp8_e4m3 (fp32 accumulate, bf16 out)", "data": "synthetic",
-        "config": {"workload": f"rec_mlp X[{M},{K}] N(0,1)+1%x100 outliers, W[{N},{K}] N(0,1/{K}), per-row E4M3, "
-                               f"bias, LayerNorm over {N}, bf16 out", "l2": f"{nbuf} rotating X/Y buffers "
-                               f"({nbuf * (x_bytes + 2 * M * N) / 1e6:.0f} MB) > L2", "parallelism": f"rows x{world}",
+        "config": {"workload": f"{args.workload}: {len(layers)} x X[{l0.M},{l0.K}] W[{l0.N},{l0.K}], {desc}, bf16 out",
+                   "l2": f"{nbuf} rotating X/Y buffer sets ({nbuf * (x_bytes + y_bytes) / 1e6:.0f} MB) > L2",
+                   "parallelism": f"rows x{world}",
                    "timing": "CUDA graph of K steps, CUDA events on the launching stream"},
         "roofline": roofline, "path_roofline": path_roofline, "kernels_us": {k: v * 1e6 for k, v in kern.items()},
         "compare": compare, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
