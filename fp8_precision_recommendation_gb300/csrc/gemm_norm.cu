@@ -9,7 +9,7 @@
 // section I (LRMs are wide ensembles of small GEMMs: several independent
 // layers share one launch here).
 //
-// Design (one CTA per SM, persistent, warp-specialized, 320 threads):
+// Design (one CTA per SM, persistent, warp-specialized, 576 threads):
 //   warp 0      TMA producer: 128-byte K slices of A (and of B when W does
 //               not stay resident) into a shared-memory ring, 128B-swizzled,
 //               one mbarrier per stage.  When N x K of the weights fits in
@@ -33,6 +33,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "loka_internal.h"
 #include "ptx.cuh"
@@ -45,8 +46,8 @@ constexpr int kBM = 128;                 // rows per tile (= TMEM lanes)
 constexpr int kSliceBytes = 128;         // bytes of K per stage per row
 constexpr uint32_t kABytes = kBM * kSliceBytes;
 constexpr int kTmemCols = 512;
-constexpr int kThreads = 320;
-constexpr int kEpiThreads = 256;
+constexpr int kThreads = 576;
+constexpr int kEpiThreads = 512;
 constexpr int kEpiBar = 1;               // named barrier id for the epilogue warps
 constexpr int kMaxStages = 8;
 constexpr size_t kSmemLimit = 227 * 1024;
@@ -174,8 +175,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
     mbar_init(smem_u32(w_full), 1);
     mbar_init(smem_u32(w_free), 1);
     // each of the cluster's CTAs sends its statistics from 4 warps x 8 lanes
-    mbar_init(smem_u32(&cl_bar[0]), 32 * CL);
-    mbar_init(smem_u32(&cl_bar[1]), 32 * CL);
+    // the lanes with ch == 0 and cp == 0 (8 warps x 8 lanes) of every CTA
+    mbar_init(smem_u32(&cl_bar[0]), 64 * CL);
+    mbar_init(smem_u32(&cl_bar[1]), 64 * CL);
     *abort_flag = misaligned ? 1 : 0;
     if (misaligned) atomicOr(p.status, kErrMisaligned);
     fence_barrier_init();
@@ -354,36 +356,40 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // Eight warps, two per TMEM lane quadrant: warp (quad q, part w) covers
-    // rows 32q..32q+31 and the 32-column chunks c = w + 2s.  The 16x256b
-    // load shape gives thread t rows t/4 + {0, 8, 16, 24} and column pairs
-    // 8i + 2(t%4) of each chunk.  Chunk reads are pipelined one ahead.
-    const int et = threadIdx.x - 64;         // 0..255
+    // Sixteen warps, four per TMEM lane quadrant: warp (quad q, row half h,
+    // column part w) covers rows 32q + 16h .. 32q + 16h + 15 and the 32-column
+    // chunks c = w + 2s.  The 16x256b load shape gives thread t rows
+    // t/4 + {0, 8} of its 16-lane half and column pairs 8i + 2(t%4) of each
+    // chunk, so a per-column value read from shared memory serves 2 rows.
+    // Chunk reads are pipelined one ahead.
+    const int et = threadIdx.x - 64;         // 0..511
     const int quad = warp & 3;               // TMEM lane quadrant this warp may access
-    constexpr int NPART = kEpiThreads / 128; // warps per lane quadrant
-    const int part = (warp - 2) >> 2;        // which half of the chunks
+    const int part = (warp - 2) >> 2;        // 0..3
+    const int rh = part & 1;                 // row half of the quadrant
+    constexpr int NCP = 2;                   // column parts per row
+    const int ch = part >> 1;                // column part
     const int g4 = lane >> 2;                // row within each 8-row group
     const int cp = lane & 3;                 // column pair within each 8-column group
-    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32 + rh * 16) << 16;
     constexpr int NCHUNK = N / 32;
-    static_assert(NCHUNK % NPART == 0, "chunks split evenly between the parts");
-    constexpr int CH = NCHUNK / NPART;       // chunks per warp
+    static_assert(NCHUNK % NCP == 0, "chunks split evenly between the column parts");
+    constexpr int CH = NCHUNK / NCP;         // chunks per warp
     constexpr bool kBf16Out = OUT == static_cast<int>(OutKind::kBf16);
     const int norm = p.norm;
     const float eps = p.eps;
-    int rowk[4];
+    int rowk[2];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) rowk[k] = quad * 32 + g4 + 8 * k;
+    for (int k = 0; k < 2; ++k) rowk[k] = quad * 32 + rh * 16 + g4 + 8 * k;
 
-    // activation scales of a tile's four rows of this thread (per-tensor
+    // activation scales of a tile's two rows of this thread (per-tensor
     // weight scales fold in); loaded one tile ahead to hide the latency
-    auto row_scales = [&](int tile, float (&out)[4]) {
+    auto row_scales = [&](int tile, float (&out)[2]) {
       const int g = group_of(p, tile);
       const GemmGroup& G = p.g[g];
       const int m0 = (tile - G.tile_begin) * kBM;
       const float swc = (G.sw != nullptr && !G.sw_per_row) ? G.sw[0] : 1.0f;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < 2; ++k) {
         const int64_t m = static_cast<int64_t>(m0) + rowk[k];
         float sx = 1.0f;
         if (G.sx != nullptr) sx = G.sx_per_row ? (m < G.M ? G.sx[m] : 0.0f) : G.sx[0];
@@ -393,39 +399,42 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
     auto vec2 = [&](const float* vec, int c0, int i) {
       return *reinterpret_cast<const float2*>(vec + c0 + 8 * i + 2 * cp);
     };
-    auto acc2 = [&](const uint32_t (&ra)[16], const uint32_t (&rb)[16], int k, int i) {
-      const uint32_t* r = k < 2 ? ra : rb;
-      const int o = 4 * i + 2 * (k & 1);
+    auto acc2 = [&](const uint32_t (&r)[16], int k, int i) {
+      const int o = 4 * i + 2 * k;
       return make_float2(__uint_as_float(r[o]), __uint_as_float(r[o + 1]));
     };
-    // Runs fn(ra, rb, c) over this warp's chunks, the TMEM read of chunk
-    // s + 1 in flight while chunk s is processed.
+    // Runs fn(r, c) over this warp's chunks, the TMEM read of chunk s + 1 in
+    // flight while chunk s is processed.
     auto for_chunks = [&](uint32_t t_base, auto&& fn) {
-      uint32_t ra[2][16], rb[2][16];
-      tmem_ld_16x256b_x4(t_base + part * 32, ra[0]);
-      tmem_ld_16x256b_x4(t_base + (16u << 16) + part * 32, rb[0]);
+      uint32_t r[2][16];
+      tmem_ld_16x256b_x4(t_base + ch * 32, r[0]);
       tmem_ld_wait();
-      reg_fence(ra[0]);
-      reg_fence(rb[0]);
+      reg_fence(r[0]);
 #pragma unroll
       for (int s = 0; s < CH; ++s) {
-        const int c = part + NPART * s;
-        if (s + 1 < CH) {
-          tmem_ld_16x256b_x4(t_base + (c + NPART) * 32, ra[(s + 1) & 1]);
-          tmem_ld_16x256b_x4(t_base + (16u << 16) + (c + NPART) * 32, rb[(s + 1) & 1]);
-        }
-        fn(ra[s & 1], rb[s & 1], c);
+        const int c = ch + NCP * s;
+        if (s + 1 < CH) tmem_ld_16x256b_x4(t_base + (c + NCP) * 32, r[(s + 1) & 1]);
+        fn(r[s & 1], c);
         if (s + 1 < CH) {
           tmem_ld_wait();
-          reg_fence(ra[(s + 1) & 1]);
-          reg_fence(rb[(s + 1) & 1]);
+          reg_fence(r[(s + 1) & 1]);
         }
       }
+    };
+    // v = acc * sx (* sw) + b for the pair; SWV: per-column weight scales
+    // (rowwise W); otherwise they are folded into the row factor
+    auto vpair = [&](auto swv_tag, const uint32_t (&r)[16], int k, int i, float2 sx2, float2 sw, float2 b) {
+      constexpr bool SWV = decltype(swv_tag)::value;
+      if constexpr (SWV)
+        return __ffma2_rn(__fmul2_rn(acc2(r, k, i), sx2), sw, b);
+      else
+        return __ffma2_rn(acc2(r, k, i), sx2, b);
     };
 
     int cur_group = -1;
     int local = 0;
-    float sx_next[4] = {1.f, 1.f, 1.f, 1.f};
+    bool has_swv = false, affine = false;
+    float sx_next[2] = {1.f, 1.f};
     if (cid < p.total_tiles) row_scales(cid, sx_next);
     for (int tile = cid; tile < p.total_tiles; tile += ncl, ++local) {
       const int g = group_of(p, tile);
@@ -440,22 +449,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
           vec_g[n] = (G.gamma == nullptr || !normed) ? 1.0f : bf16_to_f(G.gamma[gn]);
           vec_be[n] = (G.beta == nullptr || norm != kNormLayer) ? 0.0f : bf16_to_f(G.beta[gn]);
         }
+        has_swv = G.sw != nullptr && G.sw_per_row;
+        affine = normed && (G.gamma != nullptr || (G.beta != nullptr && norm == kNormLayer));
         named_bar_sync(kEpiBar, kEpiThreads);
         cur_group = g;
       }
-      float sxr[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) sxr[k] = sx_next[k];
+      float sxr[2] = {sx_next[0], sx_next[1]};
       const int m0 = (tile - G.tile_begin) * kBM;
       // output row addresses and validity, once per tile
       const int64_t Mg = G.M;
-      uint8_t* rowp[4];
-      uint32_t ok[4];
+      uint8_t* rowp[2];
+      uint32_t ok[2];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < 2; ++k) {
         const int64_t m = static_cast<int64_t>(m0) + rowk[k];
         ok[k] = m < Mg ? 1u : 0u;
-        rowp[k] = static_cast<uint8_t*>(G.y) + (m * NG + col0 + 2 * cp) * (kBf16Out ? 2 : 4);
+        // bf16: the 4 lanes of a row group store 16 contiguous bytes each
+        // after a transpose; fp32: column pairs straight from registers
+        rowp[k] = static_cast<uint8_t*>(G.y) + (m * NG + col0 + (kBf16Out ? 8 : 2) * cp) * (kBf16Out ? 2 : 4);
       }
       const int buf = NBUF == 2 ? (local & 1) : 0;
       const uint32_t use = NBUF == 2 ? (local >> 1) : local;
@@ -467,72 +478,77 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
       tc_fence_after();
       if (tile + ncl < p.total_tiles) row_scales(tile + ncl, sx_next);
       const uint32_t t_base = tmem_base + lane_addr + static_cast<uint32_t>(buf * N);
+      const float2 sx2[2] = {dup2(sxr[0]), dup2(sxr[1])};
 
       // pass 1: row statistics of v = acc * sx * sw + b
-      float mean[4] = {0.f, 0.f, 0.f, 0.f}, m2[4] = {0.f, 0.f, 0.f, 0.f};
-      if (norm == kNormLayer) {
-        // shifted sums: with K the mean of the row's first 8-value piece,
-        // s1 += v - K and s2 += (v - K)^2; no division, little cancellation
-        float shift[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-        for_chunks(t_base, [&](const uint32_t (&ra)[16], const uint32_t (&rb)[16], int c) {
-          const int c0 = c * 32;
-          float2 sw[4], b[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            sw[i] = vec2(vec_sw, c0, i);
-            b[i] = vec2(vec_b, c0, i);
-          }
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            float2 v[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) v[i] = __ffma2_rn(__fmul2_rn(acc2(ra, rb, k, i), dup2(sxr[k])), sw[i], b[i]);
-            if (c == part) {
-              const float2 t = __fadd2_rn(__fadd2_rn(v[0], v[1]), __fadd2_rn(v[2], v[3]));
-              shift[k] = (t.x + t.y) * 0.125f;
-            }
-            const float2 nk = dup2(-shift[k]);
-            float2 a1 = make_float2(0.f, 0.f), a2 = make_float2(0.f, 0.f);
+      float mean[2] = {0.f, 0.f}, m2[2] = {0.f, 0.f};
+      auto stats_pass = [&](auto swv_tag) {
+        if (norm == kNormLayer) {
+          // shifted sums: with K the mean of the row's first 8-value piece,
+          // s1 += v - K and s2 += (v - K)^2; no division, little cancellation
+          float shift[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};
+          for_chunks(t_base, [&](const uint32_t (&r)[16], int c) {
+            const int c0 = c * 32;
+            float2 sw[4], b[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const float2 d = __fadd2_rn(v[i], nk);
-              a1 = __fadd2_rn(a1, d);
-              a2 = __ffma2_rn(d, d, a2);
+              if constexpr (decltype(swv_tag)::value) sw[i] = vec2(vec_sw, c0, i);
+              b[i] = vec2(vec_b, c0, i);
             }
-            s1[k] += a1.x + a1.y;
-            m2[k] += a2.x + a2.y;
-          }
-        });
-        constexpr float kInvMe = 1.0f / (8.0f * CH);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float d = s1[k] * kInvMe;
-          mean[k] = shift[k] + d;
-          m2[k] = fmaxf(m2[k] - s1[k] * d, 0.0f);
+            for (int k = 0; k < 2; ++k) {
+              float2 v[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) v[i] = vpair(swv_tag, r, k, i, sx2[k], sw[i], b[i]);
+              if (c == ch) {
+                const float2 t = __fadd2_rn(__fadd2_rn(v[0], v[1]), __fadd2_rn(v[2], v[3]));
+                shift[k] = (t.x + t.y) * 0.125f;
+              }
+              const float2 nk = dup2(-shift[k]);
+              float2 a1 = make_float2(0.f, 0.f), a2 = make_float2(0.f, 0.f);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float2 d = __fadd2_rn(v[i], nk);
+                a1 = __fadd2_rn(a1, d);
+                a2 = __ffma2_rn(d, d, a2);
+              }
+              s1[k] += a1.x + a1.y;
+              m2[k] += a2.x + a2.y;
+            }
+          });
+          constexpr float kInvMe = 1.0f / (8.0f * CH);
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const float d = s1[k] * kInvMe;
+            mean[k] = shift[k] + d;
+            m2[k] = fmaxf(m2[k] - s1[k] * d, 0.0f);
+          }
+        } else if (norm == kNormRms) {
+          for_chunks(t_base, [&](const uint32_t (&r)[16], int c) {
+            const int c0 = c * 32;
+            float2 sw[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              if constexpr (decltype(swv_tag)::value) sw[i] = vec2(vec_sw, c0, i);
+              b[i] = vec2(vec_b, c0, i);
+            }
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              float2 q = make_float2(0.f, 0.f);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float2 v = vpair(swv_tag, r, k, i, sx2[k], sw[i], b[i]);
+                q = __ffma2_rn(v, v, q);
+              }
+              m2[k] += q.x + q.y;
+            }
+          });
         }
-      } else if (norm == kNormRms) {
-        for_chunks(t_base, [&](const uint32_t (&ra)[16], const uint32_t (&rb)[16], int c) {
-          const int c0 = c * 32;
-          float2 sw[4], b[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            sw[i] = vec2(vec_sw, c0, i);
-            b[i] = vec2(vec_b, c0, i);
-          }
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            float2 q = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float2 v = __ffma2_rn(__fmul2_rn(acc2(ra, rb, k, i), dup2(sxr[k])), sw[i], b[i]);
-              q = __ffma2_rn(v, v, q);
-            }
-            m2[k] += q.x + q.y;
-          }
-        });
-      }
+      };
+      if (has_swv) stats_pass(std::true_type{});
+      else stats_pass(std::false_type{});
 
-      float rstd[4] = {1.f, 1.f, 1.f, 1.f};
+      float rstd[2] = {1.f, 1.f};
       if (norm != kNormNone) {
         // merge the 4 lanes of a row group (equal counts) with an ordered
         // expression so all four end bit-identical
@@ -542,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
           const float half_n = 4.0f * CH * static_cast<float>(off);   // n_a n_b / (n_a + n_b)
           const bool lo_side = (lane & off) == 0;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
+          for (int k = 0; k < 2; ++k) {
             const float om = __shfl_xor_sync(0xffffffffu, mean[k], off);
             const float oq = __shfl_xor_sync(0xffffffffu, m2[k], off);
             const float lm = lo_side ? mean[k] : om, hm = lo_side ? om : mean[k];
@@ -554,13 +570,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
         }
         if (cp == 0) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) stat_part[part * kBM + rowk[k]] = make_float2(mean[k], m2[k]);
+          for (int k = 0; k < 2; ++k) stat_part[ch * kBM + rowk[k]] = make_float2(mean[k], m2[k]);
         }
         named_bar_sync(kEpiBar, kEpiThreads);
-        // the two parts hold N/2 elements each
-        float qrow[4];
+        // the two column parts hold N/2 elements each
+        float qrow[2];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < 2; ++k) {
           const float2 lo = stat_part[rowk[k]];
           const float2 hi = stat_part[kBM + rowk[k]];
           const float delta = hi.x - lo.x;
@@ -569,14 +585,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
         }
         if constexpr (CL > 1) {
           // exchange (mean, M2) of this CTA's N columns with the cluster:
-          // part-0 lanes with cp == 0 hold one row each and write it into
-          // every CTA's slot [buffer][rank][row], then arrive there
+          // column-part-0 lanes with cp == 0 hold one row each and write it
+          // into every CTA's slot [buffer][rank][row], then arrive there
           const int cb = local & 1;
-          if (part == 0 && cp == 0) {
+          if (ch == 0 && cp == 0) {
 #pragma unroll
             for (int j = 0; j < CL; ++j) {
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
+              for (int k = 0; k < 2; ++k) {
                 const uint32_t a = smem_u32(&cl_stats[(cb * CL + static_cast<int>(rank)) * kBM + rowk[k]]);
                 st_cluster_f32x2(mapa_shared(a, j), mean[k], qrow[k]);
               }
@@ -589,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
           if (*abort_flag) break;
           // merge the CTAs' statistics in rank order (N elements each)
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
+          for (int k = 0; k < 2; ++k) {
             float mA = 0.f, qA = 0.f;
 #pragma unroll
             for (int j = 0; j < CL; ++j) {
@@ -611,29 +627,56 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
           }
         }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) rstd[k] = rsqrtf(qrow[k] * (1.0f / NG) + eps);
+        for (int k = 0; k < 2; ++k) rstd[k] = rsqrtf(qrow[k] * (1.0f / NG) + eps);
       }
+      // y = v * rstd - mean * rstd, then * gamma + beta when present
+      const float2 rstd2[2] = {dup2(rstd[0]), dup2(rstd[1])};
+      const float2 nmr2[2] = {dup2(-mean[0] * rstd[0]), dup2(-mean[1] * rstd[1])};
 
-      // pass 2: y = ((v - mean) * rstd) * gamma + beta, stored straight from
-      // registers (column pairs; the rows of a ragged last tile are masked)
-      for_chunks(t_base, [&](const uint32_t (&ra)[16], const uint32_t (&rb)[16], int c) {
-        const int c0 = c * 32;
+      // pass 2: normalize and store from registers (rows of a ragged last
+      // tile are masked).  bf16: a chunk's 4 column pairs per row are packed,
+      // transposed across the 4 lanes of the row group, and stored as one
+      // 16-byte vector per lane (64 contiguous bytes per row per warp store)
+      auto out_pass = [&](auto swv_tag, auto aff_tag) {
+        for_chunks(t_base, [&](const uint32_t (&r)[16], int c) {
+          const int c0 = c * 32;
+          [[maybe_unused]] uint32_t pk[2][4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 sw = vec2(vec_sw, c0, i), b = vec2(vec_b, c0, i);
-          const float2 gm = vec2(vec_g, c0, i), be = vec2(vec_be, c0, i);
-          const int col = c0 + 8 * i;
+          for (int i = 0; i < 4; ++i) {
+            float2 sw = make_float2(1.f, 1.f), gm = make_float2(1.f, 1.f), be = make_float2(0.f, 0.f);
+            if constexpr (decltype(swv_tag)::value) sw = vec2(vec_sw, c0, i);
+            const float2 b = vec2(vec_b, c0, i);
+            if constexpr (decltype(aff_tag)::value) {
+              gm = vec2(vec_g, c0, i);
+              be = vec2(vec_be, c0, i);
+            }
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float2 v = __ffma2_rn(__fmul2_rn(acc2(ra, rb, k, i), dup2(sxr[k])), sw, b);
-            const float2 y = __ffma2_rn(__fmul2_rn(__fadd2_rn(v, dup2(-mean[k])), dup2(rstd[k])), gm, be);
-            if (kBf16Out)
-              st_global_pred_b32(rowp[k] + col * 2, pack_bf16x2(y.x, y.y), ok[k]);
-            else
-              st_global_pred_v2f32(rowp[k] + col * 4, y, ok[k]);
+            for (int k = 0; k < 2; ++k) {
+              const float2 v = vpair(swv_tag, r, k, i, sx2[k], sw, b);
+              float2 y = __ffma2_rn(v, rstd2[k], nmr2[k]);
+              if constexpr (decltype(aff_tag)::value) y = __ffma2_rn(y, gm, be);
+              if constexpr (kBf16Out)
+                pk[k][i] = pack_bf16x2(y.x, y.y);
+              else
+                st_global_pred_v2f32(rowp[k] + (c0 + 8 * i) * 4, y, ok[k]);
+            }
           }
-        }
-      });
+          if constexpr (kBf16Out) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              transpose4_lanes(pk[k], cp);
+              st_global_pred_v4b32(rowp[k] + c0 * 2, pk[k], ok[k]);
+            }
+          }
+        });
+      };
+      if (has_swv) {
+        if (affine) out_pass(std::true_type{}, std::true_type{});
+        else out_pass(std::true_type{}, std::false_type{});
+      } else {
+        if (affine) out_pass(std::false_type{}, std::true_type{});
+        else out_pass(std::false_type{}, std::false_type{});
+      }
       // all reads of this accumulator are done: hand it back to the MMA warp
       tc_fence_before();
       __syncwarp();

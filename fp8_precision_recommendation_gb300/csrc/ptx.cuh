@@ -361,6 +361,36 @@ __device__ __forceinline__ void st_global_pred_v2f32(void* ptr, float2 v, uint32
       : "memory");
 }
 
+__device__ __forceinline__ void st_global_pred_v4b32(void* ptr, const uint32_t (&v)[4], uint32_t pred) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %5, 0;\n\t@p st.global.v4.b32 [%0], {%1, %2, %3, %4};\n\t}" ::"l"(ptr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(pred)
+      : "memory");
+}
+
+// Transposes a 4 x 4 block of 32-bit values held by the 4 lanes of a group
+// (lane bits 0-1 = q): on return, element j of lane q is what element q of
+// lane j was.  Two butterfly stages, each swapping one bit of the lane index
+// with the same bit of the element index.
+__device__ __forceinline__ void transpose4_lanes(uint32_t (&x)[4], int q) {
+  const bool b0 = (q & 1) != 0;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t send = b0 ? x[2 * h] : x[2 * h + 1];
+    const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 1);
+    if (b0) x[2 * h] = recv;
+    else x[2 * h + 1] = recv;
+  }
+  const bool b1 = (q & 2) != 0;
+#pragma unroll
+  for (int l = 0; l < 2; ++l) {
+    const uint32_t send = b1 ? x[l] : x[l + 2];
+    const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 2);
+    if (b1) x[l] = recv;
+    else x[l + 2] = recv;
+  }
+}
+
 // -------------------------------------------------------------- conversions
 // Two fp32 -> two E4M3 codes, round to nearest even, saturating to +-448
 // (NaN stays NaN).  `lo` lands in the low byte.
