@@ -37,6 +37,7 @@
 
 #include "loka_internal.h"
 #include "ptx.cuh"
+#include "quant_math.cuh"
 
 namespace loka {
 
@@ -46,8 +47,11 @@ constexpr int kBM = 128;                 // rows per tile (= TMEM lanes)
 constexpr int kSliceBytes = 128;         // bytes of K per stage per row
 constexpr uint32_t kABytes = kBM * kSliceBytes;
 constexpr int kTmemCols = 512;
-constexpr int kThreads = 576;
-constexpr int kEpiThreads = 512;
+constexpr int kQuantWarps = 8;           // kRowQuantX: warps 18..25 quantize X
+constexpr int kQuantWarp0 = 18;
+constexpr int kSxSlots = 4;              // kRowQuantX: row-scale slots (tile % 4)
+constexpr int kOpRowQuantX = static_cast<int>(OperandKind::kRowQuantX);
+__host__ __device__ constexpr int threads_for(int op) { return op == kOpRowQuantX ? 576 + 32 * kQuantWarps : 576; }
 constexpr int kEpiBar = 1;               // named barrier id for the epilogue warps
 constexpr int kMaxStages = 8;
 constexpr size_t kSmemLimit = 227 * 1024;
@@ -56,11 +60,14 @@ constexpr size_t kResidentWLimit = 128 * 1024;
 // Shared-memory carve-up (all offsets from a 1024-byte-aligned base):
 //   ring     stages x (A slice [| B slice])
 //   w        resident W: K/KE slices of N rows x 128 bytes (when resident)
-//   vectors  4 x N fp32 (weight scale, bias, gamma, beta)
-//   stats    4 x 128 float2 partial row statistics
+//   vectors  2 teams x 4 x N fp32 (weight scale, bias, gamma, beta)
+//   stats    clusters: 2 x CL x 128 float2 row statistics of the CTAs
+//   sx       kRowQuantX: 4 x 128 fp32 row scales of X written by the quantizing warps
 //   barriers
+// kRowQuantX keeps whole quantized A tiles (128 rows x K bytes, as K/128
+// swizzled 16 KB slices) in the ring instead of K slices.
 struct Layout {
-  uint32_t stage_bytes, ring, w, vec, stats, bars, total;
+  uint32_t stage_bytes, ring, w, vec, stats, sxr, bars, total;
 };
 
 // MX scale blocks: 512 bytes per 128 rows per 128-element K slice.
@@ -68,24 +75,26 @@ constexpr uint32_t kSfBlock = 512;
 __host__ __device__ constexpr int sfb_blocks(int N) { return (N + 127) / 128; }
 
 __host__ __device__ inline Layout make_layout(int N, int K, int elem_bytes, bool resident, int stages, bool mx,
-                                              int cl = 1) {
+                                              int cl = 1, bool fused = false) {
   Layout L;
   const uint32_t b_slice = static_cast<uint32_t>(N) * kSliceBytes;
   const uint32_t sfa = mx ? kSfBlock : 0u;
   const uint32_t sfb = mx ? kSfBlock * sfb_blocks(N) : 0u;
-  // stage: [A slice][B slice, streamed W][A scales][B scales, streamed W]
-  L.stage_bytes = kABytes + (resident ? 0u : b_slice) + sfa + (resident ? 0u : sfb);
+  // stage: [A slice][B slice, streamed W][A scales][B scales, streamed W];
+  // fused: one whole A tile
+  L.stage_bytes = fused ? static_cast<uint32_t>(kBM) * K : kABytes + (resident ? 0u : b_slice) + sfa + (resident ? 0u : sfb);
   L.ring = 0;
   L.w = L.ring + static_cast<uint32_t>(stages) * L.stage_bytes;
   const int nkb = K * elem_bytes / kSliceBytes;
   // resident W: [nkb B slices][nkb x B scale blocks]
   const uint32_t w_bytes = resident ? static_cast<uint32_t>(nkb) * (b_slice + sfb) : 0u;
   L.vec = L.w + w_bytes;
-  L.stats = L.vec + 4u * N * sizeof(float);
-  // [4][128] partial row statistics, then [2][cluster][128] row statistics of
-  // the cluster's CTAs (written remotely, double-buffered by tile parity)
-  L.bars = L.stats + 4u * kBM * sizeof(float2) + (cl > 1 ? 2u * cl * kBM * sizeof(float2) : 0u);
-  L.total = L.bars + 256;
+  L.stats = L.vec + 2u * 4u * N * sizeof(float);
+  // [2][cluster][128] row statistics of the cluster's CTAs (written
+  // remotely, double-buffered by tile parity)
+  L.sxr = L.stats + (cl > 1 ? 2u * cl * kBM * sizeof(float2) : 0u);
+  L.bars = L.sxr + (fused ? static_cast<uint32_t>(kSxSlots * kBM * sizeof(float)) : 0u);
+  L.total = L.bars + 512;
   return L;
 }
 
@@ -99,13 +108,71 @@ __device__ __forceinline__ float bf16_to_f(uint16_t h) { return __uint_as_float(
 
 __device__ __forceinline__ float2 dup2(float a) { return make_float2(a, a); }
 
+// kRowQuantX: quantizes the 128 rows of one tile of bf16 X (K = 256 V) into
+// the A operand layout, per row like quant_rows_kernel (same arithmetic):
+// amax over the row, scale = amax/448, codes = E4M3(x * 448/amax).  Warp qw
+// takes rows qw + 8j; a lane holds 8-element vectors i = 0..V-1 of a row
+// (elements 8(32i + lane) ..), loaded three rows ahead.  The codes go to
+// shared memory as K/128 slices of 128 rows x 128 bytes with the 128-byte
+// swizzle the MMA descriptors expect (16-byte chunk c of row r at chunk
+// c ^ (r % 8)); rows past M become zeros with scale 1.
+template <int V>
+__device__ __forceinline__ void quant_tile(const uint16_t* __restrict__ xb, int64_t M, int64_t m0, uint8_t* A,
+                                           float* sxs, int qw, int lane) {
+  constexpr int K = 256 * V;
+  constexpr int R = kBM / kQuantWarps;   // rows per warp
+  constexpr int P = 3;                   // rows in flight ahead of the one being cast
+  uint4 v[P + 1][V];
+  auto load = [&](int j, uint4 (&dst)[V]) {
+    const int64_t m = m0 + qw + kQuantWarps * j;
+    const uint4* src = reinterpret_cast<const uint4*>(xb + m * K);
+#pragma unroll
+    for (int i = 0; i < V; ++i) dst[i] = m < M ? __ldcs(src + i * 32 + lane) : make_uint4(0, 0, 0, 0);
+  };
+#pragma unroll
+  for (int j = 0; j < P; ++j) load(j, v[j]);
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    if (j + P < R) load(j + P, v[(j + P) % (P + 1)]);
+    const uint4(&x)[V] = v[j % (P + 1)];
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) m = abs_max8(x[i], m);
+    m = warp_max(m);
+    float inv, scale;
+    row_scales(m, inv, scale);
+    const int r = qw + kQuantWarps * j;
+    uint8_t* row = A + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int e = 32 * i + lane;       // 8-byte unit along K
+      const int c = (e & 15) >> 1;       // 16-byte chunk within the slice row
+      *reinterpret_cast<uint2*>(row + (e >> 4) * kABytes + ((c ^ (r & 7)) << 4) + ((e & 1) << 3)) = cast8(x[i], inv);
+    }
+    if (lane == 0) sxs[r] = scale;
+  }
+}
+
+// kRowQuantX: asks L2 for the bf16 rows of `tile` ahead of their use.
+__device__ __forceinline__ void prefetch_x_tile(const GemmParams& p, int tile) {
+  const int g = group_of(p, tile);
+  const GemmGroup& G = p.g[g];
+  const int64_t m0 = static_cast<int64_t>(tile - G.tile_begin) * kBM;
+  const int64_t rows = G.M - m0 < kBM ? G.M - m0 : kBM;
+  const uint8_t* src = reinterpret_cast<const uint8_t*>(G.xb + m0 * p.K);
+  const int64_t bytes = rows * p.K * 2;
+  constexpr int64_t kPiece = 32 * 1024;
+  for (int64_t o = 0; o < bytes; o += kPiece)
+    prefetch_l2_bulk(src + o, static_cast<uint32_t>(bytes - o < kPiece ? bytes - o : kPiece));
+}
+
 // N = the columns this CTA owns (<= 256); CL = CTAs per cluster sharing each
 // 128-row tile (the layer's output has N * CL columns; CTA r owns columns
 // [r N, r N + N) and the CTAs of a cluster merge their row statistics
 // through distributed shared memory, so a row wider than one CTA's tensor
 // memory is still normalized in the epilogue).
 template <int N, int CL, int OP, int OUT, bool RESIDENT>
-__global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(threads_for(OP), 1) gemm_norm_kernel(const __grid_constant__ GemmParams p) {
   static_assert(N <= 256, "one MMA per K step");
   constexpr int NG = N * CL;                        // columns of the whole output row
   constexpr int SF_COLS_MAX = OP == static_cast<int>(OperandKind::kMxE4M3) ? kMaxStages * (4 + 4 * sfb_blocks(N)) : 0;
@@ -115,6 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
   constexpr int N_SPLIT = N / N_MMA;
   constexpr bool kBf16Op = OP == static_cast<int>(OperandKind::kBf16);
   constexpr bool kMx = OP == static_cast<int>(OperandKind::kMxE4M3);
+  constexpr bool kFused = OP == kOpRowQuantX;
+  static_assert(!kFused || (RESIDENT && CL == 1), "in-kernel X quantization keeps W resident, one CTA per tile");
   constexpr int NSFB = sfb_blocks(N);
   constexpr uint32_t SFB_BYTES = kMx ? kSfBlock * NSFB : 0u;
   constexpr uint32_t SF_COLS = kMx ? 4 + 4 * NSFB : 0;    // TMEM columns of one stage's scales
@@ -126,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
 
   const int stages = p.stages;
   const int num_kb = p.K / KE;
-  const Layout L = make_layout(N, p.K, EB, RESIDENT, stages, kMx, CL);
+  const Layout L = make_layout(N, p.K, EB, RESIDENT, stages, kMx, CL, kFused);
   const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
   const int col0 = static_cast<int>(rank) * N;      // first output column of this CTA
   const int cid = static_cast<int>(blockIdx.x) / CL;
@@ -141,12 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
   const bool misaligned = (smem_u32(smem) & 1023u) != 0;
   uint8_t* ring = smem + L.ring;
   uint8_t* wres = smem + L.w;
-  float* vec_sw = reinterpret_cast<float*>(smem + L.vec);
-  float* vec_b = vec_sw + N;
-  float* vec_g = vec_b + N;
-  float* vec_be = vec_g + N;
-  float2* stat_part = reinterpret_cast<float2*>(smem + L.stats);   // [4][128] partial row statistics
-  float2* cl_stats = stat_part + 4 * kBM;                           // [2][CL][128] cluster row statistics
+  float* vec_base = reinterpret_cast<float*>(smem + L.vec);        // [2 teams][4][N]
+  float2* cl_stats = reinterpret_cast<float2*>(smem + L.stats);     // [2][CL][128] cluster row statistics
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* full = bars;
   uint64_t* empty = full + kMaxStages;
@@ -156,7 +221,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
   uint64_t* w_full = mma_done + 1;
   uint64_t* w_free = w_full + 1;
   uint64_t* cl_bar = w_free + 1;                                    // [2] cluster statistics arrivals
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cl_bar + 2);
+  uint64_t* sx_full = cl_bar + 2;                                   // [4] kRowQuantX row scales written
+  uint64_t* cl_free = sx_full + kSxSlots;                           // [2] cluster statistics buffers read
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cl_free + 2);
+  float* sx_ring = reinterpret_cast<float*>(smem + L.sxr);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -164,20 +232,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
+      // kRowQuantX: an A tile is full once every quantizing warp has arrived
+      mbar_init(smem_u32(&full[s]), kFused ? kQuantWarps : 1);
       mbar_init(smem_u32(&empty[s]), 1);
     }
+    for (int s = 0; s < kSxSlots; ++s) mbar_init(smem_u32(&sx_full[s]), kQuantWarps);
     for (int b = 0; b < NBUF; ++b) {
       mbar_init(smem_u32(&tfull[b]), 1);
-      mbar_init(smem_u32(&tempty[b]), kEpiThreads / 32);
+      mbar_init(smem_u32(&tempty[b]), 8);   // the eight warps of the team that owns buffer b
     }
     mbar_init(smem_u32(mma_done), 1);
     mbar_init(smem_u32(w_full), 1);
     mbar_init(smem_u32(w_free), 1);
-    // each of the cluster's CTAs sends its statistics from 4 warps x 8 lanes
-    // the lanes with ch == 0 and cp == 0 (8 warps x 8 lanes) of every CTA
+    // a tile's statistics come from the cp == 0 lanes (8 warps x 8 lanes)
+    // of every CTA of the cluster; its buffer is freed by 8 warps per CTA
     mbar_init(smem_u32(&cl_bar[0]), 64 * CL);
     mbar_init(smem_u32(&cl_bar[1]), 64 * CL);
+    mbar_init(smem_u32(&cl_free[0]), 8 * CL);
+    mbar_init(smem_u32(&cl_free[1]), 8 * CL);
     *abort_flag = misaligned ? 1 : 0;
     if (misaligned) atomicOr(p.status, kErrMisaligned);
     fence_barrier_init();
@@ -185,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
   if (warp == 0 && lane == 0) {
     for (int g = 0; g < p.num_groups; ++g) {
       if (p.g[g].M == 0) continue;   // no tiles, descriptors not encoded
-      tma_prefetch_desc(&p.g[g].tm_a);
+      if (!kFused) tma_prefetch_desc(&p.g[g].tm_a);
       tma_prefetch_desc(&p.g[g].tm_b);
       tma_prefetch_desc(&p.g[g].tm_y);
     }
@@ -240,7 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
           ++w_loads;
           cur_group = g;
         }
-        for (int kb = 0; kb < num_kb; ++kb) {
+        // kRowQuantX: the quantizing warps fill A; only W is loaded here
+        for (int kb = 0; kb < (kFused ? 0 : num_kb); ++kb) {
           if (!wait_parity(wd, smem_u32(&empty[stage]), phase ^ 1u, kErrProducerWait)) {
             ok = false;
             break;
@@ -305,7 +378,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
         if (!wait_parity(wd, smem_u32(&tempty[buf]), (use & 1u) ^ 1u, kErrMmaWait)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * N);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        if constexpr (kFused) {
+          // the whole quantized A tile, then its K slices against resident W
+          const int slot = local % stages;
+          if (!wait_parity(wd, smem_u32(&full[slot]), static_cast<uint32_t>(local / stages) & 1u, kErrMmaWait)) break;
+          tc_fence_after();
+          const uint32_t a_tile = smem_u32(ring + static_cast<size_t>(slot) * L.stage_bytes);
+          for (int kb = 0; kb < num_kb; ++kb) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t adesc = sdesc_k128_sw128(a_tile + kb * kABytes + k * 32);
+              const uint64_t bdesc = sdesc_k128_sw128(smem_u32(wres + kb * B_SLICE) + k * 32);
+              mma_f8f6f4(d_tmem, adesc, bdesc, IDESC, (kb | k) != 0 ? 1u : 0u);
+            }
+          }
+          mma_commit(smem_u32(&empty[slot]));   // A tile free once these MMAs finish
+        }
+        for (int kb = 0; kb < (kFused ? 0 : num_kb); ++kb) {
           if (!wait_parity(wd, smem_u32(&full[stage]), phase, kErrMmaWait)) {
             ok = false;
             break;
@@ -354,29 +443,69 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
       mma_commit(smem_u32(mma_done));
       wait_parity_drain(wd, smem_u32(mma_done), 0);
     }
+  } else if (kFused && warp >= kQuantWarp0) {
+    // ------------------------------------------------- X quantization (fused)
+    // Each tile's bf16 rows are requested into L2 two tiles ahead, then read
+    // once, quantized per row and written to the A tile in shared memory.
+    const int qw = warp - kQuantWarp0;
+    if (qw == 0 && lane == 0) {
+      if (cid < p.total_tiles) prefetch_x_tile(p, cid);
+      if (cid + ncl < p.total_tiles) prefetch_x_tile(p, cid + ncl);
+    }
+    int local = 0;
+    for (int tile = cid; tile < p.total_tiles; tile += ncl, ++local) {
+      if (qw == 0 && lane == 0 && tile + 2 * ncl < p.total_tiles) prefetch_x_tile(p, tile + 2 * ncl);
+      const GemmGroup& G = p.g[group_of(p, tile)];
+      const int64_t m0 = static_cast<int64_t>(tile - G.tile_begin) * kBM;
+      const int slot = local % stages;
+      // one lane waits, the warp follows its verdict
+      int okw = 1;
+      if (lane == 0)
+        okw = wait_parity(wd, smem_u32(&empty[slot]), (static_cast<uint32_t>(local / stages) & 1u) ^ 1u,
+                          kErrProducerWait) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, okw, 0)) break;
+      uint8_t* a_tile = ring + static_cast<size_t>(slot) * L.stage_bytes;
+      float* sxs = sx_ring + (local % kSxSlots) * kBM;
+      if (p.K == 512) quant_tile<2>(G.xb, G.M, m0, a_tile, sxs, qw, lane);
+      else quant_tile<1>(G.xb, G.M, m0, a_tile, sxs, qw, lane);
+      // the generic-proxy stores must be visible to the tensor core's reads
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&sx_full[local % kSxSlots]));
+        mbar_arrive(smem_u32(&full[slot]));
+      }
+    }
   } else {
     // ------------------------------------------------------------ epilogue
-    // Sixteen warps, four per TMEM lane quadrant: warp (quad q, row half h,
-    // column part w) covers rows 32q + 16h .. 32q + 16h + 15 and the 32-column
-    // chunks c = w + 2s.  The 16x256b load shape gives thread t rows
-    // t/4 + {0, 8} of its 16-lane half and column pairs 8i + 2(t%4) of each
-    // chunk, so a per-column value read from shared memory serves 2 rows.
-    // Chunk reads are pipelined one ahead.
-    const int et = threadIdx.x - 64;         // 0..511
-    const int quad = warp & 3;               // TMEM lane quadrant this warp may access
-    const int part = (warp - 2) >> 2;        // 0..3
-    const int rh = part & 1;                 // row half of the quadrant
-    constexpr int NCP = 2;                   // column parts per row
-    const int ch = part >> 1;                // column part
-    const int g4 = lane >> 2;                // row within each 8-row group
-    const int cp = lane & 3;                 // column pair within each 8-column group
+    // Sixteen warps in two teams of eight.  Team e takes the tiles whose
+    // local index is e (mod 2), i.e. accumulator buffer e, so two tiles are
+    // normalized at once (with one accumulator buffer team 0 takes every
+    // tile).  In a team, warp (quad q, row half h) owns rows
+    // 32q + 16h .. 32q + 16h + 15 of the tile over all of this CTA's N
+    // columns, so its row statistics need only 4-lane shuffles and no
+    // barrier couples the warps of a tile.  The 16x256b load shape gives
+    // thread t rows t/4 + {0, 8} of the 16 and column pairs 8i + 2(t%4) of
+    // each 32-column chunk; a per-column value read from shared memory serves
+    // both rows.  Chunk reads are pipelined one ahead.
+    const int ew = warp - 2;                        // 0..15
+    const int team = NBUF == 2 ? (ew >> 3) : 0;
+    const bool active = NBUF == 2 || ew < 8;
+    const int tstep = NBUF == 2 ? 2 : 1;            // a team's tiles are tstep apart
+    const uint32_t team_bar = kEpiBar + static_cast<uint32_t>(team);
+    const int quad = warp & 3;                      // TMEM lane quadrant this warp may access
+    const int rh = (ew >> 2) & 1;                   // row half of the quadrant
+    const int g4 = lane >> 2;                       // row within each 8-row group
+    const int cp = lane & 3;                        // column pair within each 8-column group
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32 + rh * 16) << 16;
     constexpr int NCHUNK = N / 32;
-    static_assert(NCHUNK % NCP == 0, "chunks split evenly between the column parts");
-    constexpr int CH = NCHUNK / NCP;         // chunks per warp
     constexpr bool kBf16Out = OUT == static_cast<int>(OutKind::kBf16);
     const int norm = p.norm;
     const float eps = p.eps;
+    float* vec_sw = vec_base + team * 4 * N;        // this team's copy of the column vectors
+    float* vec_b = vec_sw + N;
+    float* vec_g = vec_b + N;
+    float* vec_be = vec_g + N;
     int rowk[2];
 #pragma unroll
     for (int k = 0; k < 2; ++k) rowk[k] = quad * 32 + rh * 16 + g4 + 8 * k;
@@ -403,21 +532,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
       const int o = 4 * i + 2 * k;
       return make_float2(__uint_as_float(r[o]), __uint_as_float(r[o + 1]));
     };
-    // Runs fn(r, c) over this warp's chunks, the TMEM read of chunk s + 1 in
-    // flight while chunk s is processed.
+    // Runs fn(r, c) over the chunks c = 0 .. NCHUNK-1, the TMEM read of chunk
+    // c + 1 in flight while chunk c is processed.
     auto for_chunks = [&](uint32_t t_base, auto&& fn) {
       uint32_t r[2][16];
-      tmem_ld_16x256b_x4(t_base + ch * 32, r[0]);
+      tmem_ld_16x256b_x4(t_base, r[0]);
       tmem_ld_wait();
       reg_fence(r[0]);
 #pragma unroll
-      for (int s = 0; s < CH; ++s) {
-        const int c = ch + NCP * s;
-        if (s + 1 < CH) tmem_ld_16x256b_x4(t_base + (c + NCP) * 32, r[(s + 1) & 1]);
-        fn(r[s & 1], c);
-        if (s + 1 < CH) {
+      for (int c = 0; c < NCHUNK; ++c) {
+        if (c + 1 < NCHUNK) tmem_ld_16x256b_x4(t_base + (c + 1) * 32, r[(c + 1) & 1]);
+        fn(r[c & 1], c);
+        if (c + 1 < NCHUNK) {
           tmem_ld_wait();
-          reg_fence(r[(s + 1) & 1]);
+          reg_fence(r[(c + 1) & 1]);
         }
       }
     };
@@ -430,19 +558,30 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
       else
         return __ffma2_rn(acc2(r, k, i), sx2, b);
     };
+    // one lane waits, the whole warp follows its verdict
+    auto warp_wait = [&](uint32_t bar, uint32_t parity, bool cluster_scope) {
+      int okw = 1;
+      if (lane == 0)
+        okw = (cluster_scope ? wait_parity_cluster(wd, bar, parity, kErrClusterWait)
+                             : wait_parity(wd, bar, parity, kErrEpilogueWait)) ? 1 : 0;
+      return __shfl_sync(0xffffffffu, okw, 0) != 0;
+    };
 
     int cur_group = -1;
-    int local = 0;
     bool has_swv = false, affine = false;
     float sx_next[2] = {1.f, 1.f};
-    if (cid < p.total_tiles) row_scales(cid, sx_next);
-    for (int tile = cid; tile < p.total_tiles; tile += ncl, ++local) {
+    int local = team;
+    int tile = cid + team * ncl;
+    if (!kFused && active && tile < p.total_tiles) row_scales(tile, sx_next);
+    for (; active && tile < p.total_tiles; tile += tstep * ncl, local += tstep) {
       const int g = group_of(p, tile);
       const GemmGroup& G = p.g[g];
       if (g != cur_group) {
-        named_bar_sync(kEpiBar, kEpiThreads);
+        // this team's column vectors for the group; the barrier's OR makes
+        // the abort decision the same for all of the team's warps
+        if (named_bar_or(team_bar, 256, *abort_flag != 0)) break;
         const bool normed = norm != kNormNone;
-        for (int n = et; n < N; n += kEpiThreads) {
+        for (int n = (ew & 7) * 32 + lane; n < N; n += 256) {
           const int gn = col0 + n;
           vec_sw[n] = (G.sw != nullptr && G.sw_per_row) ? G.sw[gn] : 1.0f;
           vec_b[n] = G.bias == nullptr ? 0.0f : bf16_to_f(G.bias[gn]);
@@ -451,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
         }
         has_swv = G.sw != nullptr && G.sw_per_row;
         affine = normed && (G.gamma != nullptr || (G.beta != nullptr && norm == kNormLayer));
-        named_bar_sync(kEpiBar, kEpiThreads);
+        named_bar_sync(team_bar, 256);
         cur_group = g;
       }
       float sxr[2] = {sx_next[0], sx_next[1]};
@@ -468,15 +607,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
         // after a transpose; fp32: column pairs straight from registers
         rowp[k] = static_cast<uint8_t*>(G.y) + (m * NG + col0 + (kBf16Out ? 8 : 2) * cp) * (kBf16Out ? 2 : 4);
       }
-      const int buf = NBUF == 2 ? (local & 1) : 0;
-      const uint32_t use = NBUF == 2 ? (local >> 1) : local;
-      wait_parity(wd, smem_u32(&tfull[buf]), use & 1u, kErrEpilogueWait);
-      // every epilogue thread takes the same decision, so none is left at a
-      // named barrier that the others have abandoned
-      named_bar_sync(kEpiBar, kEpiThreads);
-      if (*abort_flag) break;
+      const int buf = NBUF == 2 ? team : 0;
+      const uint32_t use = NBUF == 2 ? static_cast<uint32_t>(local >> 1) : static_cast<uint32_t>(local);
+      if (!warp_wait(smem_u32(&tfull[buf]), use & 1u, false)) break;
+      if (kFused && !warp_wait(smem_u32(&sx_full[local % kSxSlots]), (local / kSxSlots) & 1, false)) break;
       tc_fence_after();
-      if (tile + ncl < p.total_tiles) row_scales(tile + ncl, sx_next);
+      if constexpr (kFused) {
+        // this tile's row scales, written by the quantizing warps
+#pragma unroll
+        for (int k = 0; k < 2; ++k) sxr[k] = sx_ring[(local % kSxSlots) * kBM + rowk[k]];
+      } else if (tile + tstep * ncl < p.total_tiles) {
+        row_scales(tile + tstep * ncl, sx_next);
+      }
       const uint32_t t_base = tmem_base + lane_addr + static_cast<uint32_t>(buf * N);
       const float2 sx2[2] = {dup2(sxr[0]), dup2(sxr[1])};
 
@@ -500,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
               float2 v[4];
 #pragma unroll
               for (int i = 0; i < 4; ++i) v[i] = vpair(swv_tag, r, k, i, sx2[k], sw[i], b[i]);
-              if (c == ch) {
+              if (c == 0) {
                 const float2 t = __fadd2_rn(__fadd2_rn(v[0], v[1]), __fadd2_rn(v[2], v[3]));
                 shift[k] = (t.x + t.y) * 0.125f;
               }
@@ -516,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
               m2[k] += a2.x + a2.y;
             }
           });
-          constexpr float kInvMe = 1.0f / (8.0f * CH);
+          constexpr float kInvMe = 1.0f / (8.0f * NCHUNK);
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
             const float d = s1[k] * kInvMe;
@@ -555,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
 #pragma unroll
         for (int lvl = 0; lvl < 2; ++lvl) {
           const int off = 1 << lvl;
-          const float half_n = 4.0f * CH * static_cast<float>(off);   // n_a n_b / (n_a + n_b)
+          const float half_n = 4.0f * NCHUNK * static_cast<float>(off);   // n_a n_b / (n_a + n_b)
           const bool lo_side = (lane & off) == 0;
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
@@ -568,41 +710,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
             mean[k] = norm == kNormRms ? 0.0f : 0.5f * (lm + hm);
           }
         }
-        if (cp == 0) {
-#pragma unroll
-          for (int k = 0; k < 2; ++k) stat_part[ch * kBM + rowk[k]] = make_float2(mean[k], m2[k]);
-        }
-        named_bar_sync(kEpiBar, kEpiThreads);
-        // the two column parts hold N/2 elements each
-        float qrow[2];
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const float2 lo = stat_part[rowk[k]];
-          const float2 hi = stat_part[kBM + rowk[k]];
-          const float delta = hi.x - lo.x;
-          qrow[k] = norm == kNormRms ? lo.y + hi.y : (lo.y + hi.y) + delta * delta * (0.25f * N);
-          mean[k] = norm == kNormRms ? 0.0f : 0.5f * (lo.x + hi.x);
-        }
         if constexpr (CL > 1) {
-          // exchange (mean, M2) of this CTA's N columns with the cluster:
-          // column-part-0 lanes with cp == 0 hold one row each and write it
-          // into every CTA's slot [buffer][rank][row], then arrive there
+          // exchange (mean, M2) of this CTA's N columns with the cluster.
+          // Buffer cb holds the statistics of every other tile; before
+          // reusing it a writer waits until every CTA has read the previous
+          // contents (cl_free), then the cp == 0 lanes write their two rows
+          // into every CTA's slot [cb][rank][row] and arrive there.
           const int cb = local & 1;
-          if (ch == 0 && cp == 0) {
+          const uint32_t cphase = static_cast<uint32_t>(local >> 1) & 1u;
+          if (!warp_wait(smem_u32(&cl_free[cb]), cphase ^ 1u, true)) break;
+          if (cp == 0) {
 #pragma unroll
             for (int j = 0; j < CL; ++j) {
 #pragma unroll
               for (int k = 0; k < 2; ++k) {
                 const uint32_t a = smem_u32(&cl_stats[(cb * CL + static_cast<int>(rank)) * kBM + rowk[k]]);
-                st_cluster_f32x2(mapa_shared(a, j), mean[k], qrow[k]);
+                st_cluster_f32x2(mapa_shared(a, j), mean[k], m2[k]);
               }
             }
 #pragma unroll
             for (int j = 0; j < CL; ++j) mbar_arrive_cluster(mapa_shared(smem_u32(&cl_bar[cb]), j));
           }
-          wait_parity_cluster(wd, smem_u32(&cl_bar[cb]), (local >> 1) & 1, kErrClusterWait);
-          named_bar_sync(kEpiBar, kEpiThreads);
-          if (*abort_flag) break;
+          if (!warp_wait(smem_u32(&cl_bar[cb]), cphase, true)) break;
           // merge the CTAs' statistics in rank order (N elements each)
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
@@ -623,11 +752,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
               }
             }
             mean[k] = norm == kNormRms ? 0.0f : mA;
-            qrow[k] = qA;
+            m2[k] = qA;
+          }
+          // this warp's reads of buffer cb are done: tell every CTA
+          __syncwarp();
+          if (lane == 0) {
+#pragma unroll
+            for (int j = 0; j < CL; ++j) mbar_arrive_cluster(mapa_shared(smem_u32(&cl_free[cb]), j));
           }
         }
 #pragma unroll
-        for (int k = 0; k < 2; ++k) rstd[k] = rsqrtf(qrow[k] * (1.0f / NG) + eps);
+        for (int k = 0; k < 2; ++k) rstd[k] = rsqrtf(m2[k] * (1.0f / NG) + eps);
       }
       // y = v * rstd - mean * rstd, then * gamma + beta when present
       const float2 rstd2[2] = {dup2(rstd[0]), dup2(rstd[1])};
@@ -677,7 +812,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
         if (affine) out_pass(std::false_type{}, std::true_type{});
         else out_pass(std::false_type{}, std::false_type{});
       }
-      // all reads of this accumulator are done: hand it back to the MMA warp
+      // all of this warp's reads of the accumulator are done
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));
@@ -700,8 +835,17 @@ struct Plan {
   size_t smem;
 };
 
-Plan plan_for(int N, int K, int elem_bytes, bool mx, int cl) {
+Plan plan_for(int N, int K, int elem_bytes, bool mx, int cl, bool fused = false) {
   Plan pl{false, 0, 0};
+  if (fused) {
+    // whole A tiles (two when they fit) next to resident W; K = 256 or 512
+    if (cl != 1 || (K != 256 && K != 512) || static_cast<size_t>(N) * K > kResidentWLimit) return pl;
+    for (int na = 2; na >= 1; --na) {
+      const Layout L = make_layout(N, K, 1, true, na, false, 1, true);
+      if (L.total <= kSmemLimit) return Plan{true, na, L.total};
+    }
+    return pl;
+  }
   const size_t w_bytes = static_cast<size_t>(N) * K * elem_bytes;
   for (int pass = 0; pass < 2; ++pass) {
     const bool resident = pass == 0;
@@ -745,7 +889,7 @@ cudaError_t launch_one(const GemmParams& p, size_t smem, int sms, cudaStream_t s
   if (clusters < 1) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * CL));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads_for(OP));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -769,6 +913,16 @@ cudaError_t launch_res(const GemmParams& p, const Plan& pl, int sms, cudaStream_
 // N here is the width one CTA owns; CL CTAs of a cluster cover N * CL columns.
 template <int N, int CL>
 cudaError_t launch_n(GemmParams& p, OperandKind op, OutKind out, int sms, cudaStream_t stream) {
+  if (op == OperandKind::kRowQuantX) {
+    if constexpr (CL == 1) {
+      const Plan pl = plan_for(N, p.K, 1, false, 1, true);
+      if (pl.stages == 0 || out != OutKind::kBf16) return cudaErrorInvalidValue;
+      p.stages = pl.stages;
+      return launch_one<N, 1, kOpRowQuantX, 0, true>(p, pl.smem, sms, stream);
+    } else {
+      return cudaErrorInvalidValue;
+    }
+  }
   const int eb = op == OperandKind::kBf16 ? 2 : 1;
   const Plan pl = plan_for(N, p.K, eb, op == OperandKind::kMxE4M3, CL);
   if (pl.stages == 0) return cudaErrorInvalidValue;
@@ -798,6 +952,7 @@ bool split_n(int N, int* local, int* cl) {
 bool gemm_supported(int N, int K, OperandKind op) {
   int local = 0, cl = 0;
   if (!split_n(N, &local, &cl)) return false;
+  if (op == OperandKind::kRowQuantX) return plan_for(local, K, 1, false, cl, true).stages > 0;
   return plan_for(local, K, op == OperandKind::kBf16 ? 2 : 1, op == OperandKind::kMxE4M3, cl).stages > 0;
 }
 

@@ -13,66 +13,11 @@
 // grouped layer) are handled by one launch through a job table.
 #include "loka_internal.h"
 #include "ptx.cuh"
+#include "quant_math.cuh"
 
 namespace loka {
 
 namespace {
-
-constexpr float kE4M3Max = 448.0f;
-
-__device__ __forceinline__ float abs_max8(const uint4& v, float m) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    m = fmaxf(m, fabsf(bf16lo(w[i])));
-    m = fmaxf(m, fabsf(bf16hi(w[i])));
-  }
-  return m;
-}
-
-// 8 bf16 * mul -> 8 E4M3 codes; the multiply is one fp32 round-to-nearest.
-__device__ __forceinline__ uint2 cast8(const uint4& v, float mul) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t out[2];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const uint16_t a = cvt_e4m3x2(__fmul_rn(bf16lo(w[2 * i]), mul), __fmul_rn(bf16hi(w[2 * i]), mul));
-    const uint16_t b = cvt_e4m3x2(__fmul_rn(bf16lo(w[2 * i + 1]), mul), __fmul_rn(bf16hi(w[2 * i + 1]), mul));
-    out[i] = static_cast<uint32_t>(a) | (static_cast<uint32_t>(b) << 16);
-  }
-  return make_uint2(out[0], out[1]);
-}
-
-__device__ __forceinline__ float warp_max(float m) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  return m;
-}
-
-// inv = 448/amax and scale = amax/448, one IEEE division each; amax 0 -> 1.
-__device__ __forceinline__ void row_scales(float amax, float& inv, float& scale) {
-  if (amax == 0.0f) {
-    inv = 1.0f;
-    scale = 1.0f;
-  } else {
-    inv = __fdiv_rn(kE4M3Max, amax);
-    scale = __fdiv_rn(amax, kE4M3Max);
-  }
-}
-
-// E8M0 exponent of a block from the fp32 exponent field of its amax:
-// e = clamp(floor(log2 amax) - 8, -127, 127).  A subnormal or zero amax has
-// field 0, which lands below -127 and clamps; Inf/NaN have field 255.
-__device__ __forceinline__ int mx_exponent(float amax) {
-  const int field = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
-  int e = field - 127 - 8;
-  e = e < -127 ? -127 : e;
-  e = e > 127 ? 127 : e;
-  return e;
-}
-
-// 2^-e as an fp32 (exact: e is in [-127, 120], so 127 - e is in [7, 254]).
-__device__ __forceinline__ float pow2_neg(int e) { return __uint_as_float(static_cast<uint32_t>(127 - e) << 23); }
 
 __device__ __forceinline__ int find_job(const QuantJobs& jobs, int64_t gr) {
   int j = 0;

@@ -242,6 +242,66 @@ def test_prequantized_inputs_match_bf16_inputs(lib):
     assert torch.equal(y.cpu(), y_ref)
 
 
+def _two_step(inps):
+    """The same layers with X quantized by loka_quantize_fp8 first and handed
+    to the GEMM as E4M3 (the path without in-kernel quantization)."""
+    layers = []
+    for inp in inps:
+        x, w = _gpu(inp.x), _gpu(inp.w)
+        qx, sx = loka.quantize_fp8(x, inp.mode)
+        qw, sw = loka.quantize_fp8(w, inp.mode)
+        layers.append(loka.Layer(x=qx, w=qw, x_scales=sx, w_scales=sw, bias=_gpu(inp.bias), gamma=_gpu(inp.gamma),
+                                 beta=_gpu(inp.beta), mode=inp.mode, norm=inp.norm, eps=inp.eps))
+    ys = loka.fp8_linear_norm(layers)
+    torch.cuda.synchronize()
+    return [y.cpu() for y in ys]
+
+
+@pytest.mark.parametrize("K", [256, 512])
+@pytest.mark.parametrize("N", [64, 128, 192, 256])
+@pytest.mark.parametrize("norm", [W.NORM_NONE, W.NORM_LAYER, W.NORM_RMS])
+def test_in_kernel_x_quantization_matches_two_step_path(lib, K, N, norm):
+    # rowwise bf16 X with K = 256/512 and N <= 256 is quantized inside the
+    # GEMM; codes, scales and hence outputs must equal the two-step path's
+    inps = [W.make_layer(m, K, N, mode=W.SCALE_ROW, norm=norm, seed=m + K + N, bias_var=0.02, outlier_frac=0.01,
+                         gamma_uniform=True, eps=1e-5 if norm != W.NORM_RMS else 1e-6)
+            for m in (1000, 129, 1)]
+    ys = _run(inps)
+    ref = _two_step(inps)
+    for inp, y, r in zip(inps, ys, ref):
+        assert torch.equal(y.view(torch.int16), r.view(torch.int16)), f"M={inp.M}"
+    _check_layer(inps[0], ys[0], what="oracle")
+
+
+def test_in_kernel_x_quantization_special_rows(lib):
+    # zero rows (scale 1), rows of subnormals, huge values, and Inf/NaN
+    # entries go through the in-kernel quantizer exactly as through the
+    # standalone one
+    inp = W.make_layer(777, 512, 256, mode=W.SCALE_ROW, norm=W.NORM_LAYER, seed=11, bias_var=0.02)
+    x = inp.x.clone()
+    x[0] = 0
+    x[5] = torch.tensor(2.0 ** -130, dtype=torch.float32).to(torch.bfloat16)
+    x[6, ::7] = 1.0e15
+    x[200, 3] = float("inf")
+    x[201, 9] = float("nan")
+    x[776] = -x[776]
+    inp.x = x
+    (y,) = _run([inp])
+    (r,) = _two_step([inp])
+    assert torch.equal(y.view(torch.int16), r.view(torch.int16))
+    ok = [m for m in range(inp.M) if m not in (200, 201)]
+    _check_layer(inp, y, rows=np.array(ok[:64] + ok[-64:]), what="finite rows")
+
+
+def test_in_kernel_x_quantization_grouped_ragged(lib):
+    inps = [W.make_layer(m, 256, 256, mode=W.SCALE_ROW, norm=W.NORM_RMS, seed=m, gamma_uniform=True, eps=1e-6)
+            for m in (4099, 0, 128, 3, 2000)]
+    ys = _run(inps)
+    ref = _two_step(inps)
+    for inp, y, r in zip(inps, ys, ref):
+        assert torch.equal(y.view(torch.int16), r.view(torch.int16)), f"M={inp.M}"
+
+
 def test_deterministic(lib):
     inp = W.make_layer(1000, 512, 256, mode=W.SCALE_ROW, norm=W.NORM_LAYER, seed=4, bias_var=0.02)
     (a,) = _run([inp])
