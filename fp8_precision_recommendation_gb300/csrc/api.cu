@@ -147,17 +147,14 @@ struct OperandSlots {   // workspace offsets of one group's quantized operands
   size_t sx_tc, sw_tc;   // MX: scale codes in the tensor-memory copy layout
 };
 
-bool fuse_x_quant(const loka_linear_desc& a);
-
 // Lays out the quantized operands of every group; returns the total bytes.
-// With `fused`, X quantized inside the GEMM needs no workspace.
-size_t layout_operands(const loka_linear_desc* d, int n, std::vector<OperandSlots>* slots, bool fused = false) {
+size_t layout_operands(const loka_linear_desc* d, int n, std::vector<OperandSlots>* slots) {
   size_t off = 0;
   if (slots) slots->assign(n, OperandSlots{0, 0, 0, 0, 0, 0, 0});
   for (int i = 0; i < n; ++i) {
     OperandSlots s{0, 0, 0, 0, 0, 0, 0};
     if (d[i].mode != kBf16) {
-      if (!d[i].x_is_fp8 && !fused) {
+      if (!d[i].x_is_fp8) {
         s.xq = off;
         off = align_up(off + static_cast<size_t>(d[i].M) * d[i].K);
         s.sx = off;
@@ -189,17 +186,6 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 OperandKind operand_kind(int mode) {
   return mode == kBf16 ? OperandKind::kBf16 : (mode == kScaleMx32 ? OperandKind::kMxE4M3 : OperandKind::kE4M3);
-}
-
-// Rowwise scaling of a bf16 X quantizes X inside the GEMM (LoKA section
-// III-B, case 1: the (de)quantization fuses into the kernel) when the shape
-// has a plan for it; X then makes one HBM read and no E4M3 round trip.
-bool fuse_x_quant(const loka_linear_desc& a) {
-  // off: with X fed through registers the quantizing warps keep too few
-  // bytes in flight to stream X at HBM rate (measured slower than two steps)
-  constexpr bool kEnabled = false;
-  return kEnabled && a.mode == kScaleRow && !a.x_is_fp8 &&
-         gemm_supported(static_cast<int>(a.N), static_cast<int>(a.K), OperandKind::kRowQuantX);
 }
 
 loka_status validate(const loka_linear_desc* d, int n, bool probe) {
@@ -248,7 +234,7 @@ loka_status validate(const loka_linear_desc* d, int n, bool probe) {
 // workspace locations of operands quantized by this call (bf16 inputs).
 loka_status build_gemm(const loka_linear_desc* d, int n, const std::vector<OperandSlots>& slots, uint8_t* ws,
                        bool bf16_operands, OutKind out, void* const* y_override, int norm, DeviceInfo* dev,
-                       GemmParams* p, bool fused_x = false) {
+                       GemmParams* p) {
   std::memset(p, 0, sizeof(*p));
   const int mode = d[0].mode;
   int tiles = 0;
@@ -270,16 +256,11 @@ loka_status build_gemm(const loka_linear_desc* d, int n, const std::vector<Opera
       if ((s = encode_2d(&G.tm_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.x, g.K, g.M, 128)) != LOKA_OK) return s;
       if ((s = encode_2d(&G.tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.w, g.K, g.N, g.N > 256 ? 256 : g.N)) != LOKA_OK) return s;
     } else {
+      const void* xq = g.x_is_fp8 ? g.x : ws + slots[i].xq;
       const void* wq = g.w_is_fp8 ? g.w : ws + slots[i].wq;
+      const void* sx = g.x_is_fp8 ? g.x_scales : ws + slots[i].sx;
       const void* sw = g.w_is_fp8 ? g.w_scales : ws + slots[i].sw;
-      const void* sx = nullptr;
-      if (fused_x) {   // bf16 X, read and quantized by the GEMM (row scales stay on chip)
-        G.xb = static_cast<const uint16_t*>(g.x);
-      } else {
-        const void* xq = g.x_is_fp8 ? g.x : ws + slots[i].xq;
-        sx = g.x_is_fp8 ? g.x_scales : ws + slots[i].sx;
-        if ((s = encode_2d(&G.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xq, g.K, g.M, 128)) != LOKA_OK) return s;
-      }
+      if ((s = encode_2d(&G.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xq, g.K, g.M, 128)) != LOKA_OK) return s;
       if ((s = encode_2d(&G.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wq, g.K, g.N, g.N > 256 ? 256 : g.N)) != LOKA_OK) return s;
       if (mode == kScaleMx32) {   // the block scales are applied inside the MMA
         G.sfa_tc = ws + slots[i].sx_tc;
@@ -310,13 +291,13 @@ loka_status build_gemm(const loka_linear_desc* d, int n, const std::vector<Opera
 // Quantizes every bf16 operand of the groups into the workspace (one launch
 // for X and W of all groups; tensorwise scaling takes an amax launch first).
 loka_status quantize_operands(const loka_linear_desc* d, int n, const std::vector<OperandSlots>& slots, uint8_t* ws,
-                              DeviceInfo* dev, cudaStream_t stream, bool skip_x = false) {
+                              DeviceInfo* dev, cudaStream_t stream) {
   QuantJobs jobs;
   std::memset(&jobs, 0, sizeof(jobs));
   int64_t rows = 0;
   for (int i = 0; i < n; ++i) {
     const loka_linear_desc& g = d[i];
-    if (!g.x_is_fp8 && !skip_x && g.M > 0) {
+    if (!g.x_is_fp8 && g.M > 0) {
       QuantJob& j = jobs.j[jobs.n++];
       j.x = g.x;
       j.q = ws + slots[i].xq;
@@ -432,7 +413,7 @@ loka_status loka_quantize_fp8(const void* x, int64_t rows, int64_t cols, int32_t
 
 size_t loka_fp8_linear_norm_workspace_size(const loka_linear_desc* descs, int32_t num_groups) {
   if (descs == nullptr || num_groups < 1 || num_groups > kMaxGroups) return 0;
-  return layout_operands(descs, num_groups, nullptr, fuse_x_quant(descs[0]));
+  return layout_operands(descs, num_groups, nullptr);
 }
 
 loka_status loka_fp8_linear_norm(const loka_linear_desc* descs, int32_t num_groups, void* workspace,
@@ -440,8 +421,7 @@ loka_status loka_fp8_linear_norm(const loka_linear_desc* descs, int32_t num_grou
   loka_status s = validate(descs, num_groups, false);
   if (s != LOKA_OK) return s;
   std::vector<OperandSlots> slots;
-  const bool fused = fuse_x_quant(descs[0]);
-  const size_t need = layout_operands(descs, num_groups, &slots, fused);
+  const size_t need = layout_operands(descs, num_groups, &slots);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
     return fail(LOKA_ERR_WORKSPACE, "workspace must be >= %zu bytes, 256-byte aligned", need);
   int64_t total_m = 0;
@@ -452,8 +432,8 @@ loka_status loka_fp8_linear_norm(const loka_linear_desc* descs, int32_t num_grou
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const bool bf16 = descs[0].mode == kBf16;
-  if (!bf16 && ((!descs[0].x_is_fp8 && !fused) || !descs[0].w_is_fp8)) {
-    if ((s = quantize_operands(descs, num_groups, slots, ws, dev, st, fused)) != LOKA_OK) return s;
+  if (!bf16 && (!descs[0].x_is_fp8 || !descs[0].w_is_fp8)) {
+    if ((s = quantize_operands(descs, num_groups, slots, ws, dev, st)) != LOKA_OK) return s;
   }
   if (descs[0].mode == kScaleMx32) {   // caller-quantized MX operands: scales into the copy layout
     for (int i = 0; i < num_groups; ++i) {
@@ -467,11 +447,9 @@ loka_status loka_fp8_linear_norm(const loka_linear_desc* descs, int32_t num_grou
     }
   }
   static thread_local GemmParams p;
-  if ((s = build_gemm(descs, num_groups, slots, ws, bf16, OutKind::kBf16, nullptr, descs[0].norm, dev, &p, fused)) !=
-      LOKA_OK)
+  if ((s = build_gemm(descs, num_groups, slots, ws, bf16, OutKind::kBf16, nullptr, descs[0].norm, dev, &p)) != LOKA_OK)
     return s;
-  cudaError_t e = launch_gemm_norm(p, static_cast<int>(descs[0].N),
-                                   fused ? OperandKind::kRowQuantX : operand_kind(descs[0].mode), OutKind::kBf16,
+  cudaError_t e = launch_gemm_norm(p, static_cast<int>(descs[0].N), operand_kind(descs[0].mode), OutKind::kBf16,
                                    dev->sms, st);
   if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
   return LOKA_OK;
@@ -480,7 +458,7 @@ loka_status loka_fp8_linear_norm(const loka_linear_desc* descs, int32_t num_grou
 loka_status loka_fp8_linear_norm_static(const loka_linear_desc* descs, int32_t num_groups, void* stream) {
   loka_status s = validate(descs, num_groups, false);
   if (s != LOKA_OK) return s;
-  const size_t need = layout_operands(descs, num_groups, nullptr, fuse_x_quant(descs[0]));
+  const size_t need = layout_operands(descs, num_groups, nullptr);
   if (need > kStaticScratchBytes)
     return fail(LOKA_ERR_WORKSPACE,
                 "this call needs %zu bytes of scratch; the built-in scratch of loka_fp8_linear_norm_static holds %zu "

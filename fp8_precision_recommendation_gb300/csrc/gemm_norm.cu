@@ -47,11 +47,7 @@ constexpr int kBM = 128;                 // rows per tile (= TMEM lanes)
 constexpr int kSliceBytes = 128;         // bytes of K per stage per row
 constexpr uint32_t kABytes = kBM * kSliceBytes;
 constexpr int kTmemCols = 512;
-constexpr int kQuantWarps = 8;           // kRowQuantX: warps 18..25 quantize X
-constexpr int kQuantWarp0 = 18;
-constexpr int kSxSlots = 4;              // kRowQuantX: row-scale slots (tile % 4)
-constexpr int kOpRowQuantX = static_cast<int>(OperandKind::kRowQuantX);
-__host__ __device__ constexpr int threads_for(int op) { return op == kOpRowQuantX ? 576 + 32 * kQuantWarps : 576; }
+constexpr int kThreads = 576;             // producer, MMA, 16 epilogue warps
 constexpr int kEpiBar = 1;               // named barrier id for the epilogue warps
 constexpr int kMaxStages = 8;
 constexpr size_t kSmemLimit = 227 * 1024;
@@ -62,12 +58,9 @@ constexpr size_t kResidentWLimit = 128 * 1024;
 //   w        resident W: K/KE slices of N rows x 128 bytes (when resident)
 //   vectors  2 teams x 4 x N fp32 (weight scale, bias, gamma, beta)
 //   stats    clusters: 2 x CL x 128 float2 row statistics of the CTAs
-//   sx       kRowQuantX: 4 x 128 fp32 row scales of X written by the quantizing warps
 //   barriers
-// kRowQuantX keeps whole quantized A tiles (128 rows x K bytes, as K/128
-// swizzled 16 KB slices) in the ring instead of K slices.
 struct Layout {
-  uint32_t stage_bytes, ring, w, vec, stats, sxr, bars, total;
+  uint32_t stage_bytes, ring, w, vec, stats, bars, total;
 };
 
 // MX scale blocks: 512 bytes per 128 rows per 128-element K slice.
@@ -75,14 +68,13 @@ constexpr uint32_t kSfBlock = 512;
 __host__ __device__ constexpr int sfb_blocks(int N) { return (N + 127) / 128; }
 
 __host__ __device__ inline Layout make_layout(int N, int K, int elem_bytes, bool resident, int stages, bool mx,
-                                              int cl = 1, bool fused = false) {
+                                              int cl = 1) {
   Layout L;
   const uint32_t b_slice = static_cast<uint32_t>(N) * kSliceBytes;
   const uint32_t sfa = mx ? kSfBlock : 0u;
   const uint32_t sfb = mx ? kSfBlock * sfb_blocks(N) : 0u;
-  // stage: [A slice][B slice, streamed W][A scales][B scales, streamed W];
-  // fused: one whole A tile
-  L.stage_bytes = fused ? static_cast<uint32_t>(kBM) * K : kABytes + (resident ? 0u : b_slice) + sfa + (resident ? 0u : sfb);
+  // stage: [A slice][B slice, streamed W][A scales][B scales, streamed W]
+  L.stage_bytes = kABytes + (resident ? 0u : b_slice) + sfa + (resident ? 0u : sfb);
   L.ring = 0;
   L.w = L.ring + static_cast<uint32_t>(stages) * L.stage_bytes;
   const int nkb = K * elem_bytes / kSliceBytes;
@@ -92,8 +84,7 @@ __host__ __device__ inline Layout make_layout(int N, int K, int elem_bytes, bool
   L.stats = L.vec + 2u * 4u * N * sizeof(float);
   // [2][cluster][128] row statistics of the cluster's CTAs (written
   // remotely, double-buffered by tile parity)
-  L.sxr = L.stats + (cl > 1 ? 2u * cl * kBM * sizeof(float2) : 0u);
-  L.bars = L.sxr + (fused ? static_cast<uint32_t>(kSxSlots * kBM * sizeof(float)) : 0u);
+  L.bars = L.stats + (cl > 1 ? 2u * cl * kBM * sizeof(float2) : 0u);
   L.total = L.bars + 512;
   return L;
 }
@@ -108,71 +99,13 @@ __device__ __forceinline__ float bf16_to_f(uint16_t h) { return __uint_as_float(
 
 __device__ __forceinline__ float2 dup2(float a) { return make_float2(a, a); }
 
-// kRowQuantX: quantizes the 128 rows of one tile of bf16 X (K = 256 V) into
-// the A operand layout, per row like quant_rows_kernel (same arithmetic):
-// amax over the row, scale = amax/448, codes = E4M3(x * 448/amax).  Warp qw
-// takes rows qw + 8j; a lane holds 8-element vectors i = 0..V-1 of a row
-// (elements 8(32i + lane) ..), loaded three rows ahead.  The codes go to
-// shared memory as K/128 slices of 128 rows x 128 bytes with the 128-byte
-// swizzle the MMA descriptors expect (16-byte chunk c of row r at chunk
-// c ^ (r % 8)); rows past M become zeros with scale 1.
-template <int V>
-__device__ __forceinline__ void quant_tile(const uint16_t* __restrict__ xb, int64_t M, int64_t m0, uint8_t* A,
-                                           float* sxs, int qw, int lane) {
-  constexpr int K = 256 * V;
-  constexpr int R = kBM / kQuantWarps;   // rows per warp
-  constexpr int P = 3;                   // rows in flight ahead of the one being cast
-  uint4 v[P + 1][V];
-  auto load = [&](int j, uint4 (&dst)[V]) {
-    const int64_t m = m0 + qw + kQuantWarps * j;
-    const uint4* src = reinterpret_cast<const uint4*>(xb + m * K);
-#pragma unroll
-    for (int i = 0; i < V; ++i) dst[i] = m < M ? __ldcs(src + i * 32 + lane) : make_uint4(0, 0, 0, 0);
-  };
-#pragma unroll
-  for (int j = 0; j < P; ++j) load(j, v[j]);
-#pragma unroll
-  for (int j = 0; j < R; ++j) {
-    if (j + P < R) load(j + P, v[(j + P) % (P + 1)]);
-    const uint4(&x)[V] = v[j % (P + 1)];
-    float m = 0.0f;
-#pragma unroll
-    for (int i = 0; i < V; ++i) m = abs_max8(x[i], m);
-    m = warp_max(m);
-    float inv, scale;
-    row_scales(m, inv, scale);
-    const int r = qw + kQuantWarps * j;
-    uint8_t* row = A + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-    for (int i = 0; i < V; ++i) {
-      const int e = 32 * i + lane;       // 8-byte unit along K
-      const int c = (e & 15) >> 1;       // 16-byte chunk within the slice row
-      *reinterpret_cast<uint2*>(row + (e >> 4) * kABytes + ((c ^ (r & 7)) << 4) + ((e & 1) << 3)) = cast8(x[i], inv);
-    }
-    if (lane == 0) sxs[r] = scale;
-  }
-}
-
-// kRowQuantX: asks L2 for the bf16 rows of `tile` ahead of their use.
-__device__ __forceinline__ void prefetch_x_tile(const GemmParams& p, int tile) {
-  const int g = group_of(p, tile);
-  const GemmGroup& G = p.g[g];
-  const int64_t m0 = static_cast<int64_t>(tile - G.tile_begin) * kBM;
-  const int64_t rows = G.M - m0 < kBM ? G.M - m0 : kBM;
-  const uint8_t* src = reinterpret_cast<const uint8_t*>(G.xb + m0 * p.K);
-  const int64_t bytes = rows * p.K * 2;
-  constexpr int64_t kPiece = 32 * 1024;
-  for (int64_t o = 0; o < bytes; o += kPiece)
-    prefetch_l2_bulk(src + o, static_cast<uint32_t>(bytes - o < kPiece ? bytes - o : kPiece));
-}
-
 // N = the columns this CTA owns (<= 256); CL = CTAs per cluster sharing each
 // 128-row tile (the layer's output has N * CL columns; CTA r owns columns
 // [r N, r N + N) and the CTAs of a cluster merge their row statistics
 // through distributed shared memory, so a row wider than one CTA's tensor
 // memory is still normalized in the epilogue).
 template <int N, int CL, int OP, int OUT, bool RESIDENT>
-__global__ void __launch_bounds__(threads_for(OP), 1) gemm_norm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_constant__ GemmParams p) {
   static_assert(N <= 256, "one MMA per K step");
   constexpr int NG = N * CL;                        // columns of the whole output row
   constexpr int SF_COLS_MAX = OP == static_cast<int>(OperandKind::kMxE4M3) ? kMaxStages * (4 + 4 * sfb_blocks(N)) : 0;
@@ -182,8 +115,6 @@ __global__ void __launch_bounds__(threads_for(OP), 1) gemm_norm_kernel(const __g
   constexpr int N_SPLIT = N / N_MMA;
   constexpr bool kBf16Op = OP == static_cast<int>(OperandKind::kBf16);
   constexpr bool kMx = OP == static_cast<int>(OperandKind::kMxE4M3);
-  constexpr bool kFused = OP == kOpRowQuantX;
-  static_assert(!kFused || (RESIDENT && CL == 1), "in-kernel X quantization keeps W resident, one CTA per tile");
   constexpr int NSFB = sfb_blocks(N);
   constexpr uint32_t SFB_BYTES = kMx ? kSfBlock * NSFB : 0u;
   constexpr uint32_t SF_COLS = kMx ? 4 + 4 * NSFB : 0;    // TMEM columns of one stage's scales
@@ -195,7 +126,7 @@ __global__ void __launch_bounds__(threads_for(OP), 1) gemm_norm_kernel(const __g
 
   const int stages = p.stages;
   const int num_kb = p.K / KE;
-  const Layout L = make_layout(N, p.K, EB, RESIDENT, stages, kMx, CL, kFused);
+  const Layout L = make_layout(N, p.K, EB, RESIDENT, stages, kMx, CL);
   const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
   const int col0 = static_cast<int>(rank) * N;      // first output column of this CTA
   const int cid = static_cast<int>(blockIdx.x) / CL;
@@ -221,10 +152,8 @@ __global__ void __launch_bounds__(threads_for(OP), 1) gemm_norm_kernel(const __g
   uint64_t* w_full = mma_done + 1;
   uint64_t* w_free = w_full + 1;
   uint64_t* cl_bar = w_free + 1;                                    // [2] cluster statistics arrivals
-  uint64_t* sx_full = cl_bar + 2;                                   // [4] kRowQuantX row scales written
-  uint64_t* cl_free = sx_full + kSxSlots;                           // [2] cluster statistics buffers read
+  uint64_t* cl_free = cl_bar + 2;                                   // [2] cluster statistics buffers read
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cl_free + 2);
-  float* sx_ring = reinterpret_cast<float*>(smem + L.sxr);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -232,11 +161,9 @@ __global__ void __launch_bounds__(threads_for(OP), 1) gemm_norm_kernel(const __g
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
-      // kRowQuantX: an A tile is full once every quantizing warp has arrived
-      mbar_init(smem_u32(&full[s]), kFused ? kQuantWarps : 1);
+      mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
     }
-    for (int s = 0; s < kSxSlots; ++s) mbar_init(smem_u32(&sx_full[s]), kQuantWarps);
     for (int b = 0; b < NBUF; ++b) {
       mbar_init(smem_u32(&tfull[b]), 1);
       mbar_init(smem_u32(&tempty[b]), 8);   // the eight warps of the team that owns buffer b
@@ -244,10 +171,10 @@ __global__ void __launch_bounds__(threads_for(OP), 1) gemm_norm_kernel(const __g
     mbar_init(smem_u32(mma_done), 1);
     mbar_init(smem_u32(w_full), 1);
     mbar_init(smem_u32(w_free), 1);
-    // a tile's statistics come from the cp == 0 lanes (8 warps x 8 lanes)
-    // of every CTA of the cluster; its buffer is freed by 8 warps per CTA
-    mbar_init(smem_u32(&cl_bar[0]), 64 * CL);
-    mbar_init(smem_u32(&cl_bar[1]), 64 * CL);
+    // a tile's statistics: one arming arrival plus the bytes sent by the
+    // other CTAs; its buffer is freed by 8 warps of every CTA
+    mbar_init(smem_u32(&cl_bar[0]), 1);
+    mbar_init(smem_u32(&cl_bar[1]), 1);
     mbar_init(smem_u32(&cl_free[0]), 8 * CL);
     mbar_init(smem_u32(&cl_free[1]), 8 * CL);
     *abort_flag = misaligned ? 1 : 0;
@@ -257,7 +184,7 @@ __global__ void __launch_bounds__(threads_for(OP), 1) gemm_norm_kernel(const __g
   if (warp == 0 && lane == 0) {
     for (int g = 0; g < p.num_groups; ++g) {
       if (p.g[g].M == 0) continue;   // no tiles, descriptors not encoded
-      if (!kFused) tma_prefetch_desc(&p.g[g].tm_a);
+      tma_prefetch_desc(&p.g[g].tm_a);
       tma_prefetch_desc(&p.g[g].tm_b);
       tma_prefetch_desc(&p.g[g].tm_y);
     }
@@ -312,8 +239,7 @@ __global__ void __launch_bounds__(threads_for(OP), 1) gemm_norm_kernel(const __g
           ++w_loads;
           cur_group = g;
         }
-        // kRowQuantX: the quantizing warps fill A; only W is loaded here
-        for (int kb = 0; kb < (kFused ? 0 : num_kb); ++kb) {
+        for (int kb = 0; kb < num_kb; ++kb) {
           if (!wait_parity(wd, smem_u32(&empty[stage]), phase ^ 1u, kErrProducerWait)) {
             ok = false;
             break;
@@ -378,23 +304,7 @@ __global__ void __launch_bounds__(threads_for(OP), 1) gemm_norm_kernel(const __g
         if (!wait_parity(wd, smem_u32(&tempty[buf]), (use & 1u) ^ 1u, kErrMmaWait)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * N);
-        if constexpr (kFused) {
-          // the whole quantized A tile, then its K slices against resident W
-          const int slot = local % stages;
-          if (!wait_parity(wd, smem_u32(&full[slot]), static_cast<uint32_t>(local / stages) & 1u, kErrMmaWait)) break;
-          tc_fence_after();
-          const uint32_t a_tile = smem_u32(ring + static_cast<size_t>(slot) * L.stage_bytes);
-          for (int kb = 0; kb < num_kb; ++kb) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t adesc = sdesc_k128_sw128(a_tile + kb * kABytes + k * 32);
-              const uint64_t bdesc = sdesc_k128_sw128(smem_u32(wres + kb * B_SLICE) + k * 32);
-              mma_f8f6f4(d_tmem, adesc, bdesc, IDESC, (kb | k) != 0 ? 1u : 0u);
-            }
-          }
-          mma_commit(smem_u32(&empty[slot]));   // A tile free once these MMAs finish
-        }
-        for (int kb = 0; kb < (kFused ? 0 : num_kb); ++kb) {
+        for (int kb = 0; kb < num_kb; ++kb) {
           if (!wait_parity(wd, smem_u32(&full[stage]), phase, kErrMmaWait)) {
             ok = false;
             break;
@@ -442,39 +352,6 @@ __global__ void __launch_bounds__(threads_for(OP), 1) gemm_norm_kernel(const __g
       // all MMAs issued by this thread complete before tensor memory is freed
       mma_commit(smem_u32(mma_done));
       wait_parity_drain(wd, smem_u32(mma_done), 0);
-    }
-  } else if (kFused && warp >= kQuantWarp0) {
-    // ------------------------------------------------- X quantization (fused)
-    // Each tile's bf16 rows are requested into L2 two tiles ahead, then read
-    // once, quantized per row and written to the A tile in shared memory.
-    const int qw = warp - kQuantWarp0;
-    if (qw == 0 && lane == 0) {
-      if (cid < p.total_tiles) prefetch_x_tile(p, cid);
-      if (cid + ncl < p.total_tiles) prefetch_x_tile(p, cid + ncl);
-    }
-    int local = 0;
-    for (int tile = cid; tile < p.total_tiles; tile += ncl, ++local) {
-      if (qw == 0 && lane == 0 && tile + 2 * ncl < p.total_tiles) prefetch_x_tile(p, tile + 2 * ncl);
-      const GemmGroup& G = p.g[group_of(p, tile)];
-      const int64_t m0 = static_cast<int64_t>(tile - G.tile_begin) * kBM;
-      const int slot = local % stages;
-      // one lane waits, the warp follows its verdict
-      int okw = 1;
-      if (lane == 0)
-        okw = wait_parity(wd, smem_u32(&empty[slot]), (static_cast<uint32_t>(local / stages) & 1u) ^ 1u,
-                          kErrProducerWait) ? 1 : 0;
-      if (!__shfl_sync(0xffffffffu, okw, 0)) break;
-      uint8_t* a_tile = ring + static_cast<size_t>(slot) * L.stage_bytes;
-      float* sxs = sx_ring + (local % kSxSlots) * kBM;
-      if (p.K == 512) quant_tile<2>(G.xb, G.M, m0, a_tile, sxs, qw, lane);
-      else quant_tile<1>(G.xb, G.M, m0, a_tile, sxs, qw, lane);
-      // the generic-proxy stores must be visible to the tensor core's reads
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_u32(&sx_full[local % kSxSlots]));
-        mbar_arrive(smem_u32(&full[slot]));
-      }
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -572,7 +449,7 @@ __global__ void __launch_bounds__(threads_for(OP), 1) gemm_norm_kernel(const __g
     float sx_next[2] = {1.f, 1.f};
     int local = team;
     int tile = cid + team * ncl;
-    if (!kFused && active && tile < p.total_tiles) row_scales(tile, sx_next);
+    if (active && tile < p.total_tiles) row_scales(tile, sx_next);
     for (; active && tile < p.total_tiles; tile += tstep * ncl, local += tstep) {
       const int g = group_of(p, tile);
       const GemmGroup& G = p.g[g];
@@ -593,7 +470,7 @@ __global__ void __launch_bounds__(threads_for(OP), 1) gemm_norm_kernel(const __g
         named_bar_sync(team_bar, 256);
         cur_group = g;
       }
-      float sxr[2] = {sx_next[0], sx_next[1]};
+      const float sxr[2] = {sx_next[0], sx_next[1]};
       const int m0 = (tile - G.tile_begin) * kBM;
       // output row addresses and validity, once per tile
       const int64_t Mg = G.M;
@@ -610,15 +487,8 @@ __global__ void __launch_bounds__(threads_for(OP), 1) gemm_norm_kernel(const __g
       const int buf = NBUF == 2 ? team : 0;
       const uint32_t use = NBUF == 2 ? static_cast<uint32_t>(local >> 1) : static_cast<uint32_t>(local);
       if (!warp_wait(smem_u32(&tfull[buf]), use & 1u, false)) break;
-      if (kFused && !warp_wait(smem_u32(&sx_full[local % kSxSlots]), (local / kSxSlots) & 1, false)) break;
       tc_fence_after();
-      if constexpr (kFused) {
-        // this tile's row scales, written by the quantizing warps
-#pragma unroll
-        for (int k = 0; k < 2; ++k) sxr[k] = sx_ring[(local % kSxSlots) * kBM + rowk[k]];
-      } else if (tile + tstep * ncl < p.total_tiles) {
-        row_scales(tile + tstep * ncl, sx_next);
-      }
+      if (tile + tstep * ncl < p.total_tiles) row_scales(tile + tstep * ncl, sx_next);
       const uint32_t t_base = tmem_base + lane_addr + static_cast<uint32_t>(buf * N);
       const float2 sx2[2] = {dup2(sxr[0]), dup2(sxr[1])};
 
@@ -712,24 +582,28 @@ __global__ void __launch_bounds__(threads_for(OP), 1) gemm_norm_kernel(const __g
         }
         if constexpr (CL > 1) {
           // exchange (mean, M2) of this CTA's N columns with the cluster.
-          // Buffer cb holds the statistics of every other tile; before
-          // reusing it a writer waits until every CTA has read the previous
-          // contents (cl_free), then the cp == 0 lanes write their two rows
-          // into every CTA's slot [cb][rank][row] and arrive there.
+          // Buffer cb holds the statistics of every other tile.  A writer
+          // waits until every CTA has read the buffer's previous contents
+          // (cl_free); the cp == 0 lanes then send their two rows to every
+          // other CTA with st.async, which the receiver's cl_bar counts in
+          // bytes, so no release (which would wait for this warp's earlier
+          // global stores) is needed.  One thread per CTA arms cl_bar with
+          // the bytes it receives; a warp's own rows come from registers.
           const int cb = local & 1;
           const uint32_t cphase = static_cast<uint32_t>(local >> 1) & 1u;
+          if ((ew & 7) == 0 && lane == 0) mbar_arrive_expect_tx(smem_u32(&cl_bar[cb]), kBM * 8 * (CL - 1));
           if (!warp_wait(smem_u32(&cl_free[cb]), cphase ^ 1u, true)) break;
           if (cp == 0) {
 #pragma unroll
             for (int j = 0; j < CL; ++j) {
+              if (j == static_cast<int>(rank)) continue;
+              const uint32_t bar = mapa_shared(smem_u32(&cl_bar[cb]), j);
 #pragma unroll
               for (int k = 0; k < 2; ++k) {
                 const uint32_t a = smem_u32(&cl_stats[(cb * CL + static_cast<int>(rank)) * kBM + rowk[k]]);
-                st_cluster_f32x2(mapa_shared(a, j), mean[k], m2[k]);
+                st_async_f32x2(mapa_shared(a, j), mean[k], m2[k], bar);
               }
             }
-#pragma unroll
-            for (int j = 0; j < CL; ++j) mbar_arrive_cluster(mapa_shared(smem_u32(&cl_bar[cb]), j));
           }
           if (!warp_wait(smem_u32(&cl_bar[cb]), cphase, true)) break;
           // merge the CTAs' statistics in rank order (N elements each)
@@ -738,7 +612,8 @@ __global__ void __launch_bounds__(threads_for(OP), 1) gemm_norm_kernel(const __g
             float mA = 0.f, qA = 0.f;
 #pragma unroll
             for (int j = 0; j < CL; ++j) {
-              const float2 part_j = cl_stats[(cb * CL + j) * kBM + rowk[k]];
+              const float2 part_j = j == static_cast<int>(rank) ? make_float2(mean[k], m2[k])
+                                                                : cl_stats[(cb * CL + j) * kBM + rowk[k]];
               if (norm == kNormRms) {
                 qA += part_j.y;
               } else if (j == 0) {
@@ -754,11 +629,12 @@ __global__ void __launch_bounds__(threads_for(OP), 1) gemm_norm_kernel(const __g
             mean[k] = norm == kNormRms ? 0.0f : mA;
             m2[k] = qA;
           }
-          // this warp's reads of buffer cb are done: tell every CTA
+          // this warp's reads of buffer cb are done (their values are
+          // consumed above): tell every CTA
           __syncwarp();
           if (lane == 0) {
 #pragma unroll
-            for (int j = 0; j < CL; ++j) mbar_arrive_cluster(mapa_shared(smem_u32(&cl_free[cb]), j));
+            for (int j = 0; j < CL; ++j) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&cl_free[cb]), j));
           }
         }
 #pragma unroll
@@ -835,17 +711,8 @@ struct Plan {
   size_t smem;
 };
 
-Plan plan_for(int N, int K, int elem_bytes, bool mx, int cl, bool fused = false) {
+Plan plan_for(int N, int K, int elem_bytes, bool mx, int cl) {
   Plan pl{false, 0, 0};
-  if (fused) {
-    // whole A tiles (two when they fit) next to resident W; K = 256 or 512
-    if (cl != 1 || (K != 256 && K != 512) || static_cast<size_t>(N) * K > kResidentWLimit) return pl;
-    for (int na = 2; na >= 1; --na) {
-      const Layout L = make_layout(N, K, 1, true, na, false, 1, true);
-      if (L.total <= kSmemLimit) return Plan{true, na, L.total};
-    }
-    return pl;
-  }
   const size_t w_bytes = static_cast<size_t>(N) * K * elem_bytes;
   for (int pass = 0; pass < 2; ++pass) {
     const bool resident = pass == 0;
@@ -885,11 +752,8 @@ cudaError_t launch_one(const GemmParams& p, size_t smem, int sms, cudaStream_t s
     configured.fetch_or(bit);
   }
   int clusters = sms / CL;
-  if (p.total_tiles < clusters) clusters = p.total_tiles;
-  if (clusters < 1) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(clusters * CL));
-  cfg.blockDim = dim3(threads_for(OP));
+  cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -899,6 +763,27 @@ cudaError_t launch_one(const GemmParams& p, size_t smem, int sms, cudaStream_t s
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (CL > 1) {
+    // a cluster's CTAs share one GPC, so fewer than sms / CL clusters may be
+    // resident at once; the persistent grid takes no more than fit (per
+    // device and shared-memory size, asked once)
+    static std::atomic<uint64_t> fit[64];
+    const uint64_t key = static_cast<uint64_t>(smem) << 20;
+    uint64_t cached = fit[dev & 63].load();
+    if ((cached & ~uint64_t(0xFFFFF)) != key) {
+      int n = 0;
+      cfg.gridDim = dim3(static_cast<unsigned>(clusters * CL));
+      e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+      if (e != cudaSuccess) return e;
+      cached = key | static_cast<uint64_t>(n > 0 ? n : 1);
+      fit[dev & 63].store(cached);
+    }
+    const int n = static_cast<int>(cached & 0xFFFFF);
+    if (n < clusters) clusters = n;
+  }
+  if (p.total_tiles < clusters) clusters = p.total_tiles;
+  if (clusters < 1) return cudaSuccess;
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * CL));
   e = cudaLaunchKernelEx(&cfg, kern, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -913,16 +798,6 @@ cudaError_t launch_res(const GemmParams& p, const Plan& pl, int sms, cudaStream_
 // N here is the width one CTA owns; CL CTAs of a cluster cover N * CL columns.
 template <int N, int CL>
 cudaError_t launch_n(GemmParams& p, OperandKind op, OutKind out, int sms, cudaStream_t stream) {
-  if (op == OperandKind::kRowQuantX) {
-    if constexpr (CL == 1) {
-      const Plan pl = plan_for(N, p.K, 1, false, 1, true);
-      if (pl.stages == 0 || out != OutKind::kBf16) return cudaErrorInvalidValue;
-      p.stages = pl.stages;
-      return launch_one<N, 1, kOpRowQuantX, 0, true>(p, pl.smem, sms, stream);
-    } else {
-      return cudaErrorInvalidValue;
-    }
-  }
   const int eb = op == OperandKind::kBf16 ? 2 : 1;
   const Plan pl = plan_for(N, p.K, eb, op == OperandKind::kMxE4M3, CL);
   if (pl.stages == 0) return cudaErrorInvalidValue;
@@ -952,7 +827,6 @@ bool split_n(int N, int* local, int* cl) {
 bool gemm_supported(int N, int K, OperandKind op) {
   int local = 0, cl = 0;
   if (!split_n(N, &local, &cl)) return false;
-  if (op == OperandKind::kRowQuantX) return plan_for(local, K, 1, false, cl, true).stages > 0;
   return plan_for(local, K, op == OperandKind::kBf16 ? 2 : 1, op == OperandKind::kMxE4M3, cl).stages > 0;
 }
 

@@ -76,7 +76,6 @@ struct GemmGroup {
   const uint16_t* gamma; // bf16 [N] or null
   const uint16_t* beta;  // bf16 [N] or null
   void* y;               // output (the fp32 output is stored directly)
-  const uint16_t* xb;    // kRowQuantX: bf16 X [M,K], quantized per row inside the GEMM
   int64_t M;
   int32_t tile_begin;    // first tile of this group in the launch's tile space
   int32_t sx_per_row;    // 1: sx has M entries, 0: one entry
@@ -96,9 +95,7 @@ struct GemmParams {
   uint64_t wait_limit_ns;
 };
 
-// kRowQuantX: A is bf16 X read from global memory and quantized per row
-// (E4M3 + fp32 row scale) by the GEMM itself; B is E4M3 with row scales.
-enum class OperandKind : int { kE4M3 = 0, kBf16 = 1, kMxE4M3 = 2, kRowQuantX = 3 };
+enum class OperandKind : int { kE4M3 = 0, kBf16 = 1, kMxE4M3 = 2 };
 enum class OutKind : int { kBf16 = 0, kF32 = 1 };
 
 // Launches the persistent GEMM + epilogue kernel for N columns (fills in

@@ -137,6 +137,35 @@ __device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float a, float b
   asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
 }
 
+__device__ __forceinline__ void st_cluster_b32x2(uint32_t addr, uint2 v) {
+  asm volatile("st.shared::cluster.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(v.x), "r"(v.y) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float a) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(a) : "memory");
+}
+
+// Makes this thread's generic-proxy stores to shared memory of any CTA of
+// the cluster visible to later async-proxy (tensor core, TMA) reads.
+__device__ __forceinline__ void fence_proxy_async_cluster() {
+  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+}
+
+// Asynchronous store of two floats into shared memory of a CTA of the
+// cluster; the destination CTA's mbarrier `cluster_bar` counts the 8 bytes
+// (complete_tx) once they have landed, so the receiver needs no release from
+// the sender.
+__device__ __forceinline__ void st_async_f32x2(uint32_t cluster_addr, float a, float b, uint32_t cluster_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(cluster_addr),
+               "f"(a), "f"(b), "r"(cluster_bar)
+               : "memory");
+}
+
+// Arrive (no memory ordering) on an mbarrier of (possibly) another CTA.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
 // Arrive on an mbarrier of (possibly) another CTA, releasing this thread's
 // earlier shared::cluster stores to it.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
@@ -281,6 +310,14 @@ __device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t 
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// As mma_commit, arriving on the mbarrier at the same offset in every CTA of
+// the cluster whose rank bit is set in cta_mask.
+__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+               "h"(cta_mask)
+               : "memory");
 }
 
 // 32 lanes x 32 columns of 32-bit: thread i of the warp gets lane (base+i),

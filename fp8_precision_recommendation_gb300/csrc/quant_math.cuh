@@ -38,11 +38,43 @@ __device__ __forceinline__ float warp_max(float m) {
   return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(m)));
 }
 
-// inv = 448/amax and scale = amax/448, one IEEE division each; amax 0 -> 1.
+// inv = 448/amax and scale = amax/448, each the correctly rounded fp32
+// quotient; amax 0 -> 1.
+//
+// A row amax is the magnitude of a bf16 value, m * 2^e with m = 1 + k/128
+// (k = 0..127).  Then 448/amax = (448/m) * 2^-e and amax/448 = (m/448) * 2^e
+// exactly, and scaling a correctly rounded quotient by a power of two keeps
+// it correctly rounded while the result stays a normal float.  So the two
+// quotients are a table entry per k (IEEE fp32 division, evaluated when the
+// table is built) with e added to the exponent field: no division on the
+// per-row critical path.  Exponent fields below 10 (amax < 2^-117, where a
+// result leaves the normal range) and Inf/NaN take the divisions.
+struct RowScaleTables {
+  float inv[128];     // 448 / (1 + k/128)
+  float scale[128];   // (1 + k/128) / 448
+};
+constexpr RowScaleTables make_row_scale_tables() {
+  RowScaleTables t{};
+  for (int k = 0; k < 128; ++k) {
+    const float m = 1.0f + static_cast<float>(k) / 128.0f;   // exact
+    t.inv[k] = kE4M3Max / m;
+    t.scale[k] = m / kE4M3Max;
+  }
+  return t;
+}
+__constant__ RowScaleTables kRowScaleTables = make_row_scale_tables();
+
 __device__ __forceinline__ void row_scales(float amax, float& inv, float& scale) {
+  const uint32_t a = __float_as_uint(amax);
+  const uint32_t ef = (a >> 23) & 0xFFu;   // exponent field
   if (amax == 0.0f) {
     inv = 1.0f;
     scale = 1.0f;
+  } else if (ef >= 10u && ef <= 254u && (a & 0xFFFFu) == 0u) {
+    const int k = static_cast<int>((a >> 16) & 0x7Fu);
+    // table entries have exponent fields 134/135 (inv) and 118/119 (scale)
+    inv = __uint_as_float(__float_as_uint(kRowScaleTables.inv[k]) + ((127u - ef) << 23));
+    scale = __uint_as_float(__float_as_uint(kRowScaleTables.scale[k]) + ((ef - 127u) << 23));
   } else {
     inv = __fdiv_rn(kE4M3Max, amax);
     scale = __fdiv_rn(amax, kE4M3Max);

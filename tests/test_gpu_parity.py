@@ -85,6 +85,18 @@ def test_quantize_shapes_and_ragged_widths(lib, mode, cols):
     _check_quant(x, mode)
 
 
+def test_quantize_row_scale_for_every_bf16_amax(lib):
+    # one row per positive finite bf16 magnitude, that value as the row's
+    # only non-zero entry: every mantissa at every exponent (subnormal and
+    # tiny amax included) goes through the row-scale computation
+    pats = torch.arange(1, 0x7F80, dtype=torch.int32).to(torch.int16)
+    v = pats.view(torch.bfloat16)
+    x = torch.zeros((v.numel(), 32), dtype=torch.bfloat16)
+    x[:, 0] = v
+    x[::2, 5] = -v[::2]          # the negative twin in half of the rows
+    _check_quant(x, W.SCALE_ROW)
+
+
 def test_quantize_zero_and_extreme_rows(lib):
     x = torch.zeros((6, 64), dtype=torch.bfloat16)
     x[1, 3] = 1e-38
@@ -243,8 +255,8 @@ def test_prequantized_inputs_match_bf16_inputs(lib):
 
 
 def _two_step(inps):
-    """The same layers with X quantized by loka_quantize_fp8 first and handed
-    to the GEMM as E4M3 (the path without in-kernel quantization)."""
+    """The same layers with X and W quantized by loka_quantize_fp8 first and
+    handed to the GEMM as E4M3."""
     layers = []
     for inp in inps:
         x, w = _gpu(inp.x), _gpu(inp.w)
@@ -260,9 +272,9 @@ def _two_step(inps):
 @pytest.mark.parametrize("K", [256, 512])
 @pytest.mark.parametrize("N", [64, 128, 192, 256])
 @pytest.mark.parametrize("norm", [W.NORM_NONE, W.NORM_LAYER, W.NORM_RMS])
-def test_in_kernel_x_quantization_matches_two_step_path(lib, K, N, norm):
-    # rowwise bf16 X with K = 256/512 and N <= 256 is quantized inside the
-    # GEMM; codes, scales and hence outputs must equal the two-step path's
+def test_bf16_inputs_match_caller_quantized_inputs(lib, K, N, norm):
+    # the call with bf16 X and W quantizes them itself; handing it the
+    # codes and scales of loka_quantize_fp8 must give the same bits
     inps = [W.make_layer(m, K, N, mode=W.SCALE_ROW, norm=norm, seed=m + K + N, bias_var=0.02, outlier_frac=0.01,
                          gamma_uniform=True, eps=1e-5 if norm != W.NORM_RMS else 1e-6)
             for m in (1000, 129, 1)]
@@ -273,10 +285,10 @@ def test_in_kernel_x_quantization_matches_two_step_path(lib, K, N, norm):
     _check_layer(inps[0], ys[0], what="oracle")
 
 
-def test_in_kernel_x_quantization_special_rows(lib):
+def test_special_rows_through_the_layer(lib):
     # zero rows (scale 1), rows of subnormals, huge values, and Inf/NaN
-    # entries go through the in-kernel quantizer exactly as through the
-    # standalone one
+    # entries: the same bits with caller- and library-quantized inputs, the
+    # oracle on the finite rows, NaN rows where X holds Inf or NaN
     inp = W.make_layer(777, 512, 256, mode=W.SCALE_ROW, norm=W.NORM_LAYER, seed=11, bias_var=0.02)
     x = inp.x.clone()
     x[0] = 0
@@ -289,17 +301,9 @@ def test_in_kernel_x_quantization_special_rows(lib):
     (y,) = _run([inp])
     (r,) = _two_step([inp])
     assert torch.equal(y.view(torch.int16), r.view(torch.int16))
+    assert torch.isnan(y[200:202].float()).all()
     ok = [m for m in range(inp.M) if m not in (200, 201)]
     _check_layer(inp, y, rows=np.array(ok[:64] + ok[-64:]), what="finite rows")
-
-
-def test_in_kernel_x_quantization_grouped_ragged(lib):
-    inps = [W.make_layer(m, 256, 256, mode=W.SCALE_ROW, norm=W.NORM_RMS, seed=m, gamma_uniform=True, eps=1e-6)
-            for m in (4099, 0, 128, 3, 2000)]
-    ys = _run(inps)
-    ref = _two_step(inps)
-    for inp, y, r in zip(inps, ys, ref):
-        assert torch.equal(y.view(torch.int16), r.view(torch.int16)), f"M={inp.M}"
 
 
 def test_deterministic(lib):

@@ -44,9 +44,11 @@ def test_static_scratch_matches_workspace_entry_point_twice(lib, mode, norm):
 
 def test_static_scratch_rejects_too_large_problems(lib):
     dev = torch.device("cuda")
-    M, K, N = 16384, 512, 256          # 8 MiB of E4M3 activations > 4 MiB
+    # tensorwise scaling quantizes X into scratch first: 8 MiB of E4M3
+    # activations > 4 MiB
+    M, K, N = 16384, 512, 256
     layer = loka.Layer(x=torch.zeros((M, K), dtype=torch.bfloat16, device=dev),
-                       w=torch.zeros((N, K), dtype=torch.bfloat16, device=dev), mode=W.SCALE_ROW,
+                       w=torch.zeros((N, K), dtype=torch.bfloat16, device=dev), mode=W.SCALE_TENSOR,
                        norm=W.NORM_LAYER, eps=1e-5)
     with pytest.raises(_loka.LokaError) as e:
         _loka.loka_fp8_linear_norm_static([layer.desc()])
