@@ -199,6 +199,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
   // no CTA touches a partner's shared memory before the partner has set up
   // its barriers
   if (CL > 1) cluster_sync_all();
+  // everything above touches only this CTA's own state; inputs written by
+  // the kernel before this one (the quantized operands) are read below
+  wait_prerequisite_grids();
   const uint32_t tmem_base = *tmem_slot;
   const Watchdog wd{abort_flag, p.status, p.wait_limit_ns};
 
@@ -756,13 +759,16 @@ cudaError_t launch_one(const GemmParams& p, size_t smem, int sms, cudaStream_t s
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // the prologue may overlap the tail of the quantizer launched before
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (CL > 1) {
     // a cluster's CTAs share one GPC, so fewer than sms / CL clusters may be
     // resident at once; the persistent grid takes no more than fit (per

@@ -119,6 +119,14 @@ __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t threads, bool
   return r != 0;
 }
 
+// Programmatic dependent launch: a kernel launched after this one with
+// programmatic stream serialization may start (its prologue) once every CTA
+// of this grid has executed launch_dependents; it must call
+// wait_prerequisite_grids before touching memory this grid writes, which
+// returns once this grid has completed and its writes are visible.
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void wait_prerequisite_grids() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------ clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;

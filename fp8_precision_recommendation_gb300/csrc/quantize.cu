@@ -29,6 +29,7 @@ __device__ __forceinline__ int find_job(const QuantJobs& jobs, int64_t gr) {
 // (cols <= 256 * V).  MODE 1 = rowwise, MODE 2 = MX 1x32.
 template <int MODE, int V>
 __global__ void __launch_bounds__(256) quant_rows_kernel(const __grid_constant__ QuantJobs jobs) {
+  launch_dependents();   // the GEMM that follows may start its prologue
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -82,6 +83,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const __grid_constant__
 // the row (it is still in L1/L2).  Same arithmetic as above.
 template <int MODE>
 __global__ void __launch_bounds__(256) quant_rows_long_kernel(const __grid_constant__ QuantJobs jobs) {
+  launch_dependents();   // the GEMM that follows may start its prologue
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -144,6 +146,7 @@ __global__ void __launch_bounds__(256) amax_tensor_kernel(const __grid_constant_
 
 // Tensorwise pass 2: cast with the tensor's scale; block (0, job) writes it.
 __global__ void __launch_bounds__(256) cast_tensor_kernel(const __grid_constant__ QuantJobs jobs) {
+  launch_dependents();
   const QuantJob& job = jobs.j[blockIdx.y];
   const float amax = __uint_as_float(*reinterpret_cast<volatile unsigned*>(job.amax_slot));
   float inv, scale;
