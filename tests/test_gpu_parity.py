@@ -421,3 +421,18 @@ def test_mxfp8_layer_full_size(lib):
     yf = y.float()
     assert yf.mean(dim=1).abs().max().item() < 2e-2
     assert (yf.pow(2).mean(dim=1) - 1).abs().max().item() < 2e-2
+
+
+def test_variant_sweep_smoke(lib):
+    # the sweep that writes the dispatch table: every variant timed and its
+    # probe error measured on two small problems
+    from fp8_precision_recommendation_gb300 import sweep
+    table = sweep.run(quick=True, log=lambda *a: None)
+    rows = table["rows"]
+    assert len(rows) == 4 * len(sweep.problems(quick=True))
+    for (m, n, k, norm, o, v, t, rel, mere) in rows:
+        assert t > 0
+        if v == _loka.LOKA_BF16:
+            assert rel == 0.0
+        else:
+            assert 1e-3 < rel < 0.1

@@ -157,3 +157,29 @@ def test_dispatch_select_empty_table_is_bf16(cpu_lib):
     pol = _loka.Policy()
     pol.max_rel_err, pol.max_mere, pol.min_speedup = 1e-2, 0.2, 1.05
     assert _loka.loka_dispatch_select([], p, pol) == _loka.LOKA_BF16
+
+
+def test_measured_dispatch_table_agrees_with_oracle_selection(cpu_lib):
+    # the committed table is the variant sweep measured on a GB300 (time and
+    # probe error of each variant per problem); C selector and oracle rule
+    # must pick the same variant for every swept problem and for off-grid
+    # queries, under the pages' policy and under looser ones
+    from fp8_precision_recommendation_gb300 import sweep
+    rows = sweep.load_table(sweep.DEFAULT_TABLE)
+    probs = sweep.problems()
+    assert len(rows) == 4 * len(probs)
+    for (m, n, k, norm, o) in probs:
+        got = sorted(r[5] for r in rows if r[:5] == (m, n, k, norm, o))
+        assert got == [0, 1, 2, 3]
+    for r in rows:
+        assert r[6] > 0
+        if r[5] == 3:
+            assert r[7] == 0.0 and r[8] == 0.0
+        else:
+            assert 1e-3 < r[7] < 0.1          # E4M3 carries 3 mantissa bits
+    table = [D.Entry(*r) for r in rows]
+    queries = [p for p in probs] + [(65536, 256, 512, 1, 0.004), (8192, 1024, 2048, 1, 0.02),
+                                    (524288, 64, 128, 1, 0.0), (100000, 256, 2048, 1, 0.01)]
+    for pol in (D.Policy(1e-2, 0.2, -1.0), D.Policy(5e-2, -1.0, -1.0), D.Policy(5e-2, -1.0, 1.05)):
+        for (m, n, k, norm, o) in queries:
+            assert _c_select(table, m, n, k, norm, o, pol) == D.select(table, m, n, k, norm, o, pol)
