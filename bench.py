@@ -365,6 +365,30 @@ def run_ours(args, world, rank, local):
             lay.w = qw[gi]
     kern["gemm_norm"] = timed(lambda i: loka.fp8_linear_norm(pre[i % nbuf], workspace=wsp, stream=s), args.steps)
     torch.cuda.synchronize()
+
+    # ---- the same step with static weights (W quantized once, as a trained
+    # model's weights are): bf16 X quantized in every step, captured in a
+    # CUDA graph like the main measurement
+    static_w = [mk(i, w_scales=sw) for i in range(nbuf)]
+    for lst in static_w:
+        for gi, lay in enumerate(lst):
+            lay.w = qw[gi]
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            loka.fp8_linear_norm(static_w[i % nbuf], workspace=wsp, stream=s)
+        torch.cuda.synchronize()
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2, stream=stream, capture_error_mode="thread_local"):
+            for i in range(args.steps):
+                loka.fp8_linear_norm(static_w[i % nbuf], workspace=wsp, stream=s)
+        g2.replay()
+        torch.cuda.synchronize()
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        g2.replay()
+        b1.record(stream)
+        b1.synchronize()
+    static_w_step = b0.elapsed_time(b1) / 1e3 / args.steps
     vec_bytes = lambda l: 2 * l.N * sum(v is not None for v in (l.bias, l.gamma, l.beta))
     bytes_q = sum(3 * l.M * l.K + scale_bytes(mode, l.M, l.K) for l in layers)
     bytes_g = sum(l.M * l.K + scale_bytes(mode, l.M, l.K) + l.N * l.K + scale_bytes(mode, l.N, l.K) + vec_bytes(l)
@@ -400,6 +424,7 @@ def run_ours(args, world, rank, local):
                     torch.nn.functional.rms_norm(v, (l.N,), gs_[gi], eps=eps)
         compare["torch_bf16_linear_norm_us"] = 1e6 * timed(torch_bf16, args.steps)
         compare["loka_fp8_step_us"] = 1e6 * step_time
+        compare["loka_fp8_step_static_w_us"] = 1e6 * static_w_step
 
     # ---- end to end through the public API with pinned host buffers: every
     # step copies its bf16 X in (pinned host -> device) and its bf16 Y out

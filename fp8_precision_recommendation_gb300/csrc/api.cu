@@ -449,6 +449,11 @@ loka_status loka_fp8_linear_norm(const loka_linear_desc* descs, int32_t num_grou
   static thread_local GemmParams p;
   if ((s = build_gemm(descs, num_groups, slots, ws, bf16, OutKind::kBf16, nullptr, descs[0].norm, dev, &p)) != LOKA_OK)
     return s;
+  // Caller-quantized W may load before the GEMM waits for the launch that
+  // precedes it only when that launch is this call's own activation
+  // quantizer: it started after everything the caller queued (W included)
+  // had finished.  (MX also permutes W's scales right before the GEMM.)
+  p.w_ready = (!bf16 && descs[0].w_is_fp8 && !descs[0].x_is_fp8 && descs[0].mode != kScaleMx32) ? 1 : 0;
   cudaError_t e = launch_gemm_norm(p, static_cast<int>(descs[0].N), operand_kind(descs[0].mode), OutKind::kBf16,
                                    dev->sms, st);
   if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");

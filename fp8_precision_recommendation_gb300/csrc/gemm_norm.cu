@@ -199,8 +199,34 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
   // no CTA touches a partner's shared memory before the partner has set up
   // its barriers
   if (CL > 1) cluster_sync_all();
-  // everything above touches only this CTA's own state; inputs written by
-  // the kernel before this one (the quantized operands) are read below
+  // resident W for this CTA's first group.  When the caller's W was
+  // complete before the launch that precedes this one, it loads now, while
+  // that launch (the activation quantizer) may still run.
+  auto load_w = [&](int g) {
+    const uint32_t wb = smem_u32(w_full);
+    mbar_arrive_expect_tx(wb, static_cast<uint32_t>(num_kb) * (B_SLICE + SFB_BYTES));
+    for (int kb = 0; kb < num_kb; ++kb) {
+#pragma unroll
+      for (int s = 0; s < N_SPLIT; ++s)
+        tma_load_2d(smem_u32(wres + kb * B_SLICE + s * N_MMA * kSliceBytes), &p.g[g].tm_b, wb, kb * KE,
+                    col0 + s * N_MMA);
+      if (kMx) {
+#pragma unroll
+        for (int h = 0; h < NSFB; ++h)
+          bulk_load_1d(smem_u32(wres + num_kb * B_SLICE + (kb * NSFB + h) * kSfBlock),
+                       p.g[g].sfb_tc + (static_cast<int64_t>(rank * NSFB + h) * num_kb + kb) * kSfBlock,
+                       kSfBlock, wb);
+      }
+    }
+  };
+  int w_early_group = -1;
+  if (RESIDENT && p.w_ready && !misaligned && warp == 0 && lane == 0 && cid < p.total_tiles) {
+    w_early_group = group_of(p, cid);
+    load_w(w_early_group);
+  }
+  // everything above touches only this CTA's own state (and W when it was
+  // ready); inputs written by the kernel before this one (the quantized
+  // operands) are read below
   wait_prerequisite_grids();
   const uint32_t tmem_base = *tmem_slot;
   const Watchdog wd{abort_flag, p.status, p.wait_limit_ns};
@@ -213,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, last_parity = 0;
-      int cur_group = -1, w_loads = 0;
+      int cur_group = w_early_group, w_loads = w_early_group >= 0 ? 1 : 0;
       bool ok = true;
       for (int tile = cid; ok && tile < p.total_tiles; tile += ncl) {
         const int g = group_of(p, tile);
@@ -224,21 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
             ok = false;
             break;
           }
-          const uint32_t wb = smem_u32(w_full);
-          mbar_arrive_expect_tx(wb, static_cast<uint32_t>(num_kb) * (B_SLICE + SFB_BYTES));
-          for (int kb = 0; kb < num_kb; ++kb) {
-#pragma unroll
-            for (int s = 0; s < N_SPLIT; ++s)
-              tma_load_2d(smem_u32(wres + kb * B_SLICE + s * N_MMA * kSliceBytes), &p.g[g].tm_b, wb, kb * KE,
-                          col0 + s * N_MMA);
-            if (kMx) {
-#pragma unroll
-              for (int h = 0; h < NSFB; ++h)
-                bulk_load_1d(smem_u32(wres + num_kb * B_SLICE + (kb * NSFB + h) * kSfBlock),
-                             p.g[g].sfb_tc + (static_cast<int64_t>(rank * NSFB + h) * num_kb + kb) * kSfBlock,
-                             kSfBlock, wb);
-            }
-          }
+          load_w(g);
           ++w_loads;
           cur_group = g;
         }

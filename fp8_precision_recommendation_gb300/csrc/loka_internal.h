@@ -91,6 +91,8 @@ struct GemmParams {
   int32_t norm;
   float eps;
   int32_t stages;        // shared-memory ring depth (set by the launcher)
+  int32_t w_ready;       // 1: W and its scales were complete before the launch that precedes
+                         // this GEMM, so resident W may load before waiting for that launch
   unsigned* status;      // device status word
   uint64_t wait_limit_ns;
 };
