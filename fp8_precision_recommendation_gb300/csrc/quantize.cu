@@ -11,6 +11,8 @@
 // load, and the row amax is a warp-shuffle reduction, so the data are read
 // from HBM exactly once.  Several tensors (the X and W of every group of a
 // grouped layer) are handled by one launch through a job table.
+#include <atomic>
+
 #include "loka_internal.h"
 #include "ptx.cuh"
 #include "quant_math.cuh"
@@ -171,26 +173,39 @@ __global__ void __launch_bounds__(256) sf_permute_kernel(const uint8_t* __restri
   }
 }
 
-template <int MODE>
-cudaError_t launch_rows(const QuantJobs& jobs, int max_cols, int sms, cudaStream_t stream) {
+// One wave of the grid-stride kernel: as many 256-thread blocks as are
+// resident at once (the register count decides; asked once per kernel and
+// device), never more than one warp per row.  V = 0: the long-row kernel.
+template <int MODE, int V>
+cudaError_t launch_one_wave(const QuantJobs& jobs, int sms, cudaStream_t stream) {
   const int threads = 256;
-  const int64_t warps_needed = jobs.total_rows;
-  int64_t blocks = (warps_needed + 7) / 8;
-  const int64_t cap = static_cast<int64_t>(sms) * 8;   // 8 resident 256-thread blocks per SM
+  auto kern = V == 0 ? quant_rows_long_kernel<MODE> : quant_rows_kernel<MODE, (V > 0 ? V : 1)>;
+  static std::atomic<int> per_sm[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int occ = per_sm[dev & 63].load();
+  if (occ == 0) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, 0);
+    if (e != cudaSuccess) return e;
+    if (occ < 1) occ = 1;
+    per_sm[dev & 63].store(occ);
+  }
+  int64_t blocks = (jobs.total_rows + 7) / 8;
+  const int64_t cap = static_cast<int64_t>(sms) * occ;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  const dim3 grid(static_cast<unsigned>(blocks));
-  if (max_cols <= 256)
-    quant_rows_kernel<MODE, 1><<<grid, threads, 0, stream>>>(jobs);
-  else if (max_cols <= 512)
-    quant_rows_kernel<MODE, 2><<<grid, threads, 0, stream>>>(jobs);
-  else if (max_cols <= 1024)
-    quant_rows_kernel<MODE, 4><<<grid, threads, 0, stream>>>(jobs);
-  else if (max_cols <= 2048)
-    quant_rows_kernel<MODE, 8><<<grid, threads, 0, stream>>>(jobs);
-  else
-    quant_rows_long_kernel<MODE><<<grid, threads, 0, stream>>>(jobs);
+  kern<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(jobs);
   return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_rows(const QuantJobs& jobs, int max_cols, int sms, cudaStream_t stream) {
+  if (max_cols <= 256) return launch_one_wave<MODE, 1>(jobs, sms, stream);
+  if (max_cols <= 512) return launch_one_wave<MODE, 2>(jobs, sms, stream);
+  if (max_cols <= 1024) return launch_one_wave<MODE, 4>(jobs, sms, stream);
+  if (max_cols <= 2048) return launch_one_wave<MODE, 8>(jobs, sms, stream);
+  return launch_one_wave<MODE, 0>(jobs, sms, stream);
 }
 
 }  // namespace
