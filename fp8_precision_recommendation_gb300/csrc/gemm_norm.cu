@@ -50,6 +50,7 @@ constexpr int kTmemCols = 512;
 constexpr int kThreads = 576;             // producer, MMA, 16 epilogue warps
 constexpr int kEpiBar = 1;               // named barrier id for the epilogue warps
 constexpr int kMaxStages = 8;
+constexpr int kMaxWSlices = 16;          // resident W: 128 KB / (64 rows x 128 bytes)
 constexpr size_t kSmemLimit = 227 * 1024;
 constexpr size_t kResidentWLimit = 128 * 1024;
 
@@ -149,11 +150,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
   uint64_t* tfull = empty + kMaxStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* mma_done = tempty + 2;
-  uint64_t* w_full = mma_done + 1;
-  uint64_t* w_free = w_full + 1;
+  uint64_t* w_free = mma_done + 1;
   uint64_t* cl_bar = w_free + 1;                                    // [2] cluster statistics arrivals
   uint64_t* cl_free = cl_bar + 2;                                   // [2] cluster statistics buffers read
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cl_free + 2);
+  uint64_t* w_full = cl_free + 2;                                   // [16] resident W, one per K slice
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(w_full + kMaxWSlices);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -169,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
       mbar_init(smem_u32(&tempty[b]), 8);   // the eight warps of the team that owns buffer b
     }
     mbar_init(smem_u32(mma_done), 1);
-    mbar_init(smem_u32(w_full), 1);
+    for (int kb = 0; kb < kMaxWSlices; ++kb) mbar_init(smem_u32(&w_full[kb]), 1);
     mbar_init(smem_u32(w_free), 1);
     // a tile's statistics: one arming arrival plus the bytes sent by the
     // other CTAs; its buffer is freed by 8 warps of every CTA
@@ -202,22 +203,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
   // resident W for this CTA's first group.  When the caller's W was
   // complete before the launch that precedes this one, it loads now, while
   // that launch (the activation quantizer) may still run.
-  auto load_w = [&](int g) {
-    const uint32_t wb = smem_u32(w_full);
-    mbar_arrive_expect_tx(wb, static_cast<uint32_t>(num_kb) * (B_SLICE + SFB_BYTES));
-    for (int kb = 0; kb < num_kb; ++kb) {
+  // Each K slice of W has its own barrier, so the first tile's MMAs start
+  // on slice 0 while later slices are still arriving.
+  auto load_w_slice = [&](int g, int kb) {
+    const uint32_t wb = smem_u32(&w_full[kb]);
+    mbar_arrive_expect_tx(wb, B_SLICE + SFB_BYTES);
 #pragma unroll
-      for (int s = 0; s < N_SPLIT; ++s)
-        tma_load_2d(smem_u32(wres + kb * B_SLICE + s * N_MMA * kSliceBytes), &p.g[g].tm_b, wb, kb * KE,
-                    col0 + s * N_MMA);
-      if (kMx) {
+    for (int s = 0; s < N_SPLIT; ++s)
+      tma_load_2d(smem_u32(wres + kb * B_SLICE + s * N_MMA * kSliceBytes), &p.g[g].tm_b, wb, kb * KE,
+                  col0 + s * N_MMA);
+    if (kMx) {
 #pragma unroll
-        for (int h = 0; h < NSFB; ++h)
-          bulk_load_1d(smem_u32(wres + num_kb * B_SLICE + (kb * NSFB + h) * kSfBlock),
-                       p.g[g].sfb_tc + (static_cast<int64_t>(rank * NSFB + h) * num_kb + kb) * kSfBlock,
-                       kSfBlock, wb);
-      }
+      for (int h = 0; h < NSFB; ++h)
+        bulk_load_1d(smem_u32(wres + num_kb * B_SLICE + (kb * NSFB + h) * kSfBlock),
+                     p.g[g].sfb_tc + (static_cast<int64_t>(rank * NSFB + h) * num_kb + kb) * kSfBlock,
+                     kSfBlock, wb);
     }
+  };
+  auto load_w = [&](int g) {
+    for (int kb = 0; kb < num_kb; ++kb) load_w_slice(g, kb);
   };
   int w_early_group = -1;
   if (RESIDENT && p.w_ready && !misaligned && warp == 0 && lane == 0 && cid < p.total_tiles) {
@@ -240,6 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
       uint32_t phase = 0;
       uint32_t issued = 0, last_parity = 0;
       int cur_group = w_early_group, w_loads = w_early_group >= 0 ? 1 : 0;
+      uint32_t w_issued = w_early_group >= 0 ? 0xFFFFFFFFu : 0u;   // slices of the current W load issued
+      bool w_pending = false;   // the current group's W slices go out with its first tile's A slices
       bool ok = true;
       for (int tile = cid; ok && tile < p.total_tiles; tile += ncl) {
         const int g = group_of(p, tile);
@@ -250,7 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
             ok = false;
             break;
           }
-          load_w(g);
+          w_pending = true;
+          w_issued = 0;
           ++w_loads;
           cur_group = g;
         }
@@ -258,6 +265,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
           if (!wait_parity(wd, smem_u32(&empty[stage]), phase ^ 1u, kErrProducerWait)) {
             ok = false;
             break;
+          }
+          if (RESIDENT && w_pending) {
+            load_w_slice(g, kb);
+            w_issued |= 1u << kb;
           }
           uint8_t* a_dst = ring + static_cast<size_t>(stage) * L.stage_bytes;
           const uint32_t fb = smem_u32(&full[stage]);
@@ -288,12 +299,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
             phase ^= 1u;
           }
         }
+        w_pending = false;
       }
       if (!ok) {
         // let the copies already in flight land before the CTA exits
         for (int s = 0; s < stages; ++s)
           if (issued & (1u << s)) wait_parity_drain(wd, smem_u32(&full[s]), (last_parity >> s) & 1u);
-        if (RESIDENT && w_loads > 0) wait_parity_drain(wd, smem_u32(w_full), (w_loads - 1) & 1);
+        if (RESIDENT && w_loads > 0) {
+          for (int kb = 0; kb < num_kb; ++kb)
+            if (w_issued & (1u << kb)) wait_parity_drain(wd, smem_u32(&w_full[kb]), (w_loads - 1) & 1);
+        }
       }
     }
   } else if (warp == 1) {
@@ -309,7 +324,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
           const int g = group_of(p, tile);
           if (g != cur_group) {
             if (w_uses > 0) mma_commit(smem_u32(w_free));   // previous weights free once these MMAs finish
-            if (!wait_parity(wd, smem_u32(w_full), w_uses & 1, kErrMmaWait)) break;
             ++w_uses;
             cur_group = g;
           }
@@ -320,6 +334,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * N);
         for (int kb = 0; kb < num_kb; ++kb) {
+          // this K slice of the resident W (complete at once after the
+          // group's first tile)
+          if (RESIDENT && !wait_parity(wd, smem_u32(&w_full[kb]), (w_uses - 1) & 1, kErrMmaWait)) {
+            ok = false;
+            break;
+          }
           if (!wait_parity(wd, smem_u32(&full[stage]), phase, kErrMmaWait)) {
             ok = false;
             break;
