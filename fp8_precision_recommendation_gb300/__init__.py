@@ -94,20 +94,36 @@ class Layer:
     beta: object = None
     x_scales: object = None        # when x is E4M3
     w_scales: object = None        # when w is E4M3
-    y: object = None               # bf16 [M,N] output (allocated if None)
+    y: object = None               # bf16 [M,N] output (allocated if None, unless y_q_only)
+    # E4M3 output for the next layer (LOKA_SCALE_ROW or LOKA_SCALE_MX32), or None
+    y_q_mode: Optional[int] = None
+    y_q: object = None             # uint8 E4M3 [M,N] (allocated if None)
+    y_q_scales: object = None      # fp32 [M] or uint8 E8M0 [M,N/32] (allocated if None)
+    y_q_only: bool = False         # with y_q_mode: no bf16 copy of the output
 
     def desc(self) -> LinearDesc:
         torch = _torch()
         M, K = self.x.shape
         N = self.w.shape[0]
-        if self.y is None:
-            self.y = torch.empty((M, N), dtype=torch.bfloat16, device=self.x.device)
+        dev = self.x.device
+        quantized_out = self.y_q_mode is not None
+        if self.y is None and not (quantized_out and self.y_q_only):
+            self.y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         d = LinearDesc()
         d.M, d.N, d.K = M, N, K
         d.mode, d.norm, d.eps = self.mode, self.norm, self.eps
         d.x_is_fp8 = int(self.x.dtype == torch.uint8)
         d.w_is_fp8 = int(self.w.dtype == torch.uint8)
-        d.x, d.w, d.y = self.x.data_ptr(), self.w.data_ptr(), self.y.data_ptr()
+        d.x, d.w = self.x.data_ptr(), self.w.data_ptr()
+        d.y = self.y.data_ptr() if self.y is not None else None
+        if quantized_out:
+            if self.y_q is None:
+                self.y_q = torch.empty((M, N), dtype=torch.uint8, device=dev)
+            if self.y_q_scales is None:
+                shp, dt = scales_shape(M, N, self.y_q_mode)
+                self.y_q_scales = torch.empty(shp, dtype=getattr(torch, dt), device=dev)
+            d.y_q_mode = self.y_q_mode
+            d.y_q, d.y_q_scales = self.y_q.data_ptr(), self.y_q_scales.data_ptr()
         d.x_scales = self.x_scales.data_ptr() if self.x_scales is not None else None
         d.w_scales = self.w_scales.data_ptr() if self.w_scales is not None else None
         d.bias = self.bias.data_ptr() if self.bias is not None else None

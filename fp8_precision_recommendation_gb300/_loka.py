@@ -24,9 +24,9 @@ c_i64, c_i32, c_sz, c_p = ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t, ctype
 
 class LinearDesc(ctypes.Structure):
     _fields_ = [("M", c_i64), ("N", c_i64), ("K", c_i64), ("mode", c_i32), ("norm", c_i32),
-                ("eps", ctypes.c_float), ("x_is_fp8", c_i32), ("w_is_fp8", c_i32), ("reserved", c_i32),
+                ("eps", ctypes.c_float), ("x_is_fp8", c_i32), ("w_is_fp8", c_i32), ("y_q_mode", c_i32),
                 ("x", c_p), ("x_scales", c_p), ("w", c_p), ("w_scales", c_p), ("bias", c_p),
-                ("gamma", c_p), ("beta", c_p), ("y", c_p)]
+                ("gamma", c_p), ("beta", c_p), ("y", c_p), ("y_q", c_p), ("y_q_scales", c_p)]
 
 
 class ErrorStats(ctypes.Structure):

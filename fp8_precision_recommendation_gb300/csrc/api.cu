@@ -188,6 +188,14 @@ OperandKind operand_kind(int mode) {
   return mode == kBf16 ? OperandKind::kBf16 : (mode == kScaleMx32 ? OperandKind::kMxE4M3 : OperandKind::kE4M3);
 }
 
+// The group whose output fields (y_q, y_q_mode) speak for the call: the
+// first with rows (an empty group's tensors may have no storage at all).
+const loka_linear_desc& output_reference(const loka_linear_desc* d, int n) {
+  for (int i = 0; i < n; ++i)
+    if (d[i].M > 0) return d[i];
+  return d[0];
+}
+
 loka_status validate(const loka_linear_desc* d, int n, bool probe) {
   if (d == nullptr) return fail(LOKA_ERR_INVALID_ARG, "descs is NULL");
   if (n < 1 || n > kMaxGroups) return fail(LOKA_ERR_INVALID_ARG, "num_groups %d not in [1, %d]", n, kMaxGroups);
@@ -217,13 +225,39 @@ loka_status validate(const loka_linear_desc* d, int n, bool probe) {
     return fail(LOKA_ERR_INVALID_ARG, "LOKA_BF16 takes bf16 operands (x_is_fp8 = w_is_fp8 = 0)");
   if (probe && (a.x_is_fp8 || a.w_is_fp8))
     return fail(LOKA_ERR_INVALID_ARG, "the error probe needs bf16 x and w (it runs the high-precision reference too)");
+  // quantized output for the next layer (the probe writes its own outputs);
+  // empty groups carry no output pointers
+  const loka_linear_desc& r = output_reference(d, n);
+  const bool qout = !probe && r.y_q != nullptr;
+  if (!probe) {
+    for (int i = 0; i < n; ++i)
+      if (d[i].M > 0 && ((d[i].y_q != nullptr) != qout || (qout && d[i].y_q_mode != r.y_q_mode)))
+        return fail(LOKA_ERR_UNSUPPORTED, "group %d: set y_q (with one y_q_mode) in every group or in none", i);
+  }
+  if (qout) {
+    if (a.mode == kBf16) return fail(LOKA_ERR_UNSUPPORTED, "y_q is produced by the FP8 modes, not LOKA_BF16");
+    if (r.y_q_mode == kScaleTensor)
+      return fail(LOKA_ERR_UNSUPPORTED,
+                  "y_q_mode LOKA_SCALE_TENSOR: a tensor-wide scale needs every row's amax before the first code "
+                  "(use LOKA_SCALE_ROW or LOKA_SCALE_MX32)");
+    if (r.y_q_mode != kScaleRow && r.y_q_mode != kScaleMx32)
+      return fail(LOKA_ERR_INVALID_ARG, "y_q_mode %d is not a LOKA_SCALE_* value", r.y_q_mode);
+    if (r.y_q_mode == kScaleRow && a.N > 256)
+      return fail(LOKA_ERR_UNSUPPORTED, "y_q_mode LOKA_SCALE_ROW needs N <= 256 (a row within one thread block)");
+  }
   for (int i = 0; i < n; ++i) {
     const loka_linear_desc& g = d[i];
     if (g.M == 0) continue;
-    if (g.x == nullptr || g.w == nullptr || (!probe && g.y == nullptr))
+    if (g.x == nullptr || g.w == nullptr || (!probe && !qout && g.y == nullptr))
       return fail(LOKA_ERR_INVALID_ARG, "group %d: x, w and y must not be NULL", i);
     if (!aligned16(g.x) || !aligned16(g.w) || (!probe && !aligned16(g.y)))
       return fail(LOKA_ERR_INVALID_ARG, "group %d: x, w and y must be 16-byte aligned", i);
+    if (qout) {
+      if (g.y_q_scales == nullptr) return fail(LOKA_ERR_INVALID_ARG, "group %d: y_q_scales is NULL", i);
+      if (!aligned16(g.y_q)) return fail(LOKA_ERR_INVALID_ARG, "group %d: y_q must be 16-byte aligned", i);
+      if (r.y_q_mode == kScaleRow && (reinterpret_cast<uintptr_t>(g.y_q_scales) & 3u))
+        return fail(LOKA_ERR_INVALID_ARG, "group %d: y_q_scales must be 4-byte aligned", i);
+    }
     if (g.x_is_fp8 && g.x_scales == nullptr) return fail(LOKA_ERR_INVALID_ARG, "group %d: x_scales is NULL", i);
     if (g.w_is_fp8 && g.w_scales == nullptr) return fail(LOKA_ERR_INVALID_ARG, "group %d: w_scales is NULL", i);
   }
@@ -272,11 +306,10 @@ loka_status build_gemm(const loka_linear_desc* d, int n, const std::vector<Opera
         G.sw_per_row = mode == kScaleRow;
       }
     }
-    if (out == OutKind::kBf16)
-      s = encode_2d(&G.tm_y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y, g.N, g.M, 128);
-    else
-      s = encode_2d(&G.tm_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, y, g.N, g.M, 128);
-    if (s != LOKA_OK) return s;
+    if (out == OutKind::kQuant) {
+      G.yq = static_cast<uint8_t*>(g.y_q);
+      G.yq_scales = g.y_q_scales;
+    }
   }
   p->num_groups = n;
   p->total_tiles = tiles;
@@ -285,6 +318,7 @@ loka_status build_gemm(const loka_linear_desc* d, int n, const std::vector<Opera
   p->eps = d[0].eps;
   p->status = dev->status;
   p->wait_limit_ns = kDefaultWaitLimitNs;
+  p->yq_mode = out == OutKind::kQuant ? output_reference(d, n).y_q_mode : 0;
   return LOKA_OK;
 }
 
@@ -447,15 +481,14 @@ loka_status loka_fp8_linear_norm(const loka_linear_desc* descs, int32_t num_grou
     }
   }
   static thread_local GemmParams p;
-  if ((s = build_gemm(descs, num_groups, slots, ws, bf16, OutKind::kBf16, nullptr, descs[0].norm, dev, &p)) != LOKA_OK)
-    return s;
+  const OutKind out = output_reference(descs, num_groups).y_q != nullptr ? OutKind::kQuant : OutKind::kBf16;
+  if ((s = build_gemm(descs, num_groups, slots, ws, bf16, out, nullptr, descs[0].norm, dev, &p)) != LOKA_OK) return s;
   // Caller-quantized W may load before the GEMM waits for the launch that
   // precedes it only when that launch is this call's own activation
   // quantizer: it started after everything the caller queued (W included)
   // had finished.  (MX also permutes W's scales right before the GEMM.)
   p.w_ready = (!bf16 && descs[0].w_is_fp8 && !descs[0].x_is_fp8 && descs[0].mode != kScaleMx32) ? 1 : 0;
-  cudaError_t e = launch_gemm_norm(p, static_cast<int>(descs[0].N), operand_kind(descs[0].mode), OutKind::kBf16,
-                                   dev->sms, st);
+  cudaError_t e = launch_gemm_norm(p, static_cast<int>(descs[0].N), operand_kind(descs[0].mode), out, dev->sms, st);
   if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
   return LOKA_OK;
 }

@@ -1,0 +1,14 @@
+// Instantiations of the fused GEMM + normalization kernel for bf16 operands
+// (the high-precision path), with bf16 or fp32 output.
+#include "gemm_norm.cuh"
+
+namespace loka {
+
+cudaError_t launch_gemm_bf16(GemmParams& p, int N, OutKind out, int sms, cudaStream_t stream) {
+  constexpr int op = static_cast<int>(OperandKind::kBf16);
+  if (out == OutKind::kBf16) return launch_kind<op, static_cast<int>(OutKind::kBf16)>(p, N, sms, stream);
+  if (out == OutKind::kF32) return launch_kind<op, static_cast<int>(OutKind::kF32)>(p, N, sms, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace loka

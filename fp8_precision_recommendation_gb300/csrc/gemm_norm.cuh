@@ -1,0 +1,1071 @@
+// Fused FP8 GEMM + dequant + bias + LayerNorm/RMSNorm + store, for sm_103a
+// (private to the gemm_*.cu files: each instantiates the operand and output
+// kinds it names, so the instantiations compile in parallel; gemm_norm.cu
+// dispatches to them).
+//
+// Defined by "LoKA: Low-precision Kernel Applications for Recommendation
+// Models at Scale": section II-C (the FP8 linear y = Wx + b whose error and
+// speed the probe measures), section III-B "Block-wise Normalization" (fuse
+// the normalization into the GEMM epilogue while the output tile is on chip;
+// case 1: large batch, small N, a whole output row lives in one thread block,
+// so the statistics are local and (de)quantization fuses in too) and
+// section I (LRMs are wide ensembles of small GEMMs: several independent
+// layers share one launch here).  The quantized output kind follows the GEM
+// Training page ("Handling Quantization Overhead": activation quantization
+// fused into the preceding normalization; "Low Precision Flash Attention":
+// the fused kernels emit FP8 activations with their scales): the epilogue
+// also writes the normalized rows as E4M3 codes with per-row or MX 1x32
+// scales, exactly what the standalone quantizer makes of the bf16 output, so
+// the next layer takes them as pre-quantized activations.
+//
+// Design (one CTA per SM, persistent, warp-specialized, 576 threads):
+//   warp 0       TMA producer: 128-byte K slices of A (and of B when W does
+//                not stay resident) into a shared-memory ring, 128B-swizzled,
+//                one mbarrier per stage.  When N x K of the weights fits in
+//                128 KB, W is loaded once per CTA (per group) and stays in
+//                shared memory, so each tile streams only its activations.
+//   warp 1       allocates tensor memory and issues tcgen05.mma (one thread);
+//                the fp32 accumulator of a 128 x N tile lives in TMEM, double
+//                buffered when 2N <= 512 columns so the epilogue of tile i
+//                overlaps the MMAs of tile i+1.
+//   warps 2..17  epilogue, two teams of 8 warps taking alternate tiles (and
+//                accumulator buffers); each warp owns 16 whole rows of its
+//                team's tile.  tcgen05.ld.16x256b gives every thread 2 rows
+//                x 8 columns of a 32-column chunk, so a per-column value
+//                (scale, bias, gamma, beta) read from shared memory serves
+//                both rows, and the math runs on packed fp32 pairs
+//                (fma/mul/add .f32x2); TMEM reads are pipelined one chunk
+//                ahead.  Row statistics are fp32 shifted sums (LayerNorm) or
+//                sums of squares (RMSNorm), merged across the 4 lanes of a
+//                row (shuffles) and, for rows wider than one CTA, across the
+//                cluster's CTAs (distributed shared memory).  Normalized rows
+//                are rounded, transposed across the 4 lanes and stored as
+//                contiguous 16-byte (bf16) or 8-byte (E4M3) pieces.
+// The output makes no extra HBM round trip: Y is written once.
+#pragma once
+
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <type_traits>
+
+#include "loka_internal.h"
+#include "ptx.cuh"
+#include "quant_math.cuh"
+
+namespace loka {
+
+namespace {
+
+constexpr int kBM = 128;                 // rows per tile (= TMEM lanes)
+constexpr int kSliceBytes = 128;         // bytes of K per stage per row
+constexpr uint32_t kABytes = kBM * kSliceBytes;
+constexpr int kTmemCols = 512;
+constexpr int kThreads = 576;             // producer, MMA, 16 epilogue warps
+constexpr int kEpiBar = 1;               // named barrier id for the epilogue warps
+constexpr int kMaxStages = 8;
+constexpr int kMaxWSlices = 16;          // resident W: 128 KB / (64 rows x 128 bytes)
+constexpr size_t kSmemLimit = 227 * 1024;
+constexpr size_t kResidentWLimit = 128 * 1024;
+
+// Shared-memory carve-up (all offsets from a 1024-byte-aligned base):
+//   ring     stages x (A slice [| B slice])
+//   w        resident W: K/KE slices of N rows x 128 bytes (when resident)
+//   vectors  2 teams x 4 x N fp32 (weight scale, bias, gamma, beta)
+//   stats    clusters: 2 x CL x 128 float2 row statistics of the CTAs
+//   barriers
+struct Layout {
+  uint32_t stage_bytes, ring, w, vec, stats, bars, total;
+};
+
+// MX scale blocks: 512 bytes per 128 rows per 128-element K slice.
+constexpr uint32_t kSfBlock = 512;
+__host__ __device__ constexpr int sfb_blocks(int N) { return (N + 127) / 128; }
+
+__host__ __device__ inline Layout make_layout(int N, int K, int elem_bytes, bool resident, int stages, bool mx,
+                                              int cl = 1) {
+  Layout L;
+  const uint32_t b_slice = static_cast<uint32_t>(N) * kSliceBytes;
+  const uint32_t sfa = mx ? kSfBlock : 0u;
+  const uint32_t sfb = mx ? kSfBlock * sfb_blocks(N) : 0u;
+  // stage: [A slice][B slice, streamed W][A scales][B scales, streamed W]
+  L.stage_bytes = kABytes + (resident ? 0u : b_slice) + sfa + (resident ? 0u : sfb);
+  L.ring = 0;
+  L.w = L.ring + static_cast<uint32_t>(stages) * L.stage_bytes;
+  const int nkb = K * elem_bytes / kSliceBytes;
+  // resident W: [nkb B slices][nkb x B scale blocks]
+  const uint32_t w_bytes = resident ? static_cast<uint32_t>(nkb) * (b_slice + sfb) : 0u;
+  L.vec = L.w + w_bytes;
+  L.stats = L.vec + 2u * 4u * N * sizeof(float);
+  // [2][cluster][128] row statistics of the cluster's CTAs (written
+  // remotely, double-buffered by tile parity)
+  L.bars = L.stats + (cl > 1 ? 2u * cl * kBM * sizeof(float2) : 0u);
+  L.total = L.bars + 512;
+  return L;
+}
+
+__device__ __forceinline__ int group_of(const GemmParams& p, int tile) {
+  int g = 0;
+  while (g + 1 < p.num_groups && p.g[g + 1].tile_begin <= tile) ++g;
+  return g;
+}
+
+__device__ __forceinline__ float bf16_to_f(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
+
+__device__ __forceinline__ float2 dup2(float a) { return make_float2(a, a); }
+
+// N = the columns this CTA owns (<= 256); CL = CTAs per cluster sharing each
+// 128-row tile (the layer's output has N * CL columns; CTA r owns columns
+// [r N, r N + N) and the CTAs of a cluster merge their row statistics
+// through distributed shared memory, so a row wider than one CTA's tensor
+// memory is still normalized in the epilogue).
+template <int N, int CL, int OP, int OUT, bool RESIDENT>
+__global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_constant__ GemmParams p) {
+  static_assert(N <= 256, "one MMA per K step");
+  constexpr int NG = N * CL;                        // columns of the whole output row
+  constexpr int SF_COLS_MAX = OP == static_cast<int>(OperandKind::kMxE4M3) ? kMaxStages * (4 + 4 * sfb_blocks(N)) : 0;
+  constexpr int NBUF = (2 * N + SF_COLS_MAX <= kTmemCols) ? 2 : 1;
+  static_assert(N + SF_COLS_MAX <= kTmemCols, "accumulator and scale factors must fit in tensor memory");
+  constexpr int N_MMA = N > 256 ? 256 : N;
+  constexpr int N_SPLIT = N / N_MMA;
+  constexpr bool kBf16Op = OP == static_cast<int>(OperandKind::kBf16);
+  constexpr bool kMx = OP == static_cast<int>(OperandKind::kMxE4M3);
+  constexpr int NSFB = sfb_blocks(N);
+  constexpr uint32_t SFB_BYTES = kMx ? kSfBlock * NSFB : 0u;
+  constexpr uint32_t SF_COLS = kMx ? 4 + 4 * NSFB : 0;    // TMEM columns of one stage's scales
+  constexpr int EB = kBf16Op ? 2 : 1;               // operand element bytes
+  constexpr int KE = kSliceBytes / EB;              // K elements per 128-byte slice
+  constexpr uint32_t IDESC = kBf16Op ? idesc_dense(1, 1, kBM, N_MMA)    // bf16 x bf16 -> f32
+                                     : idesc_dense(0, 0, kBM, N_MMA);   // e4m3 x e4m3 -> f32
+  constexpr uint32_t B_SLICE = static_cast<uint32_t>(N) * kSliceBytes;
+
+  const int stages = p.stages;
+  const int num_kb = p.K / KE;
+  const Layout L = make_layout(N, p.K, EB, RESIDENT, stages, kMx, CL);
+  const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
+  const int col0 = static_cast<int>(rank) * N;      // first output column of this CTA
+  const int cid = static_cast<int>(blockIdx.x) / CL;
+  const int ncl = static_cast<int>(gridDim.x) / CL;
+
+  // Pointers are derived from the __shared__ array by plain offsets, so the
+  // compiler keeps them in the shared address space (LDS/STS, not generic
+  // loads).  The 128B-swizzled TMA/UMMA tiles need the 1024-byte alignment.
+  extern __shared__ __align__(1024) uint8_t smem[];
+  // uniform over the CTA; a misaligned CTA skips all work but still takes
+  // part in the cluster barriers below
+  const bool misaligned = (smem_u32(smem) & 1023u) != 0;
+  uint8_t* ring = smem + L.ring;
+  uint8_t* wres = smem + L.w;
+  float* vec_base = reinterpret_cast<float*>(smem + L.vec);        // [2 teams][4][N]
+  float2* cl_stats = reinterpret_cast<float2*>(smem + L.stats);     // [2][CL][128] cluster row statistics
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* full = bars;
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* tfull = empty + kMaxStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* mma_done = tempty + 2;
+  uint64_t* w_free = mma_done + 1;
+  uint64_t* cl_bar = w_free + 1;                                    // [2] cluster statistics arrivals
+  uint64_t* cl_free = cl_bar + 2;                                   // [2] cluster statistics buffers read
+  uint64_t* w_full = cl_free + 2;                                   // [16] resident W, one per K slice
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(w_full + kMaxWSlices);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < NBUF; ++b) {
+      mbar_init(smem_u32(&tfull[b]), 1);
+      mbar_init(smem_u32(&tempty[b]), 8);   // the eight warps of the team that owns buffer b
+    }
+    mbar_init(smem_u32(mma_done), 1);
+    for (int kb = 0; kb < kMaxWSlices; ++kb) mbar_init(smem_u32(&w_full[kb]), 1);
+    mbar_init(smem_u32(w_free), 1);
+    // a tile's statistics: one arming arrival plus the bytes sent by the
+    // other CTAs; its buffer is freed by 8 warps of every CTA
+    mbar_init(smem_u32(&cl_bar[0]), 1);
+    mbar_init(smem_u32(&cl_bar[1]), 1);
+    mbar_init(smem_u32(&cl_free[0]), 8 * CL);
+    mbar_init(smem_u32(&cl_free[1]), 8 * CL);
+    *abort_flag = misaligned ? 1 : 0;
+    if (misaligned) atomicOr(p.status, kErrMisaligned);
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int g = 0; g < p.num_groups; ++g) {
+      if (p.g[g].M == 0) continue;   // no tiles, descriptors not encoded
+      tma_prefetch_desc(&p.g[g].tm_a);
+      tma_prefetch_desc(&p.g[g].tm_b);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // no CTA touches a partner's shared memory before the partner has set up
+  // its barriers
+  if (CL > 1) cluster_sync_all();
+  // resident W for this CTA's first group.  When the caller's W was
+  // complete before the launch that precedes this one, it loads now, while
+  // that launch (the activation quantizer) may still run.
+  // Each K slice of W has its own barrier, so the first tile's MMAs start
+  // on slice 0 while later slices are still arriving.
+  auto load_w_slice = [&](int g, int kb) {
+    const uint32_t wb = smem_u32(&w_full[kb]);
+    mbar_arrive_expect_tx(wb, B_SLICE + SFB_BYTES);
+#pragma unroll
+    for (int s = 0; s < N_SPLIT; ++s)
+      tma_load_2d(smem_u32(wres + kb * B_SLICE + s * N_MMA * kSliceBytes), &p.g[g].tm_b, wb, kb * KE,
+                  col0 + s * N_MMA);
+    if (kMx) {
+#pragma unroll
+      for (int h = 0; h < NSFB; ++h)
+        bulk_load_1d(smem_u32(wres + num_kb * B_SLICE + (kb * NSFB + h) * kSfBlock),
+                     p.g[g].sfb_tc + (static_cast<int64_t>(rank * NSFB + h) * num_kb + kb) * kSfBlock,
+                     kSfBlock, wb);
+    }
+  };
+  auto load_w = [&](int g) {
+    for (int kb = 0; kb < num_kb; ++kb) load_w_slice(g, kb);
+  };
+  int w_early_group = -1;
+  if (RESIDENT && p.w_ready && !misaligned && warp == 0 && lane == 0 && cid < p.total_tiles) {
+    w_early_group = group_of(p, cid);
+    load_w(w_early_group);
+  }
+  // everything above touches only this CTA's own state (and W when it was
+  // ready); inputs written by the kernel before this one (the quantized
+  // operands) are read below
+  wait_prerequisite_grids();
+  const uint32_t tmem_base = *tmem_slot;
+  const Watchdog wd{abort_flag, p.status, p.wait_limit_ns};
+
+  if (misaligned) {
+    // nothing to do: fall through to the teardown barriers
+  } else if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, last_parity = 0;
+      int cur_group = w_early_group, w_loads = w_early_group >= 0 ? 1 : 0;
+      uint32_t w_issued = w_early_group >= 0 ? 0xFFFFFFFFu : 0u;   // slices of the current W load issued
+      bool w_pending = false;   // the current group's W slices go out with its first tile's A slices
+      bool ok = true;
+      for (int tile = cid; ok && tile < p.total_tiles; tile += ncl) {
+        const int g = group_of(p, tile);
+        const int m0 = (tile - p.g[g].tile_begin) * kBM;
+        if (RESIDENT && g != cur_group) {
+          // reload the resident weights once the MMAs of the previous group are done with them
+          if (w_loads > 0 && !wait_parity(wd, smem_u32(w_free), (w_loads - 1) & 1, kErrProducerWait)) {
+            ok = false;
+            break;
+          }
+          w_pending = true;
+          w_issued = 0;
+          ++w_loads;
+          cur_group = g;
+        }
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_parity(wd, smem_u32(&empty[stage]), phase ^ 1u, kErrProducerWait)) {
+            ok = false;
+            break;
+          }
+          if (RESIDENT && w_pending) {
+            load_w_slice(g, kb);
+            w_issued |= 1u << kb;
+          }
+          uint8_t* a_dst = ring + static_cast<size_t>(stage) * L.stage_bytes;
+          const uint32_t fb = smem_u32(&full[stage]);
+          mbar_arrive_expect_tx(fb, L.stage_bytes);
+          tma_load_2d(smem_u32(a_dst), &p.g[g].tm_a, fb, kb * KE, m0);
+          if (!RESIDENT) {
+            uint8_t* b_dst = a_dst + kABytes;
+#pragma unroll
+            for (int s = 0; s < N_SPLIT; ++s)
+              tma_load_2d(smem_u32(b_dst + s * N_MMA * kSliceBytes), &p.g[g].tm_b, fb, kb * KE, col0 + s * N_MMA);
+          }
+          if (kMx) {
+            uint8_t* sf_dst = a_dst + kABytes + (RESIDENT ? 0u : B_SLICE);
+            bulk_load_1d(smem_u32(sf_dst), p.g[g].sfa_tc + (static_cast<int64_t>(m0 >> 7) * num_kb + kb) * kSfBlock,
+                         kSfBlock, fb);
+            if (!RESIDENT) {
+#pragma unroll
+              for (int h = 0; h < NSFB; ++h)
+                bulk_load_1d(smem_u32(sf_dst + kSfBlock + h * kSfBlock),
+                             p.g[g].sfb_tc + (static_cast<int64_t>(rank * NSFB + h) * num_kb + kb) * kSfBlock,
+                             kSfBlock, fb);
+            }
+          }
+          issued |= 1u << stage;
+          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        w_pending = false;
+      }
+      if (!ok) {
+        // let the copies already in flight land before the CTA exits
+        for (int s = 0; s < stages; ++s)
+          if (issued & (1u << s)) wait_parity_drain(wd, smem_u32(&full[s]), (last_parity >> s) & 1u);
+        if (RESIDENT && w_loads > 0) {
+          for (int kb = 0; kb < num_kb; ++kb)
+            if (w_issued & (1u << kb)) wait_parity_drain(wd, smem_u32(&w_full[kb]), (w_loads - 1) & 1);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      int cur_group = -1, w_uses = 0;
+      bool ok = true;
+      for (int tile = cid; ok && tile < p.total_tiles; tile += ncl, ++local) {
+        if (RESIDENT) {
+          const int g = group_of(p, tile);
+          if (g != cur_group) {
+            if (w_uses > 0) mma_commit(smem_u32(w_free));   // previous weights free once these MMAs finish
+            ++w_uses;
+            cur_group = g;
+          }
+        }
+        const int buf = NBUF == 2 ? (local & 1) : 0;
+        const uint32_t use = NBUF == 2 ? (local >> 1) : local;
+        if (!wait_parity(wd, smem_u32(&tempty[buf]), (use & 1u) ^ 1u, kErrMmaWait)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * N);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          // this K slice of the resident W (complete at once after the
+          // group's first tile)
+          if (RESIDENT && !wait_parity(wd, smem_u32(&w_full[kb]), (w_uses - 1) & 1, kErrMmaWait)) {
+            ok = false;
+            break;
+          }
+          if (!wait_parity(wd, smem_u32(&full[stage]), phase, kErrMmaWait)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(ring + static_cast<size_t>(stage) * L.stage_bytes);
+          const uint32_t b_addr = RESIDENT ? smem_u32(wres + kb * B_SLICE) : a_addr + kABytes;
+          uint32_t sfa_tmem = 0, sfb_tmem = 0;
+          if (kMx) {
+            // E8M0 codes of this K slice into tensor memory: A's 128 rows to
+            // 4 columns, B's rows to 4 columns per 128 rows
+            const uint32_t sfa_smem = a_addr + kABytes + (RESIDENT ? 0u : B_SLICE);
+            const uint32_t sfb_smem = RESIDENT ? smem_u32(wres + num_kb * B_SLICE + kb * NSFB * kSfBlock)
+                                               : sfa_smem + kSfBlock;
+            sfa_tmem = tmem_base + static_cast<uint32_t>(NBUF * N + stage * SF_COLS);
+            sfb_tmem = sfa_tmem + 4;
+            tmem_cp_32x128b_warpx4(sfa_tmem, sdesc_rows16(sfa_smem));
+#pragma unroll
+            for (int h = 0; h < NSFB; ++h) tmem_cp_32x128b_warpx4(sfb_tmem + 4 * h, sdesc_rows16(sfb_smem + h * kSfBlock));
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t adesc = sdesc_k128_sw128(a_addr + k * 32);
+#pragma unroll
+            for (int s = 0; s < N_SPLIT; ++s) {
+              const uint64_t bdesc = sdesc_k128_sw128(b_addr + s * N_MMA * kSliceBytes + k * 32);
+              const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
+              if (kBf16Op)
+                mma_f16(d_tmem + s * N_MMA, adesc, bdesc, IDESC, acc);
+              else if (kMx)
+                mma_mxf8f6f4(d_tmem + s * N_MMA, adesc, bdesc, idesc_mx(kBM, N_MMA, k), sfa_tmem, sfb_tmem, acc);
+              else
+                mma_f8f6f4(d_tmem + s * N_MMA, adesc, bdesc, IDESC, acc);
+            }
+          }
+          mma_commit(smem_u32(&empty[stage]));   // frees the slot once these MMAs finish
+          if (++stage == stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&tfull[buf]));
+      }
+      // all MMAs issued by this thread complete before tensor memory is freed
+      mma_commit(smem_u32(mma_done));
+      wait_parity_drain(wd, smem_u32(mma_done), 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    // Sixteen warps in two teams of eight.  Team e takes the tiles whose
+    // local index is e (mod 2), i.e. accumulator buffer e, so two tiles are
+    // normalized at once (with one accumulator buffer team 0 takes every
+    // tile).  In a team, warp (quad q, row half h) owns rows
+    // 32q + 16h .. 32q + 16h + 15 of the tile over all of this CTA's N
+    // columns, so its row statistics need only 4-lane shuffles and no
+    // barrier couples the warps of a tile.  The 16x256b load shape gives
+    // thread t rows t/4 + {0, 8} of the 16 and column pairs 8i + 2(t%4) of
+    // each 32-column chunk; a per-column value read from shared memory serves
+    // both rows.  Chunk reads are pipelined one ahead.
+    const int ew = warp - 2;                        // 0..15
+    const int team = NBUF == 2 ? (ew >> 3) : 0;
+    const bool active = NBUF == 2 || ew < 8;
+    const int tstep = NBUF == 2 ? 2 : 1;            // a team's tiles are tstep apart
+    const uint32_t team_bar = kEpiBar + static_cast<uint32_t>(team);
+    const int quad = warp & 3;                      // TMEM lane quadrant this warp may access
+    const int rh = (ew >> 2) & 1;                   // row half of the quadrant
+    const int g4 = lane >> 2;                       // row within each 8-row group
+    const int cp = lane & 3;                        // column pair within each 8-column group
+    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32 + rh * 16) << 16;
+    constexpr int NCHUNK = N / 32;
+    constexpr bool kBf16Out = OUT == static_cast<int>(OutKind::kBf16);
+    constexpr bool kQOut = OUT == static_cast<int>(OutKind::kQuant);
+    const int norm = p.norm;
+    const float eps = p.eps;
+    float* vec_sw = vec_base + team * 4 * N;        // this team's copy of the column vectors
+    float* vec_b = vec_sw + N;
+    float* vec_g = vec_b + N;
+    float* vec_be = vec_g + N;
+    int rowk[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) rowk[k] = quad * 32 + rh * 16 + g4 + 8 * k;
+
+    // activation scales of a tile's two rows of this thread (per-tensor
+    // weight scales fold in); loaded one tile ahead to hide the latency
+    auto row_scales = [&](int tile, float (&out)[2]) {
+      const int g = group_of(p, tile);
+      const GemmGroup& G = p.g[g];
+      const int m0 = (tile - G.tile_begin) * kBM;
+      const float swc = (G.sw != nullptr && !G.sw_per_row) ? G.sw[0] : 1.0f;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int64_t m = static_cast<int64_t>(m0) + rowk[k];
+        float sx = 1.0f;
+        if (G.sx != nullptr) sx = G.sx_per_row ? (m < G.M ? G.sx[m] : 0.0f) : G.sx[0];
+        out[k] = sx * swc;
+      }
+    };
+    auto vec2 = [&](const float* vec, int c0, int i) {
+      return *reinterpret_cast<const float2*>(vec + c0 + 8 * i + 2 * cp);
+    };
+    auto acc2 = [&](const uint32_t (&r)[16], int k, int i) {
+      const int o = 4 * i + 2 * k;
+      return make_float2(__uint_as_float(r[o]), __uint_as_float(r[o + 1]));
+    };
+    // Runs fn(r, c) over the chunks c = 0 .. NCHUNK-1, the TMEM read of chunk
+    // c + 1 in flight while chunk c is processed.
+    auto for_chunks = [&](uint32_t t_base, auto&& fn) {
+      uint32_t r[2][16];
+      tmem_ld_16x256b_x4(t_base, r[0]);
+      tmem_ld_wait();
+      reg_fence(r[0]);
+#pragma unroll
+      for (int c = 0; c < NCHUNK; ++c) {
+        if (c + 1 < NCHUNK) tmem_ld_16x256b_x4(t_base + (c + 1) * 32, r[(c + 1) & 1]);
+        fn(r[c & 1], c);
+        if (c + 1 < NCHUNK) {
+          tmem_ld_wait();
+          reg_fence(r[(c + 1) & 1]);
+        }
+      }
+    };
+    // v = acc * sx (* sw) + b for the pair; SWV: per-column weight scales
+    // (rowwise W); otherwise they are folded into the row factor
+    auto vpair = [&](auto swv_tag, const uint32_t (&r)[16], int k, int i, float2 sx2, float2 sw, float2 b) {
+      constexpr bool SWV = decltype(swv_tag)::value;
+      if constexpr (SWV)
+        return __ffma2_rn(__fmul2_rn(acc2(r, k, i), sx2), sw, b);
+      else
+        return __ffma2_rn(acc2(r, k, i), sx2, b);
+    };
+    // one lane waits, the whole warp follows its verdict
+    auto warp_wait = [&](uint32_t bar, uint32_t parity, bool cluster_scope) {
+      int okw = 1;
+      if (lane == 0)
+        okw = (cluster_scope ? wait_parity_cluster(wd, bar, parity, kErrClusterWait)
+                             : wait_parity(wd, bar, parity, kErrEpilogueWait)) ? 1 : 0;
+      return __shfl_sync(0xffffffffu, okw, 0) != 0;
+    };
+
+    int cur_group = -1;
+    bool has_swv = false, affine = false;
+    float sx_next[2] = {1.f, 1.f};
+    int local = team;
+    int tile = cid + team * ncl;
+    if (active && tile < p.total_tiles) row_scales(tile, sx_next);
+    for (; active && tile < p.total_tiles; tile += tstep * ncl, local += tstep) {
+      const int g = group_of(p, tile);
+      const GemmGroup& G = p.g[g];
+      if (g != cur_group) {
+        // this team's column vectors for the group; the barrier's OR makes
+        // the abort decision the same for all of the team's warps
+        if (named_bar_or(team_bar, 256, *abort_flag != 0)) break;
+        const bool normed = norm != kNormNone;
+        for (int n = (ew & 7) * 32 + lane; n < N; n += 256) {
+          const int gn = col0 + n;
+          vec_sw[n] = (G.sw != nullptr && G.sw_per_row) ? G.sw[gn] : 1.0f;
+          vec_b[n] = G.bias == nullptr ? 0.0f : bf16_to_f(G.bias[gn]);
+          vec_g[n] = (G.gamma == nullptr || !normed) ? 1.0f : bf16_to_f(G.gamma[gn]);
+          vec_be[n] = (G.beta == nullptr || norm != kNormLayer) ? 0.0f : bf16_to_f(G.beta[gn]);
+        }
+        has_swv = G.sw != nullptr && G.sw_per_row;
+        affine = normed && (G.gamma != nullptr || (G.beta != nullptr && norm == kNormLayer));
+        named_bar_sync(team_bar, 256);
+        cur_group = g;
+      }
+      const float sxr[2] = {sx_next[0], sx_next[1]};
+      const int m0 = (tile - G.tile_begin) * kBM;
+      // output row addresses and validity, once per tile
+      const int64_t Mg = G.M;
+      uint8_t* rowp[2];
+      uint32_t ok[2];
+      // E4M3 codes of row rowk[0]; those of rowk[1] are 8 rows further
+      [[maybe_unused]] uint8_t* rowq = nullptr;
+      [[maybe_unused]] const bool has_y = G.y != nullptr;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int64_t m = static_cast<int64_t>(m0) + rowk[k];
+        ok[k] = m < Mg ? 1u : 0u;
+        // bf16: the 4 lanes of a row group store 16 contiguous bytes each
+        // after a transpose; fp32: column pairs straight from registers;
+        // E4M3 codes: 8 contiguous bytes per lane after a transpose
+        constexpr bool kWide = kBf16Out || kQOut;
+        rowp[k] = reinterpret_cast<uint8_t*>(reinterpret_cast<uintptr_t>(G.y) +
+                                             (m * NG + col0 + (kWide ? 8 : 2) * cp) * (kWide ? 2 : 4));
+        if constexpr (kQOut) {
+          if (k == 0) rowq = G.yq + m * NG + col0 + 8 * cp;
+        }
+      }
+      const int buf = NBUF == 2 ? team : 0;
+      const uint32_t use = NBUF == 2 ? static_cast<uint32_t>(local >> 1) : static_cast<uint32_t>(local);
+      if (!warp_wait(smem_u32(&tfull[buf]), use & 1u, false)) break;
+      tc_fence_after();
+      if (tile + tstep * ncl < p.total_tiles) row_scales(tile + tstep * ncl, sx_next);
+      const uint32_t t_base = tmem_base + lane_addr + static_cast<uint32_t>(buf * N);
+      const float2 sx2[2] = {dup2(sxr[0]), dup2(sxr[1])};
+
+      // pass 1: row statistics of v = acc * sx * sw + b
+      float mean[2] = {0.f, 0.f}, m2[2] = {0.f, 0.f};
+      // extremes of v, kept when they decide the E4M3 row scale (see below)
+      [[maybe_unused]] float vhi[2] = {-INFINITY, -INFINITY}, vlo[2] = {INFINITY, INFINITY};
+      auto stats_pass = [&](auto swv_tag, auto trk_tag) {
+        if (norm == kNormLayer) {
+          // shifted sums: with K the mean of the row's first 8-value piece,
+          // s1 += v - K and s2 += (v - K)^2; no division, little cancellation
+          float shift[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};
+          for_chunks(t_base, [&](const uint32_t (&r)[16], int c) {
+            const int c0 = c * 32;
+            float2 sw[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              if constexpr (decltype(swv_tag)::value) sw[i] = vec2(vec_sw, c0, i);
+              b[i] = vec2(vec_b, c0, i);
+            }
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              float2 v[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) v[i] = vpair(swv_tag, r, k, i, sx2[k], sw[i], b[i]);
+              if constexpr (decltype(trk_tag)::value) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  vhi[k] = max3f(vhi[k], v[i].x, v[i].y);
+                  vlo[k] = min3f(vlo[k], v[i].x, v[i].y);
+                }
+              }
+              if (c == 0) {
+                const float2 t = __fadd2_rn(__fadd2_rn(v[0], v[1]), __fadd2_rn(v[2], v[3]));
+                shift[k] = (t.x + t.y) * 0.125f;
+              }
+              const float2 nk = dup2(-shift[k]);
+              float2 a1 = make_float2(0.f, 0.f), a2 = make_float2(0.f, 0.f);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float2 d = __fadd2_rn(v[i], nk);
+                a1 = __fadd2_rn(a1, d);
+                a2 = __ffma2_rn(d, d, a2);
+              }
+              s1[k] += a1.x + a1.y;
+              m2[k] += a2.x + a2.y;
+            }
+          });
+          constexpr float kInvMe = 1.0f / (8.0f * NCHUNK);
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const float d = s1[k] * kInvMe;
+            mean[k] = shift[k] + d;
+            m2[k] = fmaxf(m2[k] - s1[k] * d, 0.0f);
+          }
+        } else if (norm == kNormRms) {
+          for_chunks(t_base, [&](const uint32_t (&r)[16], int c) {
+            const int c0 = c * 32;
+            float2 sw[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              if constexpr (decltype(swv_tag)::value) sw[i] = vec2(vec_sw, c0, i);
+              b[i] = vec2(vec_b, c0, i);
+            }
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              float2 q = make_float2(0.f, 0.f);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float2 v = vpair(swv_tag, r, k, i, sx2[k], sw[i], b[i]);
+                if constexpr (decltype(trk_tag)::value) {
+                  vhi[k] = max3f(vhi[k], v.x, v.y);
+                  vlo[k] = min3f(vlo[k], v.x, v.y);
+                }
+                q = __ffma2_rn(v, v, q);
+              }
+              m2[k] += q.x + q.y;
+            }
+          });
+        }
+      };
+      // E4M3 row output without gamma and beta: the extremes of v give the
+      // row's amax (see below), so the statistics pass keeps them
+      [[maybe_unused]] const bool track =
+          kQOut && CL == 1 && p.yq_mode == kScaleRow && norm != kNormNone && !affine;
+      if (kQOut && CL == 1 && track) {
+        if (has_swv) stats_pass(std::true_type{}, std::true_type{});
+        else stats_pass(std::false_type{}, std::true_type{});
+      } else {
+        if (has_swv) stats_pass(std::true_type{}, std::false_type{});
+        else stats_pass(std::false_type{}, std::false_type{});
+      }
+
+      float rstd[2] = {1.f, 1.f};
+      if (norm != kNormNone) {
+        // merge the 4 lanes of a row group (equal counts) with an ordered
+        // expression so all four end bit-identical
+#pragma unroll
+        for (int lvl = 0; lvl < 2; ++lvl) {
+          const int off = 1 << lvl;
+          const float half_n = 4.0f * NCHUNK * static_cast<float>(off);   // n_a n_b / (n_a + n_b)
+          const bool lo_side = (lane & off) == 0;
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const float om = __shfl_xor_sync(0xffffffffu, mean[k], off);
+            const float oq = __shfl_xor_sync(0xffffffffu, m2[k], off);
+            const float lm = lo_side ? mean[k] : om, hm = lo_side ? om : mean[k];
+            const float lq = lo_side ? m2[k] : oq, hq = lo_side ? oq : m2[k];
+            const float delta = hm - lm;
+            m2[k] = norm == kNormRms ? lq + hq : (lq + hq) + delta * delta * half_n;
+            mean[k] = norm == kNormRms ? 0.0f : 0.5f * (lm + hm);
+          }
+        }
+        if constexpr (CL > 1) {
+          // exchange (mean, M2) of this CTA's N columns with the cluster.
+          // Buffer cb holds the statistics of every other tile.  A writer
+          // waits until every CTA has read the buffer's previous contents
+          // (cl_free); the cp == 0 lanes then send their two rows to every
+          // other CTA with st.async, which the receiver's cl_bar counts in
+          // bytes, so no release (which would wait for this warp's earlier
+          // global stores) is needed.  One thread per CTA arms cl_bar with
+          // the bytes it receives; a warp's own rows come from registers.
+          const int cb = local & 1;
+          const uint32_t cphase = static_cast<uint32_t>(local >> 1) & 1u;
+          if ((ew & 7) == 0 && lane == 0) mbar_arrive_expect_tx(smem_u32(&cl_bar[cb]), kBM * 8 * (CL - 1));
+          if (!warp_wait(smem_u32(&cl_free[cb]), cphase ^ 1u, true)) break;
+          if (cp == 0) {
+#pragma unroll
+            for (int j = 0; j < CL; ++j) {
+              if (j == static_cast<int>(rank)) continue;
+              const uint32_t bar = mapa_shared(smem_u32(&cl_bar[cb]), j);
+#pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                const uint32_t a = smem_u32(&cl_stats[(cb * CL + static_cast<int>(rank)) * kBM + rowk[k]]);
+                st_async_f32x2(mapa_shared(a, j), mean[k], m2[k], bar);
+              }
+            }
+          }
+          if (!warp_wait(smem_u32(&cl_bar[cb]), cphase, true)) break;
+          // merge the CTAs' statistics in rank order (N elements each)
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            float mA = 0.f, qA = 0.f;
+#pragma unroll
+            for (int j = 0; j < CL; ++j) {
+              const float2 part_j = j == static_cast<int>(rank) ? make_float2(mean[k], m2[k])
+                                                                : cl_stats[(cb * CL + j) * kBM + rowk[k]];
+              if (norm == kNormRms) {
+                qA += part_j.y;
+              } else if (j == 0) {
+                mA = part_j.x;
+                qA = part_j.y;
+              } else {
+                const float delta = part_j.x - mA;
+                const float w = 1.0f / static_cast<float>(j + 1);          // n_b / n_total
+                mA = fmaf(delta, w, mA);
+                qA += part_j.y + delta * delta * (static_cast<float>(N) * j * w);
+              }
+            }
+            mean[k] = norm == kNormRms ? 0.0f : mA;
+            m2[k] = qA;
+          }
+          // this warp's reads of buffer cb are done (their values are
+          // consumed above): tell every CTA
+          __syncwarp();
+          if (lane == 0) {
+#pragma unroll
+            for (int j = 0; j < CL; ++j) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&cl_free[cb]), j));
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) rstd[k] = rsqrtf(m2[k] * (1.0f / NG) + eps);
+      }
+      // y = v * rstd - mean * rstd, then * gamma + beta when present
+      const float nmr[2] = {-mean[0] * rstd[0], -mean[1] * rstd[1]};
+      const float2 rstd2[2] = {dup2(rstd[0]), dup2(rstd[1])};
+      const float2 nmr2[2] = {dup2(nmr[0]), dup2(nmr[1])};
+      // the column vectors of pair i of chunk c0 (1, 0 where absent)
+      auto colv = [&](auto swv_tag, auto aff_tag, int c0, int i, float2& sw, float2& b, float2& gm, float2& be) {
+        sw = make_float2(1.f, 1.f);
+        gm = make_float2(1.f, 1.f);
+        be = make_float2(0.f, 0.f);
+        if constexpr (decltype(swv_tag)::value) sw = vec2(vec_sw, c0, i);
+        b = vec2(vec_b, c0, i);
+        if constexpr (decltype(aff_tag)::value) {
+          gm = vec2(vec_g, c0, i);
+          be = vec2(vec_be, c0, i);
+        }
+      };
+      // the normalized pair of row k: the one arithmetic of every pass below
+      auto ypair = [&](auto swv_tag, auto aff_tag, const uint32_t (&r)[16], int k, int i, float2 sw, float2 b,
+                       float2 gm, float2 be) {
+        const float2 v = vpair(swv_tag, r, k, i, sx2[k], sw, b);
+        float2 y = __ffma2_rn(v, rstd2[k], nmr2[k]);
+        if constexpr (decltype(aff_tag)::value) y = __ffma2_rn(y, gm, be);
+        return y;
+      };
+
+      // E4M3 output with one scale per row: the row's amax over its bf16
+      // outputs, then the standalone quantizer's scale selection, so the
+      // codes and scale equal what it makes of the bf16 row (NaN outputs
+      // never become the maximum there either).
+      [[maybe_unused]] float qinv[2] = {1.f, 1.f};
+      if constexpr (kQOut && CL == 1) {
+        if (p.yq_mode == kScaleRow) {
+          uint32_t am2[2] = {0u, 0u};   // |bf16| maxima, packed
+          if (track) {
+            // y = fma(v, rstd, -mean rstd) with rstd > 0 rounds a
+            // nondecreasing function of v, and bf16 rounding keeps the
+            // order: the row's largest and smallest outputs are those of
+            // its largest and smallest v
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+              am2[k] = absmax_bf16x2(0u, pack_bf16x2(__fmaf_rn(vhi[k], rstd[k], nmr[k]),
+                                                     __fmaf_rn(vlo[k], rstd[k], nmr[k])));
+          } else {
+            auto amax_pass = [&](auto swv_tag, auto aff_tag) {
+              for_chunks(t_base, [&](const uint32_t (&r)[16], int c) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  float2 sw, b, gm, be;
+                  colv(swv_tag, aff_tag, c * 32, i, sw, b, gm, be);
+#pragma unroll
+                  for (int k = 0; k < 2; ++k) {
+                    const float2 y = ypair(swv_tag, aff_tag, r, k, i, sw, b, gm, be);
+                    am2[k] = absmax_bf16x2(am2[k], pack_bf16x2(y.x, y.y));
+                  }
+                }
+              });
+            };
+            if (has_swv) {
+              if (affine) amax_pass(std::true_type{}, std::true_type{});
+              else amax_pass(std::true_type{}, std::false_type{});
+            } else {
+              if (affine) amax_pass(std::false_type{}, std::true_type{});
+              else amax_pass(std::false_type{}, std::false_type{});
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            // each lane's maximum covers its own columns; merge the row's 4
+            float am = fmaxf(bf16lo(am2[k]), bf16hi(am2[k]));
+            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+            float sc;
+            loka::row_scales(am, qinv[k], sc);
+            if (cp == 0 && ok[k]) static_cast<float*>(G.yq_scales)[static_cast<int64_t>(m0) + rowk[k]] = sc;
+          }
+        }
+      }
+
+      // pass 2: normalize and store from registers (rows of a ragged last
+      // tile are masked).  bf16: a chunk's 4 column pairs per row are packed,
+      // transposed across the 4 lanes of the row group, and stored as one
+      // 16-byte vector per lane (64 contiguous bytes per row per warp store)
+      auto out_pass = [&](auto swv_tag, auto aff_tag) {
+        for_chunks(t_base, [&](const uint32_t (&r)[16], int c) {
+          const int c0 = c * 32;
+          [[maybe_unused]] uint32_t pk[2][4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float2 sw, b, gm, be;
+            colv(swv_tag, aff_tag, c0, i, sw, b, gm, be);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const float2 y = ypair(swv_tag, aff_tag, r, k, i, sw, b, gm, be);
+              if constexpr (kBf16Out)
+                pk[k][i] = pack_bf16x2(y.x, y.y);
+              else
+                st_global_pred_v2f32(rowp[k] + (c0 + 8 * i) * 4, y, ok[k]);
+            }
+          }
+          if constexpr (kBf16Out) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              transpose4_lanes(pk[k], cp);
+              st_global_pred_v4b32(rowp[k] + c0 * 2, pk[k], ok[k]);
+            }
+          }
+        });
+      };
+      // pass 2 of the quantized output kind: the bf16 pairs (stored too when
+      // asked for) times the row's 448/amax, or, for MX, times 2^-e of the
+      // chunk's 32 columns (one E8M0 block: the 4 lanes of the row merge
+      // their maxima), cast to E4M3 with the quantizer's arithmetic.  The
+      // code pairs of both rows ride one 4-lane transpose; each lane then
+      // stores 8 contiguous codes per row.
+      [[maybe_unused]] auto out_pass_q = [&](auto swv_tag, auto aff_tag, auto mx_tag) {
+        constexpr bool MXO = decltype(mx_tag)::value;
+        for_chunks(t_base, [&](const uint32_t (&r)[16], int c) {
+          const int c0 = c * 32;
+          uint32_t pk[2][4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float2 sw, b, gm, be;
+            colv(swv_tag, aff_tag, c0, i, sw, b, gm, be);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const float2 y = ypair(swv_tag, aff_tag, r, k, i, sw, b, gm, be);
+              pk[k][i] = pack_bf16x2(y.x, y.y);
+            }
+          }
+          float mul[2] = {qinv[0], qinv[1]};
+          if constexpr (MXO) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const uint32_t a2 = absmax_bf16x2(absmax_bf16x2(pk[k][0], pk[k][1]), absmax_bf16x2(pk[k][2], pk[k][3]));
+              float am = fmaxf(0.0f, fmaxf(bf16lo(a2), bf16hi(a2)));
+              am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+              am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+              const int e = mx_exponent(am);
+              mul[k] = pow2_neg(e);
+              if (cp == 0 && ok[k])
+                static_cast<uint8_t*>(G.yq_scales)[(static_cast<int64_t>(m0) + rowk[k]) * (NG / 32) + (col0 + c0) / 32] =
+                    static_cast<uint8_t>(e + 127);
+            }
+          }
+          const float2 mul0 = dup2(mul[0]), mul1 = dup2(mul[1]);
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f0 = __fmul2_rn(make_float2(bf16lo(pk[0][i]), bf16hi(pk[0][i])), mul0);
+            const float2 f1 = __fmul2_rn(make_float2(bf16lo(pk[1][i]), bf16hi(pk[1][i])), mul1);
+            w[i] = static_cast<uint32_t>(cvt_e4m3x2(f0.x, f0.y)) | (static_cast<uint32_t>(cvt_e4m3x2(f1.x, f1.y)) << 16);
+          }
+          if (has_y) {   // the bf16 rows too (after the codes: pk is transposed in place)
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              transpose4_lanes(pk[k], cp);
+              st_global_pred_v4b32(rowp[0] + k * (8 * NG * 2) + c0 * 2, pk[k], ok[k]);
+            }
+          }
+          // lane cp now holds, in element t, the codes of columns 8 cp + 2t
+          // and 8 cp + 2t + 1: row 0 in the low half, row 1 in the high half
+          transpose4_lanes(w, cp);
+          st_global_pred_v2b32(rowq + c0, (w[0] & 0xFFFFu) | (w[1] << 16), (w[2] & 0xFFFFu) | (w[3] << 16), ok[0]);
+          st_global_pred_v2b32(rowq + 8 * NG + c0, (w[0] >> 16) | (w[1] & 0xFFFF0000u), (w[2] >> 16) | (w[3] & 0xFFFF0000u),
+                               ok[1]);
+        });
+      };
+      if constexpr (kQOut) {
+        const bool mxo = p.yq_mode == kScaleMx32;
+        if (has_swv) {
+          if (affine) {
+            if (mxo) out_pass_q(std::true_type{}, std::true_type{}, std::true_type{});
+            else out_pass_q(std::true_type{}, std::true_type{}, std::false_type{});
+          } else {
+            if (mxo) out_pass_q(std::true_type{}, std::false_type{}, std::true_type{});
+            else out_pass_q(std::true_type{}, std::false_type{}, std::false_type{});
+          }
+        } else {
+          if (affine) {
+            if (mxo) out_pass_q(std::false_type{}, std::true_type{}, std::true_type{});
+            else out_pass_q(std::false_type{}, std::true_type{}, std::false_type{});
+          } else {
+            if (mxo) out_pass_q(std::false_type{}, std::false_type{}, std::true_type{});
+            else out_pass_q(std::false_type{}, std::false_type{}, std::false_type{});
+          }
+        }
+      } else {
+        if (has_swv) {
+          if (affine) out_pass(std::true_type{}, std::true_type{});
+          else out_pass(std::true_type{}, std::false_type{});
+        } else {
+          if (affine) out_pass(std::false_type{}, std::true_type{});
+          else out_pass(std::false_type{}, std::false_type{});
+        }
+      }
+      // all of this warp's reads of the accumulator are done
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+  // partners may still write statistics into this CTA's shared memory until
+  // they are done: leave together
+  if (CL > 1) cluster_sync_all();
+}
+
+// Picks resident W when it fits and leaves at least three A stages.
+struct Plan {
+  bool resident;
+  int stages;
+  size_t smem;
+};
+
+Plan plan_for(int N, int K, int elem_bytes, bool mx, int cl) {
+  Plan pl{false, 0, 0};
+  const size_t w_bytes = static_cast<size_t>(N) * K * elem_bytes;
+  for (int pass = 0; pass < 2; ++pass) {
+    const bool resident = pass == 0;
+    if (resident && w_bytes > kResidentWLimit) continue;
+    const Layout base = make_layout(N, K, elem_bytes, resident, 0, mx, cl);
+    const size_t fixed = base.total;
+    const size_t per_stage = base.stage_bytes;
+    if (fixed + 2 * per_stage > kSmemLimit) continue;
+    int st = static_cast<int>((kSmemLimit - fixed) / per_stage);
+    if (st > kMaxStages) st = kMaxStages;
+    if (resident && st < 3) continue;
+    pl.resident = resident;
+    pl.stages = st;
+    pl.smem = fixed + static_cast<size_t>(st) * per_stage;
+    return pl;
+  }
+  return pl;
+}
+
+template <int N, int CL, int OP, int OUT, bool RES>
+cudaError_t launch_one(const GemmParams& p, size_t smem, int sms, cudaStream_t stream) {
+  auto kern = gemm_norm_kernel<N, CL, OP, OUT, RES>;
+  // the shared-memory opt-in is set once per device (it is not a stream
+  // operation, so it also stays out of captured CUDA graphs)
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = uint64_t(1) << (dev & 63);
+  if (!(configured.load() & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemLimit));
+    if (e != cudaSuccess) return e;
+    if (CL > 1) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+      if (e != cudaSuccess) return e;
+    }
+    configured.fetch_or(bit);
+  }
+  int clusters = sms / CL;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  // the prologue may overlap the tail of the quantizer launched before
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  if (CL > 1) {
+    // a cluster's CTAs share one GPC, so fewer than sms / CL clusters may be
+    // resident at once; the persistent grid takes no more than fit (per
+    // device and shared-memory size, asked once)
+    static std::atomic<uint64_t> fit[64];
+    const uint64_t key = static_cast<uint64_t>(smem) << 20;
+    uint64_t cached = fit[dev & 63].load();
+    if ((cached & ~uint64_t(0xFFFFF)) != key) {
+      int n = 0;
+      cfg.gridDim = dim3(static_cast<unsigned>(clusters * CL));
+      e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+      if (e != cudaSuccess) return e;
+      cached = key | static_cast<uint64_t>(n > 0 ? n : 1);
+      fit[dev & 63].store(cached);
+    }
+    const int n = static_cast<int>(cached & 0xFFFFF);
+    if (n < clusters) clusters = n;
+  }
+  if (p.total_tiles < clusters) clusters = p.total_tiles;
+  if (clusters < 1) return cudaSuccess;
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * CL));
+  e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+template <int N, int CL, int OP, int OUT>
+cudaError_t launch_res(const GemmParams& p, const Plan& pl, int sms, cudaStream_t stream) {
+  return pl.resident ? launch_one<N, CL, OP, OUT, true>(p, pl.smem, sms, stream)
+                     : launch_one<N, CL, OP, OUT, false>(p, pl.smem, sms, stream);
+}
+
+// (local width, cluster size) of an output row of N columns
+bool split_n(int N, int* local, int* cl) {
+  switch (N) {
+    case 64: case 128: case 192: case 256: *local = N; *cl = 1; return true;
+    case 512: *local = 256; *cl = 2; return true;
+    case 1024: *local = 256; *cl = 4; return true;
+    case 2048: *local = 256; *cl = 8; return true;
+    default: return false;
+  }
+}
+
+
+// Launches gemm_norm_kernel<local N, CL, OP, OUT> for an output row of N columns.
+template <int OP, int OUT>
+cudaError_t launch_kind(GemmParams& p, int N, int sms, cudaStream_t stream) {
+  int local = 0, cl = 0;
+  if (!split_n(N, &local, &cl)) return cudaErrorInvalidValue;
+  const int eb = OP == static_cast<int>(OperandKind::kBf16) ? 2 : 1;
+  const Plan pl = plan_for(local, p.K, eb, OP == static_cast<int>(OperandKind::kMxE4M3), cl);
+  if (pl.stages == 0) return cudaErrorInvalidValue;
+  p.stages = pl.stages;
+  switch (N) {
+    case 64: return launch_res<64, 1, OP, OUT>(p, pl, sms, stream);
+    case 128: return launch_res<128, 1, OP, OUT>(p, pl, sms, stream);
+    case 192: return launch_res<192, 1, OP, OUT>(p, pl, sms, stream);
+    case 256: return launch_res<256, 1, OP, OUT>(p, pl, sms, stream);
+    case 512: return launch_res<256, 2, OP, OUT>(p, pl, sms, stream);
+    case 1024: return launch_res<256, 4, OP, OUT>(p, pl, sms, stream);
+    case 2048: return launch_res<256, 8, OP, OUT>(p, pl, sms, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+// One per instantiation file (gemm_e4m3.cu, gemm_bf16.cu, gemm_mx.cu,
+// gemm_qout_e4m3.cu, gemm_qout_mx.cu).
+cudaError_t launch_gemm_e4m3(GemmParams& p, int N, OutKind out, int sms, cudaStream_t stream);
+cudaError_t launch_gemm_bf16(GemmParams& p, int N, OutKind out, int sms, cudaStream_t stream);
+cudaError_t launch_gemm_mx(GemmParams& p, int N, OutKind out, int sms, cudaStream_t stream);
+cudaError_t launch_gemm_qout_e4m3(GemmParams& p, int N, int sms, cudaStream_t stream);
+cudaError_t launch_gemm_qout_mx(GemmParams& p, int N, int sms, cudaStream_t stream);
+
+}  // namespace loka

@@ -65,9 +65,6 @@ cudaError_t launch_sf_permute(const uint8_t* logical, uint8_t* tc, int64_t rows,
 struct GemmGroup {
   CUtensorMap tm_a;      // A [M,K] (E4M3 or bf16), box {128 bytes of K, 128 rows}
   CUtensorMap tm_b;      // B [N,K], box {128 bytes of K, min(N,256) rows}
-  CUtensorMap tm_y;      // Y [M,N] (bf16 or fp32), box {128 bytes of N, 128 rows}
-  CUtensorMap tm_sfa;    // MX only: A scales, see gemm_norm.cu
-  CUtensorMap tm_sfb;    // MX only: B scales
   const float* sx;       // per-row [M] / per-tensor [1] activation scale, or null (=1)
   const float* sw;       // per-row [N] / per-tensor [1] weight scale, or null (=1)
   const uint8_t* sfa_tc; // MX: A scale codes in the tensor-memory copy layout
@@ -75,7 +72,10 @@ struct GemmGroup {
   const uint16_t* bias;  // bf16 [N] or null
   const uint16_t* gamma; // bf16 [N] or null
   const uint16_t* beta;  // bf16 [N] or null
-  void* y;               // output (the fp32 output is stored directly)
+  void* y;               // output (the fp32 output is stored directly); the quantized
+                         // output kind may leave it null (no bf16 copy)
+  uint8_t* yq;           // quantized output kind: E4M3 codes [M, N] of the bf16 output
+  void* yq_scales;       // and their scales: fp32 [M] (per row) or E8M0 [M, N/32] (MX)
   int64_t M;
   int32_t tile_begin;    // first tile of this group in the launch's tile space
   int32_t sx_per_row;    // 1: sx has M entries, 0: one entry
@@ -93,12 +93,15 @@ struct GemmParams {
   int32_t stages;        // shared-memory ring depth (set by the launcher)
   int32_t w_ready;       // 1: W and its scales were complete before the launch that precedes
                          // this GEMM, so resident W may load before waiting for that launch
+  int32_t yq_mode;       // quantized output kind: kScaleRow or kScaleMx32
   unsigned* status;      // device status word
   uint64_t wait_limit_ns;
 };
 
 enum class OperandKind : int { kE4M3 = 0, kBf16 = 1, kMxE4M3 = 2 };
-enum class OutKind : int { kBf16 = 0, kF32 = 1 };
+// kQuant: E4M3 codes and scales of the bf16 output (plus the bf16 output when
+// its pointer is set)
+enum class OutKind : int { kBf16 = 0, kF32 = 1, kQuant = 2 };
 
 // Launches the persistent GEMM + epilogue kernel for N columns (fills in
 // p.stages).

@@ -424,6 +424,13 @@ __device__ __forceinline__ void st_global_pred_v2f32(void* ptr, float2 v, uint32
       : "memory");
 }
 
+__device__ __forceinline__ void st_global_pred_v2b32(void* ptr, uint32_t a, uint32_t b, uint32_t pred) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %3, 0;\n\t@p st.global.v2.b32 [%0], {%1, %2};\n\t}" ::"l"(ptr), "r"(a),
+      "r"(b), "r"(pred)
+      : "memory");
+}
+
 __device__ __forceinline__ void st_global_pred_v4b32(void* ptr, const uint32_t (&v)[4], uint32_t pred) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %5, 0;\n\t@p st.global.v4.b32 [%0], {%1, %2, %3, %4};\n\t}" ::"l"(ptr),
@@ -461,6 +468,19 @@ __device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// max(a, b, c) / min(a, b, c) in one instruction (sm_100+); a NaN operand
+// loses to the others, as with fmaxf / fminf.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }

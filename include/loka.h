@@ -124,9 +124,21 @@ loka_status loka_quantize_fp8(const void* x, int64_t rows, int64_t cols, int32_t
  *   x: bf16 [M,K] (x_is_fp8 = 0) or E4M3 [M,K] with x_scales as produced by
  *      loka_quantize_fp8 (x_is_fp8 = 1).  Same for w / w_scales / w_is_fp8.
  *   mode: LOKA_SCALE_* (LOKA_BF16 runs the bf16 GEMM; *_is_fp8 must be 0).
- *   bias, gamma, beta: bf16 [N] or NULL (0, 1, 0).  y: bf16 [M,N].
+ *   bias, gamma, beta: bf16 [N] or NULL (0, 1, 0).  y: bf16 [M,N] (see y_q).
  *   eps: added to the variance (LayerNorm) or mean square (RMSNorm).
  * Accumulation is fp32 in tensor memory; the epilogue works in fp32.
+ * Quantized output (PreNorm fusion, the GEM Training page, "Handling
+ * Quantization Overhead": the next layer's activation quantization fused
+ * into this layer's normalization): when y_q is set, the epilogue also
+ * writes y_q and y_q_scales, equal byte for byte to what
+ * loka_quantize_fp8(Y, M, N, y_q_mode) writes for the bf16 output Y of the
+ * same call, so they feed the next layer as x / x_scales with x_is_fp8 = 1.
+ * y may then be NULL (no bf16 copy).  y_q_mode LOKA_SCALE_ROW needs
+ * N <= 256 (one CTA holds the row; LOKA_ERR_UNSUPPORTED otherwise);
+ * LOKA_SCALE_MX32 takes every N (a block is 32 columns of one CTA);
+ * LOKA_SCALE_TENSOR is LOKA_ERR_UNSUPPORTED (its amax needs every row before
+ * the first code).  y_q is 16-byte aligned, y_q_scales 4-byte aligned for
+ * ROW; every group sets y_q, or none does.  Not with mode LOKA_BF16.
  * workspace: device, loka_fp8_linear_norm_workspace_size() bytes (holds the
  * quantized operands and scales of bf16 inputs).  Asynchronous.
  * num_groups in [1, 16].  `descs` is a host array.
@@ -138,7 +150,7 @@ typedef struct loka_linear_desc {
   float eps;
   int32_t x_is_fp8;
   int32_t w_is_fp8;
-  int32_t reserved;
+  int32_t y_q_mode;      /* scaling of y_q: LOKA_SCALE_ROW or LOKA_SCALE_MX32 (read when y_q is set) */
   const void* x;         /* device */
   const void* x_scales;  /* device, used when x_is_fp8 */
   const void* w;         /* device */
@@ -146,7 +158,9 @@ typedef struct loka_linear_desc {
   const void* bias;      /* device bf16 [N] or NULL */
   const void* gamma;     /* device bf16 [N] or NULL */
   const void* beta;      /* device bf16 [N] or NULL */
-  void* y;               /* device bf16 [M,N] */
+  void* y;               /* device bf16 [M,N]; may be NULL when y_q is set */
+  void* y_q;             /* device E4M3 [M,N] of the bf16 output for the next layer, or NULL */
+  void* y_q_scales;      /* device fp32 [M] (LOKA_SCALE_ROW) or uint8 E8M0 [M,N/32] (LOKA_SCALE_MX32) */
 } loka_linear_desc;
 
 size_t loka_fp8_linear_norm_workspace_size(const loka_linear_desc* descs, int32_t num_groups);

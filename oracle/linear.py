@@ -124,3 +124,34 @@ def linear_norm_inputs(inp, rows=None):
             raise ValueError("per-tensor scaling is not row-local")
         x = inp.x[torch.as_tensor(rows, dtype=torch.long)]
     return linear_norm(x, inp.w, inp.bias, inp.gamma, inp.beta, inp.mode, inp.norm, inp.eps)
+
+
+def linear_norm_quantized(x, w, bias, gamma, beta, mode: int, norm: int, eps: float, out_mode: int):
+    """The layer, then the next layer's activation quantization of its output.
+
+    GEM Training page, "Handling Quantization Overhead" (the activation
+    quantization of a linear layer fused into the normalization before it)
+    and "Low Precision Flash Attention" (the fused kernels emit FP8
+    activations with their scale factors).  The layer's output is the bf16
+    tensor Y that ``linear_norm`` returns; what the next layer receives is Y
+    quantized like any activation (``quantize`` with ``out_mode``, per row or
+    MX 1x32 along the output columns).  Reading: the codes come from the bf16
+    Y, not from the unrounded normalized values, so the fused path hands the
+    next layer the same bytes as the unfused one (store Y, quantize it).
+
+    Returns (y_exact float64, y_bf16 float64, q uint8 [M,N], scales).
+    """
+    y, yb, _ = linear_norm(x, w, bias, gamma, beta, mode, norm, eps)
+    q, s = quantize(yb.astype(np.float32), out_mode)
+    return y, yb, q, np.asarray(s)
+
+
+def linear_norm_quantized_inputs(inp, out_mode: int, rows=None):
+    """``linear_norm_quantized`` on a ``workloads.LayerInputs`` (``rows`` as in
+    ``linear_norm_inputs``; row-local for every out_mode this takes)."""
+    x = inp.x
+    if rows is not None:
+        if inp.mode == SCALE_TENSOR:
+            raise ValueError("per-tensor scaling is not row-local")
+        x = inp.x[torch.as_tensor(rows, dtype=torch.long)]
+    return linear_norm_quantized(x, inp.w, inp.bias, inp.gamma, inp.beta, inp.mode, inp.norm, inp.eps, out_mode)

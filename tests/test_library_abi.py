@@ -4,6 +4,7 @@ host-only dispatch selector agrees with the oracle's reading of the rule."""
 import ctypes
 import os
 import re
+import subprocess
 
 import numpy as np
 import pytest
@@ -43,12 +44,28 @@ def test_library_exports_every_declared_symbol(cpu_lib):
         assert n in _loka.SIGNATURES, n
 
 
-def test_struct_layouts_match_header():
-    # sizes of the C structs (x86-64 / aarch64 LP64 ABI)
-    assert ctypes.sizeof(_loka.LinearDesc) == 3 * 8 + 6 * 4 + 8 * 8
-    assert ctypes.sizeof(_loka.ErrorStats) == 5 * 8
-    assert ctypes.sizeof(_loka.Problem) == 3 * 8 + 2 * 4 + 8
-    assert ctypes.sizeof(_loka.DispatchEntry) == 40 + 8 + 3 * 8
+def test_struct_layouts_match_header(tmp_path):
+    # the C compiler's sizeof / offsetof of every struct and field of the
+    # header against the ctypes binding
+    structs = {"loka_linear_desc": _loka.LinearDesc, "loka_error_stats": _loka.ErrorStats,
+               "loka_problem": _loka.Problem, "loka_dispatch_entry": _loka.DispatchEntry,
+               "loka_policy": _loka.Policy}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "loka.h"', "int main(void) {"]
+    for cname, cls in structs.items():
+        lines.append(f'  printf("{cname} size %zu\\n", sizeof({cname}));')
+        for fname, _ in cls._fields_:
+            lines.append(f'  printf("{cname} {fname} %zu\\n", offsetof({cname}, {fname}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    got = {tuple(l.split()[:2]): int(l.split()[2]) for l in out if l.strip()}
+    for cname, cls in structs.items():
+        assert got[(cname, "size")] == ctypes.sizeof(cls), cname
+        for fname, _ in cls._fields_:
+            assert got[(cname, fname)] == getattr(cls, fname).offset, (cname, fname)
 
 
 def test_version(cpu_lib):
@@ -88,6 +105,43 @@ def test_linear_norm_rejects_group_count_and_mismatch(cpu_lib):
     assert cpu_lib.loka_fp8_linear_norm(arr, 17, None, 0, None) == _loka.LOKA_ERR_INVALID_ARG
     arr2 = _loka.make_descs([_desc(), _desc(K=256)])
     assert cpu_lib.loka_fp8_linear_norm(arr2, 2, None, 0, None) == _loka.LOKA_ERR_UNSUPPORTED
+
+
+_Q = 1 << 21     # a fake 16-byte-aligned device address (nothing is launched)
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({"y_q_mode": 0}, _loka.LOKA_ERR_UNSUPPORTED),                  # a tensor-wide output scale
+    ({"y_q_mode": 5}, _loka.LOKA_ERR_INVALID_ARG),
+    ({"y_q_mode": 1, "N": 512}, _loka.LOKA_ERR_UNSUPPORTED),        # a row scale across a cluster
+    ({"y_q_mode": 1, "mode": 3}, _loka.LOKA_ERR_UNSUPPORTED),       # the bf16 path
+    ({"y_q_mode": 1, "y_q_scales": None}, _loka.LOKA_ERR_INVALID_ARG),
+    ({"y_q_mode": 1, "y_q": _Q + 8}, _loka.LOKA_ERR_INVALID_ARG),   # misaligned codes
+    ({"y_q_mode": 1, "y_q_scales": _Q + 2}, _loka.LOKA_ERR_INVALID_ARG),
+    ({"y_q_mode": 1, "y": None}, _loka.LOKA_ERR_WORKSPACE),         # valid: the bf16 copy is optional
+    ({"y_q_mode": 2, "N": 2048, "y_q_scales": _Q + 1}, _loka.LOKA_ERR_WORKSPACE),   # MX: any N, byte scales
+    ({"y_q_mode": 1, "mode": 0}, _loka.LOKA_ERR_WORKSPACE),         # per-tensor inputs, per-row output
+])
+def test_quantized_output_arguments_on_host(cpu_lib, kw, status):
+    kw = dict({"y_q": _Q, "y_q_scales": _Q}, **kw)
+    arr = _loka.make_descs([_desc(**kw)])
+    assert cpu_lib.loka_fp8_linear_norm(arr, 1, None, 0, None) == status, cpu_lib.loka_last_error()
+
+
+def test_quantized_output_is_all_groups_or_none(cpu_lib):
+    q = {"y_q": _Q, "y_q_scales": _Q, "y_q_mode": 1}
+    assert cpu_lib.loka_fp8_linear_norm(_loka.make_descs([_desc(**q), _desc()]), 2, None, 0, None) == \
+        _loka.LOKA_ERR_UNSUPPORTED
+    assert cpu_lib.loka_fp8_linear_norm(_loka.make_descs([_desc(**q), _desc(**dict(q, y_q_mode=2))]), 2, None, 0,
+                                        None) == _loka.LOKA_ERR_UNSUPPORTED
+    assert cpu_lib.loka_fp8_linear_norm(_loka.make_descs([_desc(**q), _desc(**q)]), 2, None, 0, None) == \
+        _loka.LOKA_ERR_WORKSPACE
+    # an empty group has no output storage: it does not count
+    assert cpu_lib.loka_fp8_linear_norm(_loka.make_descs([_desc(M=0, y=None), _desc(**q)]), 2, None, 0, None) == \
+        _loka.LOKA_ERR_WORKSPACE
+    # without y_q, y stays required
+    assert cpu_lib.loka_fp8_linear_norm(_loka.make_descs([_desc(y=None)]), 1, None, 0, None) == \
+        _loka.LOKA_ERR_INVALID_ARG
 
 
 def test_linear_norm_workspace_is_required_and_sized(cpu_lib):

@@ -311,6 +311,45 @@ def test_linear_norm_end_to_end_vs_library_composition():
 
 
 # ------------------------------------------------------------- bf16 rounding
+# ------------------------------------- quantized output for the next layer
+def test_quantized_output_rowwise_is_the_quantized_bf16_output():
+    # per row: the largest |bf16 output| maps to 448, the scale is amax/448,
+    # and every code is the nearest E4M3 value (brute force) of the fp32
+    # product bf16(y) * fl32(448/amax)
+    M, N = 40, 64
+    inp = W.make_layer(M, 128, N, mode=L.SCALE_ROW, norm=L.NORM_LAYER, seed=21, bias_var=0.02, gamma_uniform=True)
+    inp.beta = W.random_bf16((N,), seed=22, var=0.1)
+    y, yb, q, s = L.linear_norm_quantized_inputs(inp, L.SCALE_ROW)
+    assert q.shape == (M, N) and s.shape == (M,)
+    _, yb_plain, _ = L.linear_norm_inputs(inp)
+    assert np.array_equal(yb, yb_plain)
+    vals = F.e4m3_decode(q)
+    assert np.all(np.max(np.abs(vals), axis=1) == 448.0)
+    am = np.max(np.abs(yb), axis=1).astype(np.float32)
+    inv = np.array([np.float32(448.0) / a for a in am], dtype=np.float32)
+    assert np.array_equal(s, np.array([a / np.float32(448.0) for a in am], dtype=np.float32))
+    prod = (yb.astype(np.float32) * inv[:, None]).astype(np.float32)
+    assert np.array_equal(q.ravel(), _brute_force_encode(prod.ravel()))
+    # the codes are those of bf16(y), not of the unrounded y: some differ
+    prod_exact = (y.astype(np.float32) * inv[:, None]).astype(np.float32)
+    assert not np.array_equal(q.ravel(), _brute_force_encode(prod_exact.ravel()))
+
+
+def test_quantized_output_mx_blocks_run_along_the_output_row():
+    # one E8M0 exponent per 32 consecutive output columns of a row, from
+    # frexp (amax = f 2^p, f in [0.5, 1), so floor(log2 amax) = p - 1)
+    M, N = 24, 96
+    inp = W.make_layer(M, 128, N, mode=L.SCALE_MX32, norm=L.NORM_RMS, seed=23, gamma_uniform=True, eps=1e-6)
+    y, yb, q, s = L.linear_norm_quantized_inputs(inp, L.SCALE_MX32)
+    assert s.shape == (M, N // 32) and s.dtype == np.uint8
+    blocks = yb.reshape(M, N // 32, 32)
+    _, p = np.frexp(np.abs(blocks).max(axis=2))
+    e = p - 1 - 8
+    assert np.array_equal(s.astype(np.int64), e + 127)
+    prod = np.ldexp(blocks, -e[:, :, None]).astype(np.float32)     # exact: a power of two
+    assert np.array_equal(q.ravel(), _brute_force_encode(prod.ravel()))
+
+
 def test_bf16_round_matches_torch_on_float32_values():
     rng = np.random.default_rng(18)
     v = (rng.standard_normal(200000) * np.exp(rng.uniform(-30, 30, 200000))).astype(np.float32)

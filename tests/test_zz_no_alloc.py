@@ -53,3 +53,25 @@ def test_static_scratch_rejects_too_large_problems(lib):
     with pytest.raises(_loka.LokaError) as e:
         _loka.loka_fp8_linear_norm_static([layer.desc()])
     assert e.value.status == _loka.LOKA_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("out_mode", [W.SCALE_ROW, W.SCALE_MX32])
+def test_static_scratch_quantized_output(lib, out_mode):
+    # the E4M3 output for the next layer through the allocation-free call:
+    # the same codes and scales as through the workspace entry point
+    dev = torch.device("cuda")
+    inp = W.make_layer(1500, 512, 256, mode=W.SCALE_ROW, norm=W.NORM_LAYER, seed=43, bias_var=0.02)
+    mk = _layers(inp, dev)
+    ref = mk()
+    ref.y_q_mode = out_mode
+    loka.fp8_linear_norm([ref])
+    layer = mk()
+    layer.y_q_mode = out_mode
+    layer.y_q_only = True
+    d = layer.desc()
+    layer.y_q.fill_(0xFF)
+    _loka.loka_fp8_linear_norm_static([d])
+    torch.cuda.synchronize()
+    assert _loka.loka_device_status() == _loka.LOKA_OK
+    assert torch.equal(layer.y_q, ref.y_q)
+    assert torch.equal(layer.y_q_scales, ref.y_q_scales)
