@@ -129,7 +129,8 @@ def algorithmic_bytes_step(M, K, N):
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("gemm_norm.cu", "quantize.cu", "ptx.cuh", "loka_internal.h"):
+    for f in ("gemm_norm.cuh", "gemm_norm.cu", "gemm_e4m3.cu", "quantize.cu", "quant_math.cuh", "ptx.cuh",
+              "loka_internal.h"):
         with open(os.path.join(ROOT, "fp8_precision_recommendation_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -345,26 +346,62 @@ def run_ours(args, world, rank, local):
 
     # ---- per-kernel timing (same kernels, same stream) for the roofline
     kern = {}
-    qx = [torch.empty((l.M, l.K), dtype=torch.uint8, device=dev) for l in layers]
+    # E4M3 activations rotate over the same buffer sets as the bf16 ones, so
+    # the GEMM timed alone reads them from HBM, not from L2
+    qx = [[torch.empty((l.M, l.K), dtype=torch.uint8, device=dev) for l in layers] for _ in range(nbuf)]
     qw = [torch.empty((l.N, l.K), dtype=torch.uint8, device=dev) for l in layers]
     shp = [(loka.scales_shape(l.M, l.K, mode), loka.scales_shape(l.N, l.K, mode)) for l in layers]
-    sx = [torch.empty(a[0], dtype=getattr(torch, a[1]), device=dev) for a, _ in shp]
+    sx = [[torch.empty(a[0], dtype=getattr(torch, a[1]), device=dev) for a, _ in shp] for _ in range(nbuf)]
     sw = [torch.empty(b[0], dtype=getattr(torch, b[1]), device=dev) for _, b in shp]
     qws = torch.empty(max(256, _loka.loka_quantize_fp8_workspace_size(1, 32, mode)), dtype=torch.uint8, device=dev)
 
     def quantize_x(i):
+        b = i % nbuf
         for gi, l in enumerate(layers):
-            _loka.loka_quantize_fp8(xs[i % nbuf][gi], l.M, l.K, mode, qx[gi], sx[gi], qws, qws.numel(), s)
+            _loka.loka_quantize_fp8(xs[b][gi], l.M, l.K, mode, qx[b][gi], sx[b][gi], qws, qws.numel(), s)
 
     kern["quantize_x"] = timed(quantize_x, args.steps)
     for gi, l in enumerate(layers):
         _loka.loka_quantize_fp8(ws_[gi], l.N, l.K, mode, qw[gi], sw[gi], qws, qws.numel(), s)
-    pre = [mk(i, x_list=qx, x_scales=sx, w_scales=sw) for i in range(nbuf)]
+    pre = [mk(i, x_list=qx[i], x_scales=sx[i], w_scales=sw) for i in range(nbuf)]
     for lst in pre:
         for gi, lay in enumerate(lst):
             lay.w = qw[gi]
     kern["gemm_norm"] = timed(lambda i: loka.fp8_linear_norm(pre[i % nbuf], workspace=wsp, stream=s), args.steps)
     torch.cuda.synchronize()
+
+    # ---- the layer inside an FP8 stack: its input arrives as E4M3 codes and
+    # scales from the previous layer's epilogue, and it hands its own output
+    # to the next layer the same way (quantization fused into the
+    # normalization; no bf16 copy).  Against the unfused layer: the GEMM with
+    # bf16 output, then the quantizer on that output.
+    chained = None
+    out_mode = mode if mode in (1, 2) and (mode == 2 or layers[0].N <= 256) else None
+    if out_mode is not None and not args.no_compare:
+        yq = [[torch.empty((l.M, l.N), dtype=torch.uint8, device=dev) for l in layers] for _ in range(nbuf)]
+        ysh = [loka.scales_shape(l.M, l.N, out_mode) for l in layers]
+        ysq = [[torch.empty(a[0], dtype=getattr(torch, a[1]), device=dev) for a in ysh] for _ in range(nbuf)]
+        ch = [mk(i, x_list=qx[i], x_scales=sx[i], w_scales=sw) for i in range(nbuf)]
+        for i, lst in enumerate(ch):
+            for gi, lay in enumerate(lst):
+                lay.w, lay.y = qw[gi], None
+                lay.y_q_mode, lay.y_q_only, lay.y_q, lay.y_q_scales = out_mode, True, yq[i][gi], ysq[i][gi]
+        t_chain = timed(lambda i: loka.fp8_linear_norm(ch[i % nbuf], workspace=wsp, stream=s), args.steps)
+
+        def quantize_y(i):
+            b = i % nbuf
+            for gi, l in enumerate(layers):
+                _loka.loka_quantize_fp8(ys[b][gi], l.M, l.N, out_mode, yq[b][gi], ysq[b][gi], qws, qws.numel(), s)
+
+        t_qy = timed(quantize_y, args.steps)
+        bytes_c = sum(l.M * l.K + scale_bytes(mode, l.M, l.K) + l.N * l.K + scale_bytes(mode, l.N, l.K)
+                      + 2 * l.N * sum(v is not None for v in (l.bias, l.gamma, l.beta))
+                      + l.M * l.N + scale_bytes(out_mode, l.M, l.N) for l in layers)
+        bw_c = peaks()[0]["hbm_gbs"]
+        chained = {"layer_us": 1e6 * t_chain, "tflops": flops / t_chain / 1e12, "output": {1: "E4M3 per-row",
+                   2: "E4M3 MX 1x32"}[out_mode], "algorithmic_bytes": bytes_c,
+                   "achieved_gbs": bytes_c / t_chain / 1e9, "frac_of_hbm": bytes_c / t_chain / 1e9 / bw_c,
+                   "unfused_us": 1e6 * (kern["gemm_norm"] + t_qy), "quantize_y_us": 1e6 * t_qy}
 
     # ---- the same step with static weights (W quantized once, as a trained
     # model's weights are): bf16 X quantized in every step, captured in a
@@ -509,7 +546,7 @@ def run_ours(args, world, rank, local):
                    "parallelism": f"rows x{world}",
                    "timing": "CUDA graph of K steps, CUDA events on the launching stream"},
         "roofline": roofline, "path_roofline": path_roofline, "kernels_us": {k: v * 1e6 for k, v in kern.items()},
-        "compare": compare, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+        "compare": compare, "fp8_chained_layer": chained, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
         "gpu_launches": launches_per_step * args.steps,
     }
     if rank == 0:
