@@ -19,8 +19,8 @@ import dataclasses
 from typing import List, Optional, Sequence
 
 from . import _loka
-from ._loka import (LOKA_BF16, LOKA_NORM_LAYER, LOKA_NORM_NONE, LOKA_NORM_RMS, LOKA_SCALE_MX32,  # noqa: F401
-                    LOKA_SCALE_ROW, LOKA_SCALE_TENSOR, DispatchEntry, LinearDesc, LokaError, Policy, Problem)
+from ._loka import (LOKA_ACT_HARDSWISH, LOKA_ACT_NONE, LOKA_BF16, LOKA_NORM_BLOCK_RMS,  # noqa: F401
+                    LOKA_NORM_LAYER, LOKA_NORM_NONE, LOKA_NORM_RMS, LOKA_SCALE_MX32, LOKA_SCALE_ROW, LOKA_SCALE_TENSOR, DispatchEntry, LinearDesc, LokaError, Policy, Problem)
 
 __all__ = ["quantize_fp8", "fp8_linear_norm", "quant_error", "dispatch_select", "Layer", "Workspace"]
 
@@ -100,6 +100,8 @@ class Layer:
     y_q: object = None             # uint8 E4M3 [M,N] (allocated if None)
     y_q_scales: object = None      # fp32 [M] or uint8 E8M0 [M,N/32] (allocated if None)
     y_q_only: bool = False         # with y_q_mode: no bf16 copy of the output
+    norm_block: int = 256          # LOKA_NORM_BLOCK_RMS: columns per block
+    act: int = 0                   # LOKA_ACT_NONE or LOKA_ACT_HARDSWISH
 
     def desc(self) -> LinearDesc:
         torch = _torch()
@@ -112,6 +114,7 @@ class Layer:
         d = LinearDesc()
         d.M, d.N, d.K = M, N, K
         d.mode, d.norm, d.eps = self.mode, self.norm, self.eps
+        d.norm_block, d.act = self.norm_block, self.act
         d.x_is_fp8 = int(self.x.dtype == torch.uint8)
         d.w_is_fp8 = int(self.w.dtype == torch.uint8)
         d.x, d.w = self.x.data_ptr(), self.w.data_ptr()

@@ -17,7 +17,8 @@ LIB_PATH = os.path.join(HERE, "libloka.so")
 
 LOKA_OK, LOKA_ERR_INVALID_ARG, LOKA_ERR_UNSUPPORTED, LOKA_ERR_WORKSPACE, LOKA_ERR_TIMEOUT, LOKA_ERR_CUDA = range(6)
 LOKA_SCALE_TENSOR, LOKA_SCALE_ROW, LOKA_SCALE_MX32, LOKA_BF16 = range(4)
-LOKA_NORM_NONE, LOKA_NORM_LAYER, LOKA_NORM_RMS = range(3)
+LOKA_NORM_NONE, LOKA_NORM_LAYER, LOKA_NORM_RMS, LOKA_NORM_BLOCK_RMS = range(4)
+LOKA_ACT_NONE, LOKA_ACT_HARDSWISH = range(2)
 
 c_i64, c_i32, c_sz, c_p = ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t, ctypes.c_void_p
 
@@ -26,7 +27,8 @@ class LinearDesc(ctypes.Structure):
     _fields_ = [("M", c_i64), ("N", c_i64), ("K", c_i64), ("mode", c_i32), ("norm", c_i32),
                 ("eps", ctypes.c_float), ("x_is_fp8", c_i32), ("w_is_fp8", c_i32), ("y_q_mode", c_i32),
                 ("x", c_p), ("x_scales", c_p), ("w", c_p), ("w_scales", c_p), ("bias", c_p),
-                ("gamma", c_p), ("beta", c_p), ("y", c_p), ("y_q", c_p), ("y_q_scales", c_p)]
+                ("gamma", c_p), ("beta", c_p), ("y", c_p), ("y_q", c_p), ("y_q_scales", c_p),
+                ("norm_block", c_i32), ("act", c_i32)]
 
 
 class ErrorStats(ctypes.Structure):

@@ -204,13 +204,25 @@ loka_status validate(const loka_linear_desc* d, int n, bool probe) {
   for (int i = 0; i < n; ++i) {
     const loka_linear_desc& g = d[i];
     if (g.N != a.N || g.K != a.K || g.mode != a.mode || g.norm != a.norm || g.eps != a.eps ||
-        g.x_is_fp8 != a.x_is_fp8 || g.w_is_fp8 != a.w_is_fp8)
-      return fail(LOKA_ERR_UNSUPPORTED, "group %d differs from group 0 in N, K, mode, norm, eps or operand kind", i);
+        g.x_is_fp8 != a.x_is_fp8 || g.w_is_fp8 != a.w_is_fp8 || g.act != a.act ||
+        (a.norm == kNormBlockRms && g.norm_block != a.norm_block))
+      return fail(LOKA_ERR_UNSUPPORTED,
+                  "group %d differs from group 0 in N, K, mode, norm, norm_block, eps, act or operand kind", i);
     if (g.M < 0) return fail(LOKA_ERR_INVALID_ARG, "group %d: M = %lld < 0", i, static_cast<long long>(g.M));
     if (g.M > (int64_t(1) << 31)) return fail(LOKA_ERR_UNSUPPORTED, "group %d: M too large", i);
   }
   if (a.mode < 0 || a.mode > kBf16) return fail(LOKA_ERR_INVALID_ARG, "mode %d is not a LOKA_SCALE_* value", a.mode);
-  if (a.norm < 0 || a.norm > kNormRms) return fail(LOKA_ERR_INVALID_ARG, "norm %d is not a LOKA_NORM_* value", a.norm);
+  if (a.norm < 0 || a.norm > kNormBlockRms)
+    return fail(LOKA_ERR_INVALID_ARG, "norm %d is not a LOKA_NORM_* value", a.norm);
+  if (a.act != kActNone && a.act != kActHardSwish)
+    return fail(LOKA_ERR_INVALID_ARG, "act %d is not a LOKA_ACT_* value", a.act);
+  if (a.norm == kNormBlockRms) {
+    const int b = a.norm_block;
+    if (b != 32 && b != 64 && b != 128 && b != 256)
+      return fail(LOKA_ERR_UNSUPPORTED, "norm_block %d: BlockNorm blocks are 32, 64, 128 or 256 columns", b);
+    if (a.N % b != 0)
+      return fail(LOKA_ERR_INVALID_ARG, "norm_block %d does not divide N = %lld", b, static_cast<long long>(a.N));
+  }
   if (a.K < 128 || a.K % 128 != 0)
     return fail(LOKA_ERR_UNSUPPORTED, "K = %lld: K must be a positive multiple of 128", static_cast<long long>(a.K));
   if (a.K > (int64_t(1) << 20)) return fail(LOKA_ERR_UNSUPPORTED, "K too large");
@@ -319,6 +331,8 @@ loka_status build_gemm(const loka_linear_desc* d, int n, const std::vector<Opera
   p->status = dev->status;
   p->wait_limit_ns = kDefaultWaitLimitNs;
   p->yq_mode = out == OutKind::kQuant ? output_reference(d, n).y_q_mode : 0;
+  p->norm_block = norm == kNormBlockRms ? d[0].norm_block : 256;
+  p->act = out == OutKind::kF32 ? kActNone : d[0].act;   // the probe's pre-norm outputs take no activation
   return LOKA_OK;
 }
 

@@ -13,8 +13,11 @@ bool gemm_supported(int N, int K, OperandKind op) {
 
 cudaError_t launch_gemm_norm(GemmParams& p, int N, OperandKind op, OutKind out, int sms, cudaStream_t stream) {
   if (out == OutKind::kQuant) {
-    if (op == OperandKind::kE4M3) return launch_gemm_qout_e4m3(p, N, sms, stream);
-    if (op == OperandKind::kMxE4M3) return launch_gemm_qout_mx(p, N, sms, stream);
+    const bool wide = N > 256;
+    if (op == OperandKind::kE4M3)
+      return wide ? launch_gemm_qout_e4m3_wide(p, N, sms, stream) : launch_gemm_qout_e4m3(p, N, sms, stream);
+    if (op == OperandKind::kMxE4M3)
+      return wide ? launch_gemm_qout_mx_wide(p, N, sms, stream) : launch_gemm_qout_mx(p, N, sms, stream);
     return cudaErrorInvalidValue;
   }
   switch (op) {

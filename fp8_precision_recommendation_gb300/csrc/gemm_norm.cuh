@@ -428,6 +428,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
     constexpr bool kQOut = OUT == static_cast<int>(OutKind::kQuant);
     const int norm = p.norm;
     const float eps = p.eps;
+    const bool act = p.act != 0;
+    // BlockNorm: log2 of the chunks (32 columns) per block
+    const int lcpb = 31 - __clz(max(p.norm_block >> 5, 1));
     float* vec_sw = vec_base + team * 4 * N;        // this team's copy of the column vectors
     float* vec_b = vec_sw + N;
     float* vec_g = vec_b + N;
@@ -475,14 +478,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
         }
       }
     };
-    // v = acc * sx (* sw) + b for the pair; SWV: per-column weight scales
-    // (rowwise W); otherwise they are folded into the row factor
-    auto vpair = [&](auto swv_tag, const uint32_t (&r)[16], int k, int i, float2 sx2, float2 sw, float2 b) {
-      constexpr bool SWV = decltype(swv_tag)::value;
-      if constexpr (SWV)
-        return __ffma2_rn(__fmul2_rn(acc2(r, k, i), sx2), sw, b);
-      else
-        return __ffma2_rn(acc2(r, k, i), sx2, b);
+    // v = acc * sx * sw + b for the pair: sw is the per-column weight scale
+    // (rowwise W; 1 otherwise, a per-tensor weight scale folds into sx)
+    auto vpair = [&](const uint32_t (&r)[16], int k, int i, float2 sx2, float2 sw, float2 b) {
+      return __ffma2_rn(__fmul2_rn(acc2(r, k, i), sx2), sw, b);
     };
     // one lane waits, the whole warp follows its verdict
     auto warp_wait = [&](uint32_t bar, uint32_t parity, bool cluster_scope) {
@@ -494,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
     };
 
     int cur_group = -1;
-    bool has_swv = false, affine = false;
+    bool affine = false;
     float sx_next[2] = {1.f, 1.f};
     int local = team;
     int tile = cid + team * ncl;
@@ -514,7 +513,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
           vec_g[n] = (G.gamma == nullptr || !normed) ? 1.0f : bf16_to_f(G.gamma[gn]);
           vec_be[n] = (G.beta == nullptr || norm != kNormLayer) ? 0.0f : bf16_to_f(G.beta[gn]);
         }
-        has_swv = G.sw != nullptr && G.sw_per_row;
         affine = normed && (G.gamma != nullptr || (G.beta != nullptr && norm == kNormLayer));
         named_bar_sync(team_bar, 256);
         cur_group = g;
@@ -554,7 +552,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
       float mean[2] = {0.f, 0.f}, m2[2] = {0.f, 0.f};
       // extremes of v, kept when they decide the E4M3 row scale (see below)
       [[maybe_unused]] float vhi[2] = {-INFINITY, -INFINITY}, vlo[2] = {INFINITY, INFINITY};
-      auto stats_pass = [&](auto swv_tag, auto trk_tag) {
+      // BlockNorm: sums of squares of the blocks this lane keeps (b % 4 == cp; slot b / 4)
+      [[maybe_unused]] float bsq[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+      auto stats_pass = [&](auto trk_tag) {
         if (norm == kNormLayer) {
           // shifted sums: with K the mean of the row's first 8-value piece,
           // s1 += v - K and s2 += (v - K)^2; no division, little cancellation
@@ -564,14 +564,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
             float2 sw[4], b[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              if constexpr (decltype(swv_tag)::value) sw[i] = vec2(vec_sw, c0, i);
+              sw[i] = vec2(vec_sw, c0, i);
               b[i] = vec2(vec_b, c0, i);
             }
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
               float2 v[4];
 #pragma unroll
-              for (int i = 0; i < 4; ++i) v[i] = vpair(swv_tag, r, k, i, sx2[k], sw[i], b[i]);
+              for (int i = 0; i < 4; ++i) v[i] = vpair(r, k, i, sx2[k], sw[i], b[i]);
               if constexpr (decltype(trk_tag)::value) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -608,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
             float2 sw[4], b[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              if constexpr (decltype(swv_tag)::value) sw[i] = vec2(vec_sw, c0, i);
+              sw[i] = vec2(vec_sw, c0, i);
               b[i] = vec2(vec_b, c0, i);
             }
 #pragma unroll
@@ -616,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
               float2 q = make_float2(0.f, 0.f);
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
-                const float2 v = vpair(swv_tag, r, k, i, sx2[k], sw[i], b[i]);
+                const float2 v = vpair(r, k, i, sx2[k], sw[i], b[i]);
                 if constexpr (decltype(trk_tag)::value) {
                   vhi[k] = max3f(vhi[k], v.x, v.y);
                   vlo[k] = min3f(vlo[k], v.x, v.y);
@@ -626,22 +626,51 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
               m2[k] += q.x + q.y;
             }
           });
+        } else if (norm == kNormBlockRms) {
+          // BlockNorm: sums of squares per block of the row; the row's 4
+          // lanes merge each chunk's sum, and lane (b % 4) keeps block b's
+          for_chunks(t_base, [&](const uint32_t (&r)[16], int c) {
+            const int c0 = c * 32;
+            float2 sw[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              sw[i] = vec2(vec_sw, c0, i);
+              b[i] = vec2(vec_b, c0, i);
+            }
+            const int blk = c >> lcpb;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              float2 q = make_float2(0.f, 0.f);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float2 v = vpair(r, k, i, sx2[k], sw[i], b[i]);
+                q = __ffma2_rn(v, v, q);
+              }
+              float qs = q.x + q.y;
+              qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+              qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+              if ((blk & 3) == cp) {
+                if (blk & 4) bsq[k][1] += qs;
+                else bsq[k][0] += qs;
+              }
+            }
+          });
         }
       };
       // E4M3 row output without gamma and beta: the extremes of v give the
       // row's amax (see below), so the statistics pass keeps them
-      [[maybe_unused]] const bool track =
-          kQOut && CL == 1 && p.yq_mode == kScaleRow && norm != kNormNone && !affine;
+      [[maybe_unused]] const bool track = kQOut && CL == 1 && p.yq_mode == kScaleRow &&
+                                          (norm == kNormLayer || norm == kNormRms) && !affine && !act;
       if (kQOut && CL == 1 && track) {
-        if (has_swv) stats_pass(std::true_type{}, std::true_type{});
-        else stats_pass(std::false_type{}, std::true_type{});
+        stats_pass(std::true_type{});
       } else {
-        if (has_swv) stats_pass(std::true_type{}, std::false_type{});
-        else stats_pass(std::false_type{}, std::false_type{});
+        stats_pass(std::false_type{});
       }
 
       float rstd[2] = {1.f, 1.f};
-      if (norm != kNormNone) {
+      // BlockNorm: 1/rms of the blocks this lane keeps
+      [[maybe_unused]] float brs[2][2] = {{1.f, 1.f}, {1.f, 1.f}};
+      if (norm == kNormLayer || norm == kNormRms) {
         // merge the 4 lanes of a row group (equal counts) with an ordered
         // expression so all four end bit-identical
 #pragma unroll
@@ -719,30 +748,74 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
         }
 #pragma unroll
         for (int k = 0; k < 2; ++k) rstd[k] = rsqrtf(m2[k] * (1.0f / NG) + eps);
+      } else if (norm == kNormBlockRms) {
+        const float inv_b = 1.0f / static_cast<float>(p.norm_block);   // a power of two: exact
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          brs[k][0] = rsqrtf(bsq[k][0] * inv_b + eps);
+          brs[k][1] = rsqrtf(bsq[k][1] * inv_b + eps);
+        }
       }
       // y = v * rstd - mean * rstd, then * gamma + beta when present
-      const float nmr[2] = {-mean[0] * rstd[0], -mean[1] * rstd[1]};
+      const float nmr[2] = {-mean[0] * rstd[0], -mean[1] * rstd[1]};   // -0 for RMSNorm and BlockNorm
       const float2 rstd2[2] = {dup2(rstd[0]), dup2(rstd[1])};
       const float2 nmr2[2] = {dup2(nmr[0]), dup2(nmr[1])};
       // the column vectors of pair i of chunk c0 (1, 0 where absent)
-      auto colv = [&](auto swv_tag, auto aff_tag, int c0, int i, float2& sw, float2& b, float2& gm, float2& be) {
-        sw = make_float2(1.f, 1.f);
+      // post_tag: integral_constant<int, P>; P bit 0 = gamma/beta, bit 1 =
+      // Hard Swish, bit 2 = BlockNorm
+      auto colv = [&](auto post_tag, int c0, int i, float2& sw, float2& b, float2& gm, float2& be) {
         gm = make_float2(1.f, 1.f);
         be = make_float2(0.f, 0.f);
-        if constexpr (decltype(swv_tag)::value) sw = vec2(vec_sw, c0, i);
+        sw = vec2(vec_sw, c0, i);
         b = vec2(vec_b, c0, i);
-        if constexpr (decltype(aff_tag)::value) {
+        if constexpr ((decltype(post_tag)::value & 1) != 0) {
           gm = vec2(vec_g, c0, i);
           be = vec2(vec_be, c0, i);
         }
       };
       // the normalized pair of row k: the one arithmetic of every pass below
-      auto ypair = [&](auto swv_tag, auto aff_tag, const uint32_t (&r)[16], int k, int i, float2 sw, float2 b,
+      // (rs: the row's 1/rms pair for this chunk, see chunk_rstd)
+      auto ypair = [&](auto post_tag, const uint32_t (&r)[16], int k, int i, float2 rs, float2 sw, float2 b,
                        float2 gm, float2 be) {
-        const float2 v = vpair(swv_tag, r, k, i, sx2[k], sw, b);
-        float2 y = __ffma2_rn(v, rstd2[k], nmr2[k]);
-        if constexpr (decltype(aff_tag)::value) y = __ffma2_rn(y, gm, be);
+        constexpr int POST = decltype(post_tag)::value;
+        const float2 v = vpair(r, k, i, sx2[k], sw, b);
+        float2 y = __ffma2_rn(v, rs, nmr2[k]);
+        if constexpr ((POST & 1) != 0) y = __ffma2_rn(y, gm, be);
+        if constexpr ((POST & 2) != 0) {
+          // Hard Swish: y * min(max(y + 3, 0), 6) / 6
+          const float2 t = __fadd2_rn(y, make_float2(3.0f, 3.0f));
+          const float2 tc = make_float2(fminf(fmaxf(t.x, 0.0f), 6.0f), fminf(fmaxf(t.y, 0.0f), 6.0f));
+          y = __fmul2_rn(__fmul2_rn(y, tc), make_float2(1.0f / 6.0f, 1.0f / 6.0f));
+        }
         return y;
+      };
+      // 1/rms of both rows for chunk c as pairs: the row's, or (BlockNorm)
+      // the chunk's block's, from the lane of the row group that keeps it
+      auto chunk_rstd = [&](auto post_tag, int c, float2 (&rs)[2]) {
+        if constexpr ((decltype(post_tag)::value & 4) != 0) {
+          const int blk = c >> lcpb;
+          const int src = (lane & ~3) | (blk & 3);
+#pragma unroll
+          for (int k = 0; k < 2; ++k)
+            rs[k] = dup2(__shfl_sync(0xffffffffu, (blk & 4) ? brs[k][1] : brs[k][0], src));
+        } else {
+          rs[0] = rstd2[0];
+          rs[1] = rstd2[1];
+        }
+      };
+      // fn(post_tag) with the tag of this tile's group
+      auto with_tags = [&](auto&& fn) {
+        const int post = (affine ? 1 : 0) | (act ? 2 : 0) | (norm == kNormBlockRms ? 4 : 0);
+        switch (post) {
+          case 0: fn(std::integral_constant<int, 0>{}); break;
+          case 1: fn(std::integral_constant<int, 1>{}); break;
+          case 2: fn(std::integral_constant<int, 2>{}); break;
+          case 3: fn(std::integral_constant<int, 3>{}); break;
+          case 4: fn(std::integral_constant<int, 4>{}); break;
+          case 5: fn(std::integral_constant<int, 5>{}); break;
+          case 6: fn(std::integral_constant<int, 6>{}); break;
+          default: fn(std::integral_constant<int, 7>{}); break;
+        }
       };
 
       // E4M3 output with one scale per row: the row's amax over its bf16
@@ -763,27 +836,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
               am2[k] = absmax_bf16x2(0u, pack_bf16x2(__fmaf_rn(vhi[k], rstd[k], nmr[k]),
                                                      __fmaf_rn(vlo[k], rstd[k], nmr[k])));
           } else {
-            auto amax_pass = [&](auto swv_tag, auto aff_tag) {
+            auto amax_pass = [&](auto post_tag) {
               for_chunks(t_base, [&](const uint32_t (&r)[16], int c) {
+                float2 rs[2];
+                chunk_rstd(post_tag, c, rs);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                   float2 sw, b, gm, be;
-                  colv(swv_tag, aff_tag, c * 32, i, sw, b, gm, be);
+                  colv(post_tag, c * 32, i, sw, b, gm, be);
 #pragma unroll
                   for (int k = 0; k < 2; ++k) {
-                    const float2 y = ypair(swv_tag, aff_tag, r, k, i, sw, b, gm, be);
+                    const float2 y = ypair(post_tag, r, k, i, rs[k], sw, b, gm, be);
                     am2[k] = absmax_bf16x2(am2[k], pack_bf16x2(y.x, y.y));
                   }
                 }
               });
             };
-            if (has_swv) {
-              if (affine) amax_pass(std::true_type{}, std::true_type{});
-              else amax_pass(std::true_type{}, std::false_type{});
-            } else {
-              if (affine) amax_pass(std::false_type{}, std::true_type{});
-              else amax_pass(std::false_type{}, std::false_type{});
-            }
+            with_tags([&](auto post_tag) { amax_pass(post_tag); });
           }
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
@@ -802,17 +871,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
       // tile are masked).  bf16: a chunk's 4 column pairs per row are packed,
       // transposed across the 4 lanes of the row group, and stored as one
       // 16-byte vector per lane (64 contiguous bytes per row per warp store)
-      auto out_pass = [&](auto swv_tag, auto aff_tag) {
+      auto out_pass = [&](auto post_tag) {
         for_chunks(t_base, [&](const uint32_t (&r)[16], int c) {
           const int c0 = c * 32;
+          float2 rs[2];
+          chunk_rstd(post_tag, c, rs);
           [[maybe_unused]] uint32_t pk[2][4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             float2 sw, b, gm, be;
-            colv(swv_tag, aff_tag, c0, i, sw, b, gm, be);
+            colv(post_tag, c0, i, sw, b, gm, be);
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
-              const float2 y = ypair(swv_tag, aff_tag, r, k, i, sw, b, gm, be);
+              const float2 y = ypair(post_tag, r, k, i, rs[k], sw, b, gm, be);
               if constexpr (kBf16Out)
                 pk[k][i] = pack_bf16x2(y.x, y.y);
               else
@@ -834,18 +905,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
       // their maxima), cast to E4M3 with the quantizer's arithmetic.  The
       // code pairs of both rows ride one 4-lane transpose; each lane then
       // stores 8 contiguous codes per row.
-      [[maybe_unused]] auto out_pass_q = [&](auto swv_tag, auto aff_tag, auto mx_tag) {
+      [[maybe_unused]] auto out_pass_q = [&](auto post_tag, auto mx_tag) {
         constexpr bool MXO = decltype(mx_tag)::value;
         for_chunks(t_base, [&](const uint32_t (&r)[16], int c) {
           const int c0 = c * 32;
+          float2 rs[2];
+          chunk_rstd(post_tag, c, rs);
           uint32_t pk[2][4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             float2 sw, b, gm, be;
-            colv(swv_tag, aff_tag, c0, i, sw, b, gm, be);
+            colv(post_tag, c0, i, sw, b, gm, be);
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
-              const float2 y = ypair(swv_tag, aff_tag, r, k, i, sw, b, gm, be);
+              const float2 y = ypair(post_tag, r, k, i, rs[k], sw, b, gm, be);
               pk[k][i] = pack_bf16x2(y.x, y.y);
             }
           }
@@ -889,31 +962,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
       };
       if constexpr (kQOut) {
         const bool mxo = p.yq_mode == kScaleMx32;
-        if (has_swv) {
-          if (affine) {
-            if (mxo) out_pass_q(std::true_type{}, std::true_type{}, std::true_type{});
-            else out_pass_q(std::true_type{}, std::true_type{}, std::false_type{});
-          } else {
-            if (mxo) out_pass_q(std::true_type{}, std::false_type{}, std::true_type{});
-            else out_pass_q(std::true_type{}, std::false_type{}, std::false_type{});
-          }
-        } else {
-          if (affine) {
-            if (mxo) out_pass_q(std::false_type{}, std::true_type{}, std::true_type{});
-            else out_pass_q(std::false_type{}, std::true_type{}, std::false_type{});
-          } else {
-            if (mxo) out_pass_q(std::false_type{}, std::false_type{}, std::true_type{});
-            else out_pass_q(std::false_type{}, std::false_type{}, std::false_type{});
-          }
-        }
+        with_tags([&](auto post_tag) {
+          // per-row output scales need the whole row in one CTA (the host
+          // allows them for CL == 1 only)
+          if (CL > 1 || mxo) out_pass_q(post_tag, std::true_type{});
+          else if constexpr (CL == 1) out_pass_q(post_tag, std::false_type{});
+        });
       } else {
-        if (has_swv) {
-          if (affine) out_pass(std::true_type{}, std::true_type{});
-          else out_pass(std::true_type{}, std::false_type{});
-        } else {
-          if (affine) out_pass(std::false_type{}, std::true_type{});
-          else out_pass(std::false_type{}, std::false_type{});
-        }
+        with_tags([&](auto post_tag) { out_pass(post_tag); });
       }
       // all of this warp's reads of the accumulator are done
       tc_fence_before();
@@ -1037,35 +1093,55 @@ bool split_n(int N, int* local, int* cl) {
 }
 
 
-// Launches gemm_norm_kernel<local N, CL, OP, OUT> for an output row of N columns.
-template <int OP, int OUT>
-cudaError_t launch_kind(GemmParams& p, int N, int sms, cudaStream_t stream) {
-  int local = 0, cl = 0;
-  if (!split_n(N, &local, &cl)) return cudaErrorInvalidValue;
+// Plans shared memory and launches gemm_norm_kernel<LN, CL, OP, OUT> (LN =
+// the columns one CTA owns).
+template <int OP, int OUT, int LN, int CL>
+cudaError_t launch_planned(GemmParams& p, int sms, cudaStream_t stream) {
   const int eb = OP == static_cast<int>(OperandKind::kBf16) ? 2 : 1;
-  const Plan pl = plan_for(local, p.K, eb, OP == static_cast<int>(OperandKind::kMxE4M3), cl);
+  const Plan pl = plan_for(LN, p.K, eb, OP == static_cast<int>(OperandKind::kMxE4M3), CL);
   if (pl.stages == 0) return cudaErrorInvalidValue;
   p.stages = pl.stages;
+  return launch_res<LN, CL, OP, OUT>(p, pl, sms, stream);
+}
+
+// Output rows of at most 256 columns: one CTA per tile.
+template <int OP, int OUT>
+cudaError_t launch_narrow(GemmParams& p, int N, int sms, cudaStream_t stream) {
   switch (N) {
-    case 64: return launch_res<64, 1, OP, OUT>(p, pl, sms, stream);
-    case 128: return launch_res<128, 1, OP, OUT>(p, pl, sms, stream);
-    case 192: return launch_res<192, 1, OP, OUT>(p, pl, sms, stream);
-    case 256: return launch_res<256, 1, OP, OUT>(p, pl, sms, stream);
-    case 512: return launch_res<256, 2, OP, OUT>(p, pl, sms, stream);
-    case 1024: return launch_res<256, 4, OP, OUT>(p, pl, sms, stream);
-    case 2048: return launch_res<256, 8, OP, OUT>(p, pl, sms, stream);
+    case 64: return launch_planned<OP, OUT, 64, 1>(p, sms, stream);
+    case 128: return launch_planned<OP, OUT, 128, 1>(p, sms, stream);
+    case 192: return launch_planned<OP, OUT, 192, 1>(p, sms, stream);
+    case 256: return launch_planned<OP, OUT, 256, 1>(p, sms, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
+// Wider rows: a cluster of N / 256 CTAs per tile.
+template <int OP, int OUT>
+cudaError_t launch_wide(GemmParams& p, int N, int sms, cudaStream_t stream) {
+  switch (N) {
+    case 512: return launch_planned<OP, OUT, 256, 2>(p, sms, stream);
+    case 1024: return launch_planned<OP, OUT, 256, 4>(p, sms, stream);
+    case 2048: return launch_planned<OP, OUT, 256, 8>(p, sms, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int OP, int OUT>
+cudaError_t launch_kind(GemmParams& p, int N, int sms, cudaStream_t stream) {
+  return N <= 256 ? launch_narrow<OP, OUT>(p, N, sms, stream) : launch_wide<OP, OUT>(p, N, sms, stream);
+}
+
 }  // namespace
 
-// One per instantiation file (gemm_e4m3.cu, gemm_bf16.cu, gemm_mx.cu,
-// gemm_qout_e4m3.cu, gemm_qout_mx.cu).
+// One per instantiation file (gemm_e4m3.cu, gemm_bf16.cu, gemm_mx.cu and
+// gemm_qout_{e4m3,mx}{,_wide}.cu).
 cudaError_t launch_gemm_e4m3(GemmParams& p, int N, OutKind out, int sms, cudaStream_t stream);
 cudaError_t launch_gemm_bf16(GemmParams& p, int N, OutKind out, int sms, cudaStream_t stream);
 cudaError_t launch_gemm_mx(GemmParams& p, int N, OutKind out, int sms, cudaStream_t stream);
 cudaError_t launch_gemm_qout_e4m3(GemmParams& p, int N, int sms, cudaStream_t stream);
+cudaError_t launch_gemm_qout_e4m3_wide(GemmParams& p, int N, int sms, cudaStream_t stream);
 cudaError_t launch_gemm_qout_mx(GemmParams& p, int N, int sms, cudaStream_t stream);
+cudaError_t launch_gemm_qout_mx_wide(GemmParams& p, int N, int sms, cudaStream_t stream);
 
 }  // namespace loka

@@ -17,6 +17,9 @@ constexpr int kBf16 = 3;
 constexpr int kNormNone = 0;
 constexpr int kNormLayer = 1;
 constexpr int kNormRms = 2;
+constexpr int kNormBlockRms = 3;   // RMSNorm over fixed blocks of the output row (BlockNorm)
+constexpr int kActNone = 0;
+constexpr int kActHardSwish = 1;
 
 constexpr int kMaxGroups = 16;
 constexpr int kMaxQuantJobs = 2 * kMaxGroups;
@@ -94,6 +97,8 @@ struct GemmParams {
   int32_t w_ready;       // 1: W and its scales were complete before the launch that precedes
                          // this GEMM, so resident W may load before waiting for that launch
   int32_t yq_mode;       // quantized output kind: kScaleRow or kScaleMx32
+  int32_t norm_block;    // BlockNorm block (32, 64, 128 or 256 columns)
+  int32_t act;           // kActNone or kActHardSwish, after the normalization
   unsigned* status;      // device status word
   uint64_t wait_limit_ns;
 };

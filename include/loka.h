@@ -63,6 +63,9 @@ typedef int32_t loka_status;
 #define LOKA_NORM_NONE 0
 #define LOKA_NORM_LAYER 1        /* (v-mean)/sqrt(var+eps)*gamma+beta      */
 #define LOKA_NORM_RMS 2          /* v/sqrt(mean(v^2)+eps)*gamma            */
+#define LOKA_NORM_BLOCK_RMS 3    /* RMSNorm over each norm_block columns    */
+#define LOKA_ACT_NONE 0
+#define LOKA_ACT_HARDSWISH 1     /* y*min(max(y+3,0),6)/6 after the norm     */
 
 /* Library version, (major << 16) | minor. */
 int32_t loka_version(void);
@@ -127,6 +130,16 @@ loka_status loka_quantize_fp8(const void* x, int64_t rows, int64_t cols, int32_t
  *   bias, gamma, beta: bf16 [N] or NULL (0, 1, 0).  y: bf16 [M,N] (see y_q).
  *   eps: added to the variance (LayerNorm) or mean square (RMSNorm).
  * Accumulation is fp32 in tensor memory; the epilogue works in fp32.
+ * BlockNorm (LoKA section III-B 2 "Block-wise Normalization": RMSNorm
+ * applied to (Wx + b).view(-1, BlockN), an unparameterized grouped RMSNorm
+ * that needs no statistics across thread blocks): norm LOKA_NORM_BLOCK_RMS
+ * normalizes every norm_block consecutive columns of a row by their own
+ * root mean square (+ eps), then multiplies by gamma when given.
+ * norm_block is 32, 64, 128 or 256 and divides N; rows wider than 256 need
+ * no cluster exchange then.  Hard Swish (LoKA section III-B 3):
+ * act LOKA_ACT_HARDSWISH applies y * min(max(y + 3, 0), 6) / 6 to the
+ * normalized (and gamma/beta-scaled) output, before the bf16 rounding and
+ * the quantized output.  Every group shares norm, norm_block and act.
  * Quantized output (PreNorm fusion, the GEM Training page, "Handling
  * Quantization Overhead": the next layer's activation quantization fused
  * into this layer's normalization): when y_q is set, the epilogue also
@@ -161,6 +174,8 @@ typedef struct loka_linear_desc {
   void* y;               /* device bf16 [M,N]; may be NULL when y_q is set */
   void* y_q;             /* device E4M3 [M,N] of the bf16 output for the next layer, or NULL */
   void* y_q_scales;      /* device fp32 [M] (LOKA_SCALE_ROW) or uint8 E8M0 [M,N/32] (LOKA_SCALE_MX32) */
+  int32_t norm_block;    /* LOKA_NORM_BLOCK_RMS: columns per block (32, 64, 128 or 256) */
+  int32_t act;           /* LOKA_ACT_NONE or LOKA_ACT_HARDSWISH */
 } loka_linear_desc;
 
 size_t loka_fp8_linear_norm_workspace_size(const loka_linear_desc* descs, int32_t num_groups);

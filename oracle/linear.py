@@ -13,6 +13,11 @@ GEMM on the same output row; RMSNorm and LayerNorm as named there):
   LayerNorm: y = (v - mean_n v) / sqrt(var_n v + eps) * gamma + beta
              (biased variance, 1/N)
   RMSNorm:   y = v / sqrt(mean_n v^2 + eps) * gamma
+  BlockNorm: the RMSNorm of each block of `norm_block` consecutive columns
+             of a row, then * gamma (section III-B 2: RMSNorm applied to
+             (Wx + b).view(-1, BlockN), a grouped RMSNorm)
+  Hard Swish (optional, after the norm; section III-B 3):
+             y * ReLU6(y + 3) / 6
   out = bf16(y), round to nearest even from float64.
 
 The GEMM is taken in float64.  For tensorwise and rowwise scaling every
@@ -29,7 +34,8 @@ from .formats import bf16_round, e4m3_decode, e8m0_decode
 from .quantize import as_f32, quantize, MX_BLOCK
 
 SCALE_TENSOR, SCALE_ROW, SCALE_MX32, SCALE_BF16 = 0, 1, 2, 3
-NORM_NONE, NORM_LAYER, NORM_RMS = 0, 1, 2
+NORM_NONE, NORM_LAYER, NORM_RMS, NORM_BLOCK_RMS = 0, 1, 2, 3
+ACT_NONE, ACT_HARDSWISH = 0, 1
 
 
 def vec64(t, n: int, default: float) -> np.ndarray:
@@ -92,22 +98,43 @@ def rmsnorm(v: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
     return v / np.sqrt(ms + eps) * gamma[None, :]
 
 
-def normalize(v: np.ndarray, norm: int, gamma, beta, eps: float) -> np.ndarray:
+def blocknorm(v: np.ndarray, gamma: np.ndarray, eps: float, block: int) -> np.ndarray:
+    """RMSNorm of every `block` consecutive columns of each row, then gamma."""
+    M, N = v.shape
+    assert N % block == 0
+    vb = v.reshape(M, N // block, block)
+    ms = (vb * vb).mean(axis=2, keepdims=True)
+    return (vb / np.sqrt(ms + eps)).reshape(M, N) * gamma[None, :]
+
+
+def hardswish(y: np.ndarray) -> np.ndarray:
+    """h-swish(y) = y * ReLU6(y + 3) / 6, with ReLU6(t) = min(max(t, 0), 6)."""
+    return y * np.minimum(np.maximum(y + 3.0, 0.0), 6.0) / 6.0
+
+
+def normalize(v: np.ndarray, norm: int, gamma, beta, eps: float, norm_block: int = 256) -> np.ndarray:
     N = v.shape[1]
     g = vec64(gamma, N, 1.0)
     if norm == NORM_LAYER:
         return layernorm(v, g, vec64(beta, N, 0.0), eps)
     if norm == NORM_RMS:
         return rmsnorm(v, g, eps)
+    if norm == NORM_BLOCK_RMS:
+        return blocknorm(v, g, eps, norm_block)
     if norm == NORM_NONE:
         return v
     raise ValueError(norm)
 
 
-def linear_norm(x, w, bias, gamma, beta, mode: int, norm: int, eps: float):
+def linear_norm(x, w, bias, gamma, beta, mode: int, norm: int, eps: float, norm_block: int = 256,
+                act: int = ACT_NONE):
     """Full layer: returns (y_exact float64, y_bf16 float64, operands)."""
     v, ops = prenorm(x, w, bias, mode)
-    y = normalize(v, norm, gamma, beta, eps)
+    y = normalize(v, norm, gamma, beta, eps, norm_block)
+    if act == ACT_HARDSWISH:
+        y = hardswish(y)
+    elif act != ACT_NONE:
+        raise ValueError(act)
     return y, bf16_round(y), ops
 
 
@@ -123,10 +150,12 @@ def linear_norm_inputs(inp, rows=None):
         if inp.mode == SCALE_TENSOR:
             raise ValueError("per-tensor scaling is not row-local")
         x = inp.x[torch.as_tensor(rows, dtype=torch.long)]
-    return linear_norm(x, inp.w, inp.bias, inp.gamma, inp.beta, inp.mode, inp.norm, inp.eps)
+    return linear_norm(x, inp.w, inp.bias, inp.gamma, inp.beta, inp.mode, inp.norm, inp.eps,
+                       inp.norm_block, inp.act)
 
 
-def linear_norm_quantized(x, w, bias, gamma, beta, mode: int, norm: int, eps: float, out_mode: int):
+def linear_norm_quantized(x, w, bias, gamma, beta, mode: int, norm: int, eps: float, out_mode: int,
+                          norm_block: int = 256, act: int = ACT_NONE):
     """The layer, then the next layer's activation quantization of its output.
 
     GEM Training page, "Handling Quantization Overhead" (the activation
@@ -141,7 +170,7 @@ def linear_norm_quantized(x, w, bias, gamma, beta, mode: int, norm: int, eps: fl
 
     Returns (y_exact float64, y_bf16 float64, q uint8 [M,N], scales).
     """
-    y, yb, _ = linear_norm(x, w, bias, gamma, beta, mode, norm, eps)
+    y, yb, _ = linear_norm(x, w, bias, gamma, beta, mode, norm, eps, norm_block, act)
     q, s = quantize(yb.astype(np.float32), out_mode)
     return y, yb, q, np.asarray(s)
 
@@ -154,4 +183,5 @@ def linear_norm_quantized_inputs(inp, out_mode: int, rows=None):
         if inp.mode == SCALE_TENSOR:
             raise ValueError("per-tensor scaling is not row-local")
         x = inp.x[torch.as_tensor(rows, dtype=torch.long)]
-    return linear_norm_quantized(x, inp.w, inp.bias, inp.gamma, inp.beta, inp.mode, inp.norm, inp.eps, out_mode)
+    return linear_norm_quantized(x, inp.w, inp.bias, inp.gamma, inp.beta, inp.mode, inp.norm, inp.eps, out_mode,
+                                 inp.norm_block, inp.act)

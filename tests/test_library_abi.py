@@ -128,6 +128,29 @@ def test_quantized_output_arguments_on_host(cpu_lib, kw, status):
     assert cpu_lib.loka_fp8_linear_norm(arr, 1, None, 0, None) == status, cpu_lib.loka_last_error()
 
 
+@pytest.mark.parametrize("kw,status", [
+    ({"norm": 3, "norm_block": 48}, _loka.LOKA_ERR_UNSUPPORTED),       # blocks are 32..256, powers of two
+    ({"norm": 3, "norm_block": 512}, _loka.LOKA_ERR_UNSUPPORTED),
+    ({"norm": 3, "norm_block": 128, "N": 192}, _loka.LOKA_ERR_INVALID_ARG),   # does not divide N
+    ({"norm": 4}, _loka.LOKA_ERR_INVALID_ARG),
+    ({"act": 2}, _loka.LOKA_ERR_INVALID_ARG),
+    ({"norm": 3, "norm_block": 64, "N": 192, "act": 1}, _loka.LOKA_ERR_WORKSPACE),   # valid
+    ({"norm": 3, "norm_block": 256, "N": 2048}, _loka.LOKA_ERR_WORKSPACE),           # valid, wide rows
+    ({"norm": 0, "act": 1}, _loka.LOKA_ERR_WORKSPACE),                               # activation alone
+])
+def test_blocknorm_and_activation_arguments_on_host(cpu_lib, kw, status):
+    arr = _loka.make_descs([_desc(**kw)])
+    assert cpu_lib.loka_fp8_linear_norm(arr, 1, None, 0, None) == status, cpu_lib.loka_last_error()
+
+
+def test_groups_share_norm_block_and_activation(cpu_lib):
+    a = {"norm": 3, "norm_block": 64}
+    assert cpu_lib.loka_fp8_linear_norm(_loka.make_descs([_desc(**a), _desc(norm=3, norm_block=128)]), 2, None, 0,
+                                        None) == _loka.LOKA_ERR_UNSUPPORTED
+    assert cpu_lib.loka_fp8_linear_norm(_loka.make_descs([_desc(act=1), _desc()]), 2, None, 0, None) == \
+        _loka.LOKA_ERR_UNSUPPORTED
+
+
 def test_quantized_output_is_all_groups_or_none(cpu_lib):
     q = {"y_q": _Q, "y_q_scales": _Q, "y_q_mode": 1}
     assert cpu_lib.loka_fp8_linear_norm(_loka.make_descs([_desc(**q), _desc()]), 2, None, 0, None) == \

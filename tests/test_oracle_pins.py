@@ -311,6 +311,50 @@ def test_linear_norm_end_to_end_vs_library_composition():
 
 
 # ------------------------------------------------------------- bf16 rounding
+# ------------------------------------------------- BlockNorm and Hard Swish
+@pytest.mark.parametrize("block", [32, 64, 128, 256])
+def test_blocknorm_is_rms_norm_of_the_blocked_view(block):
+    # LoKA III-B 2: RMSNorm((Wx + b).view(-1, BlockN)).view(B, N); torch's
+    # rms_norm on that view is an independent library routine
+    rng = np.random.default_rng(block)
+    M, N, eps = 6, 512, 1e-6
+    v = rng.standard_normal((M, N)) * rng.uniform(0.1, 10.0, (M, 1))
+    g = rng.uniform(0.5, 1.5, N)
+    ours = L.blocknorm(v, g, eps, block)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(v).view(-1, block), (block,), eps=eps).view(M, N).numpy()
+    assert np.allclose(ours, ref * g[None, :], rtol=1e-13, atol=1e-13)
+    # gamma = 1: every block's mean square is ms / (ms + eps)
+    y = L.blocknorm(v, np.ones(N), eps, block).reshape(M, N // block, block)
+    ms = (v.reshape(M, N // block, block) ** 2).mean(axis=2)
+    assert np.allclose((y ** 2).mean(axis=2), ms / (ms + eps), rtol=1e-12)
+
+
+def test_blocknorm_over_the_whole_row_is_rmsnorm():
+    rng = np.random.default_rng(3)
+    v = rng.standard_normal((4, 256))
+    g = rng.uniform(0.5, 1.5, 256)
+    assert np.allclose(L.blocknorm(v, g, 1e-6, 256), L.rmsnorm(v, g, 1e-6), rtol=0, atol=0)
+
+
+def test_hardswish_matches_torch_and_known_points():
+    x = np.concatenate([np.linspace(-8, 8, 4001), [-3.0, -1.5, 0.0, 3.0, -3.0000001, 2.9999999]])
+    ref = torch.nn.functional.hardswish(torch.from_numpy(x)).numpy()
+    assert np.allclose(L.hardswish(x), ref, rtol=1e-15, atol=1e-15)
+    assert L.hardswish(np.array([-3.0]))[0] == 0.0 and L.hardswish(np.array([3.0]))[0] == 3.0
+    assert L.hardswish(np.array([-1.5]))[0] == -0.375              # the minimum
+    assert np.all(L.hardswish(np.array([-5.0, -100.0])) == 0.0)
+    assert np.all(L.hardswish(np.array([4.0, 50.0])) == np.array([4.0, 50.0]))
+
+
+def test_layer_applies_hard_swish_after_the_norm():
+    inp = W.make_layer(16, 128, 256, mode=L.SCALE_ROW, norm=L.NORM_BLOCK_RMS, seed=9, gamma_uniform=True)
+    inp.norm_block = 64
+    y0, _, _ = L.linear_norm_inputs(inp)
+    inp.act = L.ACT_HARDSWISH
+    y1, _, _ = L.linear_norm_inputs(inp)
+    assert np.array_equal(y1, L.hardswish(y0))
+
+
 # ------------------------------------- quantized output for the next layer
 def test_quantized_output_rowwise_is_the_quantized_bf16_output():
     # per row: the largest |bf16 output| maps to 448, the scale is amax/448,

@@ -35,7 +35,8 @@ import torch
 # Variant and normalization identifiers shared by tests and the bench.  These
 # are names, not arithmetic.
 SCALE_TENSOR, SCALE_ROW, SCALE_MX32, SCALE_BF16 = 0, 1, 2, 3
-NORM_NONE, NORM_LAYER, NORM_RMS = 0, 1, 2
+NORM_NONE, NORM_LAYER, NORM_RMS, NORM_BLOCK_RMS = 0, 1, 2, 3
+ACT_NONE, ACT_HARDSWISH = 0, 1
 EPS_LAYER = 1e-5
 EPS_RMS = 1e-6
 
@@ -52,6 +53,8 @@ class LayerInputs:
     mode: int
     norm: int
     eps: float
+    norm_block: int = 256           # NORM_BLOCK_RMS: columns per block
+    act: int = ACT_NONE             # activation after the norm
 
     @property
     def M(self) -> int:
@@ -107,7 +110,7 @@ def make_layer(M: int, K: int, N: int, *, mode: int, norm: int, seed: int = 0,
     bias = _bf16(normal(rng, (N,), var=bias_var)) if bias_var is not None else None
     gamma = _bf16(rng.uniform(0.5, 1.5, size=(N,)).astype(np.float32)) if gamma_uniform else None
     if eps is None:
-        eps = EPS_RMS if norm == NORM_RMS else EPS_LAYER
+        eps = EPS_RMS if norm in (NORM_RMS, NORM_BLOCK_RMS) else EPS_LAYER
     return LayerInputs(x=_bf16(x), w=_bf16(w), bias=bias, gamma=gamma, beta=None,
                        mode=mode, norm=norm, eps=eps)
 
