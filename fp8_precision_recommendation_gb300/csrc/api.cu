@@ -333,6 +333,7 @@ loka_status build_gemm(const loka_linear_desc* d, int n, const std::vector<Opera
   p->yq_mode = out == OutKind::kQuant ? output_reference(d, n).y_q_mode : 0;
   p->norm_block = norm == kNormBlockRms ? d[0].norm_block : 256;
   p->act = out == OutKind::kF32 ? kActNone : d[0].act;   // the probe's pre-norm outputs take no activation
+  p->slices = 1;
   return LOKA_OK;
 }
 

@@ -12,6 +12,14 @@ bool gemm_supported(int N, int K, OperandKind op) {
 }
 
 cudaError_t launch_gemm_norm(GemmParams& p, int N, OperandKind op, OutKind out, int sms, cudaStream_t stream) {
+  // Rows wider than one CTA whose epilogue needs no row statistic (no norm,
+  // or BlockNorm, whose blocks lie within a CTA's 256 columns) run as
+  // independent 256-column slices: no cluster co-scheduling, every SM busy.
+  p.slices = 1;
+  if (N > 256 && (p.norm == kNormNone || p.norm == kNormBlockRms)) {
+    p.slices = N / 256;
+    N = 256;
+  }
   if (out == OutKind::kQuant) {
     const bool wide = N > 256;
     if (op == OperandKind::kE4M3)

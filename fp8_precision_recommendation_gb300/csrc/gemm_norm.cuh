@@ -142,10 +142,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
   const int stages = p.stages;
   const int num_kb = p.K / KE;
   const Layout L = make_layout(N, p.K, EB, RESIDENT, stages, kMx, CL);
-  const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
+  // A tile's N-column slices go to the CTAs of a cluster (CL > 1, row
+  // statistics exchanged), or, when no statistic spans the row (CL == 1,
+  // p.slices > 1), to p.slices independent consecutive CTAs.  rank = this
+  // CTA's slice, cid / ncl = its unit (cluster or slice group) and their count.
+  const int slices = CL > 1 ? CL : p.slices;
+  const uint32_t rank = CL > 1 ? cluster_ctarank() : static_cast<uint32_t>(blockIdx.x) % static_cast<uint32_t>(slices);
   const int col0 = static_cast<int>(rank) * N;      // first output column of this CTA
-  const int cid = static_cast<int>(blockIdx.x) / CL;
-  const int ncl = static_cast<int>(gridDim.x) / CL;
+  const int cid = static_cast<int>(blockIdx.x) / slices;
+  const int ncl = static_cast<int>(gridDim.x) / slices;
+  const int ng = N * slices;                        // columns of the whole output row
 
   // Pointers are derived from the __shared__ array by plain offsets, so the
   // compiler keeps them in the shared address space (LDS/STS, not generic
@@ -535,9 +541,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
         // E4M3 codes: 8 contiguous bytes per lane after a transpose
         constexpr bool kWide = kBf16Out || kQOut;
         rowp[k] = reinterpret_cast<uint8_t*>(reinterpret_cast<uintptr_t>(G.y) +
-                                             (m * NG + col0 + (kWide ? 8 : 2) * cp) * (kWide ? 2 : 4));
+                                             (m * ng + col0 + (kWide ? 8 : 2) * cp) * (kWide ? 2 : 4));
         if constexpr (kQOut) {
-          if (k == 0) rowq = G.yq + m * NG + col0 + 8 * cp;
+          if (k == 0) rowq = G.yq + m * ng + col0 + 8 * cp;
         }
       }
       const int buf = NBUF == 2 ? team : 0;
@@ -933,7 +939,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
               const int e = mx_exponent(am);
               mul[k] = pow2_neg(e);
               if (cp == 0 && ok[k])
-                static_cast<uint8_t*>(G.yq_scales)[(static_cast<int64_t>(m0) + rowk[k]) * (NG / 32) + (col0 + c0) / 32] =
+                static_cast<uint8_t*>(G.yq_scales)[(static_cast<int64_t>(m0) + rowk[k]) * (ng / 32) + (col0 + c0) / 32] =
                     static_cast<uint8_t>(e + 127);
             }
           }
@@ -949,14 +955,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
               transpose4_lanes(pk[k], cp);
-              st_global_pred_v4b32(rowp[0] + k * (8 * NG * 2) + c0 * 2, pk[k], ok[k]);
+              st_global_pred_v4b32(rowp[0] + k * (8 * ng * 2) + c0 * 2, pk[k], ok[k]);
             }
           }
           // lane cp now holds, in element t, the codes of columns 8 cp + 2t
           // and 8 cp + 2t + 1: row 0 in the low half, row 1 in the high half
           transpose4_lanes(w, cp);
           st_global_pred_v2b32(rowq + c0, (w[0] & 0xFFFFu) | (w[1] << 16), (w[2] & 0xFFFFu) | (w[3] << 16), ok[0]);
-          st_global_pred_v2b32(rowq + 8 * NG + c0, (w[0] >> 16) | (w[1] & 0xFFFF0000u), (w[2] >> 16) | (w[3] & 0xFFFF0000u),
+          st_global_pred_v2b32(rowq + 8 * ng + c0, (w[0] >> 16) | (w[1] & 0xFFFF0000u), (w[2] >> 16) | (w[3] & 0xFFFF0000u),
                                ok[1]);
         });
       };
@@ -1034,7 +1040,9 @@ cudaError_t launch_one(const GemmParams& p, size_t smem, int sms, cudaStream_t s
     }
     configured.fetch_or(bit);
   }
-  int clusters = sms / CL;
+  // units: clusters of CL CTAs, or groups of p.slices CTAs (one per slice)
+  const int per_unit = CL > 1 ? CL : p.slices;
+  int clusters = sms / per_unit;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
@@ -1069,7 +1077,7 @@ cudaError_t launch_one(const GemmParams& p, size_t smem, int sms, cudaStream_t s
   }
   if (p.total_tiles < clusters) clusters = p.total_tiles;
   if (clusters < 1) return cudaSuccess;
-  cfg.gridDim = dim3(static_cast<unsigned>(clusters * CL));
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * per_unit));
   e = cudaLaunchKernelEx(&cfg, kern, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

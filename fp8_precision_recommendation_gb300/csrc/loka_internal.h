@@ -99,6 +99,7 @@ struct GemmParams {
   int32_t yq_mode;       // quantized output kind: kScaleRow or kScaleMx32
   int32_t norm_block;    // BlockNorm block (32, 64, 128 or 256 columns)
   int32_t act;           // kActNone or kActHardSwish, after the normalization
+  int32_t slices;        // CL == 1 launches: independent column slices per row (1 = none)
   unsigned* status;      // device status word
   uint64_t wait_limit_ns;
 };
