@@ -43,7 +43,8 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-compare", action="store_true")
     ap.add_argument("--M", type=int, default=None, help="rows of X per layer (default: the workload's own)")
-    ap.add_argument("--workload", default="rec_mlp", choices=["rec_mlp", "ensemble", "mxfp8", "single"])
+    ap.add_argument("--workload", default="rec_mlp",
+                    choices=["rec_mlp", "ensemble", "mxfp8", "single", "wide_blocknorm"])
     return ap.parse_args()
 
 
@@ -263,6 +264,8 @@ def workload_layers(name: str, rank: int, M):
         return [W.mxfp8(seed=rank, **({"M": M} if M else {}))]
     if name == "single":
         return [W.single(seed=rank)]
+    if name == "wide_blocknorm":
+        return [W.wide_blocknorm(seed=rank, **({"M": M} if M else {}))]
     raise ValueError(name)
 
 
@@ -295,6 +298,7 @@ def run_ours(args, world, rank, local):
     def mk(i, x_list=None, mode_=None, **kw):
         return [loka.Layer(x=(x_list or xs[i % nbuf])[gi], w=ws_[gi], bias=bs_[gi], gamma=gs_[gi], beta=bes_[gi],
                            mode=mode if mode_ is None else mode_, norm=norm, eps=eps, y=ys[i % nbuf][gi],
+                           norm_block=layers[gi].norm_block, act=layers[gi].act,
                            **{k: v[gi] for k, v in kw.items()}) for gi in range(len(layers))]
 
     def step(i):
@@ -456,9 +460,16 @@ def run_ours(args, world, rank, local):
             for gi, l in enumerate(layers):
                 v = torch.nn.functional.linear(xs[i % nbuf][gi], ws_[gi], bs_[gi])
                 if norm == 1:
-                    torch.nn.functional.layer_norm(v, (l.N,), gs_[gi], bes_[gi], eps=eps)
+                    v = torch.nn.functional.layer_norm(v, (l.N,), gs_[gi], bes_[gi], eps=eps)
                 elif norm == 2:
-                    torch.nn.functional.rms_norm(v, (l.N,), gs_[gi], eps=eps)
+                    v = torch.nn.functional.rms_norm(v, (l.N,), gs_[gi], eps=eps)
+                elif norm == 3:
+                    nb = l.norm_block
+                    v = torch.nn.functional.rms_norm(v.view(-1, nb), (nb,), eps=eps).view(l.M, l.N)
+                    if gs_[gi] is not None:
+                        v = v * gs_[gi]
+                if l.act:
+                    torch.nn.functional.hardswish(v)
         compare["torch_bf16_linear_norm_us"] = 1e6 * timed(torch_bf16, args.steps)
         compare["loka_fp8_step_us"] = 1e6 * step_time
         compare["loka_fp8_step_static_w_us"] = 1e6 * static_w_step
@@ -534,7 +545,9 @@ def run_ours(args, world, rank, local):
     desc = {"rec_mlp": "rec-MLP X N(0,1)+1%x100 outliers, per-row E4M3, bias, LayerNorm",
             "ensemble": "8-layer ensemble, per-row E4M3, RMSNorm, one grouped launch",
             "mxfp8": "Laplace X, MX 1x32 E8M0 block scaling, LayerNorm",
-            "single": "per-tensor E4M3, LayerNorm"}[args.workload]
+            "single": "per-tensor E4M3, LayerNorm",
+            "wide_blocknorm": "wide layer N(0,1)+1%x100 outliers, per-row E4M3, bias, BlockNorm 256, Hard Swish"}[
+                args.workload]
     metric = METRIC if args.workload == "rec_mlp" and not args.M else \
         f"FP8 linear+norm TFLOP/s ({args.workload} {len(layers)}x{l0.M}x{l0.K}x{l0.N}) on 1 GB300"
     line = {

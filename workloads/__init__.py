@@ -137,6 +137,15 @@ def mxfp8(seed: int = 0, M: int = 262144, K: int = 2048, N: int = 512) -> LayerI
     return make_layer(M, K, N, mode=SCALE_MX32, norm=NORM_LAYER, seed=seed, x_dist="laplace")
 
 
+def wide_blocknorm(seed: int = 0, M: int = 65536, K: int = 512, N: int = 2048) -> LayerInputs:
+    """A wide LRM layer: per-row E4M3, BlockNorm over 256-column blocks,
+    then Hard Swish (the LoKA Mods pair that keeps wide rows in one pass)."""
+    inp = make_layer(M, K, N, mode=SCALE_ROW, norm=NORM_BLOCK_RMS, seed=seed, outlier_frac=0.01, bias_var=0.02)
+    inp.norm_block = 256
+    inp.act = ACT_HARDSWISH
+    return inp
+
+
 def sweep_shapes():
     """The sweep grid: M in 4096..524288 (powers of two), K, N in 64..2048."""
     Ms = [4096 << i for i in range(8)]
