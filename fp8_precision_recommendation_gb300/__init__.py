@@ -20,7 +20,8 @@ from typing import List, Optional, Sequence
 
 from . import _loka
 from ._loka import (LOKA_ACT_HARDSWISH, LOKA_ACT_NONE, LOKA_BF16, LOKA_NORM_BLOCK_RMS,  # noqa: F401
-                    LOKA_NORM_LAYER, LOKA_NORM_NONE, LOKA_NORM_RMS, LOKA_SCALE_MX32, LOKA_SCALE_ROW, LOKA_SCALE_TENSOR, DispatchEntry, LinearDesc, LokaError, Policy, Problem)
+                    LOKA_NORM_LAYER, LOKA_NORM_NONE, LOKA_NORM_RMS, LOKA_SCALE_BLOCK32, LOKA_SCALE_MX32,
+                    LOKA_SCALE_ROW, LOKA_SCALE_TENSOR, DispatchEntry, LinearDesc, LokaError, Policy, Problem)
 
 __all__ = ["quantize_fp8", "fp8_linear_norm", "quant_error", "dispatch_select", "Layer", "Workspace"]
 
@@ -37,6 +38,8 @@ def scales_shape(rows: int, cols: int, mode: int):
         return (rows,), "float32"
     if mode == LOKA_SCALE_MX32:
         return (rows, cols // 32), "uint8"
+    if mode == LOKA_SCALE_BLOCK32:
+        return ((rows + 31) // 32, cols // 32), "uint8"
     raise ValueError(f"mode {mode} has no FP8 scales")
 
 
@@ -78,6 +81,20 @@ def quantize_fp8(x, mode: int, workspace: Optional[Workspace] = None, stream=Non
     ws, nbytes = (workspace or _ws(x.device)).get(need)
     _loka.loka_quantize_fp8(x, rows, cols, mode, q, scales, ws, nbytes, stream)
     return q, scales
+
+
+def quantize_fp8_block32(x, transposed: bool = False, stream=None):
+    """Square 32x32-block E4M3 cast of a bf16 CUDA tensor [rows, cols];
+    returns (q, scales [ceil(rows/32), cols/32], q_t [cols, rows] or None)."""
+    torch = _torch()
+    assert x.dtype == torch.bfloat16 and x.is_cuda and x.is_contiguous() and x.dim() == 2
+    rows, cols = x.shape
+    q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    shp, _ = scales_shape(rows, cols, LOKA_SCALE_BLOCK32)
+    scales = torch.empty(shp, dtype=torch.uint8, device=x.device)
+    q_t = torch.empty((cols, rows), dtype=torch.uint8, device=x.device) if transposed else None
+    _loka.loka_quantize_fp8_block32(x, rows, cols, q, q_t, scales, stream)
+    return q, scales, q_t
 
 
 @dataclasses.dataclass

@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libloka.so")
 
 LOKA_OK, LOKA_ERR_INVALID_ARG, LOKA_ERR_UNSUPPORTED, LOKA_ERR_WORKSPACE, LOKA_ERR_TIMEOUT, LOKA_ERR_CUDA = range(6)
-LOKA_SCALE_TENSOR, LOKA_SCALE_ROW, LOKA_SCALE_MX32, LOKA_BF16 = range(4)
+LOKA_SCALE_TENSOR, LOKA_SCALE_ROW, LOKA_SCALE_MX32, LOKA_BF16, LOKA_SCALE_BLOCK32 = range(5)
 LOKA_NORM_NONE, LOKA_NORM_LAYER, LOKA_NORM_RMS, LOKA_NORM_BLOCK_RMS = range(4)
 LOKA_ACT_NONE, LOKA_ACT_HARDSWISH = range(2)
 
@@ -58,6 +58,7 @@ SIGNATURES = {
     "loka_selftest_watchdog": (c_i32, [ctypes.c_uint64, c_p]),
     "loka_quantize_fp8_workspace_size": (c_sz, [c_i64, c_i64, c_i32]),
     "loka_quantize_fp8": (c_i32, [c_p, c_i64, c_i64, c_i32, c_p, c_p, c_p, c_sz, c_p]),
+    "loka_quantize_fp8_block32": (c_i32, [c_p, c_i64, c_i64, c_p, c_p, c_p, c_p]),
     "loka_fp8_linear_norm_workspace_size": (c_sz, [ctypes.POINTER(LinearDesc), c_i32]),
     "loka_fp8_linear_norm": (c_i32, [ctypes.POINTER(LinearDesc), c_i32, c_p, c_sz, c_p]),
     "loka_fp8_linear_norm_static": (c_i32, [ctypes.POINTER(LinearDesc), c_i32, c_p]),
@@ -138,6 +139,10 @@ def loka_quantize_fp8(x, rows: int, cols: int, mode: int, q, scales, workspace=N
                       stream=None) -> None:
     check(load().loka_quantize_fp8(_ptr(x), rows, cols, mode, _ptr(q), _ptr(scales), _ptr(workspace),
                                    workspace_bytes, _stream(stream)))
+
+
+def loka_quantize_fp8_block32(x, rows: int, cols: int, q, q_t, scales, stream=None) -> None:
+    check(load().loka_quantize_fp8_block32(_ptr(x), rows, cols, _ptr(q), _ptr(q_t), _ptr(scales), _stream(stream)))
 
 
 def make_descs(descs: Sequence[LinearDesc]):

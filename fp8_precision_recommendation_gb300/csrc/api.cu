@@ -139,6 +139,7 @@ size_t scale_bytes(int mode, int64_t rows, int64_t cols) {
   if (mode == kScaleTensor) return sizeof(float);
   if (mode == kScaleRow) return static_cast<size_t>(rows) * sizeof(float);
   if (mode == kScaleMx32) return static_cast<size_t>(rows) * static_cast<size_t>(cols / 32);
+  if (mode == kScaleBlock32) return static_cast<size_t>((rows + 31) / 32) * static_cast<size_t>(cols / 32);
   return 0;
 }
 
@@ -170,7 +171,7 @@ size_t layout_operands(const loka_linear_desc* d, int n, std::vector<OperandSlot
         s.amax = off;
         off = align_up(off + 2 * sizeof(unsigned));
       }
-      if (d[i].mode == kScaleMx32) {
+      if (d[i].mode == kScaleMx32 || d[i].mode == kScaleBlock32) {
         s.sx_tc = off;
         off = align_up(off + static_cast<size_t>(sf_tc_bytes(d[i].M, d[i].K)));
         s.sw_tc = off;
@@ -185,7 +186,9 @@ size_t layout_operands(const loka_linear_desc* d, int n, std::vector<OperandSlot
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 OperandKind operand_kind(int mode) {
-  return mode == kBf16 ? OperandKind::kBf16 : (mode == kScaleMx32 ? OperandKind::kMxE4M3 : OperandKind::kE4M3);
+  if (mode == kBf16) return OperandKind::kBf16;
+  // square 32x32 blocks use the block-scaled MMA like MX: each row takes its block row's scales
+  return (mode == kScaleMx32 || mode == kScaleBlock32) ? OperandKind::kMxE4M3 : OperandKind::kE4M3;
 }
 
 // The group whose output fields (y_q, y_q_mode) speak for the call: the
@@ -211,7 +214,8 @@ loka_status validate(const loka_linear_desc* d, int n, bool probe) {
     if (g.M < 0) return fail(LOKA_ERR_INVALID_ARG, "group %d: M = %lld < 0", i, static_cast<long long>(g.M));
     if (g.M > (int64_t(1) << 31)) return fail(LOKA_ERR_UNSUPPORTED, "group %d: M too large", i);
   }
-  if (a.mode < 0 || a.mode > kBf16) return fail(LOKA_ERR_INVALID_ARG, "mode %d is not a LOKA_SCALE_* value", a.mode);
+  if (a.mode < 0 || a.mode > kScaleBlock32)
+    return fail(LOKA_ERR_INVALID_ARG, "mode %d is not a LOKA_SCALE_* value", a.mode);
   if (a.norm < 0 || a.norm > kNormBlockRms)
     return fail(LOKA_ERR_INVALID_ARG, "norm %d is not a LOKA_NORM_* value", a.norm);
   if (a.act != kActNone && a.act != kActHardSwish)
@@ -308,7 +312,7 @@ loka_status build_gemm(const loka_linear_desc* d, int n, const std::vector<Opera
       const void* sw = g.w_is_fp8 ? g.w_scales : ws + slots[i].sw;
       if ((s = encode_2d(&G.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xq, g.K, g.M, 128)) != LOKA_OK) return s;
       if ((s = encode_2d(&G.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wq, g.K, g.N, g.N > 256 ? 256 : g.N)) != LOKA_OK) return s;
-      if (mode == kScaleMx32) {   // the block scales are applied inside the MMA
+      if (mode == kScaleMx32 || mode == kScaleBlock32) {   // the block scales are applied inside the MMA
         G.sfa_tc = ws + slots[i].sx_tc;
         G.sfb_tc = ws + slots[i].sw_tc;
       } else {
@@ -352,7 +356,7 @@ loka_status quantize_operands(const loka_linear_desc* d, int n, const std::vecto
       j.q = ws + slots[i].xq;
       j.scales = ws + slots[i].sx;
       j.amax_slot = reinterpret_cast<unsigned*>(ws + slots[i].amax);
-      j.sf_tc = g.mode == kScaleMx32 ? ws + slots[i].sx_tc : nullptr;
+      j.sf_tc = (g.mode == kScaleMx32 || g.mode == kScaleBlock32) ? ws + slots[i].sx_tc : nullptr;
       j.rows = g.M;
       j.cols = g.K;
       j.row_begin = rows;
@@ -364,7 +368,7 @@ loka_status quantize_operands(const loka_linear_desc* d, int n, const std::vecto
       j.q = ws + slots[i].wq;
       j.scales = ws + slots[i].sw;
       j.amax_slot = reinterpret_cast<unsigned*>(ws + slots[i].amax) + 1;
-      j.sf_tc = g.mode == kScaleMx32 ? ws + slots[i].sw_tc : nullptr;
+      j.sf_tc = (g.mode == kScaleMx32 || g.mode == kScaleBlock32) ? ws + slots[i].sw_tc : nullptr;
       j.rows = g.N;
       j.cols = g.K;
       j.row_begin = rows;
@@ -421,9 +425,11 @@ size_t loka_quantize_fp8_workspace_size(int64_t, int64_t, int32_t mode) {
   return mode == LOKA_SCALE_TENSOR ? kAlign : 0;
 }
 
-loka_status loka_quantize_fp8(const void* x, int64_t rows, int64_t cols, int32_t mode, void* q, void* scales,
-                              void* workspace, size_t workspace_bytes, void* stream) {
-  if (mode != LOKA_SCALE_TENSOR && mode != LOKA_SCALE_ROW && mode != LOKA_SCALE_MX32)
+namespace {
+
+loka_status quantize_one(const void* x, int64_t rows, int64_t cols, int32_t mode, void* q, void* q_t, void* scales,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  if (mode != LOKA_SCALE_TENSOR && mode != LOKA_SCALE_ROW && mode != LOKA_SCALE_MX32 && mode != LOKA_SCALE_BLOCK32)
     return fail(LOKA_ERR_INVALID_ARG, "mode %d is not an FP8 scaling mode", mode);
   if (rows < 0 || cols < 0) return fail(LOKA_ERR_INVALID_ARG, "negative size");
   if (cols % 32 != 0) return fail(LOKA_ERR_INVALID_ARG, "cols = %lld is not a multiple of 32", static_cast<long long>(cols));
@@ -437,7 +443,9 @@ loka_status loka_quantize_fp8(const void* x, int64_t rows, int64_t cols, int32_t
   }
   if (x == nullptr || q == nullptr || scales == nullptr) return fail(LOKA_ERR_INVALID_ARG, "x, q and scales must not be NULL");
   if (!aligned16(x) || !aligned16(q)) return fail(LOKA_ERR_INVALID_ARG, "x and q must be 16-byte aligned");
-  if (mode != LOKA_SCALE_MX32 && (reinterpret_cast<uintptr_t>(scales) & 3u))
+  if (q_t != nullptr && (rows % 32 != 0 || !aligned16(q_t)))
+    return fail(LOKA_ERR_INVALID_ARG, "the transposed codes need rows %% 32 == 0 and a 16-byte-aligned q_t");
+  if ((mode == LOKA_SCALE_TENSOR || mode == LOKA_SCALE_ROW) && (reinterpret_cast<uintptr_t>(scales) & 3u))
     return fail(LOKA_ERR_INVALID_ARG, "scales must be 4-byte aligned");
   const size_t need = loka_quantize_fp8_workspace_size(rows, cols, mode);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
@@ -450,6 +458,7 @@ loka_status loka_quantize_fp8(const void* x, int64_t rows, int64_t cols, int32_t
   jobs.n = 1;
   jobs.j[0].x = x;
   jobs.j[0].q = static_cast<uint8_t*>(q);
+  jobs.j[0].q_t = static_cast<uint8_t*>(q_t);
   jobs.j[0].scales = scales;
   jobs.j[0].amax_slot = static_cast<unsigned*>(workspace);
   jobs.j[0].rows = rows;
@@ -458,6 +467,18 @@ loka_status loka_quantize_fp8(const void* x, int64_t rows, int64_t cols, int32_t
   cudaError_t e = launch_quantize(jobs, mode, dev->sms, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
   return LOKA_OK;
+}
+
+}  // namespace
+
+loka_status loka_quantize_fp8(const void* x, int64_t rows, int64_t cols, int32_t mode, void* q, void* scales,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  return quantize_one(x, rows, cols, mode, q, nullptr, scales, workspace, workspace_bytes, stream);
+}
+
+loka_status loka_quantize_fp8_block32(const void* x, int64_t rows, int64_t cols, void* q, void* q_t, void* scales,
+                                      void* stream) {
+  return quantize_one(x, rows, cols, LOKA_SCALE_BLOCK32, q, q_t, scales, nullptr, 0, stream);
 }
 
 size_t loka_fp8_linear_norm_workspace_size(const loka_linear_desc* descs, int32_t num_groups) {
@@ -484,14 +505,18 @@ loka_status loka_fp8_linear_norm(const loka_linear_desc* descs, int32_t num_grou
   if (!bf16 && (!descs[0].x_is_fp8 || !descs[0].w_is_fp8)) {
     if ((s = quantize_operands(descs, num_groups, slots, ws, dev, st)) != LOKA_OK) return s;
   }
-  if (descs[0].mode == kScaleMx32) {   // caller-quantized MX operands: scales into the copy layout
+  if (descs[0].mode == kScaleMx32 || descs[0].mode == kScaleBlock32) {
+    // caller-quantized MX / 32x32-block operands: scales into the copy layout
+    const int row_div = descs[0].mode == kScaleBlock32 ? 32 : 1;
     for (int i = 0; i < num_groups; ++i) {
       const loka_linear_desc& g = descs[i];
       cudaError_t e = cudaSuccess;
       if (g.x_is_fp8 && g.M > 0)
-        e = launch_sf_permute(static_cast<const uint8_t*>(g.x_scales), ws + slots[i].sx_tc, g.M, g.K, dev->sms, st);
+        e = launch_sf_permute(static_cast<const uint8_t*>(g.x_scales), ws + slots[i].sx_tc, g.M, g.K, row_div, dev->sms,
+                              st);
       if (e == cudaSuccess && g.w_is_fp8)
-        e = launch_sf_permute(static_cast<const uint8_t*>(g.w_scales), ws + slots[i].sw_tc, g.N, g.K, dev->sms, st);
+        e = launch_sf_permute(static_cast<const uint8_t*>(g.w_scales), ws + slots[i].sw_tc, g.N, g.K, row_div, dev->sms,
+                              st);
       if (e != cudaSuccess) return cuda_fail(e, "scale permute launch");
     }
   }
@@ -502,7 +527,8 @@ loka_status loka_fp8_linear_norm(const loka_linear_desc* descs, int32_t num_grou
   // precedes it only when that launch is this call's own activation
   // quantizer: it started after everything the caller queued (W included)
   // had finished.  (MX also permutes W's scales right before the GEMM.)
-  p.w_ready = (!bf16 && descs[0].w_is_fp8 && !descs[0].x_is_fp8 && descs[0].mode != kScaleMx32) ? 1 : 0;
+  p.w_ready = (!bf16 && descs[0].w_is_fp8 && !descs[0].x_is_fp8 && operand_kind(descs[0].mode) != OperandKind::kMxE4M3)
+                  ? 1 : 0;
   cudaError_t e = launch_gemm_norm(p, static_cast<int>(descs[0].N), operand_kind(descs[0].mode), out, dev->sms, st);
   if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
   return LOKA_OK;

@@ -13,6 +13,7 @@ constexpr int kScaleTensor = 0;
 constexpr int kScaleRow = 1;
 constexpr int kScaleMx32 = 2;
 constexpr int kBf16 = 3;
+constexpr int kScaleBlock32 = 4;   // square 32 x 32 blocks, E8M0 scales
 
 constexpr int kNormNone = 0;
 constexpr int kNormLayer = 1;
@@ -31,10 +32,13 @@ struct QuantJob {
   uint8_t* q;
   void* scales;
   unsigned* amax_slot;   // tensorwise only: 4-byte accumulator, zeroed by the launcher
-  uint8_t* sf_tc;        // MX only, optional: E8M0 codes again in the tensor-memory copy layout
+  uint8_t* sf_tc;        // MX / 32x32 blocks, optional: E8M0 codes again in the tensor-memory copy
+                         // layout (32x32 blocks: every row of a block row repeats its codes)
+  uint8_t* q_t;          // 32x32 blocks only, optional: the codes transposed, [cols, rows]
   int64_t rows;
   int64_t cols;
-  int64_t row_begin;     // first row of this job in the launch's joint row space
+  int64_t row_begin;     // first row of this job in the launch's joint row space (32x32 blocks:
+                         // first unit of 32 rows x 256 columns, set by launch_quantize)
 };
 
 struct QuantJobs {
@@ -59,8 +63,10 @@ __host__ __device__ inline int64_t sf_tc_bytes(int64_t rows, int64_t cols) {
   return ((rows + 127) / 128) * (cols / 128) * 512;
 }
 
-// Rewrites logical [rows, cols/32] E8M0 codes into the tensor-memory copy layout.
-cudaError_t launch_sf_permute(const uint8_t* logical, uint8_t* tc, int64_t rows, int64_t cols, int sms,
+// Rewrites logical E8M0 codes into the tensor-memory copy layout: [rows,
+// cols/32] (row_div 1, MX) or [ceil(rows/32), cols/32] (row_div 32, square
+// blocks: each row takes its block row's codes).
+cudaError_t launch_sf_permute(const uint8_t* logical, uint8_t* tc, int64_t rows, int64_t cols, int row_div, int sms,
                               cudaStream_t stream);
 
 // ------------------------------------------------------------------ GEMM

@@ -163,13 +163,103 @@ __global__ void __launch_bounds__(256) cast_tensor_kernel(const __grid_constant_
 }
 
 __global__ void __launch_bounds__(256) sf_permute_kernel(const uint8_t* __restrict__ logical, uint8_t* __restrict__ tc,
-                                                         int64_t rows, int64_t cols) {
+                                                         int64_t rows, int64_t cols, int row_div) {
   const int64_t nb = cols >> 5;
   const int64_t total = rows * nb;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t m = i / nb, b = i - m * nb;
-    tc[sf_tc_offset(m, b, cols >> 7)] = logical[i];
+    tc[sf_tc_offset(m, b, cols >> 7)] = logical[(m / row_div) * nb + b];
+  }
+}
+
+// Square 32 x 32 blocks (GEM Training page, "Low Precision Flash Attention":
+// one scale per [32, 32] block, so the quantization of X^T is the transpose
+// of that of X and a tensor is quantized once for both GEMM directions).
+// One 256-thread block per unit of 32 rows x 256 columns (8 blocks): warp w
+// loads rows 4w..4w+3 of the strip, each lane 8 columns of each row (16-byte
+// vectors, 512 contiguous bytes per row per warp).  A block's amax merges the
+// 4 lanes of its 32 columns (shuffles), then the 8 warps (shared memory); the
+// exponent rule is the MX one.  Codes go out row by row; the optional
+// transposed copy is staged in shared memory and transposed 4 x 4 bytes at a
+// time (byte permutes), each thread writing 8 codes of 4 transposed rows.
+__global__ void __launch_bounds__(256) quant_block32_kernel(const __grid_constant__ QuantJobs jobs) {
+  launch_dependents();   // the GEMM that follows may start its prologue
+  __shared__ float red[8][8];                        // [warp][block] partial amax
+  __shared__ int ex[8];                              // the unit's block exponents
+  __shared__ __align__(16) uint8_t tile[32][256 + 16];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int64_t u = blockIdx.x; u < jobs.total_rows; u += gridDim.x) {
+    const QuantJob& job = jobs.j[find_job(jobs, u)];
+    const int64_t lu = u - job.row_begin;
+    const int64_t segs = (job.cols + 255) >> 8;
+    const int64_t rb = lu / segs, seg = lu - rb * segs;
+    const int64_t r0 = rb * 32, c0 = seg * 256;
+    const int64_t nvec = job.cols >> 3;
+    const uint4* src = reinterpret_cast<const uint4*>(job.x);
+    const bool col_ok = c0 + 8 * lane < job.cols;
+    uint4 v[4];
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t row = r0 + 4 * warp + i;
+      v[i] = (col_ok && row < job.rows) ? __ldcs(src + row * nvec + (c0 >> 3) + lane) : make_uint4(0, 0, 0, 0);
+      m = abs_max8(v[i], m);
+    }
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    if ((lane & 3) == 0) red[warp][lane >> 2] = m;
+    __syncthreads();
+    if (warp == 0 && lane < 8) {
+      float a = red[0][lane];
+#pragma unroll
+      for (int w = 1; w < 8; ++w) a = fmaxf(a, red[w][lane]);
+      ex[lane] = mx_exponent(a);
+    }
+    __syncthreads();
+    const float mul = pow2_neg(ex[lane >> 2]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t row = r0 + 4 * warp + i;
+      const uint2 c = cast8(v[i], mul);
+      if (col_ok && row < job.rows) reinterpret_cast<uint2*>(job.q + row * job.cols + c0)[lane] = c;
+      if (job.q_t != nullptr) reinterpret_cast<uint2*>(&tile[4 * warp + i][0])[lane] = c;
+    }
+    const int64_t nb = job.cols >> 5;
+    if (warp == 0 && lane < 8 && c0 + 32 * lane < job.cols)
+      reinterpret_cast<uint8_t*>(job.scales)[rb * nb + (c0 >> 5) + lane] = static_cast<uint8_t>(ex[lane] + 127);
+    if (job.sf_tc != nullptr) {
+      const int64_t row = r0 + (threadIdx.x >> 3);
+      const int b = threadIdx.x & 7;
+      if (row < job.rows && c0 + 32 * b < job.cols)
+        job.sf_tc[sf_tc_offset(row, (c0 >> 5) + b, job.cols >> 7)] = static_cast<uint8_t>(ex[b] + 127);
+    }
+    if (job.q_t != nullptr) {
+      __syncthreads();
+      // thread: columns 4g..4g+3 of the unit, rows 8h..8h+7 of the strip
+      const int g = threadIdx.x & 63, h = threadIdx.x >> 6;
+      if (c0 + 4 * g < job.cols) {
+        uint32_t w[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) w[r] = *reinterpret_cast<const uint32_t*>(&tile[8 * h + r][4 * g]);
+        uint32_t col[2][4];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const uint32_t* q4 = w + 4 * half;
+          const uint32_t lo01 = __byte_perm(q4[0], q4[1], 0x5140), hi01 = __byte_perm(q4[0], q4[1], 0x7362);
+          const uint32_t lo23 = __byte_perm(q4[2], q4[3], 0x5140), hi23 = __byte_perm(q4[2], q4[3], 0x7362);
+          col[half][0] = __byte_perm(lo01, lo23, 0x5410);
+          col[half][1] = __byte_perm(lo01, lo23, 0x7632);
+          col[half][2] = __byte_perm(hi01, hi23, 0x5410);
+          col[half][3] = __byte_perm(hi01, hi23, 0x7632);
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          *reinterpret_cast<uint2*>(job.q_t + (c0 + 4 * g + c) * job.rows + r0 + 8 * h) =
+              make_uint2(col[0][c], col[1][c]);
+      }
+    }
+    __syncthreads();   // the next unit reuses red, ex and tile
   }
 }
 
@@ -210,13 +300,13 @@ cudaError_t launch_rows(const QuantJobs& jobs, int max_cols, int sms, cudaStream
 
 }  // namespace
 
-cudaError_t launch_sf_permute(const uint8_t* logical, uint8_t* tc, int64_t rows, int64_t cols, int sms,
+cudaError_t launch_sf_permute(const uint8_t* logical, uint8_t* tc, int64_t rows, int64_t cols, int row_div, int sms,
                               cudaStream_t stream) {
   const int64_t total = rows * (cols >> 5);
   if (total == 0) return cudaSuccess;
   int64_t blocks = (total + 255) / 256;
   if (blocks > static_cast<int64_t>(sms) * 4) blocks = static_cast<int64_t>(sms) * 4;
-  sf_permute_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(logical, tc, rows, cols);
+  sf_permute_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(logical, tc, rows, cols, row_div);
   return cudaGetLastError();
 }
 
@@ -230,6 +320,32 @@ cudaError_t launch_quantize(const QuantJobs& jobs, int mode, int sms, cudaStream
   }
   if (mode == kScaleRow) return launch_rows<kScaleRow>(jobs, max_cols, sms, stream);
   if (mode == kScaleMx32) return launch_rows<kScaleMx32>(jobs, max_cols, sms, stream);
+  if (mode == kScaleBlock32) {
+    // units of 32 rows x 256 columns, numbered across the jobs
+    QuantJobs u = jobs;
+    int64_t units = 0;
+    for (int i = 0; i < u.n; ++i) {
+      u.j[i].row_begin = units;
+      units += ((u.j[i].rows + 31) / 32) * ((u.j[i].cols + 255) / 256);
+    }
+    u.total_rows = units;
+    if (units == 0) return cudaSuccess;
+    static std::atomic<int> per_sm[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int occ = per_sm[dev & 63].load();
+    if (occ == 0) {
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, quant_block32_kernel, 256, 0);
+      if (e != cudaSuccess) return e;
+      if (occ < 1) occ = 1;
+      per_sm[dev & 63].store(occ);
+    }
+    int64_t blocks = units;
+    if (blocks > static_cast<int64_t>(sms) * occ) blocks = static_cast<int64_t>(sms) * occ;
+    quant_block32_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(u);
+    return cudaGetLastError();
+  }
   if (mode == kScaleTensor) {
     for (int i = 0; i < jobs.n; ++i) {
       cudaError_t e = cudaMemsetAsync(jobs.j[i].amax_slot, 0, sizeof(unsigned), stream);

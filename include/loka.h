@@ -58,6 +58,7 @@ typedef int32_t loka_status;
 #define LOKA_SCALE_ROW 1         /* one fp32 scale per row                 */
 #define LOKA_SCALE_MX32 2        /* one E8M0 scale per 1x32 block along K  */
 #define LOKA_BF16 3              /* no quantization: bf16 GEMM (fallback)  */
+#define LOKA_SCALE_BLOCK32 4     /* one E8M0 scale per 32x32 block          */
 
 /* Normalization applied to each output row (LoKA section III-B). */
 #define LOKA_NORM_NONE 0
@@ -106,9 +107,26 @@ loka_status loka_selftest_watchdog(uint64_t limit_ns, void* stream);
  * allowed then).  Asynchronous.
  * ---------------------------------------------------------------------- */
 size_t loka_quantize_fp8_workspace_size(int64_t rows, int64_t cols, int32_t mode);
+/* LOKA_SCALE_BLOCK32 (also taken by loka_quantize_fp8): square 32 x 32
+ * blocks, the [32, 32] block quantization of the GEM Training page ("Low
+ * Precision Flash Attention": one scale per 32x32 block makes quantization
+ * transpose-invariant, so a tensor is quantized once for the GEMMs that take
+ * it and its transpose).  Per block of rows 32i..32i+31 and cols
+ * 32j..32j+31: e = clamp(floor(log2 amax) - 8, -127, 127) (the MX rule),
+ * q = E4M3(x * 2^-e); scales is uint8 E8M0 [ceil(rows/32), cols/32] holding
+ * e + 127 (a ragged last block row covers the rows that exist).  The
+ * quantization of the transpose is the transpose of the codes and scales. */
 loka_status loka_quantize_fp8(const void* x, int64_t rows, int64_t cols, int32_t mode,
                               void* q, void* scales, void* workspace, size_t workspace_bytes,
                               void* stream);
+
+/* loka_quantize_fp8_block32 -- LOKA_SCALE_BLOCK32 codes and scales, and in
+ * the same pass, when q_t is not NULL, the codes of x transposed: q_t uint8
+ * [cols, rows] (device, 16-byte aligned; rows % 32 == 0), equal to the codes
+ * of quantizing x^T, whose scales are the transpose of scales.
+ * Asynchronous; no workspace. */
+loka_status loka_quantize_fp8_block32(const void* x, int64_t rows, int64_t cols, void* q, void* q_t,
+                                      void* scales, void* stream);
 
 /* ------------------------------------------------------------------------
  * loka_fp8_linear_norm -- Y = Norm(dequant(E4M3(X) E4M3(W)^T) + b), bf16.
@@ -127,6 +145,9 @@ loka_status loka_quantize_fp8(const void* x, int64_t rows, int64_t cols, int32_t
  *   x: bf16 [M,K] (x_is_fp8 = 0) or E4M3 [M,K] with x_scales as produced by
  *      loka_quantize_fp8 (x_is_fp8 = 1).  Same for w / w_scales / w_is_fp8.
  *   mode: LOKA_SCALE_* (LOKA_BF16 runs the bf16 GEMM; *_is_fp8 must be 0).
+ *   LOKA_SCALE_BLOCK32 runs the block-scaled MMA of MX with each row taking
+ *   its 32-row block's scales (caller-quantized operands: the scales of
+ *   loka_quantize_fp8 with that mode).
  *   bias, gamma, beta: bf16 [N] or NULL (0, 1, 0).  y: bf16 [M,N] (see y_q).
  *   eps: added to the variance (LayerNorm) or mean square (RMSNorm).
  * Accumulation is fp32 in tensor memory; the epilogue works in fp32.

@@ -9,6 +9,7 @@ GEMM on the same output row; RMSNorm and LayerNorm as named there):
   acc[m,n] = sum_k decode(qx[m,k]) * decode(qw[n,k])            (exact)
   v[m,n]   = acc[m,n] * sx[m] * sw[n] + b[n]                     (tensor/row)
   v[m,n]   = sum_k decode(qx)*2^ex[m,k/32] * decode(qw)*2^ew[n,k/32] + b[n] (MX)
+             (square 32x32 blocks: the exponents are ex[m/32,k/32], ew[n/32,k/32])
   v[m,n]   = sum_k x[m,k] * w[n,k] + b[n]                        (BF16 path)
   LayerNorm: y = (v - mean_n v) / sqrt(var_n v + eps) * gamma + beta
              (biased variance, 1/N)
@@ -33,7 +34,7 @@ import torch
 from .formats import bf16_round, e4m3_decode, e8m0_decode
 from .quantize import as_f32, quantize, MX_BLOCK
 
-SCALE_TENSOR, SCALE_ROW, SCALE_MX32, SCALE_BF16 = 0, 1, 2, 3
+SCALE_TENSOR, SCALE_ROW, SCALE_MX32, SCALE_BF16, SCALE_BLOCK32 = 0, 1, 2, 3, 4
 NORM_NONE, NORM_LAYER, NORM_RMS, NORM_BLOCK_RMS = 0, 1, 2, 3
 ACT_NONE, ACT_HARDSWISH = 0, 1
 
@@ -57,6 +58,9 @@ def dequantize(q: np.ndarray, scales, mode: int) -> np.ndarray:
     if mode == SCALE_MX32:
         f = e8m0_decode(scales)
         return vals * np.repeat(f, MX_BLOCK, axis=1)
+    if mode == SCALE_BLOCK32:
+        f = e8m0_decode(scales)
+        return vals * np.repeat(np.repeat(f, MX_BLOCK, axis=0)[:vals.shape[0]], MX_BLOCK, axis=1)
     raise ValueError(mode)
 
 
@@ -77,7 +81,7 @@ def prenorm(x, w, bias, mode: int):
         return v + b[None, :], {}
     qx, sx = quantize(x, mode)
     qw, sw = quantize(w, mode)
-    if mode == SCALE_MX32:
+    if mode in (SCALE_MX32, SCALE_BLOCK32):
         v = dequantize(qx, sx, mode) @ dequantize(qw, sw, mode).T
     else:
         acc = gemm_exact(qx, qw)
@@ -147,8 +151,8 @@ def linear_norm_inputs(inp, rows=None):
     """
     x = inp.x
     if rows is not None:
-        if inp.mode == SCALE_TENSOR:
-            raise ValueError("per-tensor scaling is not row-local")
+        if inp.mode in (SCALE_TENSOR, SCALE_BLOCK32):
+            raise ValueError("per-tensor and 32x32-block scaling are not row-local")
         x = inp.x[torch.as_tensor(rows, dtype=torch.long)]
     return linear_norm(x, inp.w, inp.bias, inp.gamma, inp.beta, inp.mode, inp.norm, inp.eps,
                        inp.norm_block, inp.act)
@@ -180,8 +184,8 @@ def linear_norm_quantized_inputs(inp, out_mode: int, rows=None):
     ``linear_norm_inputs``; row-local for every out_mode this takes)."""
     x = inp.x
     if rows is not None:
-        if inp.mode == SCALE_TENSOR:
-            raise ValueError("per-tensor scaling is not row-local")
+        if inp.mode in (SCALE_TENSOR, SCALE_BLOCK32):
+            raise ValueError("per-tensor and 32x32-block scaling are not row-local")
         x = inp.x[torch.as_tensor(rows, dtype=torch.long)]
     return linear_norm_quantized(x, inp.w, inp.bias, inp.gamma, inp.beta, inp.mode, inp.norm, inp.eps, out_mode,
                                  inp.norm_block, inp.act)

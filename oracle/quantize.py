@@ -99,12 +99,41 @@ def quantize_mx(x):
     return q, (e + 127).astype(np.uint8)
 
 
+def quantize_block32(x):
+    """Square 32 x 32 blocks: one E8M0 exponent per block of 32 rows by 32
+    columns (GEM Training page, "Low Precision Flash Attention": [32, 32]
+    block quantization, transpose-invariant, so a tensor and its transpose
+    share one quantization).  The exponent rule is the MX one above, on the
+    block's amax; a ragged last block row covers the rows that exist.
+
+    Returns (q uint8 [R,C], e8m0 uint8 [ceil(R/32), C/32]).  C must be a
+    multiple of 32.
+    """
+    xf = as_f32(x)
+    R, C = xf.shape
+    assert C % MX_BLOCK == 0
+    RB, CB = (R + MX_BLOCK - 1) // MX_BLOCK, C // MX_BLOCK
+    am = np.zeros((RB, CB), dtype=np.float32)
+    for rb in range(RB):
+        rows = xf[rb * MX_BLOCK:(rb + 1) * MX_BLOCK]
+        for cb in range(CB):
+            am[rb, cb] = amax(rows[:, cb * MX_BLOCK:(cb + 1) * MX_BLOCK].ravel(), axis=0)
+    e = mx_exponent(am)
+    e_full = np.repeat(np.repeat(e, MX_BLOCK, axis=0)[:R], MX_BLOCK, axis=1)
+    with np.errstate(invalid="ignore", over="ignore", under="ignore"):
+        y = np.ldexp(xf, (-e_full).astype(np.int32)).astype(np.float32)
+    return e4m3_encode(y), (e + 127).astype(np.uint8)
+
+
 def quantize(x, mode: int):
-    """Dispatch on the scaling mode id (0 tensor, 1 row, 2 MX 1x32)."""
+    """Dispatch on the scaling mode id (0 tensor, 1 row, 2 MX 1x32, 4 square
+    32x32 blocks)."""
     if mode == 0:
         return quantize_tensor(x)
     if mode == 1:
         return quantize_rows(x)
     if mode == 2:
         return quantize_mx(x)
+    if mode == 4:
+        return quantize_block32(x)
     raise ValueError(f"no FP8 quantization for mode {mode}")

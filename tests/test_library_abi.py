@@ -192,6 +192,15 @@ def test_quantize_rejects_bad_arguments_on_host(cpu_lib):
     assert _loka.loka_quantize_fp8_workspace_size(4, 64, 1) == 0
 
 
+def test_block32_quantizer_rejects_bad_arguments_on_host(cpu_lib):
+    f = cpu_lib.loka_quantize_fp8_block32
+    assert f(1 << 20, 48, 64, 1 << 20, 1 << 21, 1 << 22, None) == _loka.LOKA_ERR_INVALID_ARG   # q_t: rows % 32
+    assert f(1 << 20, 64, 48, 1 << 20, None, 1 << 22, None) == _loka.LOKA_ERR_INVALID_ARG      # cols % 32
+    assert f(1 << 20, 64, 64, (1 << 20) + 8, None, 1 << 22, None) == _loka.LOKA_ERR_INVALID_ARG  # q alignment
+    assert f(1 << 20, 64, 64, 1 << 20, (1 << 21) + 8, 1 << 22, None) == _loka.LOKA_ERR_INVALID_ARG
+    assert f(1 << 20, 0, 64, 1 << 20, None, 1 << 22, None) == _loka.LOKA_OK                    # empty
+
+
 def _c_table(rows):
     out = []
     for e in rows:

@@ -161,6 +161,65 @@ def test_mx_quantize_small_block_by_hand():
     assert F.e4m3_decode_code(int(q[0, 1])) == -1.25
 
 
+# ------------------------------------------------ square 32x32 block scales
+def test_block32_is_transpose_invariant():
+    # GEM "Low Precision Flash Attention": one scale per 32x32 block, so
+    # quantizing X^T gives the transposed codes and scales of X
+    x = W.random_bf16((96, 160), seed=12, dist="laplace", outlier_frac=0.02)
+    q, s = Q.quantize_block32(x)
+    qt, st = Q.quantize_block32(x.t().contiguous())
+    assert s.shape == (3, 5) and st.shape == (5, 3)
+    assert np.array_equal(q.T, qt) and np.array_equal(s.T, st)
+
+
+def test_block32_codes_by_brute_force_and_frexp():
+    x = W.random_bf16((70, 64), seed=13, outlier_frac=0.05)      # a ragged last block row
+    q, s = Q.quantize_block32(x)
+    xf = Q.as_f32(x).astype(np.float64)
+    assert s.shape == (3, 2)
+    for rb in range(3):
+        for cb in range(2):
+            blk = xf[rb * 32:(rb + 1) * 32, cb * 32:(cb + 1) * 32]
+            _, p = np.frexp(np.abs(blk).max())
+            e = p - 1 - 8
+            assert int(s[rb, cb]) == e + 127
+            prod = np.ldexp(blk, -e).astype(np.float32)
+            assert np.array_equal(q[rb * 32:(rb + 1) * 32, cb * 32:(cb + 1) * 32].ravel(),
+                                  _brute_force_encode(prod.ravel()))
+
+
+def test_block32_equals_mx_when_every_row_holds_the_block_amax():
+    # when each row of a 32x32 block reaches the block's amax, the per-row
+    # 1x32 (MX) exponents are the block's: the two quantizations coincide
+    rng = np.random.default_rng(14)
+    xf = rng.standard_normal((64, 96)).astype(np.float32)
+    for rb in range(2):
+        for cb in range(3):
+            a = np.float32(2.0 ** rng.integers(-6, 6) * 1.5)
+            xf[rb * 32:(rb + 1) * 32, cb * 32] = a
+            xf[rb * 32:(rb + 1) * 32, cb * 32 + 1:(cb + 1) * 32] = np.clip(
+                xf[rb * 32:(rb + 1) * 32, cb * 32 + 1:(cb + 1) * 32], -a, a)
+    x = torch.from_numpy(xf).to(torch.bfloat16)
+    qb, sb = Q.quantize_block32(x)
+    qm, sm = Q.quantize_mx(x)
+    assert np.array_equal(qb, qm)
+    assert np.array_equal(np.repeat(sb, 32, axis=0), sm)
+
+
+def test_block32_layer_dequantizes_with_block_row_scales():
+    # prenorm with square blocks equals the float64 product of the
+    # dequantized operands, each element scaled by its block's 2^e
+    inp = W.make_layer(70, 128, 64, mode=4, norm=L.NORM_NONE, seed=15)
+    v, ops = L.prenorm(inp.x, inp.w, None, 4)
+    qx, sx, qw, sw = ops.get("qx"), ops.get("sx"), ops.get("qw"), ops.get("sw")
+    if qx is None:
+        qx, sx = Q.quantize_block32(inp.x)
+        qw, sw = Q.quantize_block32(inp.w)
+    dx = F.e4m3_decode(qx) * np.ldexp(1.0, np.repeat(np.repeat(sx.astype(np.int64) - 127, 32, 0)[:70], 32, 1))
+    dw = F.e4m3_decode(qw) * np.ldexp(1.0, np.repeat(np.repeat(sw.astype(np.int64) - 127, 32, 0)[:64], 32, 1))
+    assert np.allclose(v, dx @ dw.T, rtol=1e-14, atol=1e-14)
+
+
 # ------------------------------------------------------- tensor / row scales
 def test_rowwise_amax_element_maps_to_448_and_error_bound():
     x = W.random_bf16((64, 256), seed=3, outlier_frac=0.02)
