@@ -44,7 +44,7 @@ def parse():
     ap.add_argument("--no-compare", action="store_true")
     ap.add_argument("--M", type=int, default=None, help="rows of X per layer (default: the workload's own)")
     ap.add_argument("--workload", default="rec_mlp",
-                    choices=["rec_mlp", "ensemble", "mxfp8", "single", "wide_blocknorm"])
+                    choices=["rec_mlp", "ensemble", "mxfp8", "single", "wide_blocknorm", "rec_mlp_block32"])
     return ap.parse_args()
 
 
@@ -173,7 +173,7 @@ def oracle_throughput(inp, budget_s: float, rows_per_call: int = 4096):
     rng = np.random.default_rng(123)
     done, t_total = 0, 0.0
     while True:   # at least one sample, then until the time budget is spent
-        start = int(rng.integers(0, max(1, M - rows_per_call)))
+        start = int(rng.integers(0, max(1, M - rows_per_call))) // 32 * 32   # whole 32-row blocks
         rows = np.arange(start, min(M, start + rows_per_call))
         t0 = time.perf_counter()
         OL.linear_norm_inputs(inp, rows=rows)
@@ -266,11 +266,13 @@ def workload_layers(name: str, rank: int, M):
         return [W.single(seed=rank)]
     if name == "wide_blocknorm":
         return [W.wide_blocknorm(seed=rank, **({"M": M} if M else {}))]
+    if name == "rec_mlp_block32":
+        return [W.rec_mlp(seed=rank, mode=W.SCALE_BLOCK32, **({"M": M} if M else {}))]
     raise ValueError(name)
 
 
 def scale_bytes(mode, rows, cols):
-    return {0: 4, 1: 4 * rows, 2: rows * cols // 32}.get(mode, 0)
+    return {0: 4, 1: 4 * rows, 2: rows * cols // 32, 4: (rows + 31) // 32 * (cols // 32)}.get(mode, 0)
 
 
 def run_ours(args, world, rank, local):
@@ -546,7 +548,8 @@ def run_ours(args, world, rank, local):
             "ensemble": "8-layer ensemble, per-row E4M3, RMSNorm, one grouped launch",
             "mxfp8": "Laplace X, MX 1x32 E8M0 block scaling, LayerNorm",
             "single": "per-tensor E4M3, LayerNorm",
-            "wide_blocknorm": "wide layer N(0,1)+1%x100 outliers, per-row E4M3, bias, BlockNorm 256, Hard Swish"}[
+            "wide_blocknorm": "wide layer N(0,1)+1%x100 outliers, per-row E4M3, bias, BlockNorm 256, Hard Swish",
+            "rec_mlp_block32": "rec-MLP X N(0,1)+1%x100 outliers, square 32x32-block E4M3/E8M0, bias, LayerNorm"}[
                 args.workload]
     metric = METRIC if args.workload == "rec_mlp" and not args.M else \
         f"FP8 linear+norm TFLOP/s ({args.workload} {len(layers)}x{l0.M}x{l0.K}x{l0.N}) on 1 GB300"

@@ -142,6 +142,20 @@ def linear_norm(x, w, bias, gamma, beta, mode: int, norm: int, eps: float, norm_
     return y, bf16_round(y), ops
 
 
+def _check_row_sample(mode: int, rows) -> None:
+    """A row sample computes the same rows as the whole layer when the
+    activation scales are row-local (per row, MX, bf16), or, for square 32x32
+    blocks, when the sample is made of whole aligned 32-row blocks."""
+    if mode == SCALE_TENSOR:
+        raise ValueError("per-tensor scaling is not row-local")
+    if mode == SCALE_BLOCK32:
+        r = np.asarray(rows).reshape(-1)
+        ok = r.size % 32 == 0 and all(r[i] % 32 == 0 and np.array_equal(r[i:i + 32], r[i] + np.arange(32))
+                                      for i in range(0, r.size, 32))
+        if not ok:
+            raise ValueError("a 32x32-block sample must be whole aligned 32-row blocks")
+
+
 def linear_norm_inputs(inp, rows=None):
     """Run ``linear_norm`` on a ``workloads.LayerInputs``.
 
@@ -151,8 +165,7 @@ def linear_norm_inputs(inp, rows=None):
     """
     x = inp.x
     if rows is not None:
-        if inp.mode in (SCALE_TENSOR, SCALE_BLOCK32):
-            raise ValueError("per-tensor and 32x32-block scaling are not row-local")
+        _check_row_sample(inp.mode, rows)
         x = inp.x[torch.as_tensor(rows, dtype=torch.long)]
     return linear_norm(x, inp.w, inp.bias, inp.gamma, inp.beta, inp.mode, inp.norm, inp.eps,
                        inp.norm_block, inp.act)
@@ -184,8 +197,7 @@ def linear_norm_quantized_inputs(inp, out_mode: int, rows=None):
     ``linear_norm_inputs``; row-local for every out_mode this takes)."""
     x = inp.x
     if rows is not None:
-        if inp.mode in (SCALE_TENSOR, SCALE_BLOCK32):
-            raise ValueError("per-tensor and 32x32-block scaling are not row-local")
+        _check_row_sample(inp.mode, rows)
         x = inp.x[torch.as_tensor(rows, dtype=torch.long)]
     return linear_norm_quantized(x, inp.w, inp.bias, inp.gamma, inp.beta, inp.mode, inp.norm, inp.eps, out_mode,
                                  inp.norm_block, inp.act)

@@ -34,7 +34,7 @@ import torch
 
 # Variant and normalization identifiers shared by tests and the bench.  These
 # are names, not arithmetic.
-SCALE_TENSOR, SCALE_ROW, SCALE_MX32, SCALE_BF16 = 0, 1, 2, 3
+SCALE_TENSOR, SCALE_ROW, SCALE_MX32, SCALE_BF16, SCALE_BLOCK32 = 0, 1, 2, 3, 4
 NORM_NONE, NORM_LAYER, NORM_RMS, NORM_BLOCK_RMS = 0, 1, 2, 3
 ACT_NONE, ACT_HARDSWISH = 0, 1
 EPS_LAYER = 1e-5
@@ -120,9 +120,10 @@ def single(seed: int = 0) -> LayerInputs:
     return make_layer(256, 128, 128, mode=SCALE_TENSOR, norm=NORM_LAYER, seed=seed)
 
 
-def rec_mlp(seed: int = 0, M: int = 65536, K: int = 512, N: int = 256) -> LayerInputs:
-    """Recommendation MLP layer with heavy-tailed outliers, per-row scaling."""
-    return make_layer(M, K, N, mode=SCALE_ROW, norm=NORM_LAYER, seed=seed,
+def rec_mlp(seed: int = 0, M: int = 65536, K: int = 512, N: int = 256, mode: int = SCALE_ROW) -> LayerInputs:
+    """Recommendation MLP layer with heavy-tailed outliers, per-row scaling
+    (or another scaling mode on the same draw)."""
+    return make_layer(M, K, N, mode=mode, norm=NORM_LAYER, seed=seed,
                       outlier_frac=0.01, bias_var=0.02)
 
 
