@@ -302,16 +302,21 @@ loka_status build_gemm(const loka_linear_desc* d, int n, const std::vector<Opera
     G.y = y;
     if (g.M == 0) continue;
     loka_status s;
+    // W's box: the columns one CTA owns under the launch's route
+    const int box = gemm_route(static_cast<int>(g.N), bf16_operands ? OperandKind::kBf16 : operand_kind(mode), out, norm,
+                               d[0].norm_block, out == OutKind::kQuant ? output_reference(d, n).y_q_mode : 0)
+                        .local;
+    G.b_box_rows = box;
     if (bf16_operands) {
       if ((s = encode_2d(&G.tm_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.x, g.K, g.M, 128)) != LOKA_OK) return s;
-      if ((s = encode_2d(&G.tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.w, g.K, g.N, g.N > 256 ? 256 : g.N)) != LOKA_OK) return s;
+      if ((s = encode_2d(&G.tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.w, g.K, g.N, box)) != LOKA_OK) return s;
     } else {
       const void* xq = g.x_is_fp8 ? g.x : ws + slots[i].xq;
       const void* wq = g.w_is_fp8 ? g.w : ws + slots[i].wq;
       const void* sx = g.x_is_fp8 ? g.x_scales : ws + slots[i].sx;
       const void* sw = g.w_is_fp8 ? g.w_scales : ws + slots[i].sw;
       if ((s = encode_2d(&G.tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xq, g.K, g.M, 128)) != LOKA_OK) return s;
-      if ((s = encode_2d(&G.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wq, g.K, g.N, g.N > 256 ? 256 : g.N)) != LOKA_OK) return s;
+      if ((s = encode_2d(&G.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wq, g.K, g.N, box)) != LOKA_OK) return s;
       if (mode == kScaleMx32 || mode == kScaleBlock32) {   // the block scales are applied inside the MMA
         G.sfa_tc = ws + slots[i].sx_tc;
         G.sfb_tc = ws + slots[i].sw_tc;

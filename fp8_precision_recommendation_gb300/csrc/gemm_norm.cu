@@ -11,15 +11,20 @@ bool gemm_supported(int N, int K, OperandKind op) {
   return plan_for(local, K, op == OperandKind::kBf16 ? 2 : 1, op == OperandKind::kMxE4M3, cl).stages > 0;
 }
 
-cudaError_t launch_gemm_norm(GemmParams& p, int N, OperandKind op, OutKind out, int sms, cudaStream_t stream) {
+GemmRoute gemm_route(int N, OperandKind, OutKind, int norm, int, int) {
+  const bool no_row_stat = norm == kNormNone || norm == kNormBlockRms;
   // Rows wider than one CTA whose epilogue needs no row statistic (no norm,
   // or BlockNorm, whose blocks lie within a CTA's 256 columns) run as
   // independent 256-column slices: no cluster co-scheduling, every SM busy.
-  p.slices = 1;
-  if (N > 256 && (p.norm == kNormNone || p.norm == kNormBlockRms)) {
-    p.slices = N / 256;
-    N = 256;
-  }
+  if (N > 256) return no_row_stat ? GemmRoute{256, 1, N / 256} : GemmRoute{256, N / 256, 1};
+  return GemmRoute{N, 1, 1};
+}
+
+cudaError_t launch_gemm_norm(GemmParams& p, int N, OperandKind op, OutKind out, int sms, cudaStream_t stream) {
+  const GemmRoute r = gemm_route(N, op, out, p.norm, p.norm_block, p.yq_mode);
+  p.slices = r.slices;
+  // the launchers take the row width: up to 256 one CTA, wider a cluster
+  N = r.cl > 1 ? N : r.local;
   if (out == OutKind::kQuant) {
     const bool wide = N > 256;
     if (op == OperandKind::kE4M3)

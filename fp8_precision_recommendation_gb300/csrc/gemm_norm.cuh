@@ -485,9 +485,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
       }
     };
     // v = acc * sx * sw + b for the pair: sw is the per-column weight scale
-    // (rowwise W; 1 otherwise, a per-tensor weight scale folds into sx)
-    auto vpair = [&](const uint32_t (&r)[16], int k, int i, float2 sx2, float2 sw, float2 b) {
-      return __ffma2_rn(__fmul2_rn(acc2(r, k, i), sx2), sw, b);
+    // (rowwise W; 1 otherwise, a per-tensor weight scale folds into sx).  MX
+    // and bf16 operands have no per-column scale (MX scales act inside the
+    // MMA): v = acc * sx + b, one instruction, there.
+    auto vpair = [&](const uint32_t (&r)[16], int k, int i, float2 sx2, [[maybe_unused]] float2 sw, float2 b) {
+      if constexpr (kMx || kBf16Op)
+        return __ffma2_rn(acc2(r, k, i), sx2, b);
+      else
+        return __ffma2_rn(__fmul2_rn(acc2(r, k, i), sx2), sw, b);
     };
     // one lane waits, the whole warp follows its verdict
     auto warp_wait = [&](uint32_t bar, uint32_t parity, bool cluster_scope) {
@@ -1105,6 +1110,9 @@ bool split_n(int N, int* local, int* cl) {
 // the columns one CTA owns).
 template <int OP, int OUT, int LN, int CL>
 cudaError_t launch_planned(GemmParams& p, int sms, cudaStream_t stream) {
+  // W's TMA box must be one CTA's columns: the kernel's B slots hold LN rows
+  for (int g = 0; g < p.num_groups; ++g)
+    if (p.g[g].M > 0 && p.g[g].b_box_rows != LN) return cudaErrorInvalidValue;
   const int eb = OP == static_cast<int>(OperandKind::kBf16) ? 2 : 1;
   const Plan pl = plan_for(LN, p.K, eb, OP == static_cast<int>(OperandKind::kMxE4M3), CL);
   if (pl.stages == 0) return cudaErrorInvalidValue;

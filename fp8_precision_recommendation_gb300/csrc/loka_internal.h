@@ -89,7 +89,7 @@ struct GemmGroup {
   int32_t tile_begin;    // first tile of this group in the launch's tile space
   int32_t sx_per_row;    // 1: sx has M entries, 0: one entry
   int32_t sw_per_row;
-  int32_t pad;
+  int32_t b_box_rows;    // rows of tm_b's box: the columns one CTA owns (checked before a launch)
 };
 
 struct GemmParams {
@@ -115,8 +115,17 @@ enum class OperandKind : int { kE4M3 = 0, kBf16 = 1, kMxE4M3 = 2 };
 // its pointer is set)
 enum class OutKind : int { kBf16 = 0, kF32 = 1, kQuant = 2 };
 
+// How an output row of N columns is split: `local` columns per CTA; `cl`
+// CTAs of a thread-block cluster per tile (row statistics exchanged), or
+// `slices` independent CTAs per tile (no statistic spans the row).
+struct GemmRoute {
+  int local, cl, slices;
+};
+GemmRoute gemm_route(int N, OperandKind op, OutKind out, int norm, int norm_block, int yq_mode);
+
 // Launches the persistent GEMM + epilogue kernel for N columns (fills in
-// p.stages).
+// p.stages and p.slices; tm_b must have been encoded with a box of
+// gemm_route(...).local rows, recorded in b_box_rows).
 cudaError_t launch_gemm_norm(GemmParams& p, int N, OperandKind op, OutKind out, int sms, cudaStream_t stream);
 
 // Whether the kernel has a shared-memory plan for this N, K and operand type.
