@@ -173,6 +173,47 @@ def quant_error(x, w, bias, mode: int, workspace: Optional[Workspace] = None, st
             "zero_ref_count": st.zero_ref_count, "count": st.count}
 
 
+class InputStats:
+    """LoKA Probe's running input statistics of one layer (count, fp64 mean
+    and scatter matrix on the device), updated batch by batch on the GPU."""
+
+    def __init__(self, K: int, device):
+        torch = _torch()
+        self.device = torch.device(device)
+        self.mu = torch.zeros(K, dtype=torch.float64, device=self.device)
+        self.scatter = torch.zeros((K, K), dtype=torch.float64, device=self.device)
+        self.c = _loka.InputStats()
+        self.c.n, self.c.K = 0, K
+        self.c.mu, self.c.scatter = self.mu.data_ptr(), self.scatter.data_ptr()
+
+    @property
+    def n(self) -> int:
+        return self.c.n
+
+    def update(self, x, workspace: Optional[Workspace] = None, stream=None) -> None:
+        """Merge the rows of x (bf16 CUDA [B, K])."""
+        B = x.shape[0]
+        need = _loka.loka_probe_stats_workspace_size(B, self.c.K)
+        ws, nbytes = (workspace or _ws(self.device)).get(need)
+        _loka.loka_probe_stats_update(self.c, x, B, ws, nbytes, stream)
+
+    def covariance(self):
+        """The unbiased covariance scatter / (n - 1) (a torch fp64 tensor)."""
+        return self.scatter / (self.n - 1)
+
+
+def sample_inputs(mu, chol, B: int, seed: int, workspace: Optional[Workspace] = None, stream=None):
+    """B synthetic input rows Z L^T + mu (bf16 CUDA [B, K]); mu bf16 [K], chol
+    the bf16 [K, K] lower Cholesky factor of the regularized covariance."""
+    torch = _torch()
+    K = mu.shape[0]
+    out = torch.empty((B, K), dtype=torch.bfloat16, device=mu.device)
+    need = _loka.loka_probe_sample_workspace_size(B, K)
+    ws, nbytes = (workspace or _ws(mu.device)).get(need)
+    _loka.loka_probe_sample_inputs(mu, chol, B, K, seed, out, ws, nbytes, stream)
+    return out
+
+
 def dispatch_select(table, M: int, N: int, K: int, norm: int, outlier_frac: float,
                     max_rel_err: float = 1e-2, max_mere: float = 0.2, min_speedup: float = -1.0) -> int:
     """table: iterable of (M, N, K, norm, outlier_frac, variant, time_us, rel_err, mere)."""

@@ -46,6 +46,10 @@ class DispatchEntry(ctypes.Structure):
                 ("rel_err", ctypes.c_double), ("mere", ctypes.c_double)]
 
 
+class InputStats(ctypes.Structure):
+    _fields_ = [("n", c_i64), ("K", c_i64), ("mu", c_p), ("scatter", c_p)]
+
+
 class Policy(ctypes.Structure):
     _fields_ = [("max_rel_err", ctypes.c_double), ("max_mere", ctypes.c_double), ("min_speedup", ctypes.c_double)]
 
@@ -59,6 +63,10 @@ SIGNATURES = {
     "loka_quantize_fp8_workspace_size": (c_sz, [c_i64, c_i64, c_i32]),
     "loka_quantize_fp8": (c_i32, [c_p, c_i64, c_i64, c_i32, c_p, c_p, c_p, c_sz, c_p]),
     "loka_quantize_fp8_block32": (c_i32, [c_p, c_i64, c_i64, c_p, c_p, c_p, c_p]),
+    "loka_probe_stats_workspace_size": (c_sz, [c_i64, c_i64]),
+    "loka_probe_stats_update": (c_i32, [ctypes.POINTER(InputStats), c_p, c_i64, c_p, c_sz, c_p]),
+    "loka_probe_sample_workspace_size": (c_sz, [c_i64, c_i64]),
+    "loka_probe_sample_inputs": (c_i32, [c_p, c_p, c_i64, c_i64, ctypes.c_uint64, c_p, c_p, c_sz, c_p]),
     "loka_fp8_linear_norm_workspace_size": (c_sz, [ctypes.POINTER(LinearDesc), c_i32]),
     "loka_fp8_linear_norm": (c_i32, [ctypes.POINTER(LinearDesc), c_i32, c_p, c_sz, c_p]),
     "loka_fp8_linear_norm_static": (c_i32, [ctypes.POINTER(LinearDesc), c_i32, c_p]),
@@ -143,6 +151,25 @@ def loka_quantize_fp8(x, rows: int, cols: int, mode: int, q, scales, workspace=N
 
 def loka_quantize_fp8_block32(x, rows: int, cols: int, q, q_t, scales, stream=None) -> None:
     check(load().loka_quantize_fp8_block32(_ptr(x), rows, cols, _ptr(q), _ptr(q_t), _ptr(scales), _stream(stream)))
+
+
+def loka_probe_stats_workspace_size(B: int, K: int) -> int:
+    return load().loka_probe_stats_workspace_size(B, K)
+
+
+def loka_probe_stats_update(stats: InputStats, x, B: int, workspace, workspace_bytes: int, stream=None) -> None:
+    check(load().loka_probe_stats_update(ctypes.byref(stats), _ptr(x), B, _ptr(workspace), workspace_bytes,
+                                         _stream(stream)))
+
+
+def loka_probe_sample_workspace_size(B: int, K: int) -> int:
+    return load().loka_probe_sample_workspace_size(B, K)
+
+
+def loka_probe_sample_inputs(mu, chol, B: int, K: int, seed: int, out, workspace, workspace_bytes: int,
+                             stream=None) -> None:
+    check(load().loka_probe_sample_inputs(_ptr(mu), _ptr(chol), B, K, seed, _ptr(out), _ptr(workspace),
+                                          workspace_bytes, _stream(stream)))
 
 
 def make_descs(descs: Sequence[LinearDesc]):

@@ -667,3 +667,139 @@ loka_status loka_dispatch_select(const loka_dispatch_entry* table, int64_t n, co
 }
 
 }  // extern "C"
+
+namespace {
+
+// Workspace of one statistics update: X^T in G split-K groups of Bg batch
+// rows (a multiple of 128, zero-padded), column sums per 128-row tile, the
+// fp64 column sums, and the G fp32 [K, K] GEMM partials.
+struct StatsLayout {
+  int G;
+  int64_t Bg, tiles;
+  size_t xt, colpart, colsum, partials, total;
+};
+
+StatsLayout stats_layout(int64_t B, int64_t K) {
+  StatsLayout L{};
+  const int64_t chunks = (B + 127) / 128;
+  L.G = static_cast<int>(chunks < kMaxGroups ? (chunks < 1 ? 1 : chunks) : kMaxGroups);
+  L.Bg = (chunks + L.G - 1) / L.G * 128;
+  L.tiles = L.G * L.Bg / 128;
+  size_t off = 0;
+  L.xt = off;
+  off = align_up(off + static_cast<size_t>(L.G) * K * L.Bg * 2);
+  L.colpart = off;
+  off = align_up(off + static_cast<size_t>(L.tiles) * K * sizeof(float));
+  L.colsum = off;
+  off = align_up(off + static_cast<size_t>(K) * sizeof(double));
+  L.partials = off;
+  off = align_up(off + static_cast<size_t>(L.G) * K * K * sizeof(float));
+  L.total = off;
+  return L;
+}
+
+bool probe_k_ok(int64_t K) { return K == 128 || K == 256 || K == 512 || K == 1024 || K == 2048; }
+
+}  // namespace
+
+extern "C" {
+
+size_t loka_probe_stats_workspace_size(int64_t B, int64_t K) {
+  if (B <= 0 || !probe_k_ok(K)) return 0;
+  return stats_layout(B, K).total;
+}
+
+loka_status loka_probe_stats_update(loka_input_stats* stats, const void* x, int64_t B, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  if (stats == nullptr) return fail(LOKA_ERR_INVALID_ARG, "stats is NULL");
+  const int64_t K = stats->K;
+  if (!probe_k_ok(K))
+    return fail(LOKA_ERR_UNSUPPORTED, "K = %lld: the probe statistics take K in {128, 256, 512, 1024, 2048}",
+                static_cast<long long>(K));
+  if (B < 0 || stats->n < 0) return fail(LOKA_ERR_INVALID_ARG, "negative row count");
+  if (B > (int64_t(1) << 24)) return fail(LOKA_ERR_UNSUPPORTED, "B = %lld: at most 2^24 rows per update",
+                                          static_cast<long long>(B));
+  if (B == 0) return LOKA_OK;
+  if (x == nullptr || stats->mu == nullptr || stats->scatter == nullptr)
+    return fail(LOKA_ERR_INVALID_ARG, "x, mu and scatter must not be NULL");
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(stats->mu) & 7u) || (reinterpret_cast<uintptr_t>(stats->scatter) & 7u))
+    return fail(LOKA_ERR_INVALID_ARG, "x must be 16-byte aligned, mu and scatter 8-byte aligned");
+  const StatsLayout L = stats_layout(B, K);
+  if (workspace == nullptr || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(LOKA_ERR_WORKSPACE, "workspace must be >= %zu bytes, 256-byte aligned", L.total);
+  DeviceInfo* dev = nullptr;
+  loka_status s = device_info(&dev);
+  if (s != LOKA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* colpart = reinterpret_cast<float*>(ws + L.colpart);
+  float* partials = reinterpret_cast<float*>(ws + L.partials);
+  cudaError_t e = launch_stats_transpose(x, B, K, L.Bg, L.G, ws + L.xt, colpart, st);
+  if (e != cudaSuccess) return cuda_fail(e, "statistics transpose launch");
+  // the batch's raw scatter, one fp32 [K, K] partial per group: the fused
+  // GEMM with bf16 operands X^T_g (as A and as W), no norm, fp32 output
+  loka_linear_desc d[kMaxGroups];
+  void* yo[kMaxGroups];
+  for (int g = 0; g < L.G; ++g) {
+    std::memset(&d[g], 0, sizeof(d[g]));
+    d[g].M = K;
+    d[g].N = K;
+    d[g].K = L.Bg;
+    d[g].mode = kBf16;
+    d[g].norm = kNormNone;
+    d[g].x = d[g].w = ws + L.xt + static_cast<size_t>(g) * K * L.Bg * 2;
+    yo[g] = partials + static_cast<size_t>(g) * K * K;
+    d[g].y = yo[g];
+  }
+  std::vector<OperandSlots> slots;
+  layout_operands(d, L.G, &slots);
+  static thread_local GemmParams p;
+  if ((s = build_gemm(d, L.G, slots, ws, true, OutKind::kF32, yo, kNormNone, dev, &p)) != LOKA_OK) return s;
+  e = launch_gemm_norm(p, static_cast<int>(K), OperandKind::kBf16, OutKind::kF32, dev->sms, st);
+  if (e != cudaSuccess) return cuda_fail(e, "statistics GEMM launch");
+  e = launch_stats_merge(colpart, L.tiles, partials, L.G, K, reinterpret_cast<double*>(ws + L.colsum), stats->mu,
+                         stats->scatter, stats->n, B, dev->sms, st);
+  if (e != cudaSuccess) return cuda_fail(e, "statistics merge launch");
+  stats->n += B;
+  return LOKA_OK;
+}
+
+size_t loka_probe_sample_workspace_size(int64_t B, int64_t K) {
+  if (B <= 0 || !probe_k_ok(K)) return 0;
+  return align_up(static_cast<size_t>(B) * K * 2);
+}
+
+loka_status loka_probe_sample_inputs(const void* mu, const void* chol, int64_t B, int64_t K, uint64_t seed, void* out,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+  if (!probe_k_ok(K))
+    return fail(LOKA_ERR_UNSUPPORTED, "K = %lld: the sampler takes K in {128, 256, 512, 1024, 2048}",
+                static_cast<long long>(K));
+  if (B < 0) return fail(LOKA_ERR_INVALID_ARG, "B = %lld < 0", static_cast<long long>(B));
+  if (B > (int64_t(1) << 31)) return fail(LOKA_ERR_UNSUPPORTED, "B too large");
+  if (B == 0) return LOKA_OK;
+  if (mu == nullptr || chol == nullptr || out == nullptr) return fail(LOKA_ERR_INVALID_ARG, "mu, chol and out must not be NULL");
+  if (!aligned16(chol) || !aligned16(out)) return fail(LOKA_ERR_INVALID_ARG, "chol and out must be 16-byte aligned");
+  const size_t need = loka_probe_sample_workspace_size(B, K);
+  if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(LOKA_ERR_WORKSPACE, "workspace must be >= %zu bytes, 256-byte aligned", need);
+  DeviceInfo* dev = nullptr;
+  loka_status s = device_info(&dev);
+  if (s != LOKA_OK) return s;
+  cudaError_t e = launch_normals(seed, B * K, workspace, dev->sms, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "normals launch");
+  // T' = Z L^T + mu: the bf16 GEMM with L as the weights and mu as the bias
+  loka_linear_desc d;
+  std::memset(&d, 0, sizeof(d));
+  d.M = B;
+  d.N = K;
+  d.K = K;
+  d.mode = kBf16;
+  d.norm = kNormNone;
+  d.x = workspace;
+  d.w = chol;
+  d.bias = mu;
+  d.y = out;
+  return loka_fp8_linear_norm(&d, 1, nullptr, 0, stream);
+}
+
+}  // extern "C"

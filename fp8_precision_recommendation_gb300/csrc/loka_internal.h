@@ -134,6 +134,17 @@ bool gemm_supported(int N, int K, OperandKind op);
 // Probe reduction: accumulates MERE / Frobenius / max statistics of out vs ref.
 cudaError_t launch_error_reduce(const float* out, const float* ref, int64_t n, double* acc, int sms, cudaStream_t stream);
 
+// Probe statistics (probe_stats.cu): X [B,K] -> X^T as G groups [K, Bg]
+// (zero-padded) plus per-128-row-tile column sums; then the ordered merge of
+// the GEMM partials (fp32 [G][K][K]) into mu and S (fp64, Chan update); and
+// the counter-based normals of the sampler (bf16).
+cudaError_t launch_stats_transpose(const void* x, int64_t B, int64_t K, int64_t Bg, int G, void* xt, float* colpart,
+                                   cudaStream_t stream);
+cudaError_t launch_stats_merge(const float* colpart, int64_t tiles, const float* partials, int G, int64_t K,
+                               double* colsum, double* mu, double* S, int64_t n_old, int64_t nb, int sms,
+                               cudaStream_t stream);
+cudaError_t launch_normals(uint64_t seed, int64_t count, void* z, int sms, cudaStream_t stream);
+
 // Watchdog self-test: waits on a barrier that nothing completes.
 cudaError_t launch_watchdog_selftest(unsigned* status, uint64_t limit_ns, cudaStream_t stream);
 

@@ -1,0 +1,182 @@
+// LoKA Probe: online learning of a layer's input distribution (running mean
+// and scatter matrix, merged batch by batch) and sampling of synthetic
+// inputs from it.
+//
+// Defined by "LoKA: Low-precision Kernel Applications for Recommendation
+// Models at Scale", section III-A 1 "Online Distribution Learning": the batch
+// dimension is independent, so a layer's activations are modeled per feature
+// by their mean and covariance, tracked with a batched Welford / Chan update
+// (accumulated in higher precision); synthetic inputs are
+// T' = 1 mu^T + Z L^T with Z ~ N(0, I) and L the Cholesky factor of the
+// regularized covariance.
+//
+// The batch scatter X^T X is a dense contraction over the batch and runs on
+// the tensor cores through the fused GEMM (bf16 operands, fp32 output, no
+// norm), split over the batch: the transpose kernel below writes X^T as G
+// groups [K, Bg] (batch rows zero-padded to a multiple of 128, which adds
+// nothing to the sums), the grouped GEMM makes one fp32 [K, K] partial per
+// group, and the merge kernel adds the partials in group order in fp64,
+// centres them with the column sums and applies the Chan update.
+#include "loka_internal.h"
+#include "ptx.cuh"
+
+namespace loka {
+
+namespace {
+
+constexpr int kTRows = 128;   // batch rows per transpose tile
+constexpr int kTCols = 64;    // features per transpose tile
+
+// X [B, K] bf16 -> Xt [G][K][Bg] bf16 (rows b >= B are zero) and per-tile
+// column sums colpart[tile][K] (fp32, the tile's 128 rows).  One 256-thread
+// block per (128-row tile, 64-feature tile).
+__global__ void __launch_bounds__(256) stats_transpose_kernel(const uint16_t* __restrict__ x, int64_t B, int64_t K,
+                                                              int64_t Bg, uint16_t* __restrict__ xt,
+                                                              float* __restrict__ colpart) {
+  __shared__ uint16_t tile[kTRows][kTCols + 2];
+  __shared__ float part[4][kTCols];
+  const int64_t rt = blockIdx.x, ct = blockIdx.y;
+  const int64_t b0 = rt * kTRows, c0 = ct * kTCols;
+  const int t = threadIdx.x;
+  // coalesced load: 8 threads per row (16 bytes each), 32 rows per pass
+  for (int pass = 0; pass < kTRows / 32; ++pass) {
+    const int r = pass * 32 + (t >> 3), q = t & 7;
+    const int64_t b = b0 + r;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (b < B) v = *reinterpret_cast<const uint4*>(x + b * K + c0 + q * 8);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      tile[r][q * 8 + 2 * e] = static_cast<uint16_t>(w[e] & 0xFFFFu);
+      tile[r][q * 8 + 2 * e + 1] = static_cast<uint16_t>(w[e] >> 16);
+    }
+  }
+  __syncthreads();
+  // column sums: feature c = t % 64 over rows 32h .. 32h + 31, then the 4 parts
+  {
+    const int c = t & 63, h = t >> 6;
+    float s = 0.0f;
+    for (int r = 0; r < 32; ++r) s += __uint_as_float(static_cast<uint32_t>(tile[h * 32 + r][c]) << 16);
+    part[h][c] = s;
+  }
+  // transposed store: feature row c0 + c of group g gets the tile's 128
+  // batch rows, 16 bytes (8 rows) per thread, 16 threads per feature row
+  const int64_t g = b0 / Bg, lb0 = b0 - g * Bg;
+  for (int pass = 0; pass < kTCols / 16; ++pass) {
+    const int c = pass * 16 + (t >> 4), r8 = t & 15;
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      w[e] = static_cast<uint32_t>(tile[r8 * 8 + 2 * e][c]) | (static_cast<uint32_t>(tile[r8 * 8 + 2 * e + 1][c]) << 16);
+    *reinterpret_cast<uint4*>(xt + (g * K + c0 + c) * Bg + lb0 + r8 * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  __syncthreads();
+  if (t < kTCols) colpart[rt * K + c0 + t] = part[0][t] + part[1][t] + part[2][t] + part[3][t];
+}
+
+// colsum[k] = sum over tiles of colpart[tile][k], in tile order (fp64).
+__global__ void __launch_bounds__(256) stats_colsum_kernel(const float* __restrict__ colpart, int64_t tiles, int64_t K,
+                                                           double* __restrict__ colsum) {
+  const int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (k >= K) return;
+  double s = 0.0;
+  for (int64_t t = 0; t < tiles; ++t) s += static_cast<double>(colpart[t * K + k]);
+  colsum[k] = s;
+}
+
+// Chan update of the scatter matrix: S += S_b + (n_old B / n_new) d d^T with
+// S_b = sum_g Y_g - s s^T / B (raw moments centred; s = column sums) and
+// d = s / B - mu_old.  Reads mu_old only (the mean is updated afterwards).
+__global__ void __launch_bounds__(256) stats_merge_kernel(const float* __restrict__ partials, int G, int64_t K,
+                                                          const double* __restrict__ colsum, const double* __restrict__ mu,
+                                                          double* __restrict__ S, double n_old, double nb) {
+  const int64_t kk = K * K;
+  const double n_new = n_old + nb;
+  const double w = n_old * nb / n_new;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < kk;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t i = e / K, j = e - i * K;
+    double raw = 0.0;
+    for (int g = 0; g < G; ++g) raw += static_cast<double>(partials[g * kk + e]);
+    const double si = colsum[i], sj = colsum[j];
+    const double sb = raw - si * sj / nb;
+    const double di = si / nb - mu[i], dj = sj / nb - mu[j];
+    S[e] += sb + w * di * dj;
+  }
+}
+
+// mu += (B / n_new) (s / B - mu)
+__global__ void __launch_bounds__(256) stats_mean_kernel(const double* __restrict__ colsum, double* __restrict__ mu,
+                                                         int64_t K, double n_old, double nb) {
+  const int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (k >= K) return;
+  const double d = colsum[k] / nb - mu[k];
+  mu[k] += nb / (n_old + nb) * d;
+}
+
+// SplitMix64 output for state `s` (the output function of SplittableRandom).
+__device__ __forceinline__ uint64_t splitmix64(uint64_t s) {
+  uint64_t z = s;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+// Z [count] bf16: normal pair j from random numbers 2j and 2j + 1 of the
+// seed's counter-based stream (state seed + (i + 1) * golden gamma), by
+// Box-Muller on 24-bit uniforms, in fp32.
+__global__ void __launch_bounds__(256) normals_kernel(uint64_t seed, int64_t pairs, uint32_t* __restrict__ z) {
+  constexpr uint64_t kGamma = 0x9E3779B97F4A7C15ull;
+  for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < pairs;
+       j += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint64_t i0 = static_cast<uint64_t>(2 * j);
+    const uint64_t r1 = splitmix64(seed + (i0 + 1) * kGamma);
+    const uint64_t r2 = splitmix64(seed + (i0 + 2) * kGamma);
+    const float u1 = static_cast<float>((r1 >> 40) + 1) * 0x1p-24f;   // (0, 1], exact
+    const float u2 = static_cast<float>(r2 >> 40) * 0x1p-24f;         // [0, 1), exact
+    const float rad = sqrtf(-2.0f * logf(u1));
+    float s, c;
+    sincospif(2.0f * u2, &s, &c);
+    z[j] = pack_bf16x2(rad * c, rad * s);
+  }
+}
+
+int grid_for(int64_t n, int sms) {
+  int64_t b = (n + 255) / 256;
+  if (b > static_cast<int64_t>(sms) * 8) b = static_cast<int64_t>(sms) * 8;
+  return static_cast<int>(b < 1 ? 1 : b);
+}
+
+}  // namespace
+
+cudaError_t launch_stats_transpose(const void* x, int64_t B, int64_t K, int64_t Bg, int G, void* xt, float* colpart,
+                                   cudaStream_t stream) {
+  const int64_t tiles = static_cast<int64_t>(G) * Bg / kTRows;
+  const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(K / kTCols));
+  stats_transpose_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(x), B, K, Bg,
+                                                    static_cast<uint16_t*>(xt), colpart);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_stats_merge(const float* colpart, int64_t tiles, const float* partials, int G, int64_t K,
+                               double* colsum, double* mu, double* S, int64_t n_old, int64_t nb, int sms,
+                               cudaStream_t stream) {
+  stats_colsum_kernel<<<static_cast<unsigned>((K + 255) / 256), 256, 0, stream>>>(colpart, tiles, K, colsum);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  stats_merge_kernel<<<grid_for(K * K, sms), 256, 0, stream>>>(partials, G, K, colsum, mu, S,
+                                                               static_cast<double>(n_old), static_cast<double>(nb));
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  stats_mean_kernel<<<static_cast<unsigned>((K + 255) / 256), 256, 0, stream>>>(colsum, mu, K,
+                                                                               static_cast<double>(n_old),
+                                                                               static_cast<double>(nb));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_normals(uint64_t seed, int64_t count, void* z, int sms, cudaStream_t stream) {
+  const int64_t pairs = count / 2;
+  normals_kernel<<<grid_for(pairs, sms), 256, 0, stream>>>(seed, pairs, static_cast<uint32_t*>(z));
+  return cudaGetLastError();
+}
+
+}  // namespace loka

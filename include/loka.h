@@ -298,6 +298,49 @@ typedef struct loka_policy {
 loka_status loka_dispatch_select(const loka_dispatch_entry* table, int64_t n, const loka_problem* p,
                                  const loka_policy* policy, int32_t* choice);
 
+/* ------------------------------------------------------------------------
+ * LoKA Probe: online learning of a layer's input distribution, and sampling.
+ *
+ * Defined by LoKA section III-A 1 "Online Distribution Learning": the batch
+ * dimension is independent, so a layer's inputs are modeled per feature by
+ * a mean and a covariance, tracked with a batched Welford / Chan update in
+ * higher precision; synthetic inputs are T' = 1 mu^T + Z L^T with
+ * Z ~ N(0, I) and L L^T = Sigma + eps I.
+ *
+ * loka_probe_stats_update merges a batch x (bf16 [B, K], device, 16-byte
+ * aligned) into *stats: with the batch mean mu_b and scatter
+ * S_b = (x - mu_b)^T (x - mu_b), n += B, mu += (B / n_new)(mu_b - mu),
+ * scatter += S_b + (n_old B / n_new) d d^T, d = mu_b - mu_old.  mu (fp64 [K])
+ * and scatter (fp64 [K, K], the unnormalized scatter matrix; the unbiased
+ * covariance is scatter / (n - 1)) are caller-owned device arrays; n is
+ * advanced on the host when the call is queued.  x^T x runs on the tensor
+ * cores in fp32 over split-K groups of up to 4096 rows, summed and centred
+ * in fp64 (raw moments: exact enough when |mean| is not far above the
+ * standard deviation, as for normalized activations).  K is 128, 256, 512,
+ * 1024 or 2048; B <= 2^24.  workspace: loka_probe_stats_workspace_size()
+ * bytes, 256-byte aligned.  Asynchronous.
+ *
+ * loka_probe_sample_inputs writes out (bf16 [B, K]) = Z L^T + mu, Z the
+ * counter-based normals of `seed` (SplitMix64 random number i from state
+ * seed + (i + 1) * 0x9E3779B97F4A7C15; Box-Muller on 24-bit uniforms in
+ * fp32; Z[b, k] is normal b K + k), mu bf16 [K], chol = L bf16 [K, K]
+ * row-major (the caller's Cholesky factor of the regularized covariance).
+ * workspace: loka_probe_sample_workspace_size() bytes.  Asynchronous.
+ * ---------------------------------------------------------------------- */
+typedef struct loka_input_stats {
+  int64_t n;             /* rows merged so far (host) */
+  int64_t K;             /* features */
+  double* mu;            /* device fp64 [K] */
+  double* scatter;       /* device fp64 [K, K] */
+} loka_input_stats;
+
+size_t loka_probe_stats_workspace_size(int64_t B, int64_t K);
+loka_status loka_probe_stats_update(loka_input_stats* stats, const void* x, int64_t B, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+size_t loka_probe_sample_workspace_size(int64_t B, int64_t K);
+loka_status loka_probe_sample_inputs(const void* mu, const void* chol, int64_t B, int64_t K, uint64_t seed,
+                                     void* out, void* workspace, size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

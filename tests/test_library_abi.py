@@ -49,7 +49,7 @@ def test_struct_layouts_match_header(tmp_path):
     # header against the ctypes binding
     structs = {"loka_linear_desc": _loka.LinearDesc, "loka_error_stats": _loka.ErrorStats,
                "loka_problem": _loka.Problem, "loka_dispatch_entry": _loka.DispatchEntry,
-               "loka_policy": _loka.Policy}
+               "loka_policy": _loka.Policy, "loka_input_stats": _loka.InputStats}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "loka.h"', "int main(void) {"]
     for cname, cls in structs.items():
         lines.append(f'  printf("{cname} size %zu\\n", sizeof({cname}));')
@@ -199,6 +199,23 @@ def test_block32_quantizer_rejects_bad_arguments_on_host(cpu_lib):
     assert f(1 << 20, 64, 64, (1 << 20) + 8, None, 1 << 22, None) == _loka.LOKA_ERR_INVALID_ARG  # q alignment
     assert f(1 << 20, 64, 64, 1 << 20, (1 << 21) + 8, 1 << 22, None) == _loka.LOKA_ERR_INVALID_ARG
     assert f(1 << 20, 0, 64, 1 << 20, None, 1 << 22, None) == _loka.LOKA_OK                    # empty
+
+
+def test_probe_statistics_reject_bad_arguments_on_host(cpu_lib):
+    st = _loka.InputStats()
+    st.n, st.K, st.mu, st.scatter = 0, 64, 1 << 20, 1 << 21
+    upd = cpu_lib.loka_probe_stats_update
+    assert upd(ctypes.byref(st), 1 << 22, 1000, None, 0, None) == _loka.LOKA_ERR_UNSUPPORTED     # K = 64
+    st.K = 512
+    assert upd(None, 1 << 22, 1000, None, 0, None) == _loka.LOKA_ERR_INVALID_ARG
+    assert upd(ctypes.byref(st), (1 << 22) + 8, 1000, None, 0, None) == _loka.LOKA_ERR_INVALID_ARG   # x alignment
+    assert upd(ctypes.byref(st), 1 << 22, 1000, None, 0, None) == _loka.LOKA_ERR_WORKSPACE
+    assert upd(ctypes.byref(st), 1 << 22, 0, None, 0, None) == _loka.LOKA_OK and st.n == 0     # empty batch
+    # workspace: X^T in split-K groups (zero-padded to 128 rows) + sums + partials
+    assert _loka.loka_probe_stats_workspace_size(65536, 512) >= 65536 * 512 * 2 + 16 * 512 * 512 * 4
+    smp = cpu_lib.loka_probe_sample_inputs
+    assert smp(1 << 20, 1 << 21, 100, 96, 1, 1 << 22, None, 0, None) == _loka.LOKA_ERR_UNSUPPORTED
+    assert smp(1 << 20, 1 << 21, 100, 256, 1, 1 << 22, None, 0, None) == _loka.LOKA_ERR_WORKSPACE
 
 
 def _c_table(rows):

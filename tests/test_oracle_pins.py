@@ -370,6 +370,69 @@ def test_linear_norm_end_to_end_vs_library_composition():
 
 
 # ------------------------------------------------------------- bf16 rounding
+# ------------------------------------- probe: online input statistics, sampler
+from oracle import probe_stats as PS
+
+
+def test_chan_merge_equals_two_pass_statistics_of_all_rows():
+    # merging batches of any sizes gives the mean and scatter of the
+    # concatenated rows, computed directly in two passes (closed form)
+    rng = np.random.default_rng(20)
+    K = 24
+    batches = [rng.standard_normal((b, K)) * rng.uniform(0.5, 3.0, K) + rng.uniform(-2, 2, K)
+               for b in (7, 1, 64, 129, 3)]
+    n, mu, S = 0, np.zeros(K), np.zeros((K, K))
+    for xb in batches:
+        n, mu, S = PS.stats_update(n, mu, S, xb)
+    allx = np.concatenate(batches)
+    m = allx.mean(axis=0)
+    assert n == allx.shape[0]
+    assert np.allclose(mu, m, rtol=0, atol=1e-13)
+    assert np.allclose(S, (allx - m).T @ (allx - m), rtol=1e-12, atol=1e-11)
+    # the unbiased covariance is numpy's (a library routine)
+    assert np.allclose(PS.covariance(n, S), np.cov(allx, rowvar=False), rtol=1e-12, atol=1e-12)
+
+
+def test_chan_merge_first_batch_and_empty_batch():
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((10, 5))
+    n, mu, S = PS.stats_update(0, np.zeros(5), np.zeros((5, 5)), x)
+    assert n == 10 and np.allclose(mu, x.mean(0)) and np.allclose(S, (x - x.mean(0)).T @ (x - x.mean(0)))
+    n2, mu2, S2 = PS.stats_update(n, mu, S, np.zeros((0, 5)))
+    assert n2 == n and np.array_equal(mu2, mu) and np.array_equal(S2, S)
+
+
+def test_stream_normals_have_normal_moments_and_uniform_bits():
+    # invariants of the generator: the 24-bit uniforms are uniform (chi-square
+    # over 64 bins) and the Box-Muller pairs have N(0,1) moments
+    r = PS.splitmix64(7, np.arange(1 << 18, dtype=np.uint64))
+    bins = np.bincount((r >> np.uint64(58)).astype(np.int64), minlength=64)
+    chi2 = ((bins - bins.mean()) ** 2 / bins.mean()).sum()
+    assert chi2 < 63 + 5 * np.sqrt(2 * 63)
+    z = PS.normals(7, 1 << 18)
+    n = z.size
+    assert abs(z.mean()) < 4 / np.sqrt(n)
+    assert abs(z.var() - 1) < 4 * np.sqrt(2 / n)
+    assert abs((z ** 4).mean() - 3) < 4 * np.sqrt(96 / n)
+    assert abs(np.corrcoef(z[0::2], z[1::2])[0, 1]) < 4 / np.sqrt(n / 2)
+    # different seeds give different streams; a seed's stream is reproducible
+    assert not np.array_equal(PS.normals(8, 64), PS.normals(7, 64))
+    assert np.array_equal(PS.normals(7, 64), z[:64])
+
+
+def test_sampler_reproduces_mean_and_covariance():
+    rng = np.random.default_rng(22)
+    K = 16
+    A = rng.standard_normal((K, K))
+    sigma = A @ A.T / K + 0.1 * np.eye(K)
+    L = np.linalg.cholesky(sigma)
+    mu = rng.uniform(-1, 1, K)
+    Z, T = PS.sample_inputs(mu, L, 40000, seed=3)
+    assert np.allclose(T - mu, Z @ L.T)
+    assert np.allclose(T.mean(0), mu, atol=5 * np.sqrt(np.diag(sigma).max() / 40000))
+    assert np.allclose(np.cov(T, rowvar=False), sigma, atol=0.05 * np.abs(sigma).max())
+
+
 # ------------------------------------------------- BlockNorm and Hard Swish
 @pytest.mark.parametrize("block", [32, 64, 128, 256])
 def test_blocknorm_is_rms_norm_of_the_blocked_view(block):
