@@ -690,8 +690,8 @@ StatsLayout stats_layout(int64_t B, int64_t K) {
   off = align_up(off + static_cast<size_t>(L.G) * K * L.Bg * 2);
   L.colpart = off;
   off = align_up(off + static_cast<size_t>(L.tiles) * K * sizeof(float));
-  L.colsum = off;
-  off = align_up(off + static_cast<size_t>(K) * sizeof(double));
+  L.colsum = off;   // column-sum chunks and per-column terms: (32 + 3) x K fp64
+  off = align_up(off + static_cast<size_t>(35) * K * sizeof(double));
   L.partials = off;
   off = align_up(off + static_cast<size_t>(L.G) * K * K * sizeof(float));
   L.total = off;

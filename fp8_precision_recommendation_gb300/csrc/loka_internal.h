@@ -141,8 +141,8 @@ cudaError_t launch_error_reduce(const float* out, const float* ref, int64_t n, d
 cudaError_t launch_stats_transpose(const void* x, int64_t B, int64_t K, int64_t Bg, int G, void* xt, float* colpart,
                                    cudaStream_t stream);
 cudaError_t launch_stats_merge(const float* colpart, int64_t tiles, const float* partials, int G, int64_t K,
-                               double* colsum, double* mu, double* S, int64_t n_old, int64_t nb, int sms,
-                               cudaStream_t stream);
+                               double* colwork /* 35 K fp64 */, double* mu, double* S, int64_t n_old, int64_t nb,
+                               int sms, cudaStream_t stream);
 cudaError_t launch_normals(uint64_t seed, int64_t count, void* z, int sms, cudaStream_t stream);
 
 // Watchdog self-test: waits on a barrier that nothing completes.

@@ -74,44 +74,76 @@ __global__ void __launch_bounds__(256) stats_transpose_kernel(const uint16_t* __
   if (t < kTCols) colpart[rt * K + c0 + t] = part[0][t] + part[1][t] + part[2][t] + part[3][t];
 }
 
-// colsum[k] = sum over tiles of colpart[tile][k], in tile order (fp64).
-__global__ void __launch_bounds__(256) stats_colsum_kernel(const float* __restrict__ colpart, int64_t tiles, int64_t K,
-                                                           double* __restrict__ colsum) {
-  const int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (k >= K) return;
-  double s = 0.0;
-  for (int64_t t = 0; t < tiles; ++t) s += static_cast<double>(colpart[t * K + k]);
-  colsum[k] = s;
-}
+constexpr int kSumChunks = 32;   // tile chunks of the first column-sum stage
 
-// Chan update of the scatter matrix: S += S_b + (n_old B / n_new) d d^T with
-// S_b = sum_g Y_g - s s^T / B (raw moments centred; s = column sums) and
-// d = s / B - mu_old.  Reads mu_old only (the mean is updated afterwards).
-__global__ void __launch_bounds__(256) stats_merge_kernel(const float* __restrict__ partials, int G, int64_t K,
-                                                          const double* __restrict__ colsum, const double* __restrict__ mu,
-                                                          double* __restrict__ S, double n_old, double nb) {
-  const int64_t kk = K * K;
-  const double n_new = n_old + nb;
-  const double w = n_old * nb / n_new;
-  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < kk;
-       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t i = e / K, j = e - i * K;
-    double raw = 0.0;
-    for (int g = 0; g < G; ++g) raw += static_cast<double>(partials[g * kk + e]);
-    const double si = colsum[i], sj = colsum[j];
-    const double sb = raw - si * sj / nb;
-    const double di = si / nb - mu[i], dj = sj / nb - mu[j];
-    S[e] += sb + w * di * dj;
+// Column sums, stage 1: part[chunk][k] = sum of colpart[tile][k] over the
+// chunk's tiles (fp64, in tile order).  Block (column block of 32, chunk);
+// warp w takes tiles w, w + 8, ... of the chunk, then the 8 warp sums are
+// added in warp order.
+__global__ void __launch_bounds__(256) stats_colsum_kernel(const float* __restrict__ colpart, int64_t tiles, int64_t K,
+                                                           double* __restrict__ part) {
+  __shared__ double wsum[8][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t k = static_cast<int64_t>(blockIdx.x) * 32 + lane;
+  const int64_t per = (tiles + kSumChunks - 1) / kSumChunks;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.y) * per;
+  const int64_t t1 = t0 + per < tiles ? t0 + per : tiles;
+  double s = 0.0;
+  for (int64_t t = t0 + warp; t < t1; t += 8) s += static_cast<double>(colpart[t * K + k]);
+  wsum[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0) {
+    double a = wsum[0][lane];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) a += wsum[w][lane];
+    part[blockIdx.y * K + k] = a;
   }
 }
 
-// mu += (B / n_new) (s / B - mu)
-__global__ void __launch_bounds__(256) stats_mean_kernel(const double* __restrict__ colsum, double* __restrict__ mu,
-                                                         int64_t K, double n_old, double nb) {
+// Column sums, stage 2, and the per-column terms of the update: s = sum of
+// the chunks in order, m = s / B (the batch mean), d = m - mu_old.
+__global__ void __launch_bounds__(256) stats_colprep_kernel(const double* __restrict__ part, int64_t K,
+                                                            const double* __restrict__ mu, double nb,
+                                                            double* __restrict__ col) {
   const int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (k >= K) return;
-  const double d = colsum[k] / nb - mu[k];
-  mu[k] += nb / (n_old + nb) * d;
+  double s = 0.0;
+  for (int c = 0; c < kSumChunks; ++c) s += part[c * K + k];
+  const double m = s / nb;
+  col[k] = s;
+  col[K + k] = m;
+  col[2 * K + k] = m - mu[k];
+}
+
+// Chan update of the scatter matrix: S += S_b + (n_old B / n_new) d d^T with
+// S_b = sum_g Y_g - s m^T (raw moments centred; s = column sums, m = s / B).
+__global__ void __launch_bounds__(256) stats_merge_kernel(const float* __restrict__ partials, int G, int64_t K,
+                                                          const double* __restrict__ col, double* __restrict__ S,
+                                                          double w) {
+  const int64_t kk = K * K;
+  const double* s = col;
+  const double* m = col + K;
+  const double* d = col + 2 * K;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < kk;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t i = e / K, j = e - i * K;
+    // the G (<= 16) partials, loaded together, added in group order
+    float v[kMaxGroups];
+#pragma unroll
+    for (int g = 0; g < kMaxGroups; ++g) v[g] = g < G ? partials[g * kk + e] : 0.0f;
+    double raw = 0.0;
+#pragma unroll
+    for (int g = 0; g < kMaxGroups; ++g) raw += static_cast<double>(v[g]);
+    S[e] += (raw - s[i] * m[j]) + w * d[i] * d[j];
+  }
+}
+
+// mu += (B / n_new) d
+__global__ void __launch_bounds__(256) stats_mean_kernel(const double* __restrict__ col, double* __restrict__ mu,
+                                                         int64_t K, double f) {
+  const int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (k >= K) return;
+  mu[k] += f * col[2 * K + k];
 }
 
 // SplitMix64 output for state `s` (the output function of SplittableRandom).
@@ -159,17 +191,19 @@ cudaError_t launch_stats_transpose(const void* x, int64_t B, int64_t K, int64_t 
 }
 
 cudaError_t launch_stats_merge(const float* colpart, int64_t tiles, const float* partials, int G, int64_t K,
-                               double* colsum, double* mu, double* S, int64_t n_old, int64_t nb, int sms,
+                               double* colwork, double* mu, double* S, int64_t n_old, int64_t nb, int sms,
                                cudaStream_t stream) {
-  stats_colsum_kernel<<<static_cast<unsigned>((K + 255) / 256), 256, 0, stream>>>(colpart, tiles, K, colsum);
+  double* part = colwork;                        // [kSumChunks][K]
+  double* col = colwork + kSumChunks * K;        // s, m, d: [3][K]
+  const double dn = static_cast<double>(n_old), db = static_cast<double>(nb);
+  stats_colsum_kernel<<<dim3(static_cast<unsigned>(K / 32), kSumChunks), 256, 0, stream>>>(colpart, tiles, K, part);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  stats_merge_kernel<<<grid_for(K * K, sms), 256, 0, stream>>>(partials, G, K, colsum, mu, S,
-                                                               static_cast<double>(n_old), static_cast<double>(nb));
+  stats_colprep_kernel<<<static_cast<unsigned>((K + 255) / 256), 256, 0, stream>>>(part, K, mu, db, col);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  stats_mean_kernel<<<static_cast<unsigned>((K + 255) / 256), 256, 0, stream>>>(colsum, mu, K,
-                                                                               static_cast<double>(n_old),
-                                                                               static_cast<double>(nb));
+  stats_merge_kernel<<<grid_for(K * K, sms), 256, 0, stream>>>(partials, G, K, col, S, dn * db / (dn + db));
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  stats_mean_kernel<<<static_cast<unsigned>((K + 255) / 256), 256, 0, stream>>>(col, mu, K, db / (dn + db));
   return cudaGetLastError();
 }
 
