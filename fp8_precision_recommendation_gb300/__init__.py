@@ -201,6 +201,17 @@ class InputStats:
         """The unbiased covariance scatter / (n - 1) (a torch fp64 tensor)."""
         return self.scatter / (self.n - 1)
 
+    def factor(self, eps_rel: float = 1e-6, workspace: Optional[Workspace] = None, stream=None):
+        """(L, mu) in bf16 for sample_inputs: L L^T = covariance + eps I."""
+        torch = _torch()
+        K = self.c.K
+        L = torch.empty((K, K), dtype=torch.bfloat16, device=self.device)
+        mu = torch.empty(K, dtype=torch.bfloat16, device=self.device)
+        need = _loka.loka_probe_cholesky_workspace_size(K)
+        ws, nbytes = (workspace or _ws(self.device)).get(need)
+        _loka.loka_probe_cholesky(self.c, eps_rel, L, mu, ws, nbytes, stream)
+        return L, mu
+
 
 def sample_inputs(mu, chol, B: int, seed: int, workspace: Optional[Workspace] = None, stream=None):
     """B synthetic input rows Z L^T + mu (bf16 CUDA [B, K]); mu bf16 [K], chol

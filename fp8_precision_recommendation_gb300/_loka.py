@@ -15,7 +15,8 @@ from typing import Optional, Sequence
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libloka.so")
 
-LOKA_OK, LOKA_ERR_INVALID_ARG, LOKA_ERR_UNSUPPORTED, LOKA_ERR_WORKSPACE, LOKA_ERR_TIMEOUT, LOKA_ERR_CUDA = range(6)
+LOKA_OK, LOKA_ERR_INVALID_ARG, LOKA_ERR_UNSUPPORTED, LOKA_ERR_WORKSPACE, LOKA_ERR_TIMEOUT, LOKA_ERR_CUDA, \
+    LOKA_ERR_NUMERIC = range(7)
 LOKA_SCALE_TENSOR, LOKA_SCALE_ROW, LOKA_SCALE_MX32, LOKA_BF16, LOKA_SCALE_BLOCK32 = range(5)
 LOKA_NORM_NONE, LOKA_NORM_LAYER, LOKA_NORM_RMS, LOKA_NORM_BLOCK_RMS = range(4)
 LOKA_ACT_NONE, LOKA_ACT_HARDSWISH = range(2)
@@ -66,6 +67,8 @@ SIGNATURES = {
     "loka_probe_stats_workspace_size": (c_sz, [c_i64, c_i64]),
     "loka_probe_stats_update": (c_i32, [ctypes.POINTER(InputStats), c_p, c_i64, c_p, c_sz, c_p]),
     "loka_probe_sample_workspace_size": (c_sz, [c_i64, c_i64]),
+    "loka_probe_cholesky_workspace_size": (c_sz, [c_i64]),
+    "loka_probe_cholesky": (c_i32, [ctypes.POINTER(InputStats), ctypes.c_double, c_p, c_p, c_p, c_sz, c_p]),
     "loka_probe_sample_inputs": (c_i32, [c_p, c_p, c_i64, c_i64, ctypes.c_uint64, c_p, c_p, c_sz, c_p]),
     "loka_fp8_linear_norm_workspace_size": (c_sz, [ctypes.POINTER(LinearDesc), c_i32]),
     "loka_fp8_linear_norm": (c_i32, [ctypes.POINTER(LinearDesc), c_i32, c_p, c_sz, c_p]),
@@ -160,6 +163,16 @@ def loka_probe_stats_workspace_size(B: int, K: int) -> int:
 def loka_probe_stats_update(stats: InputStats, x, B: int, workspace, workspace_bytes: int, stream=None) -> None:
     check(load().loka_probe_stats_update(ctypes.byref(stats), _ptr(x), B, _ptr(workspace), workspace_bytes,
                                          _stream(stream)))
+
+
+def loka_probe_cholesky_workspace_size(K: int) -> int:
+    return load().loka_probe_cholesky_workspace_size(K)
+
+
+def loka_probe_cholesky(stats: InputStats, eps_rel: float, chol, mu_out, workspace, workspace_bytes: int,
+                        stream=None) -> None:
+    check(load().loka_probe_cholesky(ctypes.byref(stats), eps_rel, _ptr(chol), _ptr(mu_out), _ptr(workspace),
+                                     workspace_bytes, _stream(stream)))
 
 
 def loka_probe_sample_workspace_size(B: int, K: int) -> int:

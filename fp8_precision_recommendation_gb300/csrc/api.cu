@@ -764,6 +764,44 @@ loka_status loka_probe_stats_update(loka_input_stats* stats, const void* x, int6
   return LOKA_OK;
 }
 
+size_t loka_probe_cholesky_workspace_size(int64_t K) {
+  if (!probe_k_ok(K)) return 0;
+  return align_up(static_cast<size_t>(K) * K * sizeof(float)) + kAlign;
+}
+
+loka_status loka_probe_cholesky(const loka_input_stats* stats, double eps_rel, void* chol, void* mu_out,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  if (stats == nullptr || chol == nullptr || mu_out == nullptr)
+    return fail(LOKA_ERR_INVALID_ARG, "stats, chol and mu_out must not be NULL");
+  const int64_t K = stats->K;
+  if (!probe_k_ok(K))
+    return fail(LOKA_ERR_UNSUPPORTED, "K = %lld: the probe takes K in {128, 256, 512, 1024, 2048}",
+                static_cast<long long>(K));
+  if (stats->n < 2) return fail(LOKA_ERR_INVALID_ARG, "n = %lld: a covariance needs at least two rows",
+                                static_cast<long long>(stats->n));
+  if (!(eps_rel >= 0.0) || !std::isfinite(eps_rel)) return fail(LOKA_ERR_INVALID_ARG, "eps_rel must be finite and >= 0");
+  if (stats->mu == nullptr || stats->scatter == nullptr) return fail(LOKA_ERR_INVALID_ARG, "mu and scatter are NULL");
+  if (!aligned16(chol)) return fail(LOKA_ERR_INVALID_ARG, "chol must be 16-byte aligned");
+  const size_t need = loka_probe_cholesky_workspace_size(K);
+  if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(LOKA_ERR_WORKSPACE, "workspace must be >= %zu bytes, 256-byte aligned", need);
+  DeviceInfo* dev = nullptr;
+  loka_status s = device_info(&dev);
+  if (s != LOKA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* status = reinterpret_cast<int*>(ws + align_up(static_cast<size_t>(K) * K * sizeof(float)));
+  cudaError_t e = launch_cholesky(stats->scatter, stats->mu, K, stats->n, eps_rel, reinterpret_cast<float*>(ws), chol,
+                                  mu_out, status, st);
+  if (e != cudaSuccess) return cuda_fail(e, "Cholesky launch");
+  int host = 0;
+  if ((e = cudaMemcpyAsync(&host, status, sizeof(host), cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+    return cuda_fail(e, "reading the Cholesky status");
+  if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e, "Cholesky");
+  if (host != 0) return fail(LOKA_ERR_NUMERIC, "the regularized covariance is not positive definite");
+  return LOKA_OK;
+}
+
 size_t loka_probe_sample_workspace_size(int64_t B, int64_t K) {
   if (B <= 0 || !probe_k_ok(K)) return 0;
   return align_up(static_cast<size_t>(B) * K * 2);

@@ -144,6 +144,10 @@ cudaError_t launch_stats_merge(const float* colpart, int64_t tiles, const float*
                                double* colwork /* 35 K fp64 */, double* mu, double* S, int64_t n_old, int64_t nb,
                                int sms, cudaStream_t stream);
 cudaError_t launch_normals(uint64_t seed, int64_t count, void* z, int sms, cudaStream_t stream);
+// Cholesky factor of S / (n - 1) + eps I (one block, fp32; A: K x K fp32
+// scratch); L and mu_out bf16; *status = 1 if not positive definite.
+cudaError_t launch_cholesky(const double* S, const double* mu, int64_t K, int64_t n, double eps_rel, float* A,
+                            void* L, void* mu_out, int* status, cudaStream_t stream);
 
 // Watchdog self-test: waits on a barrier that nothing completes.
 cudaError_t launch_watchdog_selftest(unsigned* status, uint64_t limit_ns, cudaStream_t stream);

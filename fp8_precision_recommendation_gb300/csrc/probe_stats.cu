@@ -173,6 +173,79 @@ __global__ void __launch_bounds__(256) normals_kernel(uint64_t seed, int64_t pai
   }
 }
 
+// The regularized covariance and its Cholesky factor, on one block:
+// A = S / (n - 1) + eps I with eps = eps_rel * trace(S / (n - 1)) / K (fp32,
+// from the fp64 scatter), factored in place column by column (left-looking:
+// L_jj = sqrt(A_jj - sum_k L_jk^2), L_ij = (A_ij - sum_k L_ik L_jk) / L_jj,
+// k < j), row j's finished entries staged in shared memory.  Writes L (bf16,
+// zero above the diagonal) and mu (bf16); *status = 1 when a pivot is not
+// positive (A not positive definite).
+__global__ void __launch_bounds__(1024) cholesky_kernel(const double* __restrict__ S, const double* __restrict__ mu,
+                                                        int64_t K, double inv_n1, double eps_rel, float* __restrict__ A,
+                                                        uint16_t* __restrict__ L, uint16_t* __restrict__ mu_out,
+                                                        int* __restrict__ status) {
+  extern __shared__ float rowj[];            // K floats
+  __shared__ double red[32];
+  __shared__ float pivot;
+  __shared__ int bad;
+  const int t = threadIdx.x, nt = blockDim.x;
+  const int lane = t & 31, warp = t >> 5;
+  // trace of S / (n - 1)
+  double tr = 0.0;
+  for (int64_t i = t; i < K; i += nt) tr += S[i * K + i] * inv_n1;
+  for (int o = 16; o > 0; o >>= 1) tr += __shfl_xor_sync(0xffffffffu, tr, o);
+  if (lane == 0) red[warp] = tr;
+  if (t == 0) bad = 0;
+  __syncthreads();
+  if (t == 0) {
+    double a = 0.0;
+    for (int w = 0; w < nt / 32; ++w) a += red[w];
+    red[0] = a;
+  }
+  __syncthreads();
+  const double eps = eps_rel * red[0] / static_cast<double>(K);
+  for (int64_t e = t; e < K * K; e += nt) {
+    const int64_t i = e / K, j = e - i * K;
+    A[e] = static_cast<float>(S[e] * inv_n1 + (i == j ? eps : 0.0));
+  }
+  __syncthreads();
+  for (int64_t j = 0; j < K; ++j) {
+    for (int64_t k = t; k < j; k += nt) rowj[k] = A[j * K + k];
+    __syncthreads();
+    // diagonal
+    float s = 0.0f;
+    for (int64_t k = t; k < j; k += nt) s = fmaf(rowj[k], rowj[k], s);
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) red[warp] = s;
+    __syncthreads();
+    if (t == 0) {
+      float a = 0.0f;
+      for (int w = 0; w < nt / 32; ++w) a += static_cast<float>(red[w]);
+      const float d = A[j * K + j] - a;
+      if (!(d > 0.0f)) bad = 1;
+      pivot = d > 0.0f ? sqrtf(d) : 1.0f;
+      A[j * K + j] = pivot;
+    }
+    __syncthreads();
+    if (bad) break;
+    const float inv = 1.0f / pivot;
+    for (int64_t i = j + 1 + t; i < K; i += nt) {
+      float dot = 0.0f;
+      const float* ri = A + i * K;
+      for (int64_t k = 0; k < j; ++k) dot = fmaf(ri[k], rowj[k], dot);
+      A[i * K + j] = (A[i * K + j] - dot) * inv;
+    }
+    __syncthreads();
+  }
+  if (t == 0) *status = bad;
+  for (int64_t e = t; e < K * K; e += nt) {
+    const int64_t i = e / K, j = e - i * K;
+    const float v = j <= i ? A[e] : 0.0f;
+    L[e] = static_cast<uint16_t>(pack_bf16x2(v, 0.0f) & 0xFFFFu);
+  }
+  for (int64_t i = t; i < K; i += nt) mu_out[i] = static_cast<uint16_t>(pack_bf16x2(static_cast<float>(mu[i]), 0.0f) & 0xFFFFu);
+}
+
 int grid_for(int64_t n, int sms) {
   int64_t b = (n + 255) / 256;
   if (b > static_cast<int64_t>(sms) * 8) b = static_cast<int64_t>(sms) * 8;
@@ -204,6 +277,19 @@ cudaError_t launch_stats_merge(const float* colpart, int64_t tiles, const float*
   stats_merge_kernel<<<grid_for(K * K, sms), 256, 0, stream>>>(partials, G, K, col, S, dn * db / (dn + db));
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   stats_mean_kernel<<<static_cast<unsigned>((K + 255) / 256), 256, 0, stream>>>(col, mu, K, db / (dn + db));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cholesky(const double* S, const double* mu, int64_t K, int64_t n, double eps_rel, float* A,
+                            void* L, void* mu_out, int* status, cudaStream_t stream) {
+  const size_t smem = static_cast<size_t>(K) * sizeof(float);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(cholesky_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  cholesky_kernel<<<1, 1024, smem, stream>>>(S, mu, K, 1.0 / static_cast<double>(n - 1), eps_rel, A,
+                                             static_cast<uint16_t*>(L), static_cast<uint16_t*>(mu_out), status);
   return cudaGetLastError();
 }
 

@@ -50,6 +50,8 @@ typedef int32_t loka_status;
 #define LOKA_ERR_WORKSPACE 3     /* workspace missing or too small         */
 #define LOKA_ERR_TIMEOUT 4       /* a kernel wait ran out of time          */
 #define LOKA_ERR_CUDA 5          /* a CUDA runtime/driver call failed      */
+#define LOKA_ERR_NUMERIC 6       /* a numerical precondition failed (e.g. a
+                                    covariance not positive definite)     */
 
 /* Scaling granularity of the E4M3 cast (LoKA section II-C / Table VI name
  * tensorwise, rowwise and blockwise recipes; the GEM Training page, "Low
@@ -337,6 +339,16 @@ typedef struct loka_input_stats {
 size_t loka_probe_stats_workspace_size(int64_t B, int64_t K);
 loka_status loka_probe_stats_update(loka_input_stats* stats, const void* x, int64_t B, void* workspace,
                                     size_t workspace_bytes, void* stream);
+/* loka_probe_cholesky: L (bf16 [K, K] row-major, lower, zero above the
+ * diagonal) with L L^T = Sigma + eps I, Sigma = scatter / (n - 1) and
+ * eps = eps_rel * trace(Sigma) / K (the page suggests about 1e-6), and mu as
+ * bf16 [K]: the inputs of loka_probe_sample_inputs.  fp32 left-looking
+ * factorization on one thread block (a once-per-snapshot K x K step).
+ * n >= 2.  LOKA_ERR_NUMERIC when a pivot is not positive.  Synchronizes
+ * the stream.  workspace: loka_probe_cholesky_workspace_size() bytes. */
+size_t loka_probe_cholesky_workspace_size(int64_t K);
+loka_status loka_probe_cholesky(const loka_input_stats* stats, double eps_rel, void* chol, void* mu_out,
+                                void* workspace, size_t workspace_bytes, void* stream);
 size_t loka_probe_sample_workspace_size(int64_t B, int64_t K);
 loka_status loka_probe_sample_inputs(const void* mu, const void* chol, int64_t B, int64_t K, uint64_t seed,
                                      void* out, void* workspace, size_t workspace_bytes, void* stream);

@@ -57,6 +57,13 @@ def covariance(n: int, S: np.ndarray) -> np.ndarray:
     return S / (n - 1)
 
 
+def cholesky_factor(n: int, S: np.ndarray, eps_rel: float) -> np.ndarray:
+    """L with L L^T = S / (n - 1) + eps I, eps = eps_rel * trace(S / (n - 1)) / K."""
+    sigma = covariance(n, S)
+    K = sigma.shape[0]
+    return np.linalg.cholesky(sigma + eps_rel * np.trace(sigma) / K * np.eye(K))
+
+
 def splitmix64(seed: int, index: np.ndarray) -> np.ndarray:
     """Random numbers `index` (uint64 array) of the counter-based stream."""
     with np.errstate(over="ignore"):

@@ -100,16 +100,42 @@ def test_sampler_against_oracle_stream(lib, K, B):
         assert np.abs(c - LL).max() <= 0.15 * np.abs(LL).max()
 
 
+@pytest.mark.parametrize("K", [128, 512])
+def test_cholesky_factor_against_oracle(lib, K):
+    st = loka.InputStats(K, DEV)
+    n, mu, S = 0, np.zeros(K), np.zeros((K, K))
+    for xb in _batches(K, [3000, 5000], seed=40 + K):
+        st.update(xb.to(DEV))
+        n, mu, S = PS.stats_update(n, mu, S, xb.float().numpy())
+    L, m = st.factor(eps_rel=1e-6)
+    torch.cuda.synchronize()
+    Lo = PS.cholesky_factor(n, S, 1e-6)
+    Lg = L.double().cpu().numpy()
+    assert np.array_equal(np.triu(Lg, 1), np.zeros_like(Lg))
+    # bf16 storage (2 ulps) and the fp32 factorization's rounding
+    tol = 2.0 * F.bf16_ulp(np.abs(Lo)) + 1e-3 * np.abs(Lo).max()
+    assert (np.abs(Lg - Lo) <= tol).all(), f"K{K}: worst {np.abs(Lg - Lo).max():.3e}"
+    assert (np.abs(m.double().cpu().numpy() - mu) <= 2.0 * F.bf16_ulp(np.abs(mu)) + 1e-6).all()
+
+
+def test_cholesky_rejects_an_indefinite_covariance(lib):
+    st = loka.InputStats(128, DEV)
+    st.c.n = 10
+    st.scatter.copy_(torch.diag(torch.tensor([1.0, -1.0] + [1.0] * 126, dtype=torch.float64)))
+    with pytest.raises(loka._loka.LokaError) as e:
+        st.factor(eps_rel=0.0)
+    assert e.value.status == loka._loka.LOKA_ERR_NUMERIC
+
+
 def test_probe_on_learned_inputs(lib):
-    # the probe loop: learn a layer's input statistics, factor the covariance,
-    # sample inputs from it and measure the FP8 error on them
+    # the probe loop on the device: learn a layer's input statistics, factor
+    # the covariance, sample inputs from it and measure the FP8 error on them
     K = 512
     st = loka.InputStats(K, DEV)
     for xb in _batches(K, [8192, 8192], seed=5):
         st.update(xb.to(DEV))
-    cov = st.covariance().cpu().numpy()
-    L = np.linalg.cholesky(cov + 1e-6 * np.trace(cov) / K * np.eye(K))
-    xs = loka.sample_inputs(st.mu.to(torch.bfloat16), torch.from_numpy(L).to(torch.bfloat16).to(DEV), 4096, seed=2)
+    L, m = st.factor(eps_rel=1e-6)
+    xs = loka.sample_inputs(m, L, 4096, seed=2)
     w = W.random_bf16((256, K), seed=3, var=1.0 / K).to(DEV)
     err = loka.quant_error(xs, w, None, W.SCALE_ROW)
     assert 1e-3 < err["rel_err_fro"] < 0.1 and np.isfinite(err["mere"])

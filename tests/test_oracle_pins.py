@@ -420,6 +420,16 @@ def test_stream_normals_have_normal_moments_and_uniform_bits():
     assert np.array_equal(PS.normals(7, 64), z[:64])
 
 
+def test_cholesky_factor_reproduces_the_regularized_covariance():
+    rng = np.random.default_rng(23)
+    x = rng.standard_normal((50, 12)) @ rng.standard_normal((12, 12))
+    n, mu, S = PS.stats_update(0, np.zeros(12), np.zeros((12, 12)), x)
+    L = PS.cholesky_factor(n, S, 1e-3)
+    sigma = np.cov(x, rowvar=False)
+    assert np.allclose(np.triu(L, 1), 0) and (np.diag(L) > 0).all()
+    assert np.allclose(L @ L.T, sigma + 1e-3 * np.trace(sigma) / 12 * np.eye(12), rtol=1e-12, atol=1e-12)
+
+
 def test_sampler_reproduces_mean_and_covariance():
     rng = np.random.default_rng(22)
     K = 16
