@@ -10,7 +10,8 @@ layer's own data; here seeded synthetic activations of the pages' kind stand
 in (normal, optionally with 1% of the entries scaled by 100).
 
 The candidates are this library's variants of ``loka_fp8_linear_norm``:
-per-tensor, per-row and MX 1x32 E4M3 scaling, and the bf16 path.  For each
+per-tensor, per-row, MX 1x32 and square 32x32-block E4M3 scaling, and the
+bf16 path.  For each
 problem (M, N, K, norm, outlier fraction) and variant:
 
 * time: CUDA events around repeated calls on one stream after warm-up, with
@@ -38,10 +39,10 @@ import time
 from typing import Dict, List, Sequence, Tuple
 
 from . import _loka
-from . import (LOKA_BF16, LOKA_NORM_LAYER, LOKA_SCALE_MX32, LOKA_SCALE_ROW, LOKA_SCALE_TENSOR, Layer, Workspace,
-               fp8_linear_norm, quant_error, quantize_fp8)
+from . import (LOKA_BF16, LOKA_NORM_LAYER, LOKA_SCALE_BLOCK32, LOKA_SCALE_MX32, LOKA_SCALE_ROW, LOKA_SCALE_TENSOR,
+               Layer, Workspace, fp8_linear_norm, quant_error, quantize_fp8)
 
-VARIANTS = (LOKA_SCALE_TENSOR, LOKA_SCALE_ROW, LOKA_SCALE_MX32, LOKA_BF16)
+VARIANTS = (LOKA_SCALE_TENSOR, LOKA_SCALE_ROW, LOKA_SCALE_MX32, LOKA_BF16, LOKA_SCALE_BLOCK32)
 GRID_M = (4096, 32768, 262144)
 GRID_K = (128, 512, 2048)
 GRID_N = (64, 256, 1024)
@@ -135,7 +136,8 @@ def run(quick: bool = False, log=print) -> Dict:
         torch.cuda.empty_cache()
     return {"device": torch.cuda.get_device_name(), "seconds": round(time.time() - t0, 1),
             "columns": ["M", "N", "K", "norm", "outlier_frac", "variant", "time_us", "rel_err", "mere"],
-            "variants": {"0": "per-tensor E4M3", "1": "per-row E4M3", "2": "MX 1x32 E4M3/E8M0", "3": "bf16"},
+            "variants": {"0": "per-tensor E4M3", "1": "per-row E4M3", "2": "MX 1x32 E4M3/E8M0", "3": "bf16",
+                         "4": "square 32x32 E4M3/E8M0"},
             "rows": [list(r) for r in rows]}
 
 

@@ -429,7 +429,7 @@ def test_variant_sweep_smoke(lib):
     from fp8_precision_recommendation_gb300 import sweep
     table = sweep.run(quick=True, log=lambda *a: None)
     rows = table["rows"]
-    assert len(rows) == 4 * len(sweep.problems(quick=True))
+    assert len(rows) == len(sweep.VARIANTS) * len(sweep.problems(quick=True))
     for (m, n, k, norm, o, v, t, rel, mere) in rows:
         assert t > 0
         if v == _loka.LOKA_BF16:
