@@ -303,9 +303,7 @@ loka_status build_gemm(const loka_linear_desc* d, int n, const std::vector<Opera
     if (g.M == 0) continue;
     loka_status s;
     // W's box: the columns one CTA owns under the launch's route
-    const int box = gemm_route(static_cast<int>(g.N), bf16_operands ? OperandKind::kBf16 : operand_kind(mode), out, norm,
-                               d[0].norm_block, out == OutKind::kQuant ? output_reference(d, n).y_q_mode : 0)
-                        .local;
+    const int box = gemm_route(static_cast<int>(g.N), norm).local;
     G.b_box_rows = box;
     if (bf16_operands) {
       if ((s = encode_2d(&G.tm_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.x, g.K, g.M, 128)) != LOKA_OK) return s;

@@ -11,7 +11,7 @@ bool gemm_supported(int N, int K, OperandKind op) {
   return plan_for(local, K, op == OperandKind::kBf16 ? 2 : 1, op == OperandKind::kMxE4M3, cl).stages > 0;
 }
 
-GemmRoute gemm_route(int N, OperandKind, OutKind, int norm, int, int) {
+GemmRoute gemm_route(int N, int norm) {
   const bool no_row_stat = norm == kNormNone || norm == kNormBlockRms;
   // Rows wider than one CTA whose epilogue needs no row statistic (no norm,
   // or BlockNorm, whose blocks lie within a CTA's 256 columns) run as
@@ -21,7 +21,7 @@ GemmRoute gemm_route(int N, OperandKind, OutKind, int norm, int, int) {
 }
 
 cudaError_t launch_gemm_norm(GemmParams& p, int N, OperandKind op, OutKind out, int sms, cudaStream_t stream) {
-  const GemmRoute r = gemm_route(N, op, out, p.norm, p.norm_block, p.yq_mode);
+  const GemmRoute r = gemm_route(N, p.norm);
   p.slices = r.slices;
   // the launchers take the row width: up to 256 one CTA, wider a cluster
   N = r.cl > 1 ? N : r.local;

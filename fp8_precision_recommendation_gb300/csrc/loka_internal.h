@@ -121,7 +121,7 @@ enum class OutKind : int { kBf16 = 0, kF32 = 1, kQuant = 2 };
 struct GemmRoute {
   int local, cl, slices;
 };
-GemmRoute gemm_route(int N, OperandKind op, OutKind out, int norm, int norm_block, int yq_mode);
+GemmRoute gemm_route(int N, int norm);
 
 // Launches the persistent GEMM + epilogue kernel for N columns (fills in
 // p.stages and p.slices; tm_b must have been encoded with a box of
