@@ -9,11 +9,14 @@
  *
  *   amax -> scale -> E4M3 cast of activations X[M,K] and weights W[N,K]
  *   -> FP8 GEMM with fp32 accumulation (tcgen05 tensor cores, TMEM)
- *   -> epilogue: dequantize, add bias, LayerNorm or RMSNorm over N, bf16 store
+ *   -> epilogue: dequantize, add bias, LayerNorm, RMSNorm or BlockNorm,
+ *      optional Hard Swish, bf16 store and/or E4M3 codes for the next layer
  *
- * plus a per-layer quantization-error probe (LoKA section III-A, MERE of
- * FP8(Wx+b) against a high-precision Wx+b) and a variant selector (LoKA
- * section III-C, Dispatch).
+ * plus square 32x32-block quantization with a transposed copy (GEM Training
+ * page), a per-layer quantization-error probe (LoKA section III-A, MERE of
+ * FP8(Wx+b) against a high-precision Wx+b) with the probe's online input
+ * statistics, Cholesky factor and sampler (section III-A 1), and a variant
+ * selector (LoKA section III-C, Dispatch).
  *
  * Conventions for every call:
  *   - Pointers named as device pointers must be device memory of the current
@@ -140,10 +143,13 @@ loka_status loka_quantize_fp8_block32(const void* x, int64_t rows, int64_t cols,
  * call runs several independent layers in one launch).
  *
  * One descriptor per independent layer (group).  All groups of one call must
- * share N, K, mode, norm and eps and the *_is_fp8 flags; M may differ.
- *   M >= 0; K % 128 == 0; N in {64, 128, 192, 256, 512, 1024, 2048} (rows
- *   wider than 256 are split over a thread-block cluster of N/256 CTAs that
- *   merge their row statistics through distributed shared memory).
+ * share N, K, mode, norm, norm_block, eps, act and the *_is_fp8 flags; M
+ * may differ.
+ *   M >= 0; K % 128 == 0; N in {64, 128, 192, 256, 512, 1024, 2048}.  Rows
+ *   wider than 256 are split into 256-column slices: with LayerNorm or
+ *   RMSNorm over a thread-block cluster of N/256 CTAs that merge their row
+ *   statistics through distributed shared memory; with no norm or BlockNorm
+ *   over N/256 independent CTAs (no statistic spans the row).
  *   x: bf16 [M,K] (x_is_fp8 = 0) or E4M3 [M,K] with x_scales as produced by
  *      loka_quantize_fp8 (x_is_fp8 = 1).  Same for w / w_scales / w_is_fp8.
  *   mode: LOKA_SCALE_* (LOKA_BF16 runs the bf16 GEMM; *_is_fp8 must be 0).
