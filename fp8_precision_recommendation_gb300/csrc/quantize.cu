@@ -81,6 +81,68 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const __grid_constant__
   }
 }
 
+// Rows of at most 256 columns: one half-warp per row, two rows per warp.
+// Lane l of a half holds vectors l and l + 16 of its row (512 contiguous
+// bytes per row per load pair), so a warp keeps two rows' bytes in flight
+// where a whole warp per row would keep one; reductions stay within the
+// half (shuffle offsets 1..8).  Same arithmetic as quant_rows_kernel.
+template <int MODE>
+__global__ void __launch_bounds__(256) quant_rows_half_kernel(const __grid_constant__ QuantJobs jobs) {
+  launch_dependents();   // the GEMM that follows may start its prologue
+  const int lane = threadIdx.x & 31;
+  const int hl = lane & 15;                          // lane within the half
+  const int64_t half0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
+  const int64_t nhalves = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 4;
+  // both halves of a warp run the loop the same number of times (nhalves is
+  // even and the halves' rows differ by 1), so the full-mask shuffles below
+  // stay convergent; a half past the last row works on a dummy row
+  for (int64_t base = half0 & ~int64_t(1); base < jobs.total_rows; base += nhalves) {
+    const int64_t gr = base + (half0 & 1);
+    const bool live = gr < jobs.total_rows;
+    const QuantJob& job = jobs.j[find_job(jobs, live ? gr : base)];
+    const int64_t row = (live ? gr : base) - job.row_begin;
+    const int nvec = static_cast<int>(job.cols >> 3);
+    const uint4* src = reinterpret_cast<const uint4*>(job.x) + row * nvec;
+    uint2* dst = reinterpret_cast<uint2*>(job.q + row * job.cols);
+    uint4 v[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int idx = i * 16 + hl;
+      v[i] = (live && idx < nvec) ? __ldcs(src + idx) : make_uint4(0, 0, 0, 0);
+    }
+    if (MODE == kScaleRow) {
+      float m = abs_max8(v[1], abs_max8(v[0], 0.0f));
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      float inv, scale;
+      row_scales(m, inv, scale);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int idx = i * 16 + hl;
+        if (live && idx < nvec) dst[idx] = cast8(v[i], inv);
+      }
+      if (live && hl == 0) reinterpret_cast<float*>(job.scales)[row] = scale;
+    } else {
+      uint8_t* sc = reinterpret_cast<uint8_t*>(job.scales) + row * (job.cols >> 5);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int idx = i * 16 + hl;
+        float m = abs_max8(v[i], 0.0f);
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        const int e = mx_exponent(m);
+        if (live && idx < nvec) {
+          dst[idx] = cast8(v[i], pow2_neg(e));
+          if ((hl & 3) == 0) {
+            sc[idx >> 2] = static_cast<uint8_t>(e + 127);
+            if (job.sf_tc != nullptr) job.sf_tc[sf_tc_offset(row, idx >> 2, job.cols >> 7)] = static_cast<uint8_t>(e + 127);
+          }
+        }
+      }
+    }
+  }
+}
+
 // Rows longer than 2048 elements: amax pass, then a cast pass that re-reads
 // the row (it is still in L1/L2).  Same arithmetic as above.
 template <int MODE>
@@ -265,11 +327,13 @@ __global__ void __launch_bounds__(256) quant_block32_kernel(const __grid_constan
 
 // One wave of the grid-stride kernel: as many 256-thread blocks as are
 // resident at once (the register count decides; asked once per kernel and
-// device), never more than one warp per row.  V = 0: the long-row kernel.
+// device), never more than one warp per row.  V = 0: the long-row kernel;
+// V = -1: half-warp rows (at most 256 columns).
 template <int MODE, int V>
 cudaError_t launch_one_wave(const QuantJobs& jobs, int sms, cudaStream_t stream) {
   const int threads = 256;
-  auto kern = V == 0 ? quant_rows_long_kernel<MODE> : quant_rows_kernel<MODE, (V > 0 ? V : 1)>;
+  auto kern = V == 0 ? quant_rows_long_kernel<MODE>
+                     : (V == -1 ? quant_rows_half_kernel<MODE> : quant_rows_kernel<MODE, (V > 0 ? V : 1)>);
   static std::atomic<int> per_sm[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -281,7 +345,7 @@ cudaError_t launch_one_wave(const QuantJobs& jobs, int sms, cudaStream_t stream)
     if (occ < 1) occ = 1;
     per_sm[dev & 63].store(occ);
   }
-  int64_t blocks = (jobs.total_rows + 7) / 8;
+  int64_t blocks = (jobs.total_rows + (V == -1 ? 15 : 7)) / (V == -1 ? 16 : 8);
   const int64_t cap = static_cast<int64_t>(sms) * occ;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
@@ -291,7 +355,7 @@ cudaError_t launch_one_wave(const QuantJobs& jobs, int sms, cudaStream_t stream)
 
 template <int MODE>
 cudaError_t launch_rows(const QuantJobs& jobs, int max_cols, int sms, cudaStream_t stream) {
-  if (max_cols <= 256) return launch_one_wave<MODE, 1>(jobs, sms, stream);
+  if (max_cols <= 256) return launch_one_wave<MODE, -1>(jobs, sms, stream);   // half-warp rows
   if (max_cols <= 512) return launch_one_wave<MODE, 2>(jobs, sms, stream);
   if (max_cols <= 1024) return launch_one_wave<MODE, 4>(jobs, sms, stream);
   if (max_cols <= 2048) return launch_one_wave<MODE, 8>(jobs, sms, stream);
