@@ -244,7 +244,8 @@ __global__ void __launch_bounds__(256) sf_permute_kernel(const uint8_t* __restri
 // 4 lanes of its 32 columns (shuffles), then the 8 warps (shared memory); the
 // exponent rule is the MX one.  Codes go out row by row; the optional
 // transposed copy is staged in shared memory and transposed 4 x 4 bytes at a
-// time (byte permutes), each thread writing 8 codes of 4 transposed rows.
+// time (byte permutes), each of 64 threads writing the 32 codes of 4
+// transposed rows as whole 32-byte sectors.
 __global__ void __launch_bounds__(256) quant_block32_kernel(const __grid_constant__ QuantJobs jobs) {
   launch_dependents();   // the GEMM that follows may start its prologue
   __shared__ float red[8][8];                        // [warp][block] partial amax
@@ -298,27 +299,30 @@ __global__ void __launch_bounds__(256) quant_block32_kernel(const __grid_constan
     }
     if (job.q_t != nullptr) {
       __syncthreads();
-      // thread: columns 4g..4g+3 of the unit, rows 8h..8h+7 of the strip
-      const int g = threadIdx.x & 63, h = threadIdx.x >> 6;
-      if (c0 + 4 * g < job.cols) {
-        uint32_t w[8];
+      // threads 0..63: columns 4g..4g+3 of the unit, all 32 rows of the
+      // strip, transposed 4 x 4 bytes at a time; each transposed row then
+      // gets its 32 codes as two 16-byte stores (one whole sector)
+      const int g = threadIdx.x;
+      if (g < 64 && c0 + 4 * g < job.cols) {
+        uint32_t col[4][8];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) w[r] = *reinterpret_cast<const uint32_t*>(&tile[8 * h + r][4 * g]);
-        uint32_t col[2][4];
+        for (int rb = 0; rb < 8; ++rb) {
+          uint32_t q4[4];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const uint32_t* q4 = w + 4 * half;
+          for (int r = 0; r < 4; ++r) q4[r] = *reinterpret_cast<const uint32_t*>(&tile[4 * rb + r][4 * g]);
           const uint32_t lo01 = __byte_perm(q4[0], q4[1], 0x5140), hi01 = __byte_perm(q4[0], q4[1], 0x7362);
           const uint32_t lo23 = __byte_perm(q4[2], q4[3], 0x5140), hi23 = __byte_perm(q4[2], q4[3], 0x7362);
-          col[half][0] = __byte_perm(lo01, lo23, 0x5410);
-          col[half][1] = __byte_perm(lo01, lo23, 0x7632);
-          col[half][2] = __byte_perm(hi01, hi23, 0x5410);
-          col[half][3] = __byte_perm(hi01, hi23, 0x7632);
+          col[0][rb] = __byte_perm(lo01, lo23, 0x5410);
+          col[1][rb] = __byte_perm(lo01, lo23, 0x7632);
+          col[2][rb] = __byte_perm(hi01, hi23, 0x5410);
+          col[3][rb] = __byte_perm(hi01, hi23, 0x7632);
         }
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          *reinterpret_cast<uint2*>(job.q_t + (c0 + 4 * g + c) * job.rows + r0 + 8 * h) =
-              make_uint2(col[0][c], col[1][c]);
+        for (int c = 0; c < 4; ++c) {
+          uint4* out = reinterpret_cast<uint4*>(job.q_t + (c0 + 4 * g + c) * job.rows + r0);
+          out[0] = make_uint4(col[c][0], col[c][1], col[c][2], col[c][3]);
+          out[1] = make_uint4(col[c][4], col[c][5], col[c][6], col[c][7]);
+        }
       }
     }
     __syncthreads();   // the next unit reuses red, ex and tile
