@@ -364,11 +364,11 @@ def run_ours(args, world, rank, local):
     def quantize_x(i):
         b = i % nbuf
         for gi, l in enumerate(layers):
-            _loka.loka_quantize_fp8(xs[b][gi], l.M, l.K, mode, qx[b][gi], sx[b][gi], qws, qws.numel(), s)
+            _loka.loka_quantize_fp8(xs[b][gi], l.M, l.K, l.K, mode, qx[b][gi], sx[b][gi], qws, qws.numel(), s)
 
     kern["quantize_x"] = timed(quantize_x, args.steps)
     for gi, l in enumerate(layers):
-        _loka.loka_quantize_fp8(ws_[gi], l.N, l.K, mode, qw[gi], sw[gi], qws, qws.numel(), s)
+        _loka.loka_quantize_fp8(ws_[gi], l.N, l.K, l.K, mode, qw[gi], sw[gi], qws, qws.numel(), s)
     pre = [mk(i, x_list=qx[i], x_scales=sx[i], w_scales=sw) for i in range(nbuf)]
     for lst in pre:
         for gi, lay in enumerate(lst):
@@ -397,7 +397,7 @@ def run_ours(args, world, rank, local):
         def quantize_y(i):
             b = i % nbuf
             for gi, l in enumerate(layers):
-                _loka.loka_quantize_fp8(ys[b][gi], l.M, l.N, out_mode, yq[b][gi], ysq[b][gi], qws, qws.numel(), s)
+                _loka.loka_quantize_fp8(ys[b][gi], l.M, l.N, l.N, out_mode, yq[b][gi], ysq[b][gi], qws, qws.numel(), s)
 
         t_qy = timed(quantize_y, args.steps)
         bytes_c = sum(l.M * l.K + scale_bytes(mode, l.M, l.K) + l.N * l.K + scale_bytes(mode, l.N, l.K)

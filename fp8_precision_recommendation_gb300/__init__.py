@@ -70,16 +70,17 @@ def _ws(device) -> Workspace:
 
 
 def quantize_fp8(x, mode: int, workspace: Optional[Workspace] = None, stream=None):
-    """E4M3 cast of a bf16 CUDA tensor [rows, cols]; returns (q uint8, scales)."""
+    """E4M3 cast of a bf16 CUDA tensor [rows, cols] whose rows may be strided
+    (a column slice of a wider tensor); returns dense (q uint8, scales)."""
     torch = _torch()
-    assert x.dtype == torch.bfloat16 and x.is_cuda and x.is_contiguous() and x.dim() == 2
+    assert x.dtype == torch.bfloat16 and x.is_cuda and x.dim() == 2 and x.stride(1) == 1
     rows, cols = x.shape
     q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
     shp, dt = scales_shape(rows, cols, mode)
     scales = torch.empty(shp, dtype=getattr(torch, dt), device=x.device)
     need = _loka.loka_quantize_fp8_workspace_size(rows, cols, mode)
     ws, nbytes = (workspace or _ws(x.device)).get(need)
-    _loka.loka_quantize_fp8(x, rows, cols, mode, q, scales, ws, nbytes, stream)
+    _loka.loka_quantize_fp8(x, rows, cols, x.stride(0), mode, q, scales, ws, nbytes, stream)
     return q, scales
 
 
@@ -93,7 +94,7 @@ def quantize_fp8_block32(x, transposed: bool = False, stream=None):
     shp, _ = scales_shape(rows, cols, LOKA_SCALE_BLOCK32)
     scales = torch.empty(shp, dtype=torch.uint8, device=x.device)
     q_t = torch.empty((cols, rows), dtype=torch.uint8, device=x.device) if transposed else None
-    _loka.loka_quantize_fp8_block32(x, rows, cols, q, q_t, scales, stream)
+    _loka.loka_quantize_fp8_block32(x, rows, cols, cols, q, q_t, scales, stream)
     return q, scales, q_t
 
 
@@ -161,16 +162,20 @@ def fp8_linear_norm(layers: Sequence[Layer], workspace: Optional[Workspace] = No
     return [l.y for l in layers]
 
 
-def quant_error(x, w, bias, mode: int, workspace: Optional[Workspace] = None, stream=None) -> dict:
-    """Probe: FP8 (mode) vs high-precision pre-norm outputs of one layer."""
-    layer = Layer(x=x, w=w, bias=bias, mode=mode, norm=LOKA_NORM_NONE, eps=0.0, y=x.new_empty((0,)))
+def quant_error(x, w, bias, mode: int, norm: int = LOKA_NORM_NONE, eps: float = 0.0, gamma=None, beta=None,
+                norm_block: int = 256, act: int = LOKA_ACT_NONE, workspace: Optional[Workspace] = None,
+                stream=None) -> dict:
+    """Probe: FP8 (mode) vs high-precision outputs of one layer, before and
+    after its normalization."""
+    layer = Layer(x=x, w=w, bias=bias, gamma=gamma, beta=beta, mode=mode, norm=norm, eps=eps,
+                  norm_block=norm_block, act=act, y=x.new_empty((0,)))
     d = layer.desc()
     d.y = None
     need = _loka.loka_quant_error_workspace_size(d)
     ws, nbytes = (workspace or _ws(x.device)).get(need)
     st = _loka.loka_quant_error(d, ws, nbytes, stream)
     return {"mere": st.mere, "rel_err_fro": st.rel_err_fro, "max_abs": st.max_abs,
-            "zero_ref_count": st.zero_ref_count, "count": st.count}
+            "max_abs_post_norm": st.max_abs_post_norm, "zero_ref_count": st.zero_ref_count, "count": st.count}
 
 
 class InputStats:
@@ -197,9 +202,14 @@ class InputStats:
         ws, nbytes = (workspace or _ws(self.device)).get(need)
         _loka.loka_probe_stats_update(self.c, x, B, ws, nbytes, stream)
 
-    def covariance(self):
-        """The unbiased covariance scatter / (n - 1) (a torch fp64 tensor)."""
-        return self.scatter / (self.n - 1)
+    def covariance(self, stream=None):
+        """The unbiased covariance scatter / (n - 1), computed by the library
+        into a new fp64 CUDA tensor [K, K]."""
+        torch = _torch()
+        K = self.c.K
+        cov = torch.empty((K, K), dtype=torch.float64, device=self.device)
+        _loka.loka_probe_covariance(self.c, cov, stream)
+        return cov
 
     def factor(self, eps_rel: float = 1e-6, workspace: Optional[Workspace] = None, stream=None):
         """(L, mu) in bf16 for sample_inputs: L L^T = covariance + eps I."""

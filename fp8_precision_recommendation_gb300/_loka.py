@@ -34,7 +34,7 @@ class LinearDesc(ctypes.Structure):
 
 class ErrorStats(ctypes.Structure):
     _fields_ = [("mere", ctypes.c_double), ("rel_err_fro", ctypes.c_double), ("max_abs", ctypes.c_double),
-                ("zero_ref_count", c_i64), ("count", c_i64)]
+                ("max_abs_post_norm", ctypes.c_double), ("zero_ref_count", c_i64), ("count", c_i64)]
 
 
 class Problem(ctypes.Structure):
@@ -62,11 +62,12 @@ SIGNATURES = {
     "loka_device_status": (c_i32, [c_p]),
     "loka_selftest_watchdog": (c_i32, [ctypes.c_uint64, c_p]),
     "loka_quantize_fp8_workspace_size": (c_sz, [c_i64, c_i64, c_i32]),
-    "loka_quantize_fp8": (c_i32, [c_p, c_i64, c_i64, c_i32, c_p, c_p, c_p, c_sz, c_p]),
-    "loka_quantize_fp8_block32": (c_i32, [c_p, c_i64, c_i64, c_p, c_p, c_p, c_p]),
+    "loka_quantize_fp8": (c_i32, [c_p, c_i64, c_i64, c_i64, c_i32, c_p, c_p, c_p, c_sz, c_p]),
+    "loka_quantize_fp8_block32": (c_i32, [c_p, c_i64, c_i64, c_i64, c_p, c_p, c_p, c_p]),
     "loka_probe_stats_workspace_size": (c_sz, [c_i64, c_i64]),
     "loka_probe_stats_update": (c_i32, [ctypes.POINTER(InputStats), c_p, c_i64, c_p, c_sz, c_p]),
     "loka_probe_sample_workspace_size": (c_sz, [c_i64, c_i64]),
+    "loka_probe_covariance": (c_i32, [ctypes.POINTER(InputStats), c_p, c_p]),
     "loka_probe_cholesky_workspace_size": (c_sz, [c_i64]),
     "loka_probe_cholesky": (c_i32, [ctypes.POINTER(InputStats), ctypes.c_double, c_p, c_p, c_p, c_sz, c_p]),
     "loka_probe_sample_inputs": (c_i32, [c_p, c_p, c_i64, c_i64, ctypes.c_uint64, c_p, c_p, c_sz, c_p]),
@@ -146,14 +147,15 @@ def loka_quantize_fp8_workspace_size(rows: int, cols: int, mode: int) -> int:
     return load().loka_quantize_fp8_workspace_size(rows, cols, mode)
 
 
-def loka_quantize_fp8(x, rows: int, cols: int, mode: int, q, scales, workspace=None, workspace_bytes: int = 0,
-                      stream=None) -> None:
-    check(load().loka_quantize_fp8(_ptr(x), rows, cols, mode, _ptr(q), _ptr(scales), _ptr(workspace),
+def loka_quantize_fp8(x, rows: int, cols: int, ld: int, mode: int, q, scales, workspace=None,
+                      workspace_bytes: int = 0, stream=None) -> None:
+    check(load().loka_quantize_fp8(_ptr(x), rows, cols, ld, mode, _ptr(q), _ptr(scales), _ptr(workspace),
                                    workspace_bytes, _stream(stream)))
 
 
-def loka_quantize_fp8_block32(x, rows: int, cols: int, q, q_t, scales, stream=None) -> None:
-    check(load().loka_quantize_fp8_block32(_ptr(x), rows, cols, _ptr(q), _ptr(q_t), _ptr(scales), _stream(stream)))
+def loka_quantize_fp8_block32(x, rows: int, cols: int, ld: int, q, q_t, scales, stream=None) -> None:
+    check(load().loka_quantize_fp8_block32(_ptr(x), rows, cols, ld, _ptr(q), _ptr(q_t), _ptr(scales),
+                                           _stream(stream)))
 
 
 def loka_probe_stats_workspace_size(B: int, K: int) -> int:
@@ -163,6 +165,10 @@ def loka_probe_stats_workspace_size(B: int, K: int) -> int:
 def loka_probe_stats_update(stats: InputStats, x, B: int, workspace, workspace_bytes: int, stream=None) -> None:
     check(load().loka_probe_stats_update(ctypes.byref(stats), _ptr(x), B, _ptr(workspace), workspace_bytes,
                                          _stream(stream)))
+
+
+def loka_probe_covariance(stats: InputStats, cov, stream=None) -> None:
+    check(load().loka_probe_covariance(ctypes.byref(stats), _ptr(cov), _stream(stream)))
 
 
 def loka_probe_cholesky_workspace_size(K: int) -> int:

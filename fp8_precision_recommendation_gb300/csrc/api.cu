@@ -339,7 +339,8 @@ loka_status build_gemm(const loka_linear_desc* d, int n, const std::vector<Opera
   p->wait_limit_ns = kDefaultWaitLimitNs;
   p->yq_mode = out == OutKind::kQuant ? output_reference(d, n).y_q_mode : 0;
   p->norm_block = norm == kNormBlockRms ? d[0].norm_block : 256;
-  p->act = out == OutKind::kF32 ? kActNone : d[0].act;   // the probe's pre-norm outputs take no activation
+  // the probe's pre-norm (and the statistics') fp32 outputs take no activation
+  p->act = (out == OutKind::kF32 && norm == kNormNone) ? kActNone : d[0].act;
   p->slices = 1;
   return LOKA_OK;
 }
@@ -362,6 +363,7 @@ loka_status quantize_operands(const loka_linear_desc* d, int n, const std::vecto
       j.sf_tc = (g.mode == kScaleMx32 || g.mode == kScaleBlock32) ? ws + slots[i].sx_tc : nullptr;
       j.rows = g.M;
       j.cols = g.K;
+      j.ld = g.K;
       j.row_begin = rows;
       rows += g.M;
     }
@@ -374,6 +376,7 @@ loka_status quantize_operands(const loka_linear_desc* d, int n, const std::vecto
       j.sf_tc = (g.mode == kScaleMx32 || g.mode == kScaleBlock32) ? ws + slots[i].sw_tc : nullptr;
       j.rows = g.N;
       j.cols = g.K;
+      j.ld = g.K;
       j.row_begin = rows;
       rows += g.N;
     }
@@ -430,12 +433,15 @@ size_t loka_quantize_fp8_workspace_size(int64_t, int64_t, int32_t mode) {
 
 namespace {
 
-loka_status quantize_one(const void* x, int64_t rows, int64_t cols, int32_t mode, void* q, void* q_t, void* scales,
-                         void* workspace, size_t workspace_bytes, void* stream) {
+loka_status quantize_one(const void* x, int64_t rows, int64_t cols, int64_t ld, int32_t mode, void* q, void* q_t,
+                         void* scales, void* workspace, size_t workspace_bytes, void* stream) {
   if (mode != LOKA_SCALE_TENSOR && mode != LOKA_SCALE_ROW && mode != LOKA_SCALE_MX32 && mode != LOKA_SCALE_BLOCK32)
     return fail(LOKA_ERR_INVALID_ARG, "mode %d is not an FP8 scaling mode", mode);
   if (rows < 0 || cols < 0) return fail(LOKA_ERR_INVALID_ARG, "negative size");
   if (cols % 32 != 0) return fail(LOKA_ERR_INVALID_ARG, "cols = %lld is not a multiple of 32", static_cast<long long>(cols));
+  if (ld < cols || ld % 8 != 0)
+    return fail(LOKA_ERR_INVALID_ARG, "ld = %lld: the row stride must be >= cols and a multiple of 8 (16-byte rows)",
+                static_cast<long long>(ld));
   if (rows == 0 || cols == 0) {
     if (mode == LOKA_SCALE_TENSOR && scales != nullptr) {
       const float one = 1.0f;
@@ -466,6 +472,7 @@ loka_status quantize_one(const void* x, int64_t rows, int64_t cols, int32_t mode
   jobs.j[0].amax_slot = static_cast<unsigned*>(workspace);
   jobs.j[0].rows = rows;
   jobs.j[0].cols = cols;
+  jobs.j[0].ld = ld;
   jobs.total_rows = rows;
   cudaError_t e = launch_quantize(jobs, mode, dev->sms, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
@@ -474,14 +481,14 @@ loka_status quantize_one(const void* x, int64_t rows, int64_t cols, int32_t mode
 
 }  // namespace
 
-loka_status loka_quantize_fp8(const void* x, int64_t rows, int64_t cols, int32_t mode, void* q, void* scales,
-                              void* workspace, size_t workspace_bytes, void* stream) {
-  return quantize_one(x, rows, cols, mode, q, nullptr, scales, workspace, workspace_bytes, stream);
+loka_status loka_quantize_fp8(const void* x, int64_t rows, int64_t cols, int64_t ld, int32_t mode, void* q,
+                              void* scales, void* workspace, size_t workspace_bytes, void* stream) {
+  return quantize_one(x, rows, cols, ld, mode, q, nullptr, scales, workspace, workspace_bytes, stream);
 }
 
-loka_status loka_quantize_fp8_block32(const void* x, int64_t rows, int64_t cols, void* q, void* q_t, void* scales,
-                                      void* stream) {
-  return quantize_one(x, rows, cols, LOKA_SCALE_BLOCK32, q, q_t, scales, nullptr, 0, stream);
+loka_status loka_quantize_fp8_block32(const void* x, int64_t rows, int64_t cols, int64_t ld, void* q, void* q_t,
+                                      void* scales, void* stream) {
+  return quantize_one(x, rows, cols, ld, LOKA_SCALE_BLOCK32, q, q_t, scales, nullptr, 0, stream);
 }
 
 size_t loka_fp8_linear_norm_workspace_size(const loka_linear_desc* descs, int32_t num_groups) {
@@ -546,6 +553,9 @@ loka_status loka_fp8_linear_norm_static(const loka_linear_desc* descs, int32_t n
                 "this call needs %zu bytes of scratch; the built-in scratch of loka_fp8_linear_norm_static holds %zu "
                 "bytes (use loka_fp8_linear_norm with a caller workspace)",
                 need, kStaticScratchBytes);
+  // the architecture check first, as in every other entry point
+  DeviceInfo* dev = nullptr;
+  if ((s = device_info(&dev)) != LOKA_OK) return s;
   void* scratch = nullptr;
   if ((s = static_scratch(&scratch)) != LOKA_OK) return s;
   return loka_fp8_linear_norm(descs, num_groups, scratch, kStaticScratchBytes, stream);
@@ -595,13 +605,28 @@ loka_status loka_quant_error(const loka_linear_desc* desc, void* workspace, size
   if (e != cudaSuccess) return cuda_fail(e, "reference GEMM launch");
   e = launch_error_reduce(out, ref, desc->M * desc->N, acc, dev->sms, st);
   if (e != cudaSuccess) return cuda_fail(e, "probe reduction launch");
-  double host[5];
+  // the same two outputs after the layer's normalization (and activation):
+  // both GEMMs again with the norm in the epilogue and fp32 output, into the
+  // same buffers (stream order), reduced into the second accumulator block
+  const bool post = desc->norm != kNormNone || desc->act != kActNone;
+  if (post) {
+    if ((s = build_gemm(desc, 1, slots, ws, bf16, OutKind::kF32, y_out, desc->norm, dev, &p)) != LOKA_OK) return s;
+    e = launch_gemm_norm(p, static_cast<int>(desc->N), operand_kind(desc->mode), OutKind::kF32, dev->sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "probe post-norm GEMM launch");
+    if ((s = build_gemm(desc, 1, slots, ws, true, OutKind::kF32, y_ref, desc->norm, dev, &p)) != LOKA_OK) return s;
+    e = launch_gemm_norm(p, static_cast<int>(desc->N), OperandKind::kBf16, OutKind::kF32, dev->sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "reference post-norm GEMM launch");
+    e = launch_error_reduce(out, ref, desc->M * desc->N, acc + 8, dev->sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "probe post-norm reduction launch");
+  }
+  double host[13];
   e = cudaMemcpyAsync(host, acc, sizeof(host), cudaMemcpyDeviceToHost, st);
   if (e != cudaSuccess) return cuda_fail(e, "reading probe statistics");
   if ((s = loka_device_status(stream)) != LOKA_OK) return s;
   stats->mere = host[1] > 0 ? host[0] / host[1] : 0.0;
   stats->rel_err_fro = host[3] > 0 ? std::sqrt(host[2]) / std::sqrt(host[3]) : 0.0;
   stats->max_abs = host[4];
+  stats->max_abs_post_norm = post ? host[12] : host[4];
   stats->zero_ref_count = desc->M * desc->N - static_cast<int64_t>(host[1]);
   return LOKA_OK;
 }
@@ -759,6 +784,21 @@ loka_status loka_probe_stats_update(loka_input_stats* stats, const void* x, int6
                          stats->scatter, stats->n, B, dev->sms, st);
   if (e != cudaSuccess) return cuda_fail(e, "statistics merge launch");
   stats->n += B;
+  return LOKA_OK;
+}
+
+loka_status loka_probe_covariance(const loka_input_stats* stats, double* cov, void* stream) {
+  if (stats == nullptr || cov == nullptr) return fail(LOKA_ERR_INVALID_ARG, "stats and cov must not be NULL");
+  if (stats->K <= 0) return fail(LOKA_ERR_INVALID_ARG, "K = %lld", static_cast<long long>(stats->K));
+  if (stats->n < 2) return fail(LOKA_ERR_INVALID_ARG, "n = %lld: a covariance needs at least two rows",
+                                static_cast<long long>(stats->n));
+  if (stats->scatter == nullptr) return fail(LOKA_ERR_INVALID_ARG, "scatter is NULL");
+  if ((reinterpret_cast<uintptr_t>(cov) & 7u) != 0) return fail(LOKA_ERR_INVALID_ARG, "cov must be 8-byte aligned");
+  DeviceInfo* dev = nullptr;
+  loka_status s = device_info(&dev);
+  if (s != LOKA_OK) return s;
+  cudaError_t e = launch_covariance(stats->scatter, stats->K, stats->n, cov, dev->sms, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "covariance launch");
   return LOKA_OK;
 }
 

@@ -517,10 +517,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
         // the abort decision the same for all of the team's warps
         if (named_bar_or(team_bar, 256, *abort_flag != 0)) break;
         const bool normed = norm != kNormNone;
+        // LayerNorm is unchanged when one constant is added to every column
+        // of a row, so the bias enters centred on its own mean: a bias far
+        // above the row's spread (LoKA section III-B: LayerNorm's mean
+        // cancellation) then never reaches the fp32 statistics or the
+        // output's v - mean.  Every warp of every CTA sums the full row in
+        // the same order (lane-strided, then a butterfly, whose partners add
+        // the same two values), so all columns subtract the same number.
+        float mu_b = 0.0f;
+        if (norm == kNormLayer && G.bias != nullptr) {
+          float s = 0.0f;
+          for (int n = lane; n < ng; n += 32) s += bf16_to_f(G.bias[n]);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+          mu_b = s / static_cast<float>(ng);
+        }
         for (int n = (ew & 7) * 32 + lane; n < N; n += 256) {
           const int gn = col0 + n;
           vec_sw[n] = (G.sw != nullptr && G.sw_per_row) ? G.sw[gn] : 1.0f;
-          vec_b[n] = G.bias == nullptr ? 0.0f : bf16_to_f(G.bias[gn]);
+          vec_b[n] = G.bias == nullptr ? 0.0f : bf16_to_f(G.bias[gn]) - mu_b;
           vec_g[n] = (G.gamma == nullptr || !normed) ? 1.0f : bf16_to_f(G.gamma[gn]);
           vec_be[n] = (G.beta == nullptr || norm != kNormLayer) ? 0.0f : bf16_to_f(G.beta[gn]);
         }

@@ -37,6 +37,7 @@ struct QuantJob {
   uint8_t* q_t;          // 32x32 blocks only, optional: the codes transposed, [cols, rows]
   int64_t rows;
   int64_t cols;
+  int64_t ld;            // elements between the starts of consecutive rows of x (>= cols, % 8 == 0)
   int64_t row_begin;     // first row of this job in the launch's joint row space (32x32 blocks:
                          // first unit of 32 rows x 256 columns, set by launch_quantize)
 };
@@ -144,6 +145,8 @@ cudaError_t launch_stats_merge(const float* colpart, int64_t tiles, const float*
                                double* colwork /* 35 K fp64 */, double* mu, double* S, int64_t n_old, int64_t nb,
                                int sms, cudaStream_t stream);
 cudaError_t launch_normals(uint64_t seed, int64_t count, void* z, int sms, cudaStream_t stream);
+// cov (fp64 [K, K]) = S / (n - 1)
+cudaError_t launch_covariance(const double* S, int64_t K, int64_t n, double* cov, int sms, cudaStream_t stream);
 // Cholesky factor of S / (n - 1) + eps I (one block, fp32; A: K x K fp32
 // scratch); L and mu_out bf16; *status = 1 if not positive definite.
 cudaError_t launch_cholesky(const double* S, const double* mu, int64_t K, int64_t n, double eps_rel, float* A,

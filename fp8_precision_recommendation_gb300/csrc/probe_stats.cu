@@ -246,6 +246,15 @@ __global__ void __launch_bounds__(1024) cholesky_kernel(const double* __restrict
   for (int64_t i = t; i < K; i += nt) mu_out[i] = static_cast<uint16_t>(pack_bf16x2(static_cast<float>(mu[i]), 0.0f) & 0xFFFFu);
 }
 
+// cov = S / (n - 1): the unbiased covariance of the merged rows (fp64,
+// one IEEE division per entry).
+__global__ void __launch_bounds__(256) covariance_kernel(const double* __restrict__ S, int64_t count, double n1,
+                                                         double* __restrict__ cov) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < count;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    cov[i] = S[i] / n1;
+}
+
 int grid_for(int64_t n, int sms) {
   int64_t b = (n + 255) / 256;
   if (b > static_cast<int64_t>(sms) * 8) b = static_cast<int64_t>(sms) * 8;
@@ -290,6 +299,11 @@ cudaError_t launch_cholesky(const double* S, const double* mu, int64_t K, int64_
   }
   cholesky_kernel<<<1, 1024, smem, stream>>>(S, mu, K, 1.0 / static_cast<double>(n - 1), eps_rel, A,
                                              static_cast<uint16_t*>(L), static_cast<uint16_t*>(mu_out), status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_covariance(const double* S, int64_t K, int64_t n, double* cov, int sms, cudaStream_t stream) {
+  covariance_kernel<<<grid_for(K * K, sms), 256, 0, stream>>>(S, K * K, static_cast<double>(n - 1), cov);
   return cudaGetLastError();
 }
 

@@ -39,7 +39,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const __grid_constant__
     const QuantJob& job = jobs.j[find_job(jobs, gr)];
     const int64_t row = gr - job.row_begin;
     const int nvec = static_cast<int>(job.cols >> 3);
-    const uint4* src = reinterpret_cast<const uint4*>(job.x) + row * nvec;
+    const uint4* src = reinterpret_cast<const uint4*>(job.x) + row * (job.ld >> 3);
     uint2* dst = reinterpret_cast<uint2*>(job.q + row * job.cols);
     uint4 v[V];
 #pragma unroll
@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(256) quant_rows_half_kernel(const __grid_const
     const QuantJob& job = jobs.j[find_job(jobs, live ? gr : base)];
     const int64_t row = (live ? gr : base) - job.row_begin;
     const int nvec = static_cast<int>(job.cols >> 3);
-    const uint4* src = reinterpret_cast<const uint4*>(job.x) + row * nvec;
+    const uint4* src = reinterpret_cast<const uint4*>(job.x) + row * (job.ld >> 3);
     uint2* dst = reinterpret_cast<uint2*>(job.q + row * job.cols);
     uint4 v[2];
 #pragma unroll
@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(256) quant_rows_long_kernel(const __grid_const
     const QuantJob& job = jobs.j[find_job(jobs, gr)];
     const int64_t row = gr - job.row_begin;
     const int nvec = static_cast<int>(job.cols >> 3);
-    const uint4* src = reinterpret_cast<const uint4*>(job.x) + row * nvec;
+    const uint4* src = reinterpret_cast<const uint4*>(job.x) + row * (job.ld >> 3);
     uint2* dst = reinterpret_cast<uint2*>(job.q + row * job.cols);
     if (MODE == kScaleRow) {
       float m = 0.0f;
@@ -186,16 +186,25 @@ __global__ void __launch_bounds__(256) quant_rows_long_kernel(const __grid_const
   }
 }
 
+// Source vector of dense vector index i (8 elements) of a job whose rows may
+// be strided (ld > cols).
+__device__ __forceinline__ const uint4* strided_vec(const QuantJob& job, int64_t i) {
+  const uint4* src = reinterpret_cast<const uint4*>(job.x);
+  if (job.ld == job.cols) return src + i;
+  const int64_t cv = job.cols >> 3;
+  const int64_t r = i / cv;
+  return src + r * (job.ld >> 3) + (i - r * cv);
+}
+
 // Tensorwise pass 1: amax of each job into its slot (fp32 bits; the slot must
 // be zero beforehand).  blockIdx.y = job.
 __global__ void __launch_bounds__(256) amax_tensor_kernel(const __grid_constant__ QuantJobs jobs) {
   const QuantJob& job = jobs.j[blockIdx.y];
   const int64_t nvec = (job.rows * job.cols) >> 3;
-  const uint4* src = reinterpret_cast<const uint4*>(job.x);
   float m = 0.0f;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-    m = abs_max8(__ldg(src + i), m);
+    m = abs_max8(__ldg(strided_vec(job, i)), m);
   m = warp_max(m);
   __shared__ float red[8];
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
@@ -217,11 +226,10 @@ __global__ void __launch_bounds__(256) cast_tensor_kernel(const __grid_constant_
   row_scales(amax, inv, scale);
   if (blockIdx.x == 0 && threadIdx.x == 0) reinterpret_cast<float*>(job.scales)[0] = scale;
   const int64_t nvec = (job.rows * job.cols) >> 3;
-  const uint4* src = reinterpret_cast<const uint4*>(job.x);
   uint2* dst = reinterpret_cast<uint2*>(job.q);
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-    dst[i] = cast8(__ldcs(src + i), inv);
+    dst[i] = cast8(__ldcs(strided_vec(job, i)), inv);
 }
 
 __global__ void __launch_bounds__(256) sf_permute_kernel(const uint8_t* __restrict__ logical, uint8_t* __restrict__ tc,
@@ -258,7 +266,7 @@ __global__ void __launch_bounds__(256) quant_block32_kernel(const __grid_constan
     const int64_t segs = (job.cols + 255) >> 8;
     const int64_t rb = lu / segs, seg = lu - rb * segs;
     const int64_t r0 = rb * 32, c0 = seg * 256;
-    const int64_t nvec = job.cols >> 3;
+    const int64_t nvec = job.ld >> 3;   // source row stride in vectors
     const uint4* src = reinterpret_cast<const uint4*>(job.x);
     const bool col_ok = c0 + 8 * lane < job.cols;
     uint4 v[4];

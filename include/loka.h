@@ -97,8 +97,10 @@ loka_status loka_selftest_watchdog(uint64_t limit_ns, void* stream);
  *
  * Defined by LoKA section II-C (FP8 recipes: tensorwise, rowwise, blockwise)
  * and the MX block scaling the GEM Training page uses (scale factors along
- * K).  For x of shape [rows, cols] (bf16, device, row-major, 16-byte
- * aligned, cols % 32 == 0):
+ * K).  For x of shape [rows, cols] (bf16, device, 16-byte aligned,
+ * cols % 32 == 0) whose rows start ld elements apart (ld >= cols,
+ * ld % 8 == 0; ld == cols for a dense tensor, larger for a column slice of
+ * a wider one):
  *   LOKA_SCALE_TENSOR: amax = max|x|;  inv = fl32(448/amax); q = E4M3(fl32(x*inv));
  *                      scales[0] = fl32(amax/448)  (fp32, 1 element)
  *   LOKA_SCALE_ROW:    the same per row; scales is fp32 [rows]
@@ -107,7 +109,7 @@ loka_status loka_selftest_watchdog(uint64_t limit_ns, void* stream);
  *                      [rows, cols/32] holding e + 127
  * amax == 0 gives scale 1 (tensor/row) or E8M0 code 0 (MX).  E4M3 rounding
  * is to nearest, ties to even, saturating at +-448; NaN stays NaN.
- * q: uint8 [rows, cols] device (16-byte aligned).  workspace: device, at
+ * q: uint8 [rows, cols] device, dense (16-byte aligned).  workspace: device, at
  * least loka_quantize_fp8_workspace_size() bytes (0 for ROW and MX32; NULL
  * allowed then).  Asynchronous.
  * ---------------------------------------------------------------------- */
@@ -121,16 +123,17 @@ size_t loka_quantize_fp8_workspace_size(int64_t rows, int64_t cols, int32_t mode
  * q = E4M3(x * 2^-e); scales is uint8 E8M0 [ceil(rows/32), cols/32] holding
  * e + 127 (a ragged last block row covers the rows that exist).  The
  * quantization of the transpose is the transpose of the codes and scales. */
-loka_status loka_quantize_fp8(const void* x, int64_t rows, int64_t cols, int32_t mode,
+loka_status loka_quantize_fp8(const void* x, int64_t rows, int64_t cols, int64_t ld, int32_t mode,
                               void* q, void* scales, void* workspace, size_t workspace_bytes,
                               void* stream);
 
 /* loka_quantize_fp8_block32 -- LOKA_SCALE_BLOCK32 codes and scales, and in
  * the same pass, when q_t is not NULL, the codes of x transposed: q_t uint8
  * [cols, rows] (device, 16-byte aligned; rows % 32 == 0), equal to the codes
- * of quantizing x^T, whose scales are the transpose of scales.
+ * of quantizing x^T, whose scales are the transpose of scales.  ld is x's
+ * row stride in elements, as for loka_quantize_fp8.
  * Asynchronous; no workspace. */
-loka_status loka_quantize_fp8_block32(const void* x, int64_t rows, int64_t cols, void* q, void* q_t,
+loka_status loka_quantize_fp8_block32(const void* x, int64_t rows, int64_t cols, int64_t ld, void* q, void* q_t,
                                       void* scales, void* stream);
 
 /* ------------------------------------------------------------------------
@@ -244,11 +247,15 @@ loka_status loka_fp8_linear_norm_static(const loka_linear_desc* descs, int32_t n
  * high-precision one) and section III-A "Offline Error Quantification"
  * (loss = MERE(FP8(Wx+b), high-precision(Wx+b)) per layer, Fig. 5).
  * out = the FP8 linear output before normalization in fp32 (desc->mode);
- * ref = the bf16-input linear with fp32 accumulation.  desc->norm, gamma,
- * beta and y are ignored.  Reports, over all M*N elements:
+ * ref = the bf16-input linear with fp32 accumulation.  desc->y is ignored.
+ * Reports, over all M*N elements:
  *   mere        mean of |out-ref|/|ref| over elements with ref != 0
  *   rel_err_fro ||out-ref||_F / ||ref||_F
  *   max_abs     max |out-ref|
+ *   max_abs_post_norm  max |Norm(out) - Norm(ref)| with the layer's norm,
+ *               norm_block, eps, gamma, beta and act (fp32 outputs before
+ *               the bf16 rounding); equals max_abs when the layer has
+ *               neither a norm nor an activation
  *   zero_ref_count, count
  * workspace: loka_quant_error_workspace_size() bytes.  SYNCHRONIZES the
  * stream; `stats` is a host pointer.
@@ -257,6 +264,7 @@ typedef struct loka_error_stats {
   double mere;
   double rel_err_fro;
   double max_abs;
+  double max_abs_post_norm;
   int64_t zero_ref_count;
   int64_t count;
 } loka_error_stats;
@@ -343,6 +351,11 @@ typedef struct loka_input_stats {
 } loka_input_stats;
 
 size_t loka_probe_stats_workspace_size(int64_t B, int64_t K);
+/* loka_probe_covariance: cov (fp64 [K, K], device, caller-owned) =
+ * scatter / (n - 1), the unbiased covariance of the rows merged so far
+ * (section III-A 1: the covariance the sampler draws from).  n >= 2.
+ * Asynchronous. */
+loka_status loka_probe_covariance(const loka_input_stats* stats, double* cov, void* stream);
 loka_status loka_probe_stats_update(loka_input_stats* stats, const void* x, int64_t B, void* workspace,
                                     size_t workspace_bytes, void* stream);
 /* loka_probe_cholesky: L (bf16 [K, K] row-major, lower, zero above the

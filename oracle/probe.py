@@ -14,6 +14,10 @@ about zero references):
     of excluded zero references is reported beside it.
   * normwise relative error = ||out - ref||_F / ||ref||_F.
   * max_abs = max |out - ref|.
+  * max_abs_post_norm = max |Norm(out) - Norm(ref)|: the same two outputs
+    after the layer's normalization (and activation, when it has one), the
+    quantity the "max-abs after normalization" acceptance bound speaks of.
+    Without a normalization or activation it equals max_abs.
   * The reference is the same layer on the bf16 inputs with exact (here
     float64) accumulation; the pages use TF32.
 """
@@ -21,7 +25,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .linear import prenorm, SCALE_BF16
+from .linear import ACT_HARDSWISH, ACT_NONE, NORM_NONE, SCALE_BF16, hardswish, normalize, prenorm
 
 
 def mere(out: np.ndarray, ref: np.ndarray):
@@ -53,8 +57,20 @@ def error_stats(out: np.ndarray, ref: np.ndarray) -> dict:
             "zero_ref_count": zeros, "count": int(np.size(ref))}
 
 
-def quant_error(x, w, bias, mode: int) -> dict:
-    """Probe of one layer: FP8 pre-norm output vs the high-precision one."""
+def quant_error(x, w, bias, mode: int, norm: int = NORM_NONE, gamma=None, beta=None, eps: float = 0.0,
+                norm_block: int = 256, act: int = ACT_NONE) -> dict:
+    """Probe of one layer: FP8 pre-norm output vs the high-precision one,
+    plus the largest difference of the two after the layer's normalization."""
     out, _ = prenorm(x, w, bias, mode)
     ref, _ = prenorm(x, w, bias, SCALE_BF16)
-    return error_stats(out, ref)
+    st = error_stats(out, ref)
+    if norm == NORM_NONE and act == ACT_NONE:
+        st["max_abs_post_norm"] = st["max_abs"]
+        return st
+
+    def post(v):
+        y = normalize(v, norm, gamma, beta, eps, norm_block)
+        return hardswish(y) if act == ACT_HARDSWISH else y
+
+    st["max_abs_post_norm"] = max_abs(post(out), post(ref))
+    return st

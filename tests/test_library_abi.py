@@ -183,22 +183,24 @@ def test_linear_norm_workspace_is_required_and_sized(cpu_lib):
 
 def test_quantize_rejects_bad_arguments_on_host(cpu_lib):
     f = cpu_lib.loka_quantize_fp8
-    assert f(1 << 20, 4, 48, 1, 1 << 20, 1 << 20, None, 0, None) == _loka.LOKA_ERR_INVALID_ARG   # cols % 32
-    assert f(1 << 20, 4, 64, 5, 1 << 20, 1 << 20, None, 0, None) == _loka.LOKA_ERR_INVALID_ARG   # mode
-    assert f(None, 4, 64, 1, 1 << 20, 1 << 20, None, 0, None) == _loka.LOKA_ERR_INVALID_ARG
-    assert f((1 << 20) + 2, 4, 64, 1, 1 << 20, 1 << 20, None, 0, None) == _loka.LOKA_ERR_INVALID_ARG
-    assert f(1 << 20, 4, 64, 0, 1 << 20, 1 << 20, None, 0, None) == _loka.LOKA_ERR_WORKSPACE
+    assert f(1 << 20, 4, 48, 48, 1, 1 << 20, 1 << 20, None, 0, None) == _loka.LOKA_ERR_INVALID_ARG   # cols % 32
+    assert f(1 << 20, 4, 64, 64, 5, 1 << 20, 1 << 20, None, 0, None) == _loka.LOKA_ERR_INVALID_ARG   # mode
+    assert f(None, 4, 64, 64, 1, 1 << 20, 1 << 20, None, 0, None) == _loka.LOKA_ERR_INVALID_ARG
+    assert f((1 << 20) + 2, 4, 64, 64, 1, 1 << 20, 1 << 20, None, 0, None) == _loka.LOKA_ERR_INVALID_ARG
+    assert f(1 << 20, 4, 64, 32, 1, 1 << 20, 1 << 20, None, 0, None) == _loka.LOKA_ERR_INVALID_ARG   # ld < cols
+    assert f(1 << 20, 4, 64, 68, 1, 1 << 20, 1 << 20, None, 0, None) == _loka.LOKA_ERR_INVALID_ARG   # ld % 8
+    assert f(1 << 20, 4, 64, 64, 0, 1 << 20, 1 << 20, None, 0, None) == _loka.LOKA_ERR_WORKSPACE
     assert _loka.loka_quantize_fp8_workspace_size(4, 64, 0) > 0
     assert _loka.loka_quantize_fp8_workspace_size(4, 64, 1) == 0
 
 
 def test_block32_quantizer_rejects_bad_arguments_on_host(cpu_lib):
     f = cpu_lib.loka_quantize_fp8_block32
-    assert f(1 << 20, 48, 64, 1 << 20, 1 << 21, 1 << 22, None) == _loka.LOKA_ERR_INVALID_ARG   # q_t: rows % 32
-    assert f(1 << 20, 64, 48, 1 << 20, None, 1 << 22, None) == _loka.LOKA_ERR_INVALID_ARG      # cols % 32
-    assert f(1 << 20, 64, 64, (1 << 20) + 8, None, 1 << 22, None) == _loka.LOKA_ERR_INVALID_ARG  # q alignment
-    assert f(1 << 20, 64, 64, 1 << 20, (1 << 21) + 8, 1 << 22, None) == _loka.LOKA_ERR_INVALID_ARG
-    assert f(1 << 20, 0, 64, 1 << 20, None, 1 << 22, None) == _loka.LOKA_OK                    # empty
+    assert f(1 << 20, 48, 64, 64, 1 << 20, 1 << 21, 1 << 22, None) == _loka.LOKA_ERR_INVALID_ARG   # q_t: rows % 32
+    assert f(1 << 20, 64, 48, 48, 1 << 20, None, 1 << 22, None) == _loka.LOKA_ERR_INVALID_ARG      # cols % 32
+    assert f(1 << 20, 64, 64, 64, (1 << 20) + 8, None, 1 << 22, None) == _loka.LOKA_ERR_INVALID_ARG  # q alignment
+    assert f(1 << 20, 64, 64, 64, 1 << 20, (1 << 21) + 8, 1 << 22, None) == _loka.LOKA_ERR_INVALID_ARG
+    assert f(1 << 20, 0, 64, 64, 1 << 20, None, 1 << 22, None) == _loka.LOKA_OK                    # empty
 
 
 def test_probe_statistics_reject_bad_arguments_on_host(cpu_lib):
@@ -216,6 +218,19 @@ def test_probe_statistics_reject_bad_arguments_on_host(cpu_lib):
     smp = cpu_lib.loka_probe_sample_inputs
     assert smp(1 << 20, 1 << 21, 100, 96, 1, 1 << 22, None, 0, None) == _loka.LOKA_ERR_UNSUPPORTED
     assert smp(1 << 20, 1 << 21, 100, 256, 1, 1 << 22, None, 0, None) == _loka.LOKA_ERR_WORKSPACE
+
+
+def test_probe_covariance_rejects_bad_arguments_on_host(cpu_lib):
+    st = _loka.InputStats()
+    st.n, st.K, st.mu, st.scatter = 1, 64, 1 << 20, 1 << 21
+    cov = cpu_lib.loka_probe_covariance
+    assert cov(ctypes.byref(st), 1 << 22, None) == _loka.LOKA_ERR_INVALID_ARG          # n < 2
+    st.n = 10
+    assert cov(None, 1 << 22, None) == _loka.LOKA_ERR_INVALID_ARG
+    assert cov(ctypes.byref(st), None, None) == _loka.LOKA_ERR_INVALID_ARG
+    assert cov(ctypes.byref(st), (1 << 22) + 4, None) == _loka.LOKA_ERR_INVALID_ARG    # alignment
+    st.scatter = None
+    assert cov(ctypes.byref(st), 1 << 22, None) == _loka.LOKA_ERR_INVALID_ARG
 
 
 def _c_table(rows):

@@ -561,6 +561,32 @@ def test_quant_error_bf16_is_zero_and_fp8_is_small():
     assert s["mere"] == 0.0 and s["rel_err_fro"] == 0.0
     s = P.quant_error(inp.x, inp.w, None, W.SCALE_ROW)
     assert 0.0 < s["rel_err_fro"] < 0.1
+    assert s["max_abs_post_norm"] == s["max_abs"]      # no norm, no activation
+
+
+def test_quant_error_post_norm_against_torch_layer_norm():
+    # the post-norm error is the largest difference of the two outputs after
+    # the layer's LayerNorm: recomputed here from the pre-norm outputs with
+    # torch's own layer_norm (an independent library routine, float64)
+    import torch
+    inp = W.make_layer(40, 128, 64, mode=W.SCALE_ROW, norm=W.NORM_LAYER, seed=23, bias_var=0.02,
+                       gamma_uniform=True)
+    beta = W.random_bf16((64,), seed=2, var=0.1)
+    s = P.quant_error(inp.x, inp.w, inp.bias, W.SCALE_ROW, norm=W.NORM_LAYER, gamma=inp.gamma, beta=beta, eps=1e-5)
+    out, _ = L.prenorm(inp.x, inp.w, inp.bias, W.SCALE_ROW)
+    ref, _ = L.prenorm(inp.x, inp.w, inp.bias, W.SCALE_BF16)
+    g = inp.gamma.to(torch.float64)
+    b = beta.to(torch.float64)
+    ln = lambda v: torch.nn.functional.layer_norm(torch.from_numpy(v), (64,), g, b, eps=1e-5).numpy()
+    want = float(np.max(np.abs(ln(out) - ln(ref))))
+    assert abs(s["max_abs_post_norm"] - want) <= 1e-12 * max(1.0, want)
+    assert s["max_abs_post_norm"] > 0.0
+    # RMSNorm with an activation after it: the same definition
+    s2 = P.quant_error(inp.x, inp.w, inp.bias, W.SCALE_ROW, norm=W.NORM_RMS, gamma=inp.gamma, eps=1e-6, act=1)
+    rms = lambda v: torch.nn.functional.rms_norm(torch.from_numpy(v), (64,), g, eps=1e-6)
+    hs = lambda v: torch.nn.functional.hardswish(rms(v)).numpy()
+    want2 = float(np.max(np.abs(hs(out) - hs(ref))))
+    assert abs(s2["max_abs_post_norm"] - want2) <= 1e-12 * max(1.0, want2)
 
 
 # --------------------------------------------------------------- dispatch
