@@ -347,14 +347,15 @@ loka_status build_gemm(const loka_linear_desc* d, int n, const std::vector<Opera
 
 // Quantizes every bf16 operand of the groups into the workspace (one launch
 // for X and W of all groups; tensorwise scaling takes an amax launch first).
+// w_only: the weights alone (the GEMM quantizes X itself).
 loka_status quantize_operands(const loka_linear_desc* d, int n, const std::vector<OperandSlots>& slots, uint8_t* ws,
-                              DeviceInfo* dev, cudaStream_t stream) {
+                              DeviceInfo* dev, cudaStream_t stream, bool w_only = false) {
   QuantJobs jobs;
   std::memset(&jobs, 0, sizeof(jobs));
   int64_t rows = 0;
   for (int i = 0; i < n; ++i) {
     const loka_linear_desc& g = d[i];
-    if (!g.x_is_fp8 && g.M > 0) {
+    if (!w_only && !g.x_is_fp8 && g.M > 0) {
       QuantJob& j = jobs.j[jobs.n++];
       j.x = g.x;
       j.q = ws + slots[i].xq;
@@ -512,6 +513,25 @@ loka_status loka_fp8_linear_norm(const loka_linear_desc* descs, int32_t num_grou
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const bool bf16 = descs[0].mode == kBf16;
+  const OutKind out = output_reference(descs, num_groups).y_q != nullptr ? OutKind::kQuant : OutKind::kBf16;
+  // Per-row scaling of bf16 X with a whole output row per CTA: the GEMM
+  // quantizes X itself (LoKA section III-B case 1), so X is read from HBM
+  // once and its codes never leave the chip.  Only W is quantized before.
+  if (descs[0].mode == kScaleRow && !descs[0].x_is_fp8 &&
+      gemm_qx_supported(static_cast<int>(descs[0].N), static_cast<int>(descs[0].K), descs[0].norm, out)) {
+    const bool w_launch = !descs[0].w_is_fp8;
+    if (w_launch && (s = quantize_operands(descs, num_groups, slots, ws, dev, st, true)) != LOKA_OK) return s;
+    static thread_local GemmParams pq;
+    if ((s = build_gemm(descs, num_groups, slots, ws, false, out, nullptr, descs[0].norm, dev, &pq)) != LOKA_OK) return s;
+    for (int i = 0; i < num_groups; ++i) pq.g[i].xbf = static_cast<const uint16_t*>(descs[i].x);
+    // X was complete before this call's W quantizer started (a normal
+    // launch), so the GEMM may read X before waiting for that launch
+    pq.x_ready = w_launch ? 1 : 0;
+    pq.w_ready = 0;
+    cudaError_t e = launch_gemm_norm(pq, static_cast<int>(descs[0].N), OperandKind::kE4M3Qx, out, dev->sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
+    return LOKA_OK;
+  }
   if (!bf16 && (!descs[0].x_is_fp8 || !descs[0].w_is_fp8)) {
     if ((s = quantize_operands(descs, num_groups, slots, ws, dev, st)) != LOKA_OK) return s;
   }
@@ -531,7 +551,6 @@ loka_status loka_fp8_linear_norm(const loka_linear_desc* descs, int32_t num_grou
     }
   }
   static thread_local GemmParams p;
-  const OutKind out = output_reference(descs, num_groups).y_q != nullptr ? OutKind::kQuant : OutKind::kBf16;
   if ((s = build_gemm(descs, num_groups, slots, ws, bf16, out, nullptr, descs[0].norm, dev, &p)) != LOKA_OK) return s;
   // Caller-quantized W may load before the GEMM waits for the launch that
   // precedes it only when that launch is this call's own activation

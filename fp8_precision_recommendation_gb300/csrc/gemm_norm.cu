@@ -11,6 +11,11 @@ bool gemm_supported(int N, int K, OperandKind op) {
   return plan_for(local, K, op == OperandKind::kBf16 ? 2 : 1, op == OperandKind::kMxE4M3, cl).stages > 0;
 }
 
+bool gemm_qx_supported(int N, int K, int norm, OutKind out) {
+  const GemmRoute r = gemm_route(N, norm);
+  return out == OutKind::kBf16 && r.cl == 1 && r.slices == 1 && plan_qx(r.local, K).stages > 0;
+}
+
 GemmRoute gemm_route(int N, int norm) {
   const bool no_row_stat = norm == kNormNone || norm == kNormBlockRms;
   // Rows wider than one CTA whose epilogue needs no row statistic (no norm,
@@ -37,6 +42,7 @@ cudaError_t launch_gemm_norm(GemmParams& p, int N, OperandKind op, OutKind out, 
     case OperandKind::kE4M3: return launch_gemm_e4m3(p, N, out, sms, stream);
     case OperandKind::kBf16: return launch_gemm_bf16(p, N, out, sms, stream);
     case OperandKind::kMxE4M3: return launch_gemm_mx(p, N, out, sms, stream);
+    case OperandKind::kE4M3Qx: return out == OutKind::kBf16 ? launch_gemm_qx(p, N, sms, stream) : cudaErrorInvalidValue;
   }
   return cudaErrorInvalidValue;
 }

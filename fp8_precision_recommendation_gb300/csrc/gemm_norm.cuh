@@ -68,14 +68,34 @@ constexpr int kMaxWSlices = 16;          // resident W: 128 KB / (64 rows x 128 
 constexpr size_t kSmemLimit = 227 * 1024;
 constexpr size_t kResidentWLimit = 128 * 1024;
 
+// In-kernel activation quantization (OperandKind::kE4M3Qx): 28 warps.
+//   warp 0        bulk copies of bf16 X rows into a staging ring (and W)
+//   warp 1        MMA;  warps 2-3 idle (they fill warpgroup 0)
+//   warps 4-11    quantizers: a row per warp at a time, staging -> A tile
+//   warps 12-27   epilogue, as in the 576-thread kernel
+// Registers: launched at 72 per thread (28 warps, 7 per sub-partition), then
+// warpgroup 0 and the quantizers drop to 40 and the epilogue rises to 96:
+// per sub-partition 40 + 2 x 40 + 4 x 96 = 504 of the 512 register slots.
+constexpr int kQxThreads = 896;
+constexpr int kQxWarps = 8;              // quantizer warps
+constexpr int kQxFirstWarp = 4;
+constexpr int kQxEpiWarp = 12;           // first epilogue warp
+constexpr uint32_t kQxSlotBytes = 8192;  // staging slot: 8 KB of consecutive bf16 rows
+constexpr int kQxMaxK = 512;             // row of at most 2 x 16 bytes per lane
+
 // Shared-memory carve-up (all offsets from a 1024-byte-aligned base):
-//   ring     stages x (A slice [| B slice])
+//   ring     stages x (A slice [| B slice]), or (in-kernel quantization)
+//            stages x 8 KB staging slots of bf16 X rows
+//   a        in-kernel quantization: a_bufs x 128 x K E4M3 A tiles (128B
+//            swizzled K slices, the layout TMA would write)
 //   w        resident W: K/KE slices of N rows x 128 bytes (when resident)
 //   vectors  2 teams x 4 x N fp32 (weight scale, bias, gamma, beta)
+//   sx       in-kernel quantization: 2 x 128 fp32 row scales (per
+//            accumulator buffer)
 //   stats    clusters: 2 x CL x 128 float2 row statistics of the CTAs
 //   barriers
 struct Layout {
-  uint32_t stage_bytes, ring, w, vec, stats, bars, total;
+  uint32_t stage_bytes, ring, a, w, vec, sx, stats, bars, total;
 };
 
 // MX scale blocks: 512 bytes per 128 rows per 128-element K slice.
@@ -83,20 +103,23 @@ constexpr uint32_t kSfBlock = 512;
 __host__ __device__ constexpr int sfb_blocks(int N) { return (N + 127) / 128; }
 
 __host__ __device__ inline Layout make_layout(int N, int K, int elem_bytes, bool resident, int stages, bool mx,
-                                              int cl = 1) {
+                                              int cl = 1, int a_bufs = 0) {
   Layout L;
   const uint32_t b_slice = static_cast<uint32_t>(N) * kSliceBytes;
   const uint32_t sfa = mx ? kSfBlock : 0u;
   const uint32_t sfb = mx ? kSfBlock * sfb_blocks(N) : 0u;
-  // stage: [A slice][B slice, streamed W][A scales][B scales, streamed W]
-  L.stage_bytes = kABytes + (resident ? 0u : b_slice) + sfa + (resident ? 0u : sfb);
+  // stage: [A slice][B slice, streamed W][A scales][B scales, streamed W];
+  // with in-kernel quantization (a_bufs > 0) a staging slot of bf16 rows
+  L.stage_bytes = a_bufs > 0 ? kQxSlotBytes : kABytes + (resident ? 0u : b_slice) + sfa + (resident ? 0u : sfb);
   L.ring = 0;
-  L.w = L.ring + static_cast<uint32_t>(stages) * L.stage_bytes;
+  L.a = L.ring + static_cast<uint32_t>(stages) * L.stage_bytes;
+  L.w = L.a + static_cast<uint32_t>(a_bufs) * kBM * static_cast<uint32_t>(K);
   const int nkb = K * elem_bytes / kSliceBytes;
   // resident W: [nkb B slices][nkb x B scale blocks]
   const uint32_t w_bytes = resident ? static_cast<uint32_t>(nkb) * (b_slice + sfb) : 0u;
   L.vec = L.w + w_bytes;
-  L.stats = L.vec + 2u * 4u * N * sizeof(float);
+  L.sx = L.vec + 2u * 4u * N * sizeof(float);
+  L.stats = L.sx + (a_bufs > 0 ? 2u * kBM * sizeof(float) : 0u);
   // [2][cluster][128] row statistics of the cluster's CTAs (written
   // remotely, double-buffered by tile parity)
   L.bars = L.stats + (cl > 1 ? 2u * cl * kBM * sizeof(float2) : 0u);
@@ -120,8 +143,13 @@ __device__ __forceinline__ float2 dup2(float a) { return make_float2(a, a); }
 // through distributed shared memory, so a row wider than one CTA's tensor
 // memory is still normalized in the epilogue).
 template <int N, int CL, int OP, int OUT, bool RESIDENT>
-__global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ? kQxThreads : kThreads, 1)
+    gemm_norm_kernel(const __grid_constant__ GemmParams p) {
   static_assert(N <= 256, "one MMA per K step");
+  // in-kernel per-row quantization of bf16 X (one CTA per row, W resident)
+  constexpr bool kQx = OP == static_cast<int>(OperandKind::kE4M3Qx);
+  static_assert(!kQx || (CL == 1 && RESIDENT), "in-kernel quantization keeps W resident and rows within a CTA");
+  constexpr int EPI0 = kQx ? kQxEpiWarp : 2;       // first epilogue warp
   constexpr int NG = N * CL;                        // columns of the whole output row
   constexpr int SF_COLS_MAX = OP == static_cast<int>(OperandKind::kMxE4M3) ? kMaxStages * (4 + 4 * sfb_blocks(N)) : 0;
   constexpr int NBUF = (2 * N + SF_COLS_MAX <= kTmemCols) ? 2 : 1;
@@ -141,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
 
   const int stages = p.stages;
   const int num_kb = p.K / KE;
-  const Layout L = make_layout(N, p.K, EB, RESIDENT, stages, kMx, CL);
+  const Layout L = make_layout(N, p.K, EB, RESIDENT, stages, kMx, CL, kQx ? p.a_bufs : 0);
   // A tile's N-column slices go to the CTAs of a cluster (CL > 1, row
   // statistics exchanged), or, when no statistic spans the row (CL == 1,
   // p.slices > 1), to p.slices independent consecutive CTAs.  rank = this
@@ -174,7 +202,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
   uint64_t* cl_bar = w_free + 1;                                    // [2] cluster statistics arrivals
   uint64_t* cl_free = cl_bar + 2;                                   // [2] cluster statistics buffers read
   uint64_t* w_full = cl_free + 2;                                   // [16] resident W, one per K slice
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(w_full + kMaxWSlices);
+  // in-kernel quantization: A tiles written (quantizers) and read (MMA), row
+  // scales written (quantizers) and read (epilogue team of that buffer); the
+  // staging ring uses full / empty
+  uint64_t* afull = w_full + kMaxWSlices;                           // [2]
+  uint64_t* aempty = afull + 2;                                     // [2]
+  uint64_t* sxfull = aempty + 2;                                    // [2]
+  uint64_t* sxempty = sxfull + 2;                                   // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sxempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -183,7 +218,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), 1);
+      // a staging slot is released by every quantizer warp, an A stage by the MMA
+      mbar_init(smem_u32(&empty[s]), kQx ? kQxWarps : 1);
+    }
+    if (kQx) {
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(smem_u32(&afull[b]), kQxWarps);
+        mbar_init(smem_u32(&aempty[b]), 1);
+        mbar_init(smem_u32(&sxfull[b]), kQxWarps);
+        mbar_init(smem_u32(&sxempty[b]), 8);   // the eight warps of the epilogue team of buffer b
+      }
     }
     for (int b = 0; b < NBUF; ++b) {
       mbar_init(smem_u32(&tfull[b]), 1);
@@ -205,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
   if (warp == 0 && lane == 0) {
     for (int g = 0; g < p.num_groups; ++g) {
       if (p.g[g].M == 0) continue;   // no tiles, descriptors not encoded
-      tma_prefetch_desc(&p.g[g].tm_a);
+      if (!kQx) tma_prefetch_desc(&p.g[g].tm_a);   // in-kernel quantization reads X without a tensor map
       tma_prefetch_desc(&p.g[g].tm_b);
     }
   }
@@ -243,22 +287,99 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
     for (int kb = 0; kb < num_kb; ++kb) load_w_slice(g, kb);
   };
   int w_early_group = -1;
-  if (RESIDENT && p.w_ready && !misaligned && warp == 0 && lane == 0 && cid < p.total_tiles) {
+  if (!kQx && RESIDENT && p.w_ready && !misaligned && warp == 0 && lane == 0 && cid < p.total_tiles) {
     w_early_group = group_of(p, cid);
     load_w(w_early_group);
   }
   // everything above touches only this CTA's own state (and W when it was
   // ready); inputs written by the kernel before this one (the quantized
-  // operands) are read below
-  wait_prerequisite_grids();
+  // operands) are read below.  With in-kernel quantization the producer
+  // and the quantizers read only the caller's bf16 X until W is needed: when
+  // X was complete before the launch that precedes this one (p.x_ready) they
+  // start at once and the producer waits just before its first W load.
+  const bool x_early = kQx && p.x_ready && (warp == 0 || (warp >= kQxFirstWarp && warp < kQxEpiWarp));
+  if (!x_early) wait_prerequisite_grids();
   const uint32_t tmem_base = *tmem_slot;
   const Watchdog wd{abort_flag, p.status, p.wait_limit_ns};
+  // one lane waits, the whole warp follows its verdict
+  auto warp_wait = [&](uint32_t bar, uint32_t parity, bool cluster_scope) {
+    int okw = 1;
+    if (lane == 0)
+      okw = (cluster_scope ? wait_parity_cluster(wd, bar, parity, kErrClusterWait)
+                           : wait_parity(wd, bar, parity, kErrEpilogueWait)) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, okw, 0) != 0;
+  };
 
-  if (misaligned) {
-    // nothing to do: fall through to the teardown barriers
-  } else if (warp == 0) {
+  auto run_producer = [&]() {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    if (kQx && lane == 0) {
+      // bf16 X rows, 8 KB at a time (the rows are contiguous), into the
+      // staging ring; resident W once per group, issued once the ring is
+      // full (after waiting for the launch before, which wrote W).  A chunk
+      // past the last row still completes its slot, with zero bytes.
+      const int R = static_cast<int>(kQxSlotBytes) / (2 * p.K);   // rows per slot
+      const int chunks = kBM / R;
+      int slot = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, last_parity = 0;
+      int cur_group = -1, w_loads = 0;
+      bool waited = !p.x_ready, w_pending = false, ok = true;
+      uint32_t w_issued = 0;
+      auto issue_w = [&]() {
+        if (!waited) {
+          wait_prerequisite_grids();
+          waited = true;
+        }
+        load_w(cur_group);
+        w_issued = 0xFFFFFFFFu;
+        w_pending = false;
+      };
+      for (int tile = cid; ok && tile < p.total_tiles; tile += ncl) {
+        const int g = group_of(p, tile);
+        const GemmGroup& G = p.g[g];
+        if (g != cur_group) {
+          if (w_loads > 0 && !wait_parity(wd, smem_u32(w_free), (w_loads - 1) & 1, kErrProducerWait)) {
+            ok = false;
+            break;
+          }
+          ++w_loads;
+          cur_group = g;
+          w_pending = true;
+          w_issued = 0;
+        }
+        const int64_t m0 = static_cast<int64_t>(tile - G.tile_begin) * kBM;
+        for (int c = 0; c < chunks; ++c) {
+          if (w_pending && c == stages) issue_w();
+          if (!wait_parity(wd, smem_u32(&empty[slot]), phase ^ 1u, kErrProducerWait)) {
+            ok = false;
+            break;
+          }
+          const int64_t r0 = m0 + static_cast<int64_t>(c) * R;
+          const int64_t left = G.M - r0;
+          const int rows = left <= 0 ? 0 : (left >= R ? R : static_cast<int>(left));
+          const uint32_t bytes = static_cast<uint32_t>(rows) * static_cast<uint32_t>(p.K) * 2u;
+          const uint32_t fb = smem_u32(&full[slot]);
+          mbar_arrive_expect_tx(fb, bytes);
+          if (bytes > 0)
+            bulk_load_1d(smem_u32(ring + static_cast<size_t>(slot) * kQxSlotBytes), G.xbf + r0 * p.K, bytes, fb);
+          issued |= 1u << slot;
+          last_parity = (last_parity & ~(1u << slot)) | (phase << slot);
+          if (++slot == stages) {
+            slot = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok && w_pending) issue_w();
+      }
+      if (!ok) {
+        for (int s = 0; s < stages; ++s)
+          if (issued & (1u << s)) wait_parity_drain(wd, smem_u32(&full[s]), (last_parity >> s) & 1u);
+        if (w_loads > 0) {
+          for (int kb = 0; kb < num_kb; ++kb)
+            if (w_issued & (1u << kb)) wait_parity_drain(wd, smem_u32(&w_full[kb]), (w_loads - 1) & 1);
+        }
+      }
+    } else if (!kQx && lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, last_parity = 0;
@@ -330,7 +451,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
         }
       }
     }
-  } else if (warp == 1) {
+  };
+
+  auto run_mma = [&]() {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
       int stage = 0;
@@ -350,6 +473,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
         const int buf = NBUF == 2 ? (local & 1) : 0;
         const uint32_t use = NBUF == 2 ? (local >> 1) : local;
         if (!wait_parity(wd, smem_u32(&tempty[buf]), (use & 1u) ^ 1u, kErrMmaWait)) break;
+        // in-kernel quantization: the tile's A, written whole by the quantizers
+        const int abuf = kQx && p.a_bufs == 2 ? (local & 1) : 0;
+        const uint32_t ause = kQx && p.a_bufs == 2 ? static_cast<uint32_t>(local >> 1) : static_cast<uint32_t>(local);
+        if (kQx && !wait_parity(wd, smem_u32(&afull[abuf]), ause & 1u, kErrMmaWait)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * N);
         for (int kb = 0; kb < num_kb; ++kb) {
@@ -359,12 +486,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
             ok = false;
             break;
           }
-          if (!wait_parity(wd, smem_u32(&full[stage]), phase, kErrMmaWait)) {
+          if (!kQx && !wait_parity(wd, smem_u32(&full[stage]), phase, kErrMmaWait)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(ring + static_cast<size_t>(stage) * L.stage_bytes);
+          const uint32_t a_addr =
+              kQx ? smem_u32(smem + L.a + static_cast<size_t>(abuf) * kBM * p.K + static_cast<size_t>(kb) * kABytes)
+                  : smem_u32(ring + static_cast<size_t>(stage) * L.stage_bytes);
           const uint32_t b_addr = RESIDENT ? smem_u32(wres + kb * B_SLICE) : a_addr + kABytes;
           uint32_t sfa_tmem = 0, sfb_tmem = 0;
           if (kMx) {
@@ -394,20 +523,107 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
                 mma_f8f6f4(d_tmem + s * N_MMA, adesc, bdesc, IDESC, acc);
             }
           }
-          mma_commit(smem_u32(&empty[stage]));   // frees the slot once these MMAs finish
-          if (++stage == stages) {
-            stage = 0;
-            phase ^= 1u;
+          if (!kQx) {
+            mma_commit(smem_u32(&empty[stage]));   // frees the slot once these MMAs finish
+            if (++stage == stages) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
         }
         if (!ok) break;
+        if (kQx) mma_commit(smem_u32(&aempty[abuf]));   // the quantizers may refill this A tile
         mma_commit(smem_u32(&tfull[buf]));
       }
       // all MMAs issued by this thread complete before tensor memory is freed
       mma_commit(smem_u32(mma_done));
       wait_parity_drain(wd, smem_u32(mma_done), 0);
     }
-  } else {
+  };
+
+  [[maybe_unused]] auto run_quantizer = [&]() {
+    // ------------------------------------------------------- quantizers
+    // LoKA section III-B case 1: with a whole output row in one CTA, the
+    // activation quantization fuses into the GEMM.  Warp q takes row
+    // 8j + q of every staging slot (R = 8 KB / 2K rows per slot, j < R/8):
+    // lane l holds 16-byte vectors l and l + 32 of the row (all of it for
+    // K <= 512), so the row amax is one warp reduction; the scale is the
+    // standalone quantizer's (quant_math.cuh), and the codes go straight into
+    // the A tile in the 128B-swizzled layout the MMA descriptors describe:
+    // the 16-byte piece c of row r of a K slice sits at piece c ^ (r % 8).
+    const int qw = warp - kQxFirstWarp;
+    const int K = p.K;
+    const int kv = K >> 3;                                  // 16-byte vectors per row
+    const int R = static_cast<int>(kQxSlotBytes) / (2 * K);   // rows per staging slot
+    const int rpw = R / kQxWarps;                           // rows per warp per slot
+    const int chunks = kBM / R;
+    int slot = 0;
+    uint32_t phase = 0;
+    int local = 0;
+    for (int tile = cid; tile < p.total_tiles; tile += ncl, ++local) {
+      const int ab = p.a_bufs == 2 ? (local & 1) : 0;
+      const uint32_t ause = p.a_bufs == 2 ? static_cast<uint32_t>(local >> 1) : static_cast<uint32_t>(local);
+      const int sb = local & 1;   // row-scale buffer = the tile's accumulator buffer
+      if (!warp_wait(smem_u32(&aempty[ab]), (ause & 1u) ^ 1u, false)) break;
+      if (!warp_wait(smem_u32(&sxempty[sb]), ((local >> 1) & 1u) ^ 1u, false)) break;
+      const uint32_t abase = smem_u32(smem + L.a + static_cast<size_t>(ab) * kBM * K);
+      float* sxo = reinterpret_cast<float*>(smem + L.sx) + sb * kBM;
+      bool okq = true;
+      for (int c = 0; c < chunks; ++c) {
+        if (!warp_wait(smem_u32(&full[slot]), phase, false)) {
+          okq = false;
+          break;
+        }
+        const uint8_t* sbase = ring + static_cast<size_t>(slot) * kQxSlotBytes;
+        for (int j = 0; j < rpw; ++j) {
+          const int rs = j * kQxWarps + qw;                  // row within the slot
+          const int r = c * R + rs;                          // row within the tile
+          const uint4* src = reinterpret_cast<const uint4*>(sbase + static_cast<size_t>(rs) * K * 2);
+          uint4 v[kQxMaxK / 256];
+#pragma unroll
+          for (int i = 0; i < kQxMaxK / 256; ++i) {
+            const int idx = i * 32 + lane;
+            v[i] = idx < kv ? src[idx] : make_uint4(0, 0, 0, 0);
+          }
+          float m = 0.0f;
+#pragma unroll
+          for (int i = 0; i < kQxMaxK / 256; ++i) m = abs_max8(v[i], m);
+          m = warp_max(m);
+          float inv, sc;
+          row_scales(m, inv, sc);
+#pragma unroll
+          for (int i = 0; i < kQxMaxK / 256; ++i) {
+            const int idx = i * 32 + lane;
+            if (idx < kv) {
+              const uint32_t piece = static_cast<uint32_t>((idx & 15) >> 1) ^ static_cast<uint32_t>(r & 7);
+              const uint32_t a = abase + static_cast<uint32_t>(idx >> 4) * kABytes + static_cast<uint32_t>(r) * 128u +
+                                 piece * 16u + static_cast<uint32_t>(idx & 1) * 8u;
+              st_shared_v2(a, cast8(v[i], inv));
+            }
+          }
+          if (lane == 0) sxo[r] = sc;
+        }
+        // every lane's reads of the slot are done (the warp reduction used
+        // them all): release it to the producer
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
+        if (++slot == stages) {
+          slot = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!okq) break;
+      // the codes are read by the tensor core (async proxy)
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&afull[ab]));
+        mbar_arrive(smem_u32(&sxfull[sb]));
+      }
+    }
+  };
+
+  auto run_epilogue = [&]() {
     // ------------------------------------------------------------ epilogue
     // Sixteen warps in two teams of eight.  Team e takes the tiles whose
     // local index is e (mod 2), i.e. accumulator buffer e, so two tiles are
@@ -419,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
     // thread t rows t/4 + {0, 8} of the 16 and column pairs 8i + 2(t%4) of
     // each 32-column chunk; a per-column value read from shared memory serves
     // both rows.  Chunk reads are pipelined one ahead.
-    const int ew = warp - 2;                        // 0..15
+    const int ew = warp - EPI0;                     // 0..15
     const int team = NBUF == 2 ? (ew >> 3) : 0;
     const bool active = NBUF == 2 || ew < 8;
     const int tstep = NBUF == 2 ? 2 : 1;            // a team's tiles are tstep apart
@@ -494,21 +710,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
       else
         return __ffma2_rn(__fmul2_rn(acc2(r, k, i), sx2), sw, b);
     };
-    // one lane waits, the whole warp follows its verdict
-    auto warp_wait = [&](uint32_t bar, uint32_t parity, bool cluster_scope) {
-      int okw = 1;
-      if (lane == 0)
-        okw = (cluster_scope ? wait_parity_cluster(wd, bar, parity, kErrClusterWait)
-                             : wait_parity(wd, bar, parity, kErrEpilogueWait)) ? 1 : 0;
-      return __shfl_sync(0xffffffffu, okw, 0) != 0;
-    };
-
     int cur_group = -1;
     bool affine = false;
     float sx_next[2] = {1.f, 1.f};
     int local = team;
     int tile = cid + team * ncl;
-    if (active && tile < p.total_tiles) row_scales(tile, sx_next);
+    if (!kQx && active && tile < p.total_tiles) row_scales(tile, sx_next);
     for (; active && tile < p.total_tiles; tile += tstep * ncl, local += tstep) {
       const int g = group_of(p, tile);
       const GemmGroup& G = p.g[g];
@@ -543,7 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
         named_bar_sync(team_bar, 256);
         cur_group = g;
       }
-      const float sxr[2] = {sx_next[0], sx_next[1]};
+      float sxr[2] = {sx_next[0], sx_next[1]};
       const int m0 = (tile - G.tile_begin) * kBM;
       // output row addresses and validity, once per tile
       const int64_t Mg = G.M;
@@ -570,7 +777,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
       const uint32_t use = NBUF == 2 ? static_cast<uint32_t>(local >> 1) : static_cast<uint32_t>(local);
       if (!warp_wait(smem_u32(&tfull[buf]), use & 1u, false)) break;
       tc_fence_after();
-      if (tile + tstep * ncl < p.total_tiles) row_scales(tile + tstep * ncl, sx_next);
+      if constexpr (kQx) {
+        // the row scales the quantizers chose for this tile (buffer = the
+        // accumulator buffer); the weight scales are per column
+        if (!warp_wait(smem_u32(&sxfull[buf]), use & 1u, false)) break;
+        const float* sxs = reinterpret_cast<const float*>(smem + L.sx) + buf * kBM;
+        sxr[0] = sxs[rowk[0]];
+        sxr[1] = sxs[rowk[1]];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sxempty[buf]));
+      } else if (tile + tstep * ncl < p.total_tiles) {
+        row_scales(tile + tstep * ncl, sx_next);
+      }
       const uint32_t t_base = tmem_base + lane_addr + static_cast<uint32_t>(buf * N);
       const float2 sx2[2] = {dup2(sxr[0]), dup2(sxr[1])};
 
@@ -1002,6 +1220,38 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_norm_kernel(const __grid_con
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));
     }
+  };
+
+  if constexpr (kQx) {
+    // Each warpgroup takes its register share in its own branch and gives it
+    // back before the branches meet again, so the teardown below runs at
+    // the launch count (72) everywhere.
+    if (warp < kQxFirstWarp) {
+      regs_dec<40>();
+      if (!misaligned) {
+        if (warp == 0) run_producer();
+        else if (warp == 1) run_mma();
+      }
+      regs_inc<72>();
+    } else if (warp < kQxEpiWarp) {
+      regs_dec<40>();
+      if (!misaligned) run_quantizer();
+      regs_inc<72>();
+    } else {
+      regs_inc<96>();
+      if (!misaligned) run_epilogue();
+      regs_dec<72>();
+    }
+  } else {
+    if (misaligned) {
+      // nothing to do: fall through to the teardown barriers
+    } else if (warp == 0) {
+      run_producer();
+    } else if (warp == 1) {
+      run_mma();
+    } else {
+      run_epilogue();
+    }
   }
 
   tc_fence_before();
@@ -1064,7 +1314,7 @@ cudaError_t launch_one(const GemmParams& p, size_t smem, int sms, cudaStream_t s
   const int per_unit = CL > 1 ? CL : p.slices;
   int clusters = sms / per_unit;
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(OP == static_cast<int>(OperandKind::kE4M3Qx) ? kQxThreads : kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
@@ -1101,6 +1351,33 @@ cudaError_t launch_one(const GemmParams& p, size_t smem, int sms, cudaStream_t s
   e = cudaLaunchKernelEx(&cfg, kern, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+// In-kernel quantization: resident W, the A tiles (two when a double buffer
+// still leaves three staging slots, else one) and at least two 8 KB staging
+// slots; K = 128, 256 or 512, so that a slot holds a multiple of 8 whole
+// rows (one per quantizer warp) and a tile a whole number of slots.
+struct QxPlan {
+  int a_bufs, stages;
+  size_t smem;
+};
+
+inline QxPlan plan_qx(int N, int K) {
+  QxPlan q{0, 0, 0};
+  if ((K != 128 && K != 256 && K != 512) || K > kQxMaxK || N > 256) return q;
+  if (static_cast<size_t>(N) * K > kResidentWLimit) return q;
+  for (int a = 2; a >= 1; --a) {
+    const Layout base = make_layout(N, K, 1, true, 0, false, 1, a);
+    if (base.total + 2 * kQxSlotBytes > kSmemLimit) continue;
+    int st = static_cast<int>((kSmemLimit - base.total) / kQxSlotBytes);
+    if (st > kMaxStages) st = kMaxStages;
+    if (a == 2 && st < 3) continue;
+    q.a_bufs = a;
+    q.stages = st;
+    q.smem = base.total + static_cast<size_t>(st) * kQxSlotBytes;
+    return q;
+  }
+  return q;
 }
 
 template <int N, int CL, int OP, int OUT>
@@ -1174,5 +1451,6 @@ cudaError_t launch_gemm_qout_e4m3(GemmParams& p, int N, int sms, cudaStream_t st
 cudaError_t launch_gemm_qout_e4m3_wide(GemmParams& p, int N, int sms, cudaStream_t stream);
 cudaError_t launch_gemm_qout_mx(GemmParams& p, int N, int sms, cudaStream_t stream);
 cudaError_t launch_gemm_qout_mx_wide(GemmParams& p, int N, int sms, cudaStream_t stream);
+cudaError_t launch_gemm_qx(GemmParams& p, int N, int sms, cudaStream_t stream);
 
 }  // namespace loka

@@ -84,6 +84,7 @@ struct GemmGroup {
   const uint16_t* beta;  // bf16 [N] or null
   void* y;               // output (the fp32 output is stored directly); the quantized
                          // output kind may leave it null (no bf16 copy)
+  const uint16_t* xbf;   // in-kernel activation quantization: bf16 X [M, K] (dense rows)
   uint8_t* yq;           // quantized output kind: E4M3 codes [M, N] of the bf16 output
   void* yq_scales;       // and their scales: fp32 [M] (per row) or E8M0 [M, N/32] (MX)
   int64_t M;
@@ -103,6 +104,9 @@ struct GemmParams {
   int32_t stages;        // shared-memory ring depth (set by the launcher)
   int32_t w_ready;       // 1: W and its scales were complete before the launch that precedes
                          // this GEMM, so resident W may load before waiting for that launch
+  int32_t x_ready;       // 1: the bf16 X was complete before the launch that precedes this GEMM
+                         // (in-kernel quantization reads it before waiting for that launch)
+  int32_t a_bufs;        // in-kernel quantization: quantized A tiles in shared memory (1 or 2)
   int32_t yq_mode;       // quantized output kind: kScaleRow or kScaleMx32
   int32_t norm_block;    // BlockNorm block (32, 64, 128 or 256 columns)
   int32_t act;           // kActNone or kActHardSwish, after the normalization
@@ -111,7 +115,10 @@ struct GemmParams {
   uint64_t wait_limit_ns;
 };
 
-enum class OperandKind : int { kE4M3 = 0, kBf16 = 1, kMxE4M3 = 2 };
+// kE4M3Qx: A is the caller's bf16 X, quantized per row inside the GEMM (the
+// codes go straight into the shared-memory A tile); B is E4M3 W with per-row
+// scales.
+enum class OperandKind : int { kE4M3 = 0, kBf16 = 1, kMxE4M3 = 2, kE4M3Qx = 3 };
 // kQuant: E4M3 codes and scales of the bf16 output (plus the bf16 output when
 // its pointer is set)
 enum class OutKind : int { kBf16 = 0, kF32 = 1, kQuant = 2 };
@@ -131,6 +138,9 @@ cudaError_t launch_gemm_norm(GemmParams& p, int N, OperandKind op, OutKind out, 
 
 // Whether the kernel has a shared-memory plan for this N, K and operand type.
 bool gemm_supported(int N, int K, OperandKind op);
+// Whether the GEMM can quantize bf16 X per row itself (kE4M3Qx) for this
+// row width, K and output kind.
+bool gemm_qx_supported(int N, int K, int norm, OutKind out);
 
 // Probe reduction: accumulates MERE / Frobenius / max statistics of out vs ref.
 cudaError_t launch_error_reduce(const float* out, const float* ref, int64_t n, double* acc, int sms, cudaStream_t stream);
