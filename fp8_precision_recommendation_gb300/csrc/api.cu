@@ -116,17 +116,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D row-major tensor [outer, inner] with a 128-byte-wide, 128B-swizzled box.
+// 2-D row-major tensor [outer, inner] with a 128-byte-wide, 128B-swizzled box
+// (box_inner = 0), or an unswizzled box of box_inner elements.
 loka_status encode_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base, uint64_t inner,
-                      uint64_t outer, uint32_t box_outer) {
+                      uint64_t outer, uint32_t box_outer, uint32_t box_inner = 0) {
   auto fn = encode_fn();
   if (fn == nullptr) return fail(LOKA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {inner * static_cast<uint64_t>(elem_bytes)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elem_bytes), box_outer};
+  cuuint32_t box[2] = {box_inner > 0 ? box_inner : static_cast<cuuint32_t>(128 / elem_bytes), box_outer};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  box_inner > 0 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(LOKA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
   return LOKA_OK;
 }
@@ -523,6 +525,7 @@ loka_status loka_fp8_linear_norm(const loka_linear_desc* descs, int32_t num_grou
     if (w_launch && (s = quantize_operands(descs, num_groups, slots, ws, dev, st, true)) != LOKA_OK) return s;
     static thread_local GemmParams pq;
     if ((s = build_gemm(descs, num_groups, slots, ws, false, out, nullptr, descs[0].norm, dev, &pq)) != LOKA_OK) return s;
+    // the quantizer warps read bf16 X rows directly
     for (int i = 0; i < num_groups; ++i) pq.g[i].xbf = static_cast<const uint16_t*>(descs[i].x);
     // X was complete before this call's W quantizer started (a normal
     // launch), so the GEMM may read X before waiting for that launch

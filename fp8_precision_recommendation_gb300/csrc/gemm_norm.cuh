@@ -63,25 +63,30 @@ constexpr uint32_t kABytes = kBM * kSliceBytes;
 constexpr int kTmemCols = 512;
 constexpr int kThreads = 576;             // producer, MMA, 16 epilogue warps
 constexpr int kEpiBar = 1;               // named barrier id for the epilogue warps
-constexpr int kMaxStages = 8;
+constexpr int kQxBar = 3;                // named barrier id for the quantizer warps
+constexpr int kMaxStages = 8;            // TMA ring stages
+constexpr int kQxMaxStages = 12;         // staging slots of in-kernel quantization
+constexpr int kBarStages = 12;           // full / empty barriers (the larger of the two)
 constexpr int kMaxWSlices = 16;          // resident W: 128 KB / (64 rows x 128 bytes)
 constexpr size_t kSmemLimit = 227 * 1024;
 constexpr size_t kResidentWLimit = 128 * 1024;
 
-// In-kernel activation quantization (OperandKind::kE4M3Qx): 28 warps.
-//   warp 0        bulk copies of bf16 X rows into a staging ring (and W)
+// In-kernel activation quantization (OperandKind::kE4M3Qx): 32 warps.
+//   warp 0        W: resident (once per group) or streamed through a ring
 //   warp 1        MMA;  warps 2-3 idle (they fill warpgroup 0)
-//   warps 4-11    quantizers: a row per warp at a time, staging -> A tile
-//   warps 12-27   epilogue, as in the 576-thread kernel
-// Registers: launched at 72 per thread (28 warps, 7 per sub-partition), then
-// warpgroup 0 and the quantizers drop to 40 and the epilogue rises to 96:
-// per sub-partition 40 + 2 x 40 + 4 x 96 = 504 of the 512 register slots.
-constexpr int kQxThreads = 896;
-constexpr int kQxWarps = 8;              // quantizer warps
+//   warps 4-15    quantizers: each loads its own rows of X (cp.async into a
+//                 private ring of 1 KB slots) and writes their codes into
+//                 the A tile
+//   warps 16-31   epilogue, as in the 576-thread kernel
+// Registers: launched at 64 per thread (32 warps, 8 per sub-partition), then
+// warpgroup 0 drops to 40, the quantizers to 48 and the epilogue rises to 80:
+// per sub-partition 40 + 3 x 48 + 4 x 80 = 504 of the 512 register slots.
+constexpr int kQxThreads = 1024;
+constexpr int kQxWarps = 12;             // quantizer warps
 constexpr int kQxFirstWarp = 4;
-constexpr int kQxEpiWarp = 12;           // first epilogue warp
-constexpr uint32_t kQxSlotBytes = 8192;  // staging slot: 8 KB of consecutive bf16 rows
-constexpr int kQxMaxK = 512;             // row of at most 2 x 16 bytes per lane
+constexpr int kQxEpiWarp = 16;           // first epilogue warp
+constexpr uint32_t kQxSlotBytes = 1024;  // staging slot: one row of K = 512, two of K = 256
+constexpr int kQxMaxSlots = 8;           // slots of one quantizer warp's ring
 
 // Shared-memory carve-up (all offsets from a 1024-byte-aligned base):
 //   ring     stages x (A slice [| B slice]), or (in-kernel quantization)
@@ -91,7 +96,7 @@ constexpr int kQxMaxK = 512;             // row of at most 2 x 16 bytes per lane
 //   w        resident W: K/KE slices of N rows x 128 bytes (when resident)
 //   vectors  2 teams x 4 x N fp32 (weight scale, bias, gamma, beta)
 //   sx       in-kernel quantization: 2 x 128 fp32 row scales (per
-//            accumulator buffer)
+//            accumulator buffer), then a copy of the row-scale tables
 //   stats    clusters: 2 x CL x 128 float2 row statistics of the CTAs
 //   barriers
 struct Layout {
@@ -103,23 +108,28 @@ constexpr uint32_t kSfBlock = 512;
 __host__ __device__ constexpr int sfb_blocks(int N) { return (N + 127) / 128; }
 
 __host__ __device__ inline Layout make_layout(int N, int K, int elem_bytes, bool resident, int stages, bool mx,
-                                              int cl = 1, int a_bufs = 0) {
+                                              int cl = 1, int a_bufs = 0, int w_stages = 0) {
   Layout L;
   const uint32_t b_slice = static_cast<uint32_t>(N) * kSliceBytes;
   const uint32_t sfa = mx ? kSfBlock : 0u;
   const uint32_t sfb = mx ? kSfBlock * sfb_blocks(N) : 0u;
   // stage: [A slice][B slice, streamed W][A scales][B scales, streamed W];
-  // with in-kernel quantization (a_bufs > 0) a staging slot of bf16 rows
-  L.stage_bytes = a_bufs > 0 ? kQxSlotBytes : kABytes + (resident ? 0u : b_slice) + sfa + (resident ? 0u : sfb);
+  // with in-kernel quantization (a_bufs > 0) one staging slot of bf16 rows
+  // per quantizer warp (quantizer w's slot s at (w * stages + s) * 1 KB)
+  L.stage_bytes = a_bufs > 0 ? kQxWarps * kQxSlotBytes
+                             : kABytes + (resident ? 0u : b_slice) + sfa + (resident ? 0u : sfb);
   L.ring = 0;
   L.a = L.ring + static_cast<uint32_t>(stages) * L.stage_bytes;
   L.w = L.a + static_cast<uint32_t>(a_bufs) * kBM * static_cast<uint32_t>(K);
   const int nkb = K * elem_bytes / kSliceBytes;
-  // resident W: [nkb B slices][nkb x B scale blocks]
-  const uint32_t w_bytes = resident ? static_cast<uint32_t>(nkb) * (b_slice + sfb) : 0u;
+  // resident W: [nkb B slices][nkb x B scale blocks]; with in-kernel
+  // quantization and W streamed, a ring of w_stages B slices
+  const uint32_t w_bytes = resident ? static_cast<uint32_t>(nkb) * (b_slice + sfb)
+                                    : (a_bufs > 0 ? static_cast<uint32_t>(w_stages) * b_slice : 0u);
   L.vec = L.w + w_bytes;
   L.sx = L.vec + 2u * 4u * N * sizeof(float);
-  L.stats = L.sx + (a_bufs > 0 ? 2u * kBM * sizeof(float) : 0u);
+  // in-kernel quantization: 2 x 128 row scales, then the scale tables (1 KB)
+  L.stats = L.sx + (a_bufs > 0 ? 2u * kBM * sizeof(float) + static_cast<uint32_t>(sizeof(RowScaleTables)) : 0u);
   // [2][cluster][128] row statistics of the cluster's CTAs (written
   // remotely, double-buffered by tile parity)
   L.bars = L.stats + (cl > 1 ? 2u * cl * kBM * sizeof(float2) : 0u);
@@ -148,7 +158,10 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
   static_assert(N <= 256, "one MMA per K step");
   // in-kernel per-row quantization of bf16 X (one CTA per row, W resident)
   constexpr bool kQx = OP == static_cast<int>(OperandKind::kE4M3Qx);
-  static_assert(!kQx || (CL == 1 && RESIDENT), "in-kernel quantization keeps W resident and rows within a CTA");
+  static_assert(!kQx || CL == 1, "in-kernel quantization keeps rows within a CTA");
+  // in-kernel quantization with W streamed from L2: a ring of p.w_stages K
+  // slices of W, loaded by warp 2 (wfull = w_full[0..3], wempty = w_full[8..11])
+  constexpr bool kQxStream = kQx && !RESIDENT;
   constexpr int EPI0 = kQx ? kQxEpiWarp : 2;       // first epilogue warp
   constexpr int NG = N * CL;                        // columns of the whole output row
   constexpr int SF_COLS_MAX = OP == static_cast<int>(OperandKind::kMxE4M3) ? kMaxStages * (4 + 4 * sfb_blocks(N)) : 0;
@@ -169,7 +182,7 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
 
   const int stages = p.stages;
   const int num_kb = p.K / KE;
-  const Layout L = make_layout(N, p.K, EB, RESIDENT, stages, kMx, CL, kQx ? p.a_bufs : 0);
+  const Layout L = make_layout(N, p.K, EB, RESIDENT, stages, kMx, CL, kQx ? p.a_bufs : 0, kQx ? p.w_stages : 0);
   // A tile's N-column slices go to the CTAs of a cluster (CL > 1, row
   // statistics exchanged), or, when no statistic spans the row (CL == 1,
   // p.slices > 1), to p.slices independent consecutive CTAs.  rank = this
@@ -194,8 +207,8 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
   float2* cl_stats = reinterpret_cast<float2*>(smem + L.stats);     // [2][CL][128] cluster row statistics
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* full = bars;
-  uint64_t* empty = full + kMaxStages;
-  uint64_t* tfull = empty + kMaxStages;
+  uint64_t* empty = full + kBarStages;
+  uint64_t* tfull = empty + kBarStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* mma_done = tempty + 2;
   uint64_t* w_free = mma_done + 1;
@@ -209,7 +222,9 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
   uint64_t* aempty = afull + 2;                                     // [2]
   uint64_t* sxfull = aempty + 2;                                    // [2]
   uint64_t* sxempty = sxfull + 2;                                   // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sxempty + 2);
+  uint64_t* team_sync = sxempty + 2;                                // [2] epilogue team barriers (bounded)
+  uint64_t* epi_done = team_sync + 2;                               // the epilogue's last TMEM read
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -227,7 +242,9 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
         mbar_init(smem_u32(&aempty[b]), 1);
         mbar_init(smem_u32(&sxfull[b]), kQxWarps);
         mbar_init(smem_u32(&sxempty[b]), 8);   // the eight warps of the epilogue team of buffer b
+        mbar_init(smem_u32(&team_sync[b]), 8);
       }
+      mbar_init(smem_u32(epi_done), 16);
     }
     for (int b = 0; b < NBUF; ++b) {
       mbar_init(smem_u32(&tfull[b]), 1);
@@ -293,91 +310,74 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
   }
   // everything above touches only this CTA's own state (and W when it was
   // ready); inputs written by the kernel before this one (the quantized
-  // operands) are read below.  With in-kernel quantization the producer
-  // and the quantizers read only the caller's bf16 X until W is needed: when
-  // X was complete before the launch that precedes this one (p.x_ready) they
-  // start at once and the producer waits just before its first W load.
-  const bool x_early = kQx && p.x_ready && (warp == 0 || (warp >= kQxFirstWarp && warp < kQxEpiWarp));
+  // operands) are read below.  With in-kernel quantization the quantizer
+  // warps read only the caller's bf16 X: when X was complete before the
+  // launch that precedes this one (p.x_ready) they start at once.
+  const bool x_early = kQx && p.x_ready && warp >= kQxFirstWarp && warp < kQxEpiWarp;
   if (!x_early) wait_prerequisite_grids();
   const uint32_t tmem_base = *tmem_slot;
   const Watchdog wd{abort_flag, p.status, p.wait_limit_ns};
   // one lane waits, the whole warp follows its verdict
-  auto warp_wait = [&](uint32_t bar, uint32_t parity, bool cluster_scope) {
+  auto warp_wait = [&](uint32_t bar, uint32_t parity, bool cluster_scope, unsigned code = kErrEpilogueWait) {
     int okw = 1;
     if (lane == 0)
       okw = (cluster_scope ? wait_parity_cluster(wd, bar, parity, kErrClusterWait)
-                           : wait_parity(wd, bar, parity, kErrEpilogueWait)) ? 1 : 0;
+                           : wait_parity(wd, bar, parity, code)) ? 1 : 0;
     return __shfl_sync(0xffffffffu, okw, 0) != 0;
   };
 
   auto run_producer = [&]() {
     // ------------------------------------------------------------ producer
     if (kQx && lane == 0) {
-      // bf16 X rows, 8 KB at a time (the rows are contiguous), into the
-      // staging ring; resident W once per group, issued once the ring is
-      // full (after waiting for the launch before, which wrote W).  A chunk
-      // past the last row still completes its slot, with zero bytes.
-      const int R = static_cast<int>(kQxSlotBytes) / (2 * p.K);   // rows per slot
-      const int chunks = kBM / R;
-      int slot = 0;
-      uint32_t phase = 0;
-      uint32_t issued = 0, last_parity = 0;
-      int cur_group = -1, w_loads = 0;
-      bool waited = !p.x_ready, w_pending = false, ok = true;
-      uint32_t w_issued = 0;
-      auto issue_w = [&]() {
-        if (!waited) {
-          wait_prerequisite_grids();
-          waited = true;
-        }
-        load_w(cur_group);
-        w_issued = 0xFFFFFFFFu;
-        w_pending = false;
-      };
-      for (int tile = cid; ok && tile < p.total_tiles; tile += ncl) {
-        const int g = group_of(p, tile);
-        const GemmGroup& G = p.g[g];
-        if (g != cur_group) {
+      // W only (the quantizer warps load X themselves), after waiting for
+      // the launch before, which wrote it.  Resident: once per group, when
+      // the MMAs of the previous group are done with it.  Streamed: the K
+      // slices of every tile's W through a ring of p.w_stages slots, in the
+      // order the MMA takes them (from L2 after the first tile).
+      bool ok = true;
+      if (RESIDENT) {
+        int cur_group = -1, w_loads = 0;
+        for (int tile = cid; ok && tile < p.total_tiles; tile += ncl) {
+          const int g = group_of(p, tile);
+          if (g == cur_group) continue;
           if (w_loads > 0 && !wait_parity(wd, smem_u32(w_free), (w_loads - 1) & 1, kErrProducerWait)) {
             ok = false;
             break;
           }
           ++w_loads;
           cur_group = g;
-          w_pending = true;
-          w_issued = 0;
+          load_w(g);
         }
-        const int64_t m0 = static_cast<int64_t>(tile - G.tile_begin) * kBM;
-        for (int c = 0; c < chunks; ++c) {
-          if (w_pending && c == stages) issue_w();
-          if (!wait_parity(wd, smem_u32(&empty[slot]), phase ^ 1u, kErrProducerWait)) {
-            ok = false;
-            break;
+        if (!ok && w_loads > 0)
+          for (int kb = 0; kb < num_kb; ++kb) wait_parity_drain(wd, smem_u32(&w_full[kb]), (w_loads - 1) & 1);
+      } else {
+        int ws = 0;
+        uint32_t wphase = 0;
+        uint32_t issued = 0, last_parity = 0;
+        for (int tile = cid; ok && tile < p.total_tiles; tile += ncl) {
+          const int g = group_of(p, tile);
+          for (int kb = 0; kb < num_kb; ++kb) {
+            if (!wait_parity(wd, smem_u32(&w_full[8 + ws]), wphase ^ 1u, kErrProducerWait)) {
+              ok = false;
+              break;
+            }
+            const uint32_t wb = smem_u32(&w_full[ws]);
+            mbar_arrive_expect_tx(wb, B_SLICE);
+#pragma unroll
+            for (int s = 0; s < N_SPLIT; ++s)
+              tma_load_2d(smem_u32(wres + ws * B_SLICE + s * N_MMA * kSliceBytes), &p.g[g].tm_b, wb, kb * KE,
+                          col0 + s * N_MMA);
+            issued |= 1u << ws;
+            last_parity = (last_parity & ~(1u << ws)) | (wphase << ws);
+            if (++ws == p.w_stages) {
+              ws = 0;
+              wphase ^= 1u;
+            }
           }
-          const int64_t r0 = m0 + static_cast<int64_t>(c) * R;
-          const int64_t left = G.M - r0;
-          const int rows = left <= 0 ? 0 : (left >= R ? R : static_cast<int>(left));
-          const uint32_t bytes = static_cast<uint32_t>(rows) * static_cast<uint32_t>(p.K) * 2u;
-          const uint32_t fb = smem_u32(&full[slot]);
-          mbar_arrive_expect_tx(fb, bytes);
-          if (bytes > 0)
-            bulk_load_1d(smem_u32(ring + static_cast<size_t>(slot) * kQxSlotBytes), G.xbf + r0 * p.K, bytes, fb);
-          issued |= 1u << slot;
-          last_parity = (last_parity & ~(1u << slot)) | (phase << slot);
-          if (++slot == stages) {
-            slot = 0;
-            phase ^= 1u;
-          }
         }
-        if (ok && w_pending) issue_w();
-      }
-      if (!ok) {
-        for (int s = 0; s < stages; ++s)
-          if (issued & (1u << s)) wait_parity_drain(wd, smem_u32(&full[s]), (last_parity >> s) & 1u);
-        if (w_loads > 0) {
-          for (int kb = 0; kb < num_kb; ++kb)
-            if (w_issued & (1u << kb)) wait_parity_drain(wd, smem_u32(&w_full[kb]), (w_loads - 1) & 1);
-        }
+        if (!ok)
+          for (int s = 0; s < p.w_stages; ++s)
+            if (issued & (1u << s)) wait_parity_drain(wd, smem_u32(&w_full[s]), (last_parity >> s) & 1u);
       }
     } else if (!kQx && lane == 0) {
       int stage = 0;
@@ -460,6 +460,8 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
       uint32_t phase = 0;
       int local = 0;
       int cur_group = -1, w_uses = 0;
+      int ws = 0;                 // streamed W (in-kernel quantization): ring slot and phase
+      uint32_t wphase = 0;
       bool ok = true;
       for (int tile = cid; ok && tile < p.total_tiles; tile += ncl, ++local) {
         if (RESIDENT) {
@@ -490,11 +492,16 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
             ok = false;
             break;
           }
+          if (kQxStream && !wait_parity(wd, smem_u32(&w_full[ws]), wphase, kErrMmaWait)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint32_t a_addr =
               kQx ? smem_u32(smem + L.a + static_cast<size_t>(abuf) * kBM * p.K + static_cast<size_t>(kb) * kABytes)
                   : smem_u32(ring + static_cast<size_t>(stage) * L.stage_bytes);
-          const uint32_t b_addr = RESIDENT ? smem_u32(wres + kb * B_SLICE) : a_addr + kABytes;
+          const uint32_t b_addr = RESIDENT ? smem_u32(wres + kb * B_SLICE)
+                                           : (kQxStream ? smem_u32(wres + ws * B_SLICE) : a_addr + kABytes);
           uint32_t sfa_tmem = 0, sfb_tmem = 0;
           if (kMx) {
             // E8M0 codes of this K slice into tensor memory: A's 128 rows to
@@ -530,6 +537,13 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
               phase ^= 1u;
             }
           }
+          if (kQxStream) {
+            mma_commit(smem_u32(&w_full[8 + ws]));   // this W slice's slot may be refilled
+            if (++ws == p.w_stages) {
+              ws = 0;
+              wphase ^= 1u;
+            }
+          }
         }
         if (!ok) break;
         if (kQx) mma_commit(smem_u32(&aempty[abuf]));   // the quantizers may refill this A tile
@@ -544,72 +558,132 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
   [[maybe_unused]] auto run_quantizer = [&]() {
     // ------------------------------------------------------- quantizers
     // LoKA section III-B case 1: with a whole output row in one CTA, the
-    // activation quantization fuses into the GEMM.  Warp q takes row
-    // 8j + q of every staging slot (R = 8 KB / 2K rows per slot, j < R/8):
-    // lane l holds 16-byte vectors l and l + 32 of the row (all of it for
-    // K <= 512), so the row amax is one warp reduction; the scale is the
-    // standalone quantizer's (quant_math.cuh), and the codes go straight into
-    // the A tile in the 128B-swizzled layout the MMA descriptors describe:
-    // the 16-byte piece c of row r of a K slice sits at piece c ^ (r % 8).
+    // activation quantization fuses into the GEMM.  A tile's rows come in
+    // units of 1 KB (one row of K = 512, two rows of K = 256); quantizer
+    // warp q takes units q, q + 12, q + 24, ... of every tile.  Each warp
+    // keeps its own ring of `stages` 1 KB slots filled with its next units:
+    // every lane copies its two 16-byte pieces of a unit (cp.async through
+    // the load/store path, one commit group per unit; rows past M arrive as
+    // zeros), so no slot is shared and a slot is refilled as soon as the warp
+    // has read it.  Lane l holds the pieces at bytes 16 l and 512 + 16 l of a
+    // unit: the two halves of a K = 512 row, or the two K = 256 rows.  Per
+    // row: one warp reduction of the amax, the standalone quantizer's scales
+    // (quant_math.cuh, tables copied into shared memory), the cast, and the
+    // codes written straight into the A tile in the 128B-swizzled layout the
+    // MMA descriptors describe (16-byte piece c of row r of a K slice at
+    // piece c ^ (r % 8)).
     const int qw = warp - kQxFirstWarp;
-    const int K = p.K;
-    const int kv = K >> 3;                                  // 16-byte vectors per row
-    const int R = static_cast<int>(kQxSlotBytes) / (2 * K);   // rows per staging slot
-    const int rpw = R / kQxWarps;                           // rows per warp per slot
-    const int chunks = kBM / R;
+    const bool two_rows = p.K == 256;
+    const int rps = two_rows ? 2 : 1;                       // rows per unit
+    const int units = kBM / rps;                            // units per tile
+    const int S = stages;                                   // slots of this warp's ring (5..8)
+    const uint32_t ring_base = smem_u32(ring) + static_cast<uint32_t>(qw * S) * kQxSlotBytes;
+    RowScaleTables* tab = reinterpret_cast<RowScaleTables*>(smem + L.sx + 2 * kBM * sizeof(float));
+    {
+      const float* src_tab = &kRowScaleTables.inv[0];
+      float* dst_tab = &tab->inv[0];
+      for (int i = qw * 32 + lane; i < 256; i += kQxWarps * 32) dst_tab[i] = src_tab[i];
+      named_bar_sync(kQxBar, kQxWarps * 32);   // the quantizer warps only, before any wait
+    }
+    // load cursor: the next unit to load, in the order the warp processes
+    // them (every lane follows the same sequence).  The tile's parameters
+    // are read once per tile; per unit the cursor only advances.
+    const int my_units = (units - qw + kQxWarps - 1) / kQxWarps;   // units of a tile for this warp
+    const int64_t step = static_cast<int64_t>(kQxWarps) * rps * p.K;  // elements between its units
+    int load_tile = cid - ncl, load_left = 0;
+    const uint16_t* lbase = nullptr;   // the group's X (a valid address for zero-size copies)
+    const uint16_t* lrow = nullptr;    // first row of the next unit
+    int64_t lrows = 0;                 // rows of the group from lrow on
+    // piece 0 of a unit: its first row, bytes 16 l; piece 1: the same row's
+    // bytes 512 + 16 l (K = 512) or the next row's bytes 16 l (K = 256)
+    const int64_t off1 = two_rows ? p.K : 256;
+    auto issue = [&](int s) {
+      if (load_left == 0) {
+        load_tile += ncl;
+        if (load_tile < p.total_tiles) {
+          const GemmGroup& G = p.g[group_of(p, load_tile)];
+          const int64_t r0 = static_cast<int64_t>(load_tile - G.tile_begin) * kBM + qw * rps;
+          lbase = G.xbf;
+          lrow = G.xbf + r0 * p.K + lane * 8;
+          lrows = G.M - r0;
+          load_left = my_units;
+        }
+      }
+      if (load_left > 0) {
+        const uint32_t dst = ring_base + static_cast<uint32_t>(s) * kQxSlotBytes + static_cast<uint32_t>(lane) * 16u;
+        const bool ok0 = lrows > 0, ok1 = two_rows ? lrows > 1 : lrows > 0;
+        cp_async_16(dst, ok0 ? lrow : lbase, ok0 ? 16u : 0u);
+        cp_async_16(dst + 512u, ok1 ? lrow + off1 : lbase, ok1 ? 16u : 0u);
+        lrow += step;
+        lrows -= kQxWarps * rps;
+        --load_left;
+      }
+      cp_async_commit();   // one group per slot, empty when nothing is left to load
+    };
+    // waits for the oldest of the S groups in flight
+    auto wait_oldest = [&]() {
+      switch (S) {
+        case 5: cp_async_wait<4>(); break;
+        case 6: cp_async_wait<5>(); break;
+        case 7: cp_async_wait<6>(); break;
+        default: cp_async_wait<7>(); break;
+      }
+    };
+    for (int s = 0; s < S; ++s) issue(s);
     int slot = 0;
-    uint32_t phase = 0;
     int local = 0;
-    for (int tile = cid; tile < p.total_tiles; tile += ncl, ++local) {
+    bool okq = true;
+    for (int tile = cid; okq && tile < p.total_tiles; tile += ncl, ++local) {
       const int ab = p.a_bufs == 2 ? (local & 1) : 0;
       const uint32_t ause = p.a_bufs == 2 ? static_cast<uint32_t>(local >> 1) : static_cast<uint32_t>(local);
       const int sb = local & 1;   // row-scale buffer = the tile's accumulator buffer
-      if (!warp_wait(smem_u32(&aempty[ab]), (ause & 1u) ^ 1u, false)) break;
-      if (!warp_wait(smem_u32(&sxempty[sb]), ((local >> 1) & 1u) ^ 1u, false)) break;
-      const uint32_t abase = smem_u32(smem + L.a + static_cast<size_t>(ab) * kBM * K);
+      bool a_free = false;
+      const uint32_t abase = smem_u32(smem + L.a + static_cast<size_t>(ab) * kBM * p.K);
       float* sxo = reinterpret_cast<float*>(smem + L.sx) + sb * kBM;
-      bool okq = true;
-      for (int c = 0; c < chunks; ++c) {
-        if (!warp_wait(smem_u32(&full[slot]), phase, false)) {
-          okq = false;
-          break;
+      for (int u = qw; u < units; u += kQxWarps) {
+        wait_oldest();
+        __syncwarp();   // every lane's pieces of the unit are visible to the warp
+        const uint32_t src = ring_base + static_cast<uint32_t>(slot) * kQxSlotBytes + static_cast<uint32_t>(lane) * 16u;
+        const uint4 d0 = ld_shared_v4(src);
+        const uint4 d1 = ld_shared_v4(src + 512u);
+        const float a0 = abs_max8(d0, 0.0f), a1 = abs_max8(d1, 0.0f);
+        float inv0, inv1, sc0, sc1;
+        if (two_rows) {
+          row_scales(warp_max(a0), inv0, sc0, *tab);
+          row_scales(warp_max(a1), inv1, sc1, *tab);
+        } else {
+          row_scales(warp_max(fmaxf(a0, a1)), inv0, sc0, *tab);
+          inv1 = inv0;
+          sc1 = sc0;
         }
-        const uint8_t* sbase = ring + static_cast<size_t>(slot) * kQxSlotBytes;
-        for (int j = 0; j < rpw; ++j) {
-          const int rs = j * kQxWarps + qw;                  // row within the slot
-          const int r = c * R + rs;                          // row within the tile
-          const uint4* src = reinterpret_cast<const uint4*>(sbase + static_cast<size_t>(rs) * K * 2);
-          uint4 v[kQxMaxK / 256];
-#pragma unroll
-          for (int i = 0; i < kQxMaxK / 256; ++i) {
-            const int idx = i * 32 + lane;
-            v[i] = idx < kv ? src[idx] : make_uint4(0, 0, 0, 0);
-          }
-          float m = 0.0f;
-#pragma unroll
-          for (int i = 0; i < kQxMaxK / 256; ++i) m = abs_max8(v[i], m);
-          m = warp_max(m);
-          float inv, sc;
-          row_scales(m, inv, sc);
-#pragma unroll
-          for (int i = 0; i < kQxMaxK / 256; ++i) {
-            const int idx = i * 32 + lane;
-            if (idx < kv) {
-              const uint32_t piece = static_cast<uint32_t>((idx & 15) >> 1) ^ static_cast<uint32_t>(r & 7);
-              const uint32_t a = abase + static_cast<uint32_t>(idx >> 4) * kABytes + static_cast<uint32_t>(r) * 128u +
-                                 piece * 16u + static_cast<uint32_t>(idx & 1) * 8u;
-              st_shared_v2(a, cast8(v[i], inv));
-            }
-          }
-          if (lane == 0) sxo[r] = sc;
-        }
-        // every lane's reads of the slot are done (the warp reduction used
-        // them all): release it to the producer
+        // the slot's data are in registers (the reductions above used every
+        // lane's): refill it with this warp's next unit
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
-        if (++slot == stages) {
-          slot = 0;
-          phase ^= 1u;
+        issue(slot);
+        if (++slot == S) slot = 0;
+        if (!a_free) {
+          // the A tile and row-scale buffer of this tile are written from here on
+          if (!warp_wait(smem_u32(&aempty[ab]), (ause & 1u) ^ 1u, false, kErrQuantWait) ||
+              !warp_wait(smem_u32(&sxempty[sb]), ((local >> 1) & 1u) ^ 1u, false, kErrQuantWait)) {
+            okq = false;
+            break;
+          }
+          a_free = true;
+        }
+        // vector 0: row r0, piece idx0; vector 1: row r1, piece idx1
+        const int r0 = u * rps, r1 = two_rows ? r0 + 1 : r0;
+        const int idx0 = lane, idx1 = two_rows ? lane : lane + 32;
+        st_shared_v2(abase + static_cast<uint32_t>(idx0 >> 4) * kABytes + static_cast<uint32_t>(r0) * 128u +
+                         ((static_cast<uint32_t>((idx0 & 15) >> 1) ^ static_cast<uint32_t>(r0 & 7)) << 4) +
+                         static_cast<uint32_t>(idx0 & 1) * 8u,
+                     cast8(d0, inv0));
+        st_shared_v2(abase + static_cast<uint32_t>(idx1 >> 4) * kABytes + static_cast<uint32_t>(r1) * 128u +
+                         ((static_cast<uint32_t>((idx1 & 15) >> 1) ^ static_cast<uint32_t>(r1 & 7)) << 4) +
+                         static_cast<uint32_t>(idx1 & 1) * 8u,
+                     cast8(d1, inv1));
+        if (lane == 0) {
+          sxo[r0] = sc0;
+          if (two_rows) sxo[r1] = sc1;
         }
       }
       if (!okq) break;
@@ -621,6 +695,8 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
         mbar_arrive(smem_u32(&sxfull[sb]));
       }
     }
+    // copies still in flight into this warp's ring land before it leaves
+    cp_async_wait<0>();
   };
 
   auto run_epilogue = [&]() {
@@ -713,6 +789,20 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
     int cur_group = -1;
     bool affine = false;
     float sx_next[2] = {1.f, 1.f};
+    // in-kernel quantization: the team's barrier is an mbarrier with a time
+    // limit (the 896-thread kernel has no wait without one)
+    uint32_t team_phase = 0;
+    auto team_barrier = [&]() {
+      if constexpr (kQx) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&team_sync[team]));
+        const bool okt = warp_wait(smem_u32(&team_sync[team]), team_phase, false, kErrTeamWait);
+        team_phase ^= 1u;
+        return okt && *abort_flag == 0;
+      } else {
+        return !named_bar_or(team_bar, 256, *abort_flag != 0);
+      }
+    };
     int local = team;
     int tile = cid + team * ncl;
     if (!kQx && active && tile < p.total_tiles) row_scales(tile, sx_next);
@@ -722,7 +812,7 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
       if (g != cur_group) {
         // this team's column vectors for the group; the barrier's OR makes
         // the abort decision the same for all of the team's warps
-        if (named_bar_or(team_bar, 256, *abort_flag != 0)) break;
+        if (!team_barrier()) break;
         const bool normed = norm != kNormNone;
         // LayerNorm is unchanged when one constant is added to every column
         // of a row, so the bias enters centred on its own mean: a bias far
@@ -747,7 +837,11 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
           vec_be[n] = (G.beta == nullptr || norm != kNormLayer) ? 0.0f : bf16_to_f(G.beta[gn]);
         }
         affine = normed && (G.gamma != nullptr || (G.beta != nullptr && norm == kNormLayer));
-        named_bar_sync(team_bar, 256);
+        if constexpr (kQx) {
+          if (!team_barrier()) break;
+        } else {
+          named_bar_sync(team_bar, 256);
+        }
         cur_group = g;
       }
       float sxr[2] = {sx_next[0], sx_next[1]};
@@ -780,7 +874,7 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
       if constexpr (kQx) {
         // the row scales the quantizers chose for this tile (buffer = the
         // accumulator buffer); the weight scales are per column
-        if (!warp_wait(smem_u32(&sxfull[buf]), use & 1u, false)) break;
+        if (!warp_wait(smem_u32(&sxfull[buf]), use & 1u, false, kErrRowScaleWait)) break;
         const float* sxs = reinterpret_cast<const float*>(smem + L.sx) + buf * kBM;
         sxr[0] = sxs[rowk[0]];
         sxr[1] = sxs[rowk[1]];
@@ -1223,25 +1317,37 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
   };
 
   if constexpr (kQx) {
-    // Each warpgroup takes its register share in its own branch and gives it
-    // back before the branches meet again, so the teardown below runs at
-    // the launch count (72) everywhere.
+    // Each warpgroup takes its register share in its own branch and the
+    // branches never meet again: no barrier without a time limit.  The
+    // epilogue warps report their last tensor-memory read on epi_done; the
+    // MMA warp waits for it (bounded) and frees tensor memory; everyone else
+    // just leaves.
     if (warp < kQxFirstWarp) {
       regs_dec<40>();
       if (!misaligned) {
         if (warp == 0) run_producer();
         else if (warp == 1) run_mma();
       }
-      regs_inc<72>();
+      if (warp == 1) {
+        if (lane == 0) {
+          const bool done = wait_parity_drain(wd, smem_u32(epi_done), 0);
+          if (!done) atomicOr(p.status, kErrTeardownWait);
+        }
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+      }
     } else if (warp < kQxEpiWarp) {
-      regs_dec<40>();
+      regs_dec<48>();
       if (!misaligned) run_quantizer();
-      regs_inc<72>();
     } else {
-      regs_inc<96>();
+      regs_inc<80>();
       if (!misaligned) run_epilogue();
-      regs_dec<72>();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(epi_done));
     }
+    return;
   } else {
     if (misaligned) {
       // nothing to do: fall through to the teardown barriers
@@ -1353,28 +1459,37 @@ cudaError_t launch_one(const GemmParams& p, size_t smem, int sms, cudaStream_t s
   return cudaGetLastError();
 }
 
-// In-kernel quantization: resident W, the A tiles (two when a double buffer
-// still leaves three staging slots, else one) and at least two 8 KB staging
-// slots; K = 128, 256 or 512, so that a slot holds a multiple of 8 whole
-// rows (one per quantizer warp) and a tile a whole number of slots.
+// In-kernel quantization: K = 256 or 512 (a 1 KB staging unit is one row of
+// K = 512 or two of K = 256, so a lane's two 16-byte pieces cover it).  Each
+// of the 12 quantizer warps gets `stages` slots; at least 5 (60 KB of X in
+// flight per SM).  The first layout that fits wins, in this order: W resident
+// with two A tiles, W resident with one A tile, W streamed through two slots
+// with two A tiles, then with one.
 struct QxPlan {
-  int a_bufs, stages;
+  bool resident;
+  int a_bufs, stages, w_stages;
   size_t smem;
 };
 
 inline QxPlan plan_qx(int N, int K) {
-  QxPlan q{0, 0, 0};
-  if ((K != 128 && K != 256 && K != 512) || K > kQxMaxK || N > 256) return q;
-  if (static_cast<size_t>(N) * K > kResidentWLimit) return q;
-  for (int a = 2; a >= 1; --a) {
-    const Layout base = make_layout(N, K, 1, true, 0, false, 1, a);
-    if (base.total + 2 * kQxSlotBytes > kSmemLimit) continue;
-    int st = static_cast<int>((kSmemLimit - base.total) / kQxSlotBytes);
-    if (st > kMaxStages) st = kMaxStages;
-    if (a == 2 && st < 3) continue;
+  QxPlan q{false, 0, 0, 0, 0};
+  if ((K != 256 && K != 512) || N > 256) return q;
+  constexpr int kMinSlots = 5;
+  const size_t per_slot = static_cast<size_t>(kQxWarps) * kQxSlotBytes;
+  for (int opt = 0; opt < 4; ++opt) {
+    const bool resident = opt < 2;
+    const int a = (opt & 1) == 0 ? 2 : 1;
+    const int ws = resident ? 0 : 2;
+    if (resident && static_cast<size_t>(N) * K > kResidentWLimit) continue;
+    const Layout base = make_layout(N, K, 1, resident, 0, false, 1, a, ws);
+    if (base.total + kMinSlots * per_slot > kSmemLimit) continue;
+    int st = static_cast<int>((kSmemLimit - base.total) / per_slot);
+    if (st > kQxMaxSlots) st = kQxMaxSlots;
+    q.resident = resident;
     q.a_bufs = a;
     q.stages = st;
-    q.smem = base.total + static_cast<size_t>(st) * kQxSlotBytes;
+    q.w_stages = ws;
+    q.smem = base.total + static_cast<size_t>(st) * per_slot;
     return q;
   }
   return q;

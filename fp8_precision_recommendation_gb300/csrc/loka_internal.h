@@ -107,6 +107,7 @@ struct GemmParams {
   int32_t x_ready;       // 1: the bf16 X was complete before the launch that precedes this GEMM
                          // (in-kernel quantization reads it before waiting for that launch)
   int32_t a_bufs;        // in-kernel quantization: quantized A tiles in shared memory (1 or 2)
+  int32_t w_stages;      // in-kernel quantization with W streamed: ring slots of W K slices
   int32_t yq_mode;       // quantized output kind: kScaleRow or kScaleMx32
   int32_t norm_block;    // BlockNorm block (32, 64, 128 or 256 columns)
   int32_t act;           // kActNone or kActHardSwish, after the normalization
@@ -138,8 +139,9 @@ cudaError_t launch_gemm_norm(GemmParams& p, int N, OperandKind op, OutKind out, 
 
 // Whether the kernel has a shared-memory plan for this N, K and operand type.
 bool gemm_supported(int N, int K, OperandKind op);
-// Whether the GEMM can quantize bf16 X per row itself (kE4M3Qx) for this
-// row width, K and output kind.
+// Whether the GEMM quantizes bf16 X per row itself (kE4M3Qx) for this row
+// width, K and output kind: where it has a plan that keeps W resident beside
+// two A tiles.
 bool gemm_qx_supported(int N, int K, int norm, OutKind out);
 
 // Probe reduction: accumulates MERE / Frobenius / max statistics of out vs ref.

@@ -22,6 +22,11 @@ enum : unsigned {
   kErrSelftest = 16u,
   kErrMisaligned = 32u,
   kErrClusterWait = 64u,
+  // in-kernel quantization: which hand-off gave up
+  kErrQuantWait = 128u,      // a quantizer warp (staging slot, A tile or row-scale buffer)
+  kErrTeamWait = 256u,       // an epilogue team's shared-vector barrier
+  kErrRowScaleWait = 512u,   // the epilogue waiting for a tile's row scales
+  kErrTeardownWait = 1024u,  // the MMA warp waiting for the epilogue before freeing tensor memory
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -273,6 +278,26 @@ __device__ __forceinline__ void regs_dec() {
 template <int R>
 __device__ __forceinline__ void regs_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+
+// 16-byte asynchronous copy global -> shared through the load/store path
+// (bypassing L1); src_bytes < 16 fills the rest with zeros (0: all zeros,
+// nothing read).  Completion is tracked per thread by commit groups.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's most recent commit groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// 16 bytes from shared memory.
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+  return v;
 }
 
 // 8 bytes into shared memory.

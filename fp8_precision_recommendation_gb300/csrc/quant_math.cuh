@@ -64,7 +64,10 @@ constexpr RowScaleTables make_row_scale_tables() {
 }
 __constant__ RowScaleTables kRowScaleTables = make_row_scale_tables();
 
-__device__ __forceinline__ void row_scales(float amax, float& inv, float& scale) {
+// tab: the two 128-entry tables (constant memory, or a copy in shared memory
+// for kernels whose constant cache is busy with large parameter blocks).
+__device__ __forceinline__ void row_scales(float amax, float& inv, float& scale,
+                                           const RowScaleTables& tab = kRowScaleTables) {
   const uint32_t a = __float_as_uint(amax);
   const uint32_t ef = (a >> 23) & 0xFFu;   // exponent field
   if (amax == 0.0f) {
@@ -73,8 +76,8 @@ __device__ __forceinline__ void row_scales(float amax, float& inv, float& scale)
   } else if (ef >= 10u && ef <= 254u && (a & 0xFFFFu) == 0u) {
     const int k = static_cast<int>((a >> 16) & 0x7Fu);
     // table entries have exponent fields 134/135 (inv) and 118/119 (scale)
-    inv = __uint_as_float(__float_as_uint(kRowScaleTables.inv[k]) + ((127u - ef) << 23));
-    scale = __uint_as_float(__float_as_uint(kRowScaleTables.scale[k]) + ((ef - 127u) << 23));
+    inv = __uint_as_float(__float_as_uint(tab.inv[k]) + ((127u - ef) << 23));
+    scale = __uint_as_float(__float_as_uint(tab.scale[k]) + ((ef - 127u) << 23));
   } else {
     inv = __fdiv_rn(kE4M3Max, amax);
     scale = __fdiv_rn(amax, kE4M3Max);
