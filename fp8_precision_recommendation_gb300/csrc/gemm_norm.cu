@@ -16,10 +16,11 @@ bool gemm_qx_supported(int N, int K, int norm, OutKind out) {
   if (out != OutKind::kBf16 || r.cl != 1 || r.slices != 1) return false;
   // Chosen only where W stays resident beside two A tiles: with one A tile
   // the quantizer warps wait for every tile's MMAs, and the measured step
-  // was slower than quantizer + GEMM (rec-MLP layer, K = 512: 48 vs 35 us);
-  // with two (K = 256, the ensemble layers) it matched it.
+  // was slower than quantizer + GEMM (rec-MLP layer, K = 512, W streamed
+  // from L2: 48 vs 35 us); with two (K = 256, the ensemble layers) it
+  // matched it.
   const QxPlan q = plan_qx(r.local, K);
-  return q.stages > 0 && q.resident && q.a_bufs == 2;
+  return q.stages > 0 && q.a_bufs == 2;
 }
 
 GemmRoute gemm_route(int N, int norm) {

@@ -108,7 +108,7 @@ constexpr uint32_t kSfBlock = 512;
 __host__ __device__ constexpr int sfb_blocks(int N) { return (N + 127) / 128; }
 
 __host__ __device__ inline Layout make_layout(int N, int K, int elem_bytes, bool resident, int stages, bool mx,
-                                              int cl = 1, int a_bufs = 0, int w_stages = 0) {
+                                              int cl = 1, int a_bufs = 0) {
   Layout L;
   const uint32_t b_slice = static_cast<uint32_t>(N) * kSliceBytes;
   const uint32_t sfa = mx ? kSfBlock : 0u;
@@ -122,10 +122,8 @@ __host__ __device__ inline Layout make_layout(int N, int K, int elem_bytes, bool
   L.a = L.ring + static_cast<uint32_t>(stages) * L.stage_bytes;
   L.w = L.a + static_cast<uint32_t>(a_bufs) * kBM * static_cast<uint32_t>(K);
   const int nkb = K * elem_bytes / kSliceBytes;
-  // resident W: [nkb B slices][nkb x B scale blocks]; with in-kernel
-  // quantization and W streamed, a ring of w_stages B slices
-  const uint32_t w_bytes = resident ? static_cast<uint32_t>(nkb) * (b_slice + sfb)
-                                    : (a_bufs > 0 ? static_cast<uint32_t>(w_stages) * b_slice : 0u);
+  // resident W: [nkb B slices][nkb x B scale blocks]
+  const uint32_t w_bytes = resident ? static_cast<uint32_t>(nkb) * (b_slice + sfb) : 0u;
   L.vec = L.w + w_bytes;
   L.sx = L.vec + 2u * 4u * N * sizeof(float);
   // in-kernel quantization: 2 x 128 row scales, then the scale tables (1 KB)
@@ -158,10 +156,7 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
   static_assert(N <= 256, "one MMA per K step");
   // in-kernel per-row quantization of bf16 X (one CTA per row, W resident)
   constexpr bool kQx = OP == static_cast<int>(OperandKind::kE4M3Qx);
-  static_assert(!kQx || CL == 1, "in-kernel quantization keeps rows within a CTA");
-  // in-kernel quantization with W streamed from L2: a ring of p.w_stages K
-  // slices of W, loaded by warp 2 (wfull = w_full[0..3], wempty = w_full[8..11])
-  constexpr bool kQxStream = kQx && !RESIDENT;
+  static_assert(!kQx || (CL == 1 && RESIDENT), "in-kernel quantization keeps W resident and rows within a CTA");
   constexpr int EPI0 = kQx ? kQxEpiWarp : 2;       // first epilogue warp
   constexpr int NG = N * CL;                        // columns of the whole output row
   constexpr int SF_COLS_MAX = OP == static_cast<int>(OperandKind::kMxE4M3) ? kMaxStages * (4 + 4 * sfb_blocks(N)) : 0;
@@ -182,7 +177,7 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
 
   const int stages = p.stages;
   const int num_kb = p.K / KE;
-  const Layout L = make_layout(N, p.K, EB, RESIDENT, stages, kMx, CL, kQx ? p.a_bufs : 0, kQx ? p.w_stages : 0);
+  const Layout L = make_layout(N, p.K, EB, RESIDENT, stages, kMx, CL, kQx ? p.a_bufs : 0);
   // A tile's N-column slices go to the CTAs of a cluster (CL > 1, row
   // statistics exchanged), or, when no statistic spans the row (CL == 1,
   // p.slices > 1), to p.slices independent consecutive CTAs.  rank = this
@@ -330,55 +325,23 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
     // ------------------------------------------------------------ producer
     if (kQx && lane == 0) {
       // W only (the quantizer warps load X themselves), after waiting for
-      // the launch before, which wrote it.  Resident: once per group, when
-      // the MMAs of the previous group are done with it.  Streamed: the K
-      // slices of every tile's W through a ring of p.w_stages slots, in the
-      // order the MMA takes them (from L2 after the first tile).
+      // the launch before, which wrote it: once per group, when the MMAs of
+      // the previous group are done with it.
       bool ok = true;
-      if (RESIDENT) {
-        int cur_group = -1, w_loads = 0;
-        for (int tile = cid; ok && tile < p.total_tiles; tile += ncl) {
-          const int g = group_of(p, tile);
-          if (g == cur_group) continue;
-          if (w_loads > 0 && !wait_parity(wd, smem_u32(w_free), (w_loads - 1) & 1, kErrProducerWait)) {
-            ok = false;
-            break;
-          }
-          ++w_loads;
-          cur_group = g;
-          load_w(g);
+      int cur_group = -1, w_loads = 0;
+      for (int tile = cid; ok && tile < p.total_tiles; tile += ncl) {
+        const int g = group_of(p, tile);
+        if (g == cur_group) continue;
+        if (w_loads > 0 && !wait_parity(wd, smem_u32(w_free), (w_loads - 1) & 1, kErrProducerWait)) {
+          ok = false;
+          break;
         }
-        if (!ok && w_loads > 0)
-          for (int kb = 0; kb < num_kb; ++kb) wait_parity_drain(wd, smem_u32(&w_full[kb]), (w_loads - 1) & 1);
-      } else {
-        int ws = 0;
-        uint32_t wphase = 0;
-        uint32_t issued = 0, last_parity = 0;
-        for (int tile = cid; ok && tile < p.total_tiles; tile += ncl) {
-          const int g = group_of(p, tile);
-          for (int kb = 0; kb < num_kb; ++kb) {
-            if (!wait_parity(wd, smem_u32(&w_full[8 + ws]), wphase ^ 1u, kErrProducerWait)) {
-              ok = false;
-              break;
-            }
-            const uint32_t wb = smem_u32(&w_full[ws]);
-            mbar_arrive_expect_tx(wb, B_SLICE);
-#pragma unroll
-            for (int s = 0; s < N_SPLIT; ++s)
-              tma_load_2d(smem_u32(wres + ws * B_SLICE + s * N_MMA * kSliceBytes), &p.g[g].tm_b, wb, kb * KE,
-                          col0 + s * N_MMA);
-            issued |= 1u << ws;
-            last_parity = (last_parity & ~(1u << ws)) | (wphase << ws);
-            if (++ws == p.w_stages) {
-              ws = 0;
-              wphase ^= 1u;
-            }
-          }
-        }
-        if (!ok)
-          for (int s = 0; s < p.w_stages; ++s)
-            if (issued & (1u << s)) wait_parity_drain(wd, smem_u32(&w_full[s]), (last_parity >> s) & 1u);
+        ++w_loads;
+        cur_group = g;
+        load_w(g);
       }
+      if (!ok && w_loads > 0)
+        for (int kb = 0; kb < num_kb; ++kb) wait_parity_drain(wd, smem_u32(&w_full[kb]), (w_loads - 1) & 1);
     } else if (!kQx && lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -460,8 +423,6 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
       uint32_t phase = 0;
       int local = 0;
       int cur_group = -1, w_uses = 0;
-      int ws = 0;                 // streamed W (in-kernel quantization): ring slot and phase
-      uint32_t wphase = 0;
       bool ok = true;
       for (int tile = cid; ok && tile < p.total_tiles; tile += ncl, ++local) {
         if (RESIDENT) {
@@ -492,16 +453,11 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
             ok = false;
             break;
           }
-          if (kQxStream && !wait_parity(wd, smem_u32(&w_full[ws]), wphase, kErrMmaWait)) {
-            ok = false;
-            break;
-          }
           tc_fence_after();
           const uint32_t a_addr =
               kQx ? smem_u32(smem + L.a + static_cast<size_t>(abuf) * kBM * p.K + static_cast<size_t>(kb) * kABytes)
                   : smem_u32(ring + static_cast<size_t>(stage) * L.stage_bytes);
-          const uint32_t b_addr = RESIDENT ? smem_u32(wres + kb * B_SLICE)
-                                           : (kQxStream ? smem_u32(wres + ws * B_SLICE) : a_addr + kABytes);
+          const uint32_t b_addr = RESIDENT ? smem_u32(wres + kb * B_SLICE) : a_addr + kABytes;
           uint32_t sfa_tmem = 0, sfb_tmem = 0;
           if (kMx) {
             // E8M0 codes of this K slice into tensor memory: A's 128 rows to
@@ -535,13 +491,6 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
             if (++stage == stages) {
               stage = 0;
               phase ^= 1u;
-            }
-          }
-          if (kQxStream) {
-            mma_commit(smem_u32(&w_full[8 + ws]));   // this W slice's slot may be refilled
-            if (++ws == p.w_stages) {
-              ws = 0;
-              wphase ^= 1u;
             }
           }
         }
@@ -1460,35 +1409,28 @@ cudaError_t launch_one(const GemmParams& p, size_t smem, int sms, cudaStream_t s
 }
 
 // In-kernel quantization: K = 256 or 512 (a 1 KB staging unit is one row of
-// K = 512 or two of K = 256, so a lane's two 16-byte pieces cover it).  Each
-// of the 12 quantizer warps gets `stages` slots; at least 5 (60 KB of X in
-// flight per SM).  The first layout that fits wins, in this order: W resident
-// with two A tiles, W resident with one A tile, W streamed through two slots
-// with two A tiles, then with one.
+// K = 512 or two of K = 256, so a lane's two 16-byte pieces cover it), W
+// resident.  Each of the 12 quantizer warps gets `stages` slots, at least 5
+// (60 KB of X in flight per SM); two A tiles when they fit beside that, else
+// one.
 struct QxPlan {
-  bool resident;
-  int a_bufs, stages, w_stages;
+  int a_bufs, stages;
   size_t smem;
 };
 
 inline QxPlan plan_qx(int N, int K) {
-  QxPlan q{false, 0, 0, 0, 0};
+  QxPlan q{0, 0, 0};
   if ((K != 256 && K != 512) || N > 256) return q;
+  if (static_cast<size_t>(N) * K > kResidentWLimit) return q;
   constexpr int kMinSlots = 5;
   const size_t per_slot = static_cast<size_t>(kQxWarps) * kQxSlotBytes;
-  for (int opt = 0; opt < 4; ++opt) {
-    const bool resident = opt < 2;
-    const int a = (opt & 1) == 0 ? 2 : 1;
-    const int ws = resident ? 0 : 2;
-    if (resident && static_cast<size_t>(N) * K > kResidentWLimit) continue;
-    const Layout base = make_layout(N, K, 1, resident, 0, false, 1, a, ws);
+  for (int a = 2; a >= 1; --a) {
+    const Layout base = make_layout(N, K, 1, true, 0, false, 1, a);
     if (base.total + kMinSlots * per_slot > kSmemLimit) continue;
     int st = static_cast<int>((kSmemLimit - base.total) / per_slot);
     if (st > kQxMaxSlots) st = kQxMaxSlots;
-    q.resident = resident;
     q.a_bufs = a;
     q.stages = st;
-    q.w_stages = ws;
     q.smem = base.total + static_cast<size_t>(st) * per_slot;
     return q;
   }

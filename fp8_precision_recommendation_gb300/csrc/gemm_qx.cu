@@ -1,8 +1,7 @@
 // Instantiations of the fused GEMM + normalization kernel that quantizes its
 // bf16 activations per row itself (OperandKind::kE4M3Qx: the codes go from
 // the quantizer warps straight into the shared-memory A tile), with E4M3
-// weights kept resident or streamed from L2, and bf16 output.  Rows of at
-// most 256 columns.
+// weights kept resident and bf16 output.  Rows of at most 256 columns.
 #include "gemm_norm.cuh"
 
 namespace loka {
@@ -17,11 +16,8 @@ cudaError_t launch_qx_n(GemmParams& p, int sms, cudaStream_t stream) {
   if (q.stages == 0) return cudaErrorInvalidValue;
   p.stages = q.stages;
   p.a_bufs = q.a_bufs;
-  p.w_stages = q.w_stages;
-  constexpr int op = static_cast<int>(OperandKind::kE4M3Qx);
-  constexpr int out = static_cast<int>(OutKind::kBf16);
-  return q.resident ? launch_one<N, 1, op, out, true>(p, q.smem, sms, stream)
-                    : launch_one<N, 1, op, out, false>(p, q.smem, sms, stream);
+  return launch_one<N, 1, static_cast<int>(OperandKind::kE4M3Qx), static_cast<int>(OutKind::kBf16), true>(
+      p, q.smem, sms, stream);
 }
 
 }  // namespace

@@ -107,7 +107,6 @@ struct GemmParams {
   int32_t x_ready;       // 1: the bf16 X was complete before the launch that precedes this GEMM
                          // (in-kernel quantization reads it before waiting for that launch)
   int32_t a_bufs;        // in-kernel quantization: quantized A tiles in shared memory (1 or 2)
-  int32_t w_stages;      // in-kernel quantization with W streamed: ring slots of W K slices
   int32_t yq_mode;       // quantized output kind: kScaleRow or kScaleMx32
   int32_t norm_block;    // BlockNorm block (32, 64, 128 or 256 columns)
   int32_t act;           // kActNone or kActHardSwish, after the normalization
