@@ -16,7 +16,8 @@ Sources (by page and section):
     high-precision reference, Fig. 5), section III-B (normalization after the
     GEMM, fused into the epilogue; RMSNorm vs LayerNorm), section III-C
     (Dispatch: error and speedup filters, then the fastest candidate),
-    section III-A 1 (the probe's online input statistics and sampler).
+    section III-A 1 (the probe's online input statistics and sampler, and
+    its matrix-normal weight model and weight sampler).
   * "GEM Training: How Meta Doubled the Efficiency ..." section "Low Precision
     Flash Attention" (MXFP8 block-scaled MMA, scale factors along K).
   * The pages name FP8 and MX formats without defining their bits; the E4M3
@@ -28,4 +29,4 @@ Parity status: every function here is pinned by tests in
 ``tests/test_oracle_pins.py`` (exhaustive code tables, brute force on tiny
 inputs, library special cases and invariants).
 """
-from . import formats, quantize, linear, probe, probe_stats, dispatch  # noqa: F401
+from . import formats, quantize, linear, probe, probe_stats, probe_weights, dispatch  # noqa: F401

@@ -630,3 +630,87 @@ def test_dispatch_brute_force_random_tables():
         ok = [e for e in tab if e.variant != 3 and e.rel_err <= 0.01 and e.mere < 0.2 and t_ref / e.time_us > 1.05]
         want = min(ok, key=lambda e: e.time_us).variant if ok else 3
         assert got == want
+
+
+# ------------------------------------------------- probe: weight model
+from oracle import probe_weights as PW
+
+
+def _spd(n, seed, cond=5.0):
+    rng = np.random.default_rng(seed)
+    q, _ = np.linalg.qr(rng.standard_normal((n, n)))
+    return (q * np.linspace(1.0, cond, n)) @ q.T
+
+
+def test_weight_model_second_update_closed_form():
+    # After the first update (M = W1, U = I, V = I) and with no jitter, the
+    # second update is: Wc = W2 - W1, U' = Wc Wc^T / C, V' = Wc^T Wc / R,
+    # U = m I + (1-m) U', V = m I + (1-m) V' (already symmetric), then
+    # s = trace(U) / R, U / s, V * s, M = m W1 + (1-m) W2.  Written out here
+    # element by element.
+    rng = np.random.default_rng(3)
+    R, C, m = 4, 3, 0.9
+    W1, W2 = rng.standard_normal((R, C)), rng.standard_normal((R, C))
+    st = PW.weight_update(None, W1, m, 0.0)
+    assert st.n == 1 and np.array_equal(st.M, W1) and np.array_equal(st.U, np.eye(R))
+    st = PW.weight_update(st, W2, m, 0.0)
+    d = W2 - W1
+    U = np.array([[m * (i == j) + (1 - m) * sum(d[i, k] * d[j, k] for k in range(C)) / C for j in range(R)]
+                  for i in range(R)])
+    V = np.array([[m * (i == j) + (1 - m) * sum(d[k, i] * d[k, j] for k in range(R)) / R for j in range(C)]
+                  for i in range(C)])
+    s = sum(U[i, i] for i in range(R)) / R
+    assert np.allclose(st.U, U / s, rtol=1e-12, atol=1e-14)
+    assert np.allclose(st.V, V * s, rtol=1e-12, atol=1e-14)
+    assert np.allclose(st.M, m * W1 + (1 - m) * W2, rtol=0, atol=1e-15)
+
+
+def test_weight_model_invariants_every_update():
+    rng = np.random.default_rng(4)
+    st = None
+    for t in range(20):
+        st = PW.weight_update(st, rng.standard_normal((6, 5)) * (1 + t % 3), 0.9, 1e-6)
+        assert abs(np.trace(st.U) - 6) < 1e-9                      # the scale renormalization
+        assert np.array_equal(st.U, st.U.T) and np.array_equal(st.V, st.V.T)
+        assert np.linalg.eigvalsh(st.U).min() > 0 and np.linalg.eigvalsh(st.V).min() > 0
+
+
+def test_weight_model_recovers_a_known_kronecker_covariance():
+    # weights drawn from MN(M0, U0, V0): the tracked V (x) U approaches
+    # V0 (x) U0 (the pair itself is defined up to (cU, V/c)) and M
+    # approaches M0
+    R, C = 6, 5
+    U0, V0 = _spd(R, 11), _spd(C, 12)
+    LU0, LV0 = np.linalg.cholesky(U0), np.linalg.cholesky(V0)
+    rng = np.random.default_rng(13)
+    M0 = rng.standard_normal((R, C))
+    st = None
+    for _ in range(3000):
+        st = PW.weight_update(st, M0 + LU0 @ rng.standard_normal((R, C)) @ LV0.T, 0.995, 1e-6)
+    want = np.kron(V0, U0)
+    got = np.kron(st.V, st.U)
+    assert np.linalg.norm(got - want) / np.linalg.norm(want) < 0.15
+    assert np.abs(st.M - M0).max() < 0.5
+    # a transposed Kronecker order (U (x) V) is far off
+    assert np.linalg.norm(np.kron(st.U, st.V) - want) / np.linalg.norm(want) > 0.3
+
+
+def test_weight_sampler_has_the_kronecker_covariance():
+    # vec(W') of the sampler: mean vec(M), covariance V (x) U (plus the
+    # jitter), checked on the sample moments of many seeds
+    R, C = 4, 3
+    st = PW.WeightStats(5, np.arange(R * C, dtype=np.float64).reshape(R, C) / 7.0, _spd(R, 21), _spd(C, 22))
+    samples = np.stack([PW.weight_sample(st, 1e-6, seed)[1].T.reshape(-1) for seed in range(6000)])
+    mean = samples.mean(axis=0)
+    cov = np.cov(samples.T)
+    assert np.abs(mean - st.M.T.reshape(-1)).max() < 0.15
+    want = np.kron(st.V, st.U)
+    assert np.linalg.norm(cov - want) / np.linalg.norm(want) < 0.06
+
+
+def test_forward_solve_residual():
+    rng = np.random.default_rng(5)
+    L = np.tril(rng.standard_normal((7, 7))) + 7 * np.eye(7)
+    B = rng.standard_normal((7, 4))
+    X = PW.forward_solve(L, B)
+    assert np.abs(L @ X - B).max() < 1e-12
