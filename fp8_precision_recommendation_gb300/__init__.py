@@ -223,6 +223,44 @@ class InputStats:
         return L, mu
 
 
+class WeightModel:
+    """LoKA Probe's matrix-normal model of one weight [R, C]: fp32 mean,
+    row covariance U and column covariance V on the device, updated weight by
+    weight on the GPU (loka_probe_weight_update)."""
+
+    def __init__(self, R: int, C: int, device):
+        torch = _torch()
+        self.device = torch.device(device)
+        self.mean = torch.zeros((R, C), dtype=torch.float32, device=self.device)
+        self.U = torch.zeros((R, R), dtype=torch.float32, device=self.device)
+        self.V = torch.zeros((C, C), dtype=torch.float32, device=self.device)
+        self.c = _loka.WeightStats()
+        self.c.n, self.c.R, self.c.C = 0, R, C
+        self.c.mean, self.c.U, self.c.V = self.mean.data_ptr(), self.U.data_ptr(), self.V.data_ptr()
+
+    @property
+    def n(self) -> int:
+        return self.c.n
+
+    def _ws(self, workspace):
+        need = _loka.loka_probe_weight_workspace_size(self.c.R, self.c.C)
+        return (workspace or _ws(self.device)).get(need)
+
+    def update(self, w, momentum: float = 0.95, eps_rel: float = 1e-6, workspace: Optional[Workspace] = None,
+               stream=None) -> None:
+        """Merge the weight w (bf16 CUDA [R, C])."""
+        ws, nbytes = self._ws(workspace)
+        _loka.loka_probe_weight_update(self.c, w, momentum, eps_rel, ws, nbytes, stream)
+
+    def sample(self, seed: int, eps_rel: float = 1e-6, workspace: Optional[Workspace] = None, stream=None):
+        """A synthetic weight M + L_U Z L_V^T (bf16 CUDA [R, C])."""
+        torch = _torch()
+        out = torch.empty((self.c.R, self.c.C), dtype=torch.bfloat16, device=self.device)
+        ws, nbytes = self._ws(workspace)
+        _loka.loka_probe_sample_weights(self.c, eps_rel, seed, out, ws, nbytes, stream)
+        return out
+
+
 def sample_inputs(mu, chol, B: int, seed: int, workspace: Optional[Workspace] = None, stream=None):
     """B synthetic input rows Z L^T + mu (bf16 CUDA [B, K]); mu bf16 [K], chol
     the bf16 [K, K] lower Cholesky factor of the regularized covariance."""

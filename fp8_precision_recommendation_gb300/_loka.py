@@ -51,6 +51,10 @@ class InputStats(ctypes.Structure):
     _fields_ = [("n", c_i64), ("K", c_i64), ("mu", c_p), ("scatter", c_p)]
 
 
+class WeightStats(ctypes.Structure):
+    _fields_ = [("n", c_i64), ("R", c_i64), ("C", c_i64), ("mean", c_p), ("U", c_p), ("V", c_p)]
+
+
 class Policy(ctypes.Structure):
     _fields_ = [("max_rel_err", ctypes.c_double), ("max_mere", ctypes.c_double), ("min_speedup", ctypes.c_double)]
 
@@ -71,6 +75,11 @@ SIGNATURES = {
     "loka_probe_cholesky_workspace_size": (c_sz, [c_i64]),
     "loka_probe_cholesky": (c_i32, [ctypes.POINTER(InputStats), ctypes.c_double, c_p, c_p, c_p, c_sz, c_p]),
     "loka_probe_sample_inputs": (c_i32, [c_p, c_p, c_i64, c_i64, ctypes.c_uint64, c_p, c_p, c_sz, c_p]),
+    "loka_probe_weight_workspace_size": (c_sz, [c_i64, c_i64]),
+    "loka_probe_weight_update": (c_i32, [ctypes.POINTER(WeightStats), c_p, ctypes.c_double, ctypes.c_double, c_p,
+                                         c_sz, c_p]),
+    "loka_probe_sample_weights": (c_i32, [ctypes.POINTER(WeightStats), ctypes.c_double, ctypes.c_uint64, c_p, c_p,
+                                          c_sz, c_p]),
     "loka_fp8_linear_norm_workspace_size": (c_sz, [ctypes.POINTER(LinearDesc), c_i32]),
     "loka_fp8_linear_norm": (c_i32, [ctypes.POINTER(LinearDesc), c_i32, c_p, c_sz, c_p]),
     "loka_fp8_linear_norm_static": (c_i32, [ctypes.POINTER(LinearDesc), c_i32, c_p]),
@@ -189,6 +198,22 @@ def loka_probe_sample_inputs(mu, chol, B: int, K: int, seed: int, out, workspace
                              stream=None) -> None:
     check(load().loka_probe_sample_inputs(_ptr(mu), _ptr(chol), B, K, seed, _ptr(out), _ptr(workspace),
                                           workspace_bytes, _stream(stream)))
+
+
+def loka_probe_weight_workspace_size(R: int, C: int) -> int:
+    return load().loka_probe_weight_workspace_size(R, C)
+
+
+def loka_probe_weight_update(stats: WeightStats, w, momentum: float, eps_rel: float, workspace, workspace_bytes: int,
+                             stream=None) -> None:
+    check(load().loka_probe_weight_update(ctypes.byref(stats), _ptr(w), momentum, eps_rel, _ptr(workspace),
+                                          workspace_bytes, _stream(stream)))
+
+
+def loka_probe_sample_weights(stats: WeightStats, eps_rel: float, seed: int, out, workspace, workspace_bytes: int,
+                              stream=None) -> None:
+    check(load().loka_probe_sample_weights(ctypes.byref(stats), eps_rel, seed, _ptr(out), _ptr(workspace),
+                                           workspace_bytes, _stream(stream)))
 
 
 def make_descs(descs: Sequence[LinearDesc]):

@@ -901,3 +901,115 @@ loka_status loka_probe_sample_inputs(const void* mu, const void* chol, int64_t B
 }
 
 }  // extern "C"
+
+namespace {
+
+// Workspace of the probe's weight model: Wc, W_V, W_U [R, C]; L_U, U' [R, R];
+// L_V, V' [C, C] (fp32); 2 fp64 traces; 2 status words.
+WeightWork weight_layout(int64_t R, int64_t C, uint8_t* base, size_t* total) {
+  WeightWork w{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes);
+    return base + o;
+  };
+  const size_t rc = static_cast<size_t>(R) * C * sizeof(float);
+  w.wc = reinterpret_cast<float*>(take(rc));
+  w.wv = reinterpret_cast<float*>(take(rc));
+  w.wu = reinterpret_cast<float*>(take(rc));
+  w.lu = reinterpret_cast<float*>(take(static_cast<size_t>(R) * R * sizeof(float)));
+  w.u1 = reinterpret_cast<float*>(take(static_cast<size_t>(R) * R * sizeof(float)));
+  w.lv = reinterpret_cast<float*>(take(static_cast<size_t>(C) * C * sizeof(float)));
+  w.v1 = reinterpret_cast<float*>(take(static_cast<size_t>(C) * C * sizeof(float)));
+  w.trace = reinterpret_cast<double*>(take(2 * sizeof(double)));
+  w.status = reinterpret_cast<int*>(take(2 * sizeof(int)));
+  if (total) *total = off;
+  return w;
+}
+
+bool weight_dims_ok(int64_t R, int64_t C) { return R >= 2 && C >= 2 && R <= 2048 && C <= 2048 && C % 2 == 0; }
+
+loka_status weight_check(const loka_weight_stats* st, void* workspace, size_t workspace_bytes, WeightWork* w) {
+  if (st == nullptr) return fail(LOKA_ERR_INVALID_ARG, "stats is NULL");
+  if (!weight_dims_ok(st->R, st->C))
+    return fail(LOKA_ERR_UNSUPPORTED, "R = %lld, C = %lld: the weight model takes 2 <= R, C <= 2048, C even",
+                static_cast<long long>(st->R), static_cast<long long>(st->C));
+  if (st->mean == nullptr || st->U == nullptr || st->V == nullptr)
+    return fail(LOKA_ERR_INVALID_ARG, "mean, U and V must not be NULL");
+  if ((reinterpret_cast<uintptr_t>(st->mean) | reinterpret_cast<uintptr_t>(st->U) | reinterpret_cast<uintptr_t>(st->V)) & 3u)
+    return fail(LOKA_ERR_INVALID_ARG, "mean, U and V must be 4-byte aligned");
+  size_t need = 0;
+  weight_layout(st->R, st->C, nullptr, &need);
+  if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(LOKA_ERR_WORKSPACE, "workspace must be >= %zu bytes, 256-byte aligned", need);
+  *w = weight_layout(st->R, st->C, static_cast<uint8_t*>(workspace), nullptr);
+  return LOKA_OK;
+}
+
+// Reads the two factorization status words after the stream has finished.
+loka_status weight_status(const WeightWork& w, cudaStream_t st) {
+  int host[2] = {0, 0};
+  cudaError_t e = cudaMemcpyAsync(host, w.status, sizeof(host), cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the factorization status");
+  if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e, "weight model");
+  if (host[0] || host[1])
+    return fail(LOKA_ERR_NUMERIC, "the regularized %s covariance is not positive definite", host[0] ? "row" : "column");
+  return LOKA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t loka_probe_weight_workspace_size(int64_t R, int64_t C) {
+  if (!weight_dims_ok(R, C)) return 0;
+  size_t need = 0;
+  weight_layout(R, C, nullptr, &need);
+  return need;
+}
+
+loka_status loka_probe_weight_update(loka_weight_stats* stats, const void* w, double momentum, double eps_rel,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+  WeightWork ww{};
+  loka_status s = weight_check(stats, workspace, workspace_bytes, &ww);
+  if (s != LOKA_OK) return s;
+  if (w == nullptr || (reinterpret_cast<uintptr_t>(w) & 1u)) return fail(LOKA_ERR_INVALID_ARG, "w must be a bf16 array");
+  if (!(momentum >= 0.0 && momentum < 1.0)) return fail(LOKA_ERR_INVALID_ARG, "momentum must be in [0, 1)");
+  if (!(eps_rel >= 0.0) || !std::isfinite(eps_rel)) return fail(LOKA_ERR_INVALID_ARG, "eps_rel must be finite and >= 0");
+  if (stats->n < 0) return fail(LOKA_ERR_INVALID_ARG, "negative update count");
+  DeviceInfo* dev = nullptr;
+  if ((s = device_info(&dev)) != LOKA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (stats->n == 0) {
+    e = launch_weight_init(w, stats->R, stats->C, stats->mean, stats->U, stats->V, dev->sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "weight model start");
+    stats->n = 1;
+    return LOKA_OK;
+  }
+  e = launch_weight_update(w, stats->R, stats->C, momentum, eps_rel, stats->mean, stats->U, stats->V, ww, dev->sms, st);
+  if (e != cudaSuccess) return cuda_fail(e, "weight model update");
+  if ((s = weight_status(ww, st)) != LOKA_OK) return s;
+  stats->n += 1;
+  return LOKA_OK;
+}
+
+loka_status loka_probe_sample_weights(const loka_weight_stats* stats, double eps_rel, uint64_t seed, void* out,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  WeightWork ww{};
+  loka_status s = weight_check(stats, workspace, workspace_bytes, &ww);
+  if (s != LOKA_OK) return s;
+  if (stats->n < 1) return fail(LOKA_ERR_INVALID_ARG, "the weight model has no update yet");
+  if (out == nullptr || (reinterpret_cast<uintptr_t>(out) & 1u)) return fail(LOKA_ERR_INVALID_ARG, "out must be a bf16 array");
+  if (!(eps_rel >= 0.0) || !std::isfinite(eps_rel)) return fail(LOKA_ERR_INVALID_ARG, "eps_rel must be finite and >= 0");
+  DeviceInfo* dev = nullptr;
+  if ((s = device_info(&dev)) != LOKA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_weight_sample(stats->mean, stats->U, stats->V, stats->R, stats->C, eps_rel, seed, out, ww,
+                                       dev->sms, st);
+  if (e != cudaSuccess) return cuda_fail(e, "weight sampler");
+  return weight_status(ww, st);
+}
+
+}  // extern "C"

@@ -156,6 +156,25 @@ cudaError_t launch_stats_merge(const float* colpart, int64_t tiles, const float*
                                double* colwork /* 35 K fp64 */, double* mu, double* S, int64_t n_old, int64_t nb,
                                int sms, cudaStream_t stream);
 cudaError_t launch_normals(uint64_t seed, int64_t count, void* z, int sms, cudaStream_t stream);
+cudaError_t launch_normals_f32(uint64_t seed, int64_t count, float* z, int sms, cudaStream_t stream);
+
+// Probe weight model (probe_weights.cu): the matrix-normal W ~ MN(M, U, V)
+// of a weight [R, C].  Workspace (fp32 unless noted): Wc, W_V, W_U [R, C];
+// L_U, U' [R, R]; L_V, V' [C, C]; 2 fp64 traces and a status word.
+struct WeightWork {
+  float *wc, *wv, *wu, *lu, *u1, *lv, *v1;
+  double* trace;   // [2]
+  int* status;     // [2]: a non-positive pivot in the factor of U (0) or V (1)
+};
+// First update: M = W, U = I, V = I.
+cudaError_t launch_weight_init(const void* w, int64_t R, int64_t C, float* M, float* U, float* V, int sms,
+                               cudaStream_t stream);
+// One flip-flop update of (M, U, V) with W (bf16 [R, C]), momentum m.
+cudaError_t launch_weight_update(const void* w, int64_t R, int64_t C, double m, double eps_rel, float* M, float* U,
+                                 float* V, const WeightWork& ws, int sms, cudaStream_t stream);
+// W' = M + L_U Z L_V^T (bf16 [R, C]); Z: the seed's counter-based normals.
+cudaError_t launch_weight_sample(const float* M, const float* U, const float* V, int64_t R, int64_t C, double eps_rel,
+                                 uint64_t seed, void* out, const WeightWork& ws, int sms, cudaStream_t stream);
 // cov (fp64 [K, K]) = S / (n - 1)
 cudaError_t launch_covariance(const double* S, int64_t K, int64_t n, double* cov, int sms, cudaStream_t stream);
 // Cholesky factor of S / (n - 1) + eps I (one block, fp32; A: K x K fp32

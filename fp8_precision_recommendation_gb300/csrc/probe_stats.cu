@@ -157,7 +157,9 @@ __device__ __forceinline__ uint64_t splitmix64(uint64_t s) {
 // Z [count] bf16: normal pair j from random numbers 2j and 2j + 1 of the
 // seed's counter-based stream (state seed + (i + 1) * golden gamma), by
 // Box-Muller on 24-bit uniforms, in fp32.
-__global__ void __launch_bounds__(256) normals_kernel(uint64_t seed, int64_t pairs, uint32_t* __restrict__ z) {
+// Normal pair j as bf16 (packed, F32 = false) or fp32 (F32 = true).
+template <bool F32>
+__global__ void __launch_bounds__(256) normals_kernel(uint64_t seed, int64_t pairs, void* __restrict__ z) {
   constexpr uint64_t kGamma = 0x9E3779B97F4A7C15ull;
   for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < pairs;
        j += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -169,7 +171,10 @@ __global__ void __launch_bounds__(256) normals_kernel(uint64_t seed, int64_t pai
     const float rad = sqrtf(-2.0f * logf(u1));
     float s, c;
     sincospif(2.0f * u2, &s, &c);
-    z[j] = pack_bf16x2(rad * c, rad * s);
+    if (F32)
+      static_cast<float2*>(z)[j] = make_float2(rad * c, rad * s);
+    else
+      static_cast<uint32_t*>(z)[j] = pack_bf16x2(rad * c, rad * s);
   }
 }
 
@@ -309,7 +314,13 @@ cudaError_t launch_covariance(const double* S, int64_t K, int64_t n, double* cov
 
 cudaError_t launch_normals(uint64_t seed, int64_t count, void* z, int sms, cudaStream_t stream) {
   const int64_t pairs = count / 2;
-  normals_kernel<<<grid_for(pairs, sms), 256, 0, stream>>>(seed, pairs, static_cast<uint32_t*>(z));
+  normals_kernel<false><<<grid_for(pairs, sms), 256, 0, stream>>>(seed, pairs, z);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_normals_f32(uint64_t seed, int64_t count, float* z, int sms, cudaStream_t stream) {
+  const int64_t pairs = count / 2;
+  normals_kernel<true><<<grid_for(pairs, sms), 256, 0, stream>>>(seed, pairs, z);
   return cudaGetLastError();
 }
 

@@ -372,6 +372,54 @@ size_t loka_probe_sample_workspace_size(int64_t B, int64_t K);
 loka_status loka_probe_sample_inputs(const void* mu, const void* chol, int64_t B, int64_t K, uint64_t seed,
                                      void* out, void* workspace, size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------------------------------
+ * LoKA Probe: the weight model.
+ *
+ * Defined by LoKA section III-A 1, "Optimized Weight Distribution Modeling"
+ * and "Sampling learned distributions" (b): a weight W [R, C] is modeled as
+ * matrix-normal, W ~ MN(M, U, V), vec(W) ~ N(vec(M), V (x) U), with the row
+ * covariance U [R, R] and column covariance V [C, C] tracked by a
+ * Kronecker-factor (flip-flop) update smoothed by an exponential moving
+ * average, through linear solves against regularized Cholesky factors.
+ *
+ * loka_probe_weight_update merges one weight w (bf16 [R, C], device) into
+ * *stats.  The first call (n == 0) starts the model: M = W, U = I, V = I.
+ * Every later call, with eps_A = eps_rel * trace(A) / dim(A) on the matrix A
+ * it regularizes (the page suggests eps_rel about 1e-6):
+ *   Wc = W - M;  L_V L_V^T = V + eps_V I,  U' = (Wc L_V^-T)(Wc L_V^-T)^T / C;
+ *   L_U L_U^T = U + eps_U I,  V' = (L_U^-1 Wc)^T (L_U^-1 Wc) / R
+ *   (both with the U, V held before the call);
+ *   U'' = m U + (1-m) U',  V'' = m V + (1-m) V'  (m = momentum, in [0, 1));
+ *   U = (U'' + U''^T)/2 + eps_U I,  V = (V'' + V''^T)/2 + eps_V I;
+ *   s = trace(U)/R,  U /= s,  V *= s  (V (x) U unchanged);  M = m M + (1-m) W.
+ * mean (fp32 [R, C]), U (fp32 [R, R]) and V (fp32 [C, C], all row-major)
+ * are caller-owned device arrays; n is advanced on the host.  fp32 SIMT
+ * kernels (a once-per-probe-interval step off the data-parallel path).
+ * 2 <= R, C <= 2048, C even.  LOKA_ERR_NUMERIC when a factor's pivot is not
+ * positive.  Synchronizes the stream (except for the first call).
+ *
+ * loka_probe_sample_weights writes out (bf16 [R, C]) = M + L_U Z L_V^T with
+ * L_U L_U^T = U + eps_U I, L_V L_V^T = V + eps_V I and Z the counter-based
+ * normals of `seed` (Z[r, c] is normal r C + c, the stream of
+ * loka_probe_sample_inputs, in fp32).  Synchronizes the stream.
+ * workspace: loka_probe_weight_workspace_size(R, C) bytes, 256-byte aligned,
+ * for both calls.
+ * ---------------------------------------------------------------------- */
+typedef struct loka_weight_stats {
+  int64_t n;             /* updates merged so far (host) */
+  int64_t R;             /* weight rows */
+  int64_t C;             /* weight columns */
+  float* mean;           /* device fp32 [R, C] */
+  float* U;              /* device fp32 [R, R] */
+  float* V;              /* device fp32 [C, C] */
+} loka_weight_stats;
+
+size_t loka_probe_weight_workspace_size(int64_t R, int64_t C);
+loka_status loka_probe_weight_update(loka_weight_stats* stats, const void* w, double momentum, double eps_rel,
+                                     void* workspace, size_t workspace_bytes, void* stream);
+loka_status loka_probe_sample_weights(const loka_weight_stats* stats, double eps_rel, uint64_t seed, void* out,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -49,7 +49,8 @@ def test_struct_layouts_match_header(tmp_path):
     # header against the ctypes binding
     structs = {"loka_linear_desc": _loka.LinearDesc, "loka_error_stats": _loka.ErrorStats,
                "loka_problem": _loka.Problem, "loka_dispatch_entry": _loka.DispatchEntry,
-               "loka_policy": _loka.Policy, "loka_input_stats": _loka.InputStats}
+               "loka_policy": _loka.Policy, "loka_input_stats": _loka.InputStats,
+               "loka_weight_stats": _loka.WeightStats}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "loka.h"', "int main(void) {"]
     for cname, cls in structs.items():
         lines.append(f'  printf("{cname} size %zu\\n", sizeof({cname}));')
@@ -231,6 +232,25 @@ def test_probe_covariance_rejects_bad_arguments_on_host(cpu_lib):
     assert cov(ctypes.byref(st), (1 << 22) + 4, None) == _loka.LOKA_ERR_INVALID_ARG    # alignment
     st.scatter = None
     assert cov(ctypes.byref(st), 1 << 22, None) == _loka.LOKA_ERR_INVALID_ARG
+
+
+def test_weight_model_rejects_bad_arguments_on_host(cpu_lib):
+    st = _loka.WeightStats()
+    st.n, st.R, st.C, st.mean, st.U, st.V = 0, 64, 96, 1 << 20, 1 << 21, 1 << 22
+    upd = cpu_lib.loka_probe_weight_update
+    assert upd(ctypes.byref(st), 1 << 23, 0.9, 1e-6, None, 0, None) == _loka.LOKA_ERR_WORKSPACE
+    need = _loka.loka_probe_weight_workspace_size(64, 96)
+    assert need >= 3 * 64 * 96 * 4 + 2 * 64 * 64 * 4 + 2 * 96 * 96 * 4
+    assert upd(ctypes.byref(st), 1 << 23, 1.0, 1e-6, 1 << 24, need, None) == _loka.LOKA_ERR_INVALID_ARG   # momentum
+    assert upd(ctypes.byref(st), None, 0.9, 1e-6, 1 << 24, need, None) == _loka.LOKA_ERR_INVALID_ARG
+    st.C = 97
+    assert upd(ctypes.byref(st), 1 << 23, 0.9, 1e-6, 1 << 24, need, None) == _loka.LOKA_ERR_UNSUPPORTED  # odd C
+    st.C, st.R = 96, 4096
+    assert upd(ctypes.byref(st), 1 << 23, 0.9, 1e-6, 1 << 24, need, None) == _loka.LOKA_ERR_UNSUPPORTED  # R too large
+    assert _loka.loka_probe_weight_workspace_size(4096, 96) == 0
+    st.R = 64
+    smp = cpu_lib.loka_probe_sample_weights
+    assert smp(ctypes.byref(st), 1e-6, 1, 1 << 23, 1 << 24, need, None) == _loka.LOKA_ERR_INVALID_ARG    # n == 0
 
 
 def _c_table(rows):
