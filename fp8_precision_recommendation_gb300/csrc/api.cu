@@ -145,6 +145,14 @@ size_t scale_bytes(int mode, int64_t rows, int64_t cols) {
   return 0;
 }
 
+// Columns the GEMM's CTAs span for an output row of N: the kernel width up
+// to 256, else the cluster's (or slices') 256-column CTAs.
+int64_t padded_cols(int64_t N) {
+  int local = 0, cl = 0;
+  if (!split_n_host(static_cast<int>(N), &local, &cl)) return N;
+  return N <= 256 ? local : ((N + 255) / 256 > cl ? (N + 255) / 256 : cl) * 256;
+}
+
 struct OperandSlots {   // workspace offsets of one group's quantized operands
   size_t xq, sx, wq, sw, amax;
   size_t sx_tc, sw_tc;   // MX: scale codes in the tensor-memory copy layout
@@ -177,7 +185,9 @@ size_t layout_operands(const loka_linear_desc* d, int n, std::vector<OperandSlot
         s.sx_tc = off;
         off = align_up(off + static_cast<size_t>(sf_tc_bytes(d[i].M, d[i].K)));
         s.sw_tc = off;
-        off = align_up(off + static_cast<size_t>(sf_tc_bytes(d[i].N, d[i].K)));
+        // the CTAs load whole 128-row blocks of W's codes for all the columns
+        // they span, past N when the row does not fill them
+        off = align_up(off + static_cast<size_t>(sf_tc_bytes(padded_cols(d[i].N), d[i].K)));
       }
     }
     if (slots) (*slots)[i] = s;
@@ -229,12 +239,11 @@ loka_status validate(const loka_linear_desc* d, int n, bool probe) {
     if (a.N % b != 0)
       return fail(LOKA_ERR_INVALID_ARG, "norm_block %d does not divide N = %lld", b, static_cast<long long>(a.N));
   }
-  if (a.K < 128 || a.K % 128 != 0)
-    return fail(LOKA_ERR_UNSUPPORTED, "K = %lld: K must be a positive multiple of 128", static_cast<long long>(a.K));
+  if (a.K < 32 || a.K % 32 != 0)
+    return fail(LOKA_ERR_UNSUPPORTED, "K = %lld: K must be a positive multiple of 32", static_cast<long long>(a.K));
   if (a.K > (int64_t(1) << 20)) return fail(LOKA_ERR_UNSUPPORTED, "K too large");
-  if (!(a.N == 64 || a.N == 128 || a.N == 192 || a.N == 256 || a.N == 512 || a.N == 1024 || a.N == 2048))
-    return fail(LOKA_ERR_UNSUPPORTED, "N = %lld: supported N are 64, 128, 192, 256, 512, 1024, 2048",
-                static_cast<long long>(a.N));
+  if (a.N < 32 || a.N > 2048 || a.N % 32 != 0)
+    return fail(LOKA_ERR_UNSUPPORTED, "N = %lld: N must be a multiple of 32 in [32, 2048]", static_cast<long long>(a.N));
   if (!gemm_supported(static_cast<int>(a.N), static_cast<int>(a.K), operand_kind(a.mode)) ||
       (probe && !gemm_supported(static_cast<int>(a.N), static_cast<int>(a.K), OperandKind::kBf16)))
     return fail(LOKA_ERR_UNSUPPORTED, "no shared-memory plan for N = %lld, K = %lld", static_cast<long long>(a.N),
@@ -347,6 +356,15 @@ loka_status build_gemm(const loka_linear_desc* d, int n, const std::vector<Opera
   return LOKA_OK;
 }
 
+// Block-scaled operands whose K is not a multiple of 128: the tensor-memory
+// copy of their scale codes has a partial last K block, whose codes past K
+// must be finite (the MMA multiplies the zeros read past K by them), so the
+// whole copy starts as E8M0 127 (2^0) before the real codes are written.
+cudaError_t pad_scale_codes(uint8_t* sf_tc, int64_t rows, int64_t cols, cudaStream_t stream) {
+  if (sf_tc == nullptr || cols % 128 == 0 || rows == 0) return cudaSuccess;
+  return cudaMemsetAsync(sf_tc, 127, static_cast<size_t>(sf_tc_bytes(rows, cols)), stream);
+}
+
 // Quantizes every bf16 operand of the groups into the workspace (one launch
 // for X and W of all groups; tensorwise scaling takes an amax launch first).
 // w_only: the weights alone (the GEMM quantizes X itself).
@@ -386,6 +404,10 @@ loka_status quantize_operands(const loka_linear_desc* d, int n, const std::vecto
   }
   jobs.total_rows = rows;
   if (jobs.n == 0) return LOKA_OK;
+  for (int i = 0; i < jobs.n; ++i) {
+    cudaError_t e = pad_scale_codes(jobs.j[i].sf_tc, jobs.j[i].rows, jobs.j[i].cols, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "scale-code padding");
+  }
   cudaError_t e = launch_quantize(jobs, d[0].mode, dev->sms, stream);
   if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
   return LOKA_OK;
@@ -544,7 +566,9 @@ loka_status loka_fp8_linear_norm(const loka_linear_desc* descs, int32_t num_grou
     for (int i = 0; i < num_groups; ++i) {
       const loka_linear_desc& g = descs[i];
       cudaError_t e = cudaSuccess;
-      if (g.x_is_fp8 && g.M > 0)
+      if (g.x_is_fp8 && g.M > 0) e = pad_scale_codes(ws + slots[i].sx_tc, g.M, g.K, st);
+      if (e == cudaSuccess && g.w_is_fp8) e = pad_scale_codes(ws + slots[i].sw_tc, g.N, g.K, st);
+      if (e == cudaSuccess && g.x_is_fp8 && g.M > 0)
         e = launch_sf_permute(static_cast<const uint8_t*>(g.x_scales), ws + slots[i].sx_tc, g.M, g.K, row_div, dev->sms,
                               st);
       if (e == cudaSuccess && g.w_is_fp8)

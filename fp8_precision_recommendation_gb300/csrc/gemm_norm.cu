@@ -11,6 +11,8 @@ bool gemm_supported(int N, int K, OperandKind op) {
   return plan_for(local, K, op == OperandKind::kBf16 ? 2 : 1, op == OperandKind::kMxE4M3, cl).stages > 0;
 }
 
+bool split_n_host(int N, int* local, int* cl) { return split_n(N, local, cl); }
+
 bool gemm_qx_supported(int N, int K, int norm, OutKind out) {
   const GemmRoute r = gemm_route(N, norm);
   if (out != OutKind::kBf16 || r.cl != 1 || r.slices != 1) return false;
@@ -25,18 +27,24 @@ bool gemm_qx_supported(int N, int K, int norm, OutKind out) {
 
 GemmRoute gemm_route(int N, int norm) {
   const bool no_row_stat = norm == kNormNone || norm == kNormBlockRms;
+  int local = 0, cl = 0;
+  if (!split_n(N, &local, &cl)) return GemmRoute{0, 0, 0};
   // Rows wider than one CTA whose epilogue needs no row statistic (no norm,
   // or BlockNorm, whose blocks lie within a CTA's 256 columns) run as
-  // independent 256-column slices: no cluster co-scheduling, every SM busy.
-  if (N > 256) return no_row_stat ? GemmRoute{256, 1, N / 256} : GemmRoute{256, N / 256, 1};
-  return GemmRoute{N, 1, 1};
+  // independent 256-column slices, the last one partial: no cluster
+  // co-scheduling, every SM busy.
+  if (N > 256 && no_row_stat) return GemmRoute{256, 1, (N + 255) / 256};
+  return GemmRoute{local, cl, 1};
 }
 
 cudaError_t launch_gemm_norm(GemmParams& p, int N, OperandKind op, OutKind out, int sms, cudaStream_t stream) {
   const GemmRoute r = gemm_route(N, p.norm);
+  if (r.local == 0) return cudaErrorInvalidValue;
   p.slices = r.slices;
-  // the launchers take the row width: up to 256 one CTA, wider a cluster
-  N = r.cl > 1 ? N : r.local;
+  p.n_cols = N;
+  // the launchers take the kernel's width: up to 256 one CTA, wider a
+  // cluster of r.cl CTAs of 256 columns
+  N = r.cl > 1 ? r.cl * 256 : r.local;
   if (out == OutKind::kQuant) {
     const bool wide = N > 256;
     if (op == OperandKind::kE4M3)

@@ -121,7 +121,7 @@ __host__ __device__ inline Layout make_layout(int N, int K, int elem_bytes, bool
   L.ring = 0;
   L.a = L.ring + static_cast<uint32_t>(stages) * L.stage_bytes;
   L.w = L.a + static_cast<uint32_t>(a_bufs) * kBM * static_cast<uint32_t>(K);
-  const int nkb = K * elem_bytes / kSliceBytes;
+  const int nkb = (K * elem_bytes + kSliceBytes - 1) / kSliceBytes;   // the last slice may be partial
   // resident W: [nkb B slices][nkb x B scale blocks]
   const uint32_t w_bytes = resident ? static_cast<uint32_t>(nkb) * (b_slice + sfb) : 0u;
   L.vec = L.w + w_bytes;
@@ -158,7 +158,6 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
   constexpr bool kQx = OP == static_cast<int>(OperandKind::kE4M3Qx);
   static_assert(!kQx || (CL == 1 && RESIDENT), "in-kernel quantization keeps W resident and rows within a CTA");
   constexpr int EPI0 = kQx ? kQxEpiWarp : 2;       // first epilogue warp
-  constexpr int NG = N * CL;                        // columns of the whole output row
   constexpr int SF_COLS_MAX = OP == static_cast<int>(OperandKind::kMxE4M3) ? kMaxStages * (4 + 4 * sfb_blocks(N)) : 0;
   constexpr int NBUF = (2 * N + SF_COLS_MAX <= kTmemCols) ? 2 : 1;
   static_assert(N + SF_COLS_MAX <= kTmemCols, "accumulator and scale factors must fit in tensor memory");
@@ -176,7 +175,9 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
   constexpr uint32_t B_SLICE = static_cast<uint32_t>(N) * kSliceBytes;
 
   const int stages = p.stages;
-  const int num_kb = p.K / KE;
+  // K slices of 128 bytes; a partial last slice reads zeros past K (the
+  // tensor maps' out-of-range fill), which add nothing to the sums
+  const int num_kb = (p.K + KE - 1) / KE;
   const Layout L = make_layout(N, p.K, EB, RESIDENT, stages, kMx, CL, kQx ? p.a_bufs : 0);
   // A tile's N-column slices go to the CTAs of a cluster (CL > 1, row
   // statistics exchanged), or, when no statistic spans the row (CL == 1,
@@ -187,7 +188,14 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
   const int col0 = static_cast<int>(rank) * N;      // first output column of this CTA
   const int cid = static_cast<int>(blockIdx.x) / slices;
   const int ncl = static_cast<int>(gridDim.x) / slices;
-  const int ng = N * slices;                        // columns of the whole output row
+  // columns of the whole output row (the row pitch of the outputs), and the
+  // ones this CTA holds: the kernel's N columns from col0 on, fewer (down to
+  // none) when the row is narrower than the CTAs' columns (rows of any
+  // multiple of 32 run on the next wider kernel; the weight rows past the
+  // row width read as zeros)
+  const int ng = p.n_cols;
+  const int nvalid = ng - col0 < 0 ? 0 : (ng - col0 > N ? N : ng - col0);
+  const int nvc = nvalid / 32;                      // valid 32-column chunks
 
   // Pointers are derived from the __shared__ array by plain offsets, so the
   // compiler keeps them in the shared address space (LDS/STS, not generic
@@ -708,18 +716,21 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
       const int o = 4 * i + 2 * k;
       return make_float2(__uint_as_float(r[o]), __uint_as_float(r[o + 1]));
     };
-    // Runs fn(r, c) over the chunks c = 0 .. NCHUNK-1, the TMEM read of chunk
+    // Runs fn(r, c) over the valid chunks c = 0 .. nvc-1, the TMEM read of chunk
     // c + 1 in flight while chunk c is processed.
     auto for_chunks = [&](uint32_t t_base, auto&& fn) {
+      if (nvc == 0) return;
       uint32_t r[2][16];
       tmem_ld_16x256b_x4(t_base, r[0]);
       tmem_ld_wait();
       reg_fence(r[0]);
 #pragma unroll
       for (int c = 0; c < NCHUNK; ++c) {
-        if (c + 1 < NCHUNK) tmem_ld_16x256b_x4(t_base + (c + 1) * 32, r[(c + 1) & 1]);
+        if (c >= nvc) break;
+        const bool more = c + 1 < nvc;   // uniform over the warp
+        if (more) tmem_ld_16x256b_x4(t_base + (c + 1) * 32, r[(c + 1) & 1]);
         fn(r[c & 1], c);
-        if (c + 1 < NCHUNK) {
+        if (more) {
           tmem_ld_wait();
           reg_fence(r[(c + 1) & 1]);
         }
@@ -780,10 +791,11 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
         }
         for (int n = (ew & 7) * 32 + lane; n < N; n += 256) {
           const int gn = col0 + n;
-          vec_sw[n] = (G.sw != nullptr && G.sw_per_row) ? G.sw[gn] : 1.0f;
-          vec_b[n] = G.bias == nullptr ? 0.0f : bf16_to_f(G.bias[gn]) - mu_b;
-          vec_g[n] = (G.gamma == nullptr || !normed) ? 1.0f : bf16_to_f(G.gamma[gn]);
-          vec_be[n] = (G.beta == nullptr || norm != kNormLayer) ? 0.0f : bf16_to_f(G.beta[gn]);
+          const bool in = n < nvalid;   // the kernel's columns past the row hold nothing
+          vec_sw[n] = (in && G.sw != nullptr && G.sw_per_row) ? G.sw[gn] : 1.0f;
+          vec_b[n] = (!in || G.bias == nullptr) ? 0.0f : bf16_to_f(G.bias[gn]) - mu_b;
+          vec_g[n] = (!in || G.gamma == nullptr || !normed) ? 1.0f : bf16_to_f(G.gamma[gn]);
+          vec_be[n] = (!in || G.beta == nullptr || norm != kNormLayer) ? 0.0f : bf16_to_f(G.beta[gn]);
         }
         affine = normed && (G.gamma != nullptr || (G.beta != nullptr && norm == kNormLayer));
         if constexpr (kQx) {
@@ -882,10 +894,11 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
               m2[k] += a2.x + a2.y;
             }
           });
-          constexpr float kInvMe = 1.0f / (8.0f * NCHUNK);
+          // each lane holds 8 values of a row per valid chunk
+          const float inv_me = nvc > 0 ? 1.0f / (8.0f * static_cast<float>(nvc)) : 0.0f;
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
-            const float d = s1[k] * kInvMe;
+            const float d = s1[k] * inv_me;
             mean[k] = shift[k] + d;
             m2[k] = fmaxf(m2[k] - s1[k] * d, 0.0f);
           }
@@ -963,7 +976,7 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
 #pragma unroll
         for (int lvl = 0; lvl < 2; ++lvl) {
           const int off = 1 << lvl;
-          const float half_n = 4.0f * NCHUNK * static_cast<float>(off);   // n_a n_b / (n_a + n_b)
+          const float half_n = 4.0f * static_cast<float>(nvc) * static_cast<float>(off);   // n_a n_b / (n_a + n_b)
           const bool lo_side = (lane & off) == 0;
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
@@ -1002,24 +1015,30 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
             }
           }
           if (!warp_wait(smem_u32(&cl_bar[cb]), cphase, true)) break;
-          // merge the CTAs' statistics in rank order (N elements each)
+          // merge the CTAs' statistics in rank order (Chan: CTA j holds the
+          // row's valid columns from j N on, possibly none)
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
-            float mA = 0.f, qA = 0.f;
+            float mA = 0.f, qA = 0.f, nA = 0.f;
 #pragma unroll
             for (int j = 0; j < CL; ++j) {
               const float2 part_j = j == static_cast<int>(rank) ? make_float2(mean[k], m2[k])
                                                                 : cl_stats[(cb * CL + j) * kBM + rowk[k]];
+              const int left = ng - j * N;
+              const float nb = static_cast<float>(left <= 0 ? 0 : (left > N ? N : left));
               if (norm == kNormRms) {
                 qA += part_j.y;
-              } else if (j == 0) {
-                mA = part_j.x;
-                qA = part_j.y;
-              } else {
-                const float delta = part_j.x - mA;
-                const float w = 1.0f / static_cast<float>(j + 1);          // n_b / n_total
-                mA = fmaf(delta, w, mA);
-                qA += part_j.y + delta * delta * (static_cast<float>(N) * j * w);
+              } else if (nb > 0.0f) {
+                if (nA == 0.0f) {
+                  mA = part_j.x;
+                  qA = part_j.y;
+                } else {
+                  const float delta = part_j.x - mA;
+                  const float w = nb / (nA + nb);                        // n_b / n_total
+                  mA = fmaf(delta, w, mA);
+                  qA += part_j.y + delta * delta * (nA * w);             // n_a n_b / n_total
+                }
+                nA += nb;
               }
             }
             mean[k] = norm == kNormRms ? 0.0f : mA;
@@ -1033,8 +1052,9 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
             for (int j = 0; j < CL; ++j) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&cl_free[cb]), j));
           }
         }
+        const float inv_ng = 1.0f / static_cast<float>(ng);
 #pragma unroll
-        for (int k = 0; k < 2; ++k) rstd[k] = rsqrtf(m2[k] * (1.0f / NG) + eps);
+        for (int k = 0; k < 2; ++k) rstd[k] = rsqrtf(m2[k] * inv_ng + eps);
       } else if (norm == kNormBlockRms) {
         const float inv_b = 1.0f / static_cast<float>(p.norm_block);   // a power of two: exact
 #pragma unroll
@@ -1443,15 +1463,21 @@ cudaError_t launch_res(const GemmParams& p, const Plan& pl, int sms, cudaStream_
                      : launch_one<N, CL, OP, OUT, false>(p, pl.smem, sms, stream);
 }
 
-// (local width, cluster size) of an output row of N columns
+// (columns per CTA, cluster size) of an output row of N columns (a multiple
+// of 32 up to 2048) when its statistics span the row: up to 256 columns one
+// CTA of the next instantiated width (64, 128, 192, 256); wider, a cluster of
+// 2, 4 or 8 CTAs of 256 columns, the last ones holding the remainder (or
+// nothing).
 bool split_n(int N, int* local, int* cl) {
-  switch (N) {
-    case 64: case 128: case 192: case 256: *local = N; *cl = 1; return true;
-    case 512: *local = 256; *cl = 2; return true;
-    case 1024: *local = 256; *cl = 4; return true;
-    case 2048: *local = 256; *cl = 8; return true;
-    default: return false;
+  if (N < 32 || N > 2048 || N % 32 != 0) return false;
+  if (N <= 256) {
+    *local = N <= 64 ? 64 : (N <= 128 ? 128 : (N <= 192 ? 192 : 256));
+    *cl = 1;
+  } else {
+    *local = 256;
+    *cl = N <= 512 ? 2 : (N <= 1024 ? 4 : 8);
   }
+  return true;
 }
 
 

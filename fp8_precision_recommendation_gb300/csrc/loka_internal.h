@@ -52,7 +52,7 @@ cudaError_t launch_quantize(const QuantJobs& jobs, int mode, int sms, cudaStream
 
 // MX scale factors in the tensor-memory copy layout: for row block rb (128
 // rows) and K block kb (128 elements = 4 codes per row), a 512-byte block at
-// (rb * (K/128) + kb) * 512; inside it row m, code kk sits at byte
+// (rb * ceil(K/128) + kb) * 512; inside it row m, code kk sits at byte
 // (m % 32) * 16 + ((m % 128) / 32) * 4 + kk.  tcgen05.cp.32x128b.warpx4 of
 // such a block puts the codes of row m in TMEM lane m, column (m % 128) / 32,
 // byte kk.
@@ -61,7 +61,7 @@ __host__ __device__ inline int64_t sf_tc_offset(int64_t m, int64_t blk32, int64_
   return (rb * kb128_count + kb) * 512 + (m & 31) * 16 + ((m & 127) >> 5) * 4 + kk;
 }
 __host__ __device__ inline int64_t sf_tc_bytes(int64_t rows, int64_t cols) {
-  return ((rows + 127) / 128) * (cols / 128) * 512;
+  return ((rows + 127) / 128) * ((cols + 127) / 128) * 512;
 }
 
 // Rewrites logical E8M0 codes into the tensor-memory copy layout: [rows,
@@ -111,6 +111,7 @@ struct GemmParams {
   int32_t norm_block;    // BlockNorm block (32, 64, 128 or 256 columns)
   int32_t act;           // kActNone or kActHardSwish, after the normalization
   int32_t slices;        // CL == 1 launches: independent column slices per row (1 = none)
+  int32_t n_cols;        // columns of an output row (the layer's N; set by the launcher)
   unsigned* status;      // device status word
   uint64_t wait_limit_ns;
 };
@@ -130,6 +131,9 @@ struct GemmRoute {
   int local, cl, slices;
 };
 GemmRoute gemm_route(int N, int norm);
+// (columns per CTA, cluster size) of a row of N columns whose statistics
+// span it; false when N is not a multiple of 32 in [32, 2048].
+bool split_n_host(int N, int* local, int* cl);
 
 // Launches the persistent GEMM + epilogue kernel for N columns (fills in
 // p.stages and p.slices; tm_b must have been encoded with a box of

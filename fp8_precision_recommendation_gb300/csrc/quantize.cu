@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const __grid_constant__
           dst[idx] = cast8(v[i], pow2_neg(e));
           if ((lane & 3) == 0) {
             sc[idx >> 2] = static_cast<uint8_t>(e + 127);
-            if (job.sf_tc != nullptr) job.sf_tc[sf_tc_offset(row, idx >> 2, job.cols >> 7)] = static_cast<uint8_t>(e + 127);
+            if (job.sf_tc != nullptr) job.sf_tc[sf_tc_offset(row, idx >> 2, (job.cols + 127) >> 7)] = static_cast<uint8_t>(e + 127);
           }
         }
       }
@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(256) quant_rows_half_kernel(const __grid_const
           dst[idx] = cast8(v[i], pow2_neg(e));
           if ((hl & 3) == 0) {
             sc[idx >> 2] = static_cast<uint8_t>(e + 127);
-            if (job.sf_tc != nullptr) job.sf_tc[sf_tc_offset(row, idx >> 2, job.cols >> 7)] = static_cast<uint8_t>(e + 127);
+            if (job.sf_tc != nullptr) job.sf_tc[sf_tc_offset(row, idx >> 2, (job.cols + 127) >> 7)] = static_cast<uint8_t>(e + 127);
           }
         }
       }
@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(256) quant_rows_long_kernel(const __grid_const
           dst[idx] = cast8(v, pow2_neg(e));
           if ((lane & 3) == 0) {
             sc[idx >> 2] = static_cast<uint8_t>(e + 127);
-            if (job.sf_tc != nullptr) job.sf_tc[sf_tc_offset(row, idx >> 2, job.cols >> 7)] = static_cast<uint8_t>(e + 127);
+            if (job.sf_tc != nullptr) job.sf_tc[sf_tc_offset(row, idx >> 2, (job.cols + 127) >> 7)] = static_cast<uint8_t>(e + 127);
           }
         }
       }
@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(256) sf_permute_kernel(const uint8_t* __restri
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t m = i / nb, b = i - m * nb;
-    tc[sf_tc_offset(m, b, cols >> 7)] = logical[(m / row_div) * nb + b];
+    tc[sf_tc_offset(m, b, (cols + 127) >> 7)] = logical[(m / row_div) * nb + b];
   }
 }
 
@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(256) quant_block32_kernel(const __grid_constan
       const int64_t row = r0 + (threadIdx.x >> 3);
       const int b = threadIdx.x & 7;
       if (row < job.rows && c0 + 32 * b < job.cols)
-        job.sf_tc[sf_tc_offset(row, (c0 >> 5) + b, job.cols >> 7)] = static_cast<uint8_t>(ex[b] + 127);
+        job.sf_tc[sf_tc_offset(row, (c0 >> 5) + b, (job.cols + 127) >> 7)] = static_cast<uint8_t>(ex[b] + 127);
     }
     if (job.q_t != nullptr) {
       __syncthreads();

@@ -531,3 +531,67 @@ def test_variant_sweep_smoke(lib):
             assert rel == 0.0
         else:
             assert 1e-3 < rel < 0.1
+
+
+# ------------------------------------------------- general layer shapes
+# Any K and N that are multiples of 32 (LoKA section II-C's production GEMM
+# shapes are not all multiples of 128): the last K slice reads zeros past K;
+# rows narrower than the kernel's columns skip the empty chunks; rows wider
+# than a CTA split over 256-column CTAs, the last one partial or empty.
+@pytest.mark.parametrize("K", [32, 64, 96, 160, 320])
+@pytest.mark.parametrize("mode", [W.SCALE_TENSOR, W.SCALE_ROW, W.SCALE_MX32, W.SCALE_BF16, W.SCALE_BLOCK32])
+def test_k_multiple_of_32(lib, K, mode):
+    inp = W.make_layer(389, K, 256, mode=mode, norm=W.NORM_LAYER, seed=K + 11 * mode, outlier_frac=0.01,
+                       bias_var=0.02, gamma_uniform=True)
+    (y,) = _run([inp])
+    _check_layer(inp, y, what=f"K{K} mode{mode}")
+
+
+@pytest.mark.parametrize("N", [32, 96, 160, 224])
+@pytest.mark.parametrize("mode,norm", [(W.SCALE_ROW, W.NORM_LAYER), (W.SCALE_MX32, W.NORM_RMS),
+                                       (W.SCALE_TENSOR, W.NORM_NONE), (W.SCALE_BF16, W.NORM_LAYER)])
+def test_narrow_n_multiple_of_32(lib, N, mode, norm):
+    inp = W.make_layer(300, 256, N, mode=mode, norm=norm, seed=N + 5 * mode, outlier_frac=0.01,
+                       bias_var=0.02, gamma_uniform=True)
+    inp.beta = W.random_bf16((N,), seed=3, var=0.1)
+    (y,) = _run([inp])
+    _check_layer(inp, y, what=f"N{N} mode{mode} norm{norm}")
+
+
+@pytest.mark.parametrize("N", [320, 768, 1056, 2016])
+@pytest.mark.parametrize("mode,norm", [(W.SCALE_ROW, W.NORM_LAYER), (W.SCALE_MX32, W.NORM_RMS),
+                                       (W.SCALE_ROW, W.NORM_NONE), (W.SCALE_MX32, W.NORM_LAYER)])
+def test_wide_n_multiple_of_32(lib, N, mode, norm):
+    inp = W.make_layer(200, 128, N, mode=mode, norm=norm, seed=N + 7 * mode + norm, x_dist="laplace",
+                       bias_var=0.02, gamma_uniform=True)
+    inp.beta = W.random_bf16((N,), seed=4, var=0.1)
+    (y,) = _run([inp])
+    _check_layer(inp, y, what=f"N{N} mode{mode} norm{norm}")
+
+
+@pytest.mark.parametrize("N", [96, 320])
+def test_odd_width_blocknorm_and_quantized_output(lib, N):
+    # BlockNorm over 32-column blocks on a partial CTA, and E4M3 output rows
+    # (per-row output scales need N <= 256; MX scales any width)
+    inp = W.make_layer(257, 96, N, mode=W.SCALE_ROW, norm=W.NORM_BLOCK_RMS, seed=N, outlier_frac=0.01,
+                       bias_var=0.02, gamma_uniform=True)
+    inp.norm_block = 32
+
+    def lay(out_mode=None):
+        return loka.Layer(x=_gpu(inp.x), w=_gpu(inp.w), bias=_gpu(inp.bias), gamma=_gpu(inp.gamma),
+                          beta=_gpu(inp.beta), mode=inp.mode, norm=inp.norm, eps=inp.eps, norm_block=32,
+                          y_q_mode=out_mode)
+
+    (y,) = loka.fp8_linear_norm([lay()])
+    torch.cuda.synchronize()
+    assert loka._loka.loka_device_status() == 0
+    _check_layer(inp, y.cpu(), what=f"BlockNorm N{N}")
+    for out_mode in ([W.SCALE_ROW, W.SCALE_MX32] if N <= 256 else [W.SCALE_MX32]):
+        layer = lay(out_mode)
+        loka.fp8_linear_norm([layer])
+        torch.cuda.synchronize()
+        assert torch.equal(layer.y.cpu(), y.cpu())
+        q, s = loka.quantize_fp8(layer.y, out_mode)
+        torch.cuda.synchronize()
+        assert torch.equal(layer.y_q, q), f"N{N} out{out_mode}"
+        assert torch.equal(layer.y_q_scales.view(torch.uint8), s.view(torch.uint8)), f"N{N} out{out_mode}"

@@ -84,7 +84,12 @@ def _desc(**kw):
 
 @pytest.mark.parametrize("kw,status", [
     ({"N": 100}, _loka.LOKA_ERR_UNSUPPORTED), ({"N": 4096}, _loka.LOKA_ERR_UNSUPPORTED),
-    ({"K": 96}, _loka.LOKA_ERR_UNSUPPORTED),
+    ({"N": 16}, _loka.LOKA_ERR_UNSUPPORTED), ({"K": 80}, _loka.LOKA_ERR_UNSUPPORTED),
+    ({"K": 16}, _loka.LOKA_ERR_UNSUPPORTED),
+    # any multiple of 32 passes validation (then the missing workspace stops it)
+    ({"K": 96}, _loka.LOKA_ERR_WORKSPACE), ({"K": 32}, _loka.LOKA_ERR_WORKSPACE),
+    ({"N": 96}, _loka.LOKA_ERR_WORKSPACE), ({"N": 768}, _loka.LOKA_ERR_WORKSPACE),
+    ({"N": 2016, "norm": 2}, _loka.LOKA_ERR_WORKSPACE), ({"N": 320, "mode": 2}, _loka.LOKA_ERR_WORKSPACE),
     ({"M": -1}, _loka.LOKA_ERR_INVALID_ARG),
     ({"mode": 7}, _loka.LOKA_ERR_INVALID_ARG),
     ({"norm": 9}, _loka.LOKA_ERR_INVALID_ARG),
