@@ -42,6 +42,15 @@ cudaError_t launch_gemm_norm(GemmParams& p, int N, OperandKind op, OutKind out, 
   if (r.local == 0) return cudaErrorInvalidValue;
   p.slices = r.slices;
   p.n_cols = N;
+  p.inv_n_cols = 1.0f / static_cast<float>(N);
+  for (int j = 0; j < 8; ++j) {
+    const int left = N - j * 256;
+    const float na = static_cast<float>(j * 256);
+    const float nb = static_cast<float>(left <= 0 ? 0 : (left > 256 ? 256 : left));
+    const float w = nb > 0.0f ? nb / (na + nb) : 0.0f;
+    p.chan_w[j] = w;
+    p.chan_c[j] = na * w;
+  }
   // the launchers take the kernel's width: up to 256 one CTA, wider a
   // cluster of r.cl CTAs of 256 columns
   N = r.cl > 1 ? r.cl * 256 : r.local;

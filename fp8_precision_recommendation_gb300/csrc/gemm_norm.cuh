@@ -717,20 +717,19 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
       return make_float2(__uint_as_float(r[o]), __uint_as_float(r[o + 1]));
     };
     // Runs fn(r, c) over the valid chunks c = 0 .. nvc-1, the TMEM read of chunk
-    // c + 1 in flight while chunk c is processed.
+    // c + 1 in flight while chunk c is processed.  The loop and its reads
+    // run over all NCHUNK chunks (a loop whose trip count is known keeps r in
+    // registers); only fn is skipped past the row's end.
     auto for_chunks = [&](uint32_t t_base, auto&& fn) {
-      if (nvc == 0) return;
       uint32_t r[2][16];
       tmem_ld_16x256b_x4(t_base, r[0]);
       tmem_ld_wait();
       reg_fence(r[0]);
 #pragma unroll
       for (int c = 0; c < NCHUNK; ++c) {
-        if (c >= nvc) break;
-        const bool more = c + 1 < nvc;   // uniform over the warp
-        if (more) tmem_ld_16x256b_x4(t_base + (c + 1) * 32, r[(c + 1) & 1]);
-        fn(r[c & 1], c);
-        if (more) {
+        if (c + 1 < NCHUNK) tmem_ld_16x256b_x4(t_base + (c + 1) * 32, r[(c + 1) & 1]);
+        if (c < nvc) fn(r[c & 1], c);   // uniform over the warp
+        if (c + 1 < NCHUNK) {
           tmem_ld_wait();
           reg_fence(r[(c + 1) & 1]);
         }
@@ -1019,26 +1018,21 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
           // row's valid columns from j N on, possibly none)
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
-            float mA = 0.f, qA = 0.f, nA = 0.f;
+            float mA = 0.f, qA = 0.f;
 #pragma unroll
             for (int j = 0; j < CL; ++j) {
+              if (j > 0 && p.chan_w[j] == 0.0f) continue;   // CTA j holds none of the row
               const float2 part_j = j == static_cast<int>(rank) ? make_float2(mean[k], m2[k])
                                                                 : cl_stats[(cb * CL + j) * kBM + rowk[k]];
-              const int left = ng - j * N;
-              const float nb = static_cast<float>(left <= 0 ? 0 : (left > N ? N : left));
               if (norm == kNormRms) {
                 qA += part_j.y;
-              } else if (nb > 0.0f) {
-                if (nA == 0.0f) {
-                  mA = part_j.x;
-                  qA = part_j.y;
-                } else {
-                  const float delta = part_j.x - mA;
-                  const float w = nb / (nA + nb);                        // n_b / n_total
-                  mA = fmaf(delta, w, mA);
-                  qA += part_j.y + delta * delta * (nA * w);             // n_a n_b / n_total
-                }
-                nA += nb;
+              } else if (j == 0) {
+                mA = part_j.x;
+                qA = part_j.y;
+              } else {
+                const float delta = part_j.x - mA;
+                mA = fmaf(delta, p.chan_w[j], mA);
+                qA += part_j.y + delta * delta * p.chan_c[j];
               }
             }
             mean[k] = norm == kNormRms ? 0.0f : mA;
@@ -1052,9 +1046,8 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
             for (int j = 0; j < CL; ++j) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&cl_free[cb]), j));
           }
         }
-        const float inv_ng = 1.0f / static_cast<float>(ng);
 #pragma unroll
-        for (int k = 0; k < 2; ++k) rstd[k] = rsqrtf(m2[k] * inv_ng + eps);
+        for (int k = 0; k < 2; ++k) rstd[k] = rsqrtf(m2[k] * p.inv_n_cols + eps);
       } else if (norm == kNormBlockRms) {
         const float inv_b = 1.0f / static_cast<float>(p.norm_block);   // a power of two: exact
 #pragma unroll

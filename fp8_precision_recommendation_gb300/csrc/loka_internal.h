@@ -112,6 +112,13 @@ struct GemmParams {
   int32_t act;           // kActNone or kActHardSwish, after the normalization
   int32_t slices;        // CL == 1 launches: independent column slices per row (1 = none)
   int32_t n_cols;        // columns of an output row (the layer's N; set by the launcher)
+  float inv_n_cols;      // 1 / n_cols
+  // cluster merge of row statistics (Chan), CTA j of a cluster holding the
+  // row's columns from j * 256 on: chan_w[j] = n_b / (n_a + n_b) and
+  // chan_c[j] = n_a n_b / (n_a + n_b) with n_a = 256 j and n_b its columns
+  // (0 for a CTA past the row's end); set by the launcher
+  float chan_w[8];
+  float chan_c[8];
   unsigned* status;      // device status word
   uint64_t wait_limit_ns;
 };

@@ -43,9 +43,11 @@ from . import (LOKA_BF16, LOKA_NORM_LAYER, LOKA_SCALE_BLOCK32, LOKA_SCALE_MX32, 
                Layer, Workspace, fp8_linear_norm, quant_error, quantize_fp8)
 
 VARIANTS = (LOKA_SCALE_TENSOR, LOKA_SCALE_ROW, LOKA_SCALE_MX32, LOKA_BF16, LOKA_SCALE_BLOCK32)
-GRID_M = (4096, 32768, 262144)
-GRID_K = (128, 512, 2048)
-GRID_N = (64, 256, 1024)
+# the pages' sweep: M = 4096 .. 524288 in powers of two, K and N from 64 to
+# 2048, with and without 1% of the entries of X scaled by 100
+GRID_M = tuple(4096 << i for i in range(8))
+GRID_K = (64, 128, 256, 512, 1024, 2048)
+GRID_N = (64, 128, 256, 512, 1024, 2048)
 OUTLIERS = (0.0, 0.01)
 
 Row = Tuple[int, int, int, int, float, int, float, float, float]
