@@ -42,6 +42,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-compare", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="default workload only: skip the ensemble / MX layer lines and the tensor-core peak")
     ap.add_argument("--M", type=int, default=None, help="rows of X per layer (default: the workload's own)")
     ap.add_argument("--workload", default="rec_mlp",
                     choices=["rec_mlp", "ensemble", "mxfp8", "single", "wide_blocknorm", "rec_mlp_block32"])
@@ -275,15 +277,98 @@ def scale_bytes(mode, rows, cols):
     return {0: 4, 1: 4 * rows, 2: rows * cols // 32, 4: (rows + 31) // 32 * (cols // 32)}.get(mode, 0)
 
 
+def tensor_peaks(dev, stream, clock_index):
+    """Dense tcgen05 throughput measured by the library's own microbenchmark
+    (one CTA per SM issuing back-to-back M=128, N=256 MMAs from shared
+    memory): E4M3 as a burst (one ~15 ms launch) and sustained (launches
+    back to back for about 2 s, clocks sampled), bf16 as a burst (to check
+    the microbenchmark against the measured cuBLAS bf16 peak)."""
+    import torch
+    from fp8_precision_recommendation_gb300 import _loka
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    s = stream.cuda_stream
+    out = {"sms": sms, "shape": "M=128 N=256 per MMA, cta_group::1, fp32 accumulation in tensor memory"}
+
+    def run(kind, mmas, launches):
+        with torch.cuda.stream(stream):
+            _loka.loka_selftest_mma_peak(kind, 4096, s)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(launches):
+                _loka.loka_selftest_mma_peak(kind, mmas, s)
+            b.record(stream)
+            b.synchronize()
+        k = 32 if kind == 0 else 16
+        return sms * mmas * launches * 2.0 * 128 * 256 * k / (a.elapsed_time(b) / 1e3) / 1e12
+
+    out["e4m3_burst_tflops"] = run(0, 200_000, 1)
+    out["bf16_burst_tflops"] = run(1, 200_000, 1)
+    with ClockSampler(clock_index) as clk:
+        time.sleep(0.2)
+        out["e4m3_sustained_tflops"] = run(0, 2_000_000, 14)
+    out["sustained_clocks"] = clk.summary()
+    if _loka.loka_device_status() != 0:
+        raise RuntimeError("tensor-core peak microbenchmark timed out")
+    return out
+
+
+def link_bandwidth(dev):
+    """Plain pinned host <-> device copies of 64 MB (CUDA events, best of 5):
+    the ceiling of the end-to-end measurement's copies."""
+    import torch
+    n = 64 << 20
+    h = torch.empty(n, dtype=torch.uint8).pin_memory()
+    d = torch.empty(n, dtype=torch.uint8, device=dev)
+    res = {}
+    for name, dst, src in (("h2d_gbs", d, h), ("d2h_gbs", h, d)):
+        best = 0.0
+        for _ in range(6):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            dst.copy_(src, non_blocking=True)
+            b.record()
+            b.synchronize()
+            best = max(best, n / (a.elapsed_time(b) / 1e3) / 1e9)
+        res[name] = best
+    res["bytes"] = n
+    return res
+
+
 def run_ours(args, world, rank, local):
+    import torch
+    from fp8_precision_recommendation_gb300 import _loka
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _loka.load()
+    line = measure(args, args.workload, world, rank, local, dev, main=True)
+    extra = args.workload == "rec_mlp" and not args.M and not args.no_extra
+    if extra:
+        # the grouped ensemble and the MX layer, measured the same way (device
+        # time of a CUDA graph of steps, rotating buffers past L2), so their
+        # step and kernel rooflines are on record beside the headline
+        torch.cuda.empty_cache()
+        sub = argparse.Namespace(**{**vars(args), "no_e2e": True, "no_cpu": True})
+        line["workloads"] = {}
+        for name in ("ensemble", "mxfp8"):
+            w = measure(sub, name, world, rank, local, dev, main=False)
+            line["workloads"][name] = {k: w[k] for k in ("metric", "value", "unit", "ms_per_step", "config",
+                                                           "step_roofline", "roofline", "kernels_us", "compare",
+                                                           "fp8_chained_layer", "clocks")}
+            torch.cuda.empty_cache()
+        line["tensor_peak"] = tensor_peaks(dev, torch.cuda.Stream(device=dev), local)
+        mx = line["workloads"]["mxfp8"]
+        pk = line["tensor_peak"]["e4m3_sustained_tflops"]
+        mx["tensor_frac_of_measured_e4m3"] = mx["value"] / pk
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def measure(args, name, world, rank, local, dev, main):
     import torch
     import fp8_precision_recommendation_gb300 as loka
     from fp8_precision_recommendation_gb300 import _loka
 
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    _loka.load()
-    layers = workload_layers(args.workload, rank, args.M)
+    layers = workload_layers(name, rank, args.M if main else None)
     mode, norm, eps = layers[0].mode, layers[0].norm, layers[0].eps
     flops = sum(2.0 * l.M * l.N * l.K for l in layers)
     x_bytes = sum(2 * l.M * l.K for l in layers)
@@ -442,14 +527,17 @@ def run_ours(args, world, rank, local):
     dom_bytes = bytes_g if dom == "gemm_norm" else bytes_q
     achieved = dom_bytes / kern[dom] / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": bw, "unit": "GB/s", "frac": achieved / bw,
-                "traffic": recorded_traffic(dom) if args.workload == "rec_mlp" and not args.M else None,
+                "traffic": recorded_traffic(dom) if name == "rec_mlp" and not args.M else None,
                 "kernel": dom, "peak_source": f"{src} hbm_gbs",
                 "algorithmic_bytes_per_launch": dom_bytes, "launch_us": kern[dom] * 1e6}
     step_bytes = sum(algorithmic_bytes_step(l.M, l.K, l.N) for l in layers)
     step_time = t / args.steps
-    path_roofline = {"bytes_per_step": step_bytes, "floor_us": step_bytes / (bw * 1e9) * 1e6,
-                     "frac_of_hbm_floor": (step_bytes / (bw * 1e9)) / step_time,
-                     "achieved_gbs": step_bytes / step_time / 1e9}
+    # the whole step against the HBM floor of the layer it computes (bf16 X
+    # and W read once, bf16 Y written once): the fraction the metric's
+    # "% roofline" refers to; `roofline` above is the dominant kernel's
+    step_roofline = {"bound": "hbm", "bytes_per_step": step_bytes, "floor_us": step_bytes / (bw * 1e9) * 1e6,
+                     "frac": (step_bytes / (bw * 1e9)) / step_time, "achieved_gbs": step_bytes / step_time / 1e9,
+                     "peak_gbs": bw, "peak_source": f"{src} hbm_gbs"}
 
     # ---- comparators: our bf16 GEMM+norm and torch eager bf16 linear + norm
     compare = {}
@@ -530,8 +618,14 @@ def run_ours(args, world, rank, local):
         a1.synchronize()
         te = a0.elapsed_time(a1) / 1e3 / n_e2e
         te = max_over_ranks(world, te, dev)
+        link = link_bandwidth(dev)
+        # copies in and out overlap each other and the compute: the slower
+        # direction bounds a step
+        t_link = max(x_bytes / (link["h2d_gbs"] * 1e9), y_bytes / (link["d2h_gbs"] * 1e9), step_time)
         e2e = {"value": world * flops / te / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": x_bytes,
-               "d2h_bytes_per_step": y_bytes, "pipelined": "2 buffer sets, H2D / compute / D2H streams"}
+               "d2h_bytes_per_step": y_bytes, "pipelined": "2 buffer sets, H2D / compute / D2H streams",
+               "link": link, "ceiling": world * flops / t_link / 1e12,
+               "frac_of_ceiling": (world * flops / te / 1e12) / (world * flops / t_link / 1e12)}
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -550,23 +644,22 @@ def run_ours(args, world, rank, local):
             "single": "per-tensor E4M3, LayerNorm",
             "wide_blocknorm": "wide layer N(0,1)+1%x100 outliers, per-row E4M3, bias, BlockNorm 256, Hard Swish",
             "rec_mlp_block32": "rec-MLP X N(0,1)+1%x100 outliers, square 32x32-block E4M3/E8M0, bias, LayerNorm"}[
-                args.workload]
-    metric = METRIC if args.workload == "rec_mlp" and not args.M else \
-        f"FP8 linear+norm TFLOP/s ({args.workload} {len(layers)}x{l0.M}x{l0.K}x{l0.N}) on 1 GB300"
+                name]
+    metric = METRIC if name == "rec_mlp" and not args.M else \
+        f"FP8 linear+norm TFLOP/s ({name} {len(layers)}x{l0.M}x{l0.K}x{l0.N}) on 1 GB300"
     line = {
         "metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * step_time, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp8_e4m3 (fp32 accumulate, bf16 out)", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {len(layers)} x X[{l0.M},{l0.K}] W[{l0.N},{l0.K}], {desc}, bf16 out",
+        "config": {"workload": f"{name}: {len(layers)} x X[{l0.M},{l0.K}] W[{l0.N},{l0.K}], {desc}, bf16 out",
                    "l2": f"{nbuf} rotating X/Y buffer sets ({nbuf * (x_bytes + y_bytes) / 1e6:.0f} MB) > L2",
                    "parallelism": f"rows x{world}",
                    "timing": "CUDA graph of K steps, CUDA events on the launching stream"},
-        "roofline": roofline, "path_roofline": path_roofline, "kernels_us": {k: v * 1e6 for k, v in kern.items()},
+        "roofline": roofline, "step_roofline": step_roofline, "kernels_us": {k: v * 1e6 for k, v in kern.items()},
         "compare": compare, "fp8_chained_layer": chained, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
         "gpu_launches": launches_per_step * args.steps,
     }
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    return line
 
 
 def main():

@@ -65,6 +65,7 @@ SIGNATURES = {
     "loka_last_error": (ctypes.c_char_p, []),
     "loka_device_status": (c_i32, [c_p]),
     "loka_selftest_watchdog": (c_i32, [ctypes.c_uint64, c_p]),
+    "loka_selftest_mma_peak": (c_i32, [c_i32, ctypes.c_int64, c_p]),
     "loka_quantize_fp8_workspace_size": (c_sz, [c_i64, c_i64, c_i32]),
     "loka_quantize_fp8": (c_i32, [c_p, c_i64, c_i64, c_i64, c_i32, c_p, c_p, c_p, c_sz, c_p]),
     "loka_quantize_fp8_block32": (c_i32, [c_p, c_i64, c_i64, c_i64, c_p, c_p, c_p, c_p]),
@@ -150,6 +151,10 @@ def loka_device_status(stream=None) -> int:
 
 def loka_selftest_watchdog(limit_ns: int, stream=None) -> None:
     check(load().loka_selftest_watchdog(limit_ns, _stream(stream)))
+
+
+def loka_selftest_mma_peak(kind: int, mmas_per_sm: int, stream=None) -> None:
+    check(load().loka_selftest_mma_peak(kind, mmas_per_sm, _stream(stream)))
 
 
 def loka_quantize_fp8_workspace_size(rows: int, cols: int, mode: int) -> int:

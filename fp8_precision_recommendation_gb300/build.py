@@ -20,7 +20,7 @@ BUILD = os.path.join(ROOT, "_build", "loka")
 LIB = os.path.join(HERE, "libloka.so")
 SOURCES = ["api.cu", "quantize.cu", "gemm_norm.cu", "gemm_e4m3.cu", "gemm_bf16.cu", "gemm_mx.cu",
            "gemm_qout_e4m3.cu", "gemm_qout_e4m3_wide.cu", "gemm_qout_mx.cu", "gemm_qout_mx_wide.cu", "gemm_qx.cu", "probe.cu", "probe_weights.cu",
-           "probe_stats.cu"]
+           "probe_stats.cu", "mma_peak.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

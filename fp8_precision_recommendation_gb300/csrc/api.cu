@@ -452,6 +452,19 @@ loka_status loka_selftest_watchdog(uint64_t limit_ns, void* stream) {
   return LOKA_OK;
 }
 
+loka_status loka_selftest_mma_peak(int32_t kind, int64_t mmas_per_sm, void* stream) {
+  DeviceInfo* dev = nullptr;
+  loka_status s = device_info(&dev);
+  if (s != LOKA_OK) return s;
+  if (kind != 0 && kind != 1) return fail(LOKA_ERR_INVALID_ARG, "kind %d: 0 (E4M3) or 1 (bf16)", kind);
+  if (mmas_per_sm < 1 || mmas_per_sm > (int64_t{1} << 32))
+    return fail(LOKA_ERR_INVALID_ARG, "mmas_per_sm = %lld is outside [1, 2^32]", static_cast<long long>(mmas_per_sm));
+  // the last MMAs drain within microseconds of the issue loop's end
+  cudaError_t e = launch_mma_peak(kind, mmas_per_sm, dev->sms, dev->status, 1000000000ull, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "tensor-core peak launch");
+  return LOKA_OK;
+}
+
 size_t loka_quantize_fp8_workspace_size(int64_t, int64_t, int32_t mode) {
   return mode == LOKA_SCALE_TENSOR ? kAlign : 0;
 }

@@ -195,5 +195,8 @@ cudaError_t launch_cholesky(const double* S, const double* mu, int64_t K, int64_
 
 // Watchdog self-test: waits on a barrier that nothing completes.
 cudaError_t launch_watchdog_selftest(unsigned* status, uint64_t limit_ns, cudaStream_t stream);
+// Tensor-core peak: one CTA per SM issuing `mmas` back-to-back MMAs (kind 0
+// E4M3, 1 bf16) on shared-memory tiles (mma_peak.cu).
+cudaError_t launch_mma_peak(int kind, int64_t mmas, int sms, unsigned* status, uint64_t limit_ns, cudaStream_t stream);
 
 }  // namespace loka

@@ -435,6 +435,29 @@ def test_watchdog_turns_a_stuck_wait_into_a_status(lib):
     _check_layer(inp, y, what="after watchdog")
 
 
+def test_tensor_peak_microbenchmark(lib):
+    # the tcgen05 peak the contraction's tensor-pipe share is measured
+    # against: both kinds complete with a clean status, and E4M3 (K = 32 per
+    # MMA) runs at least 1.5x the bf16 FLOP rate (K = 16 in the same time)
+    dev = torch.device(DEV)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    rate = {}
+    for kind, k in ((0, 32), (1, 16)):
+        _loka.loka_selftest_mma_peak(kind, 1024)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        _loka.loka_selftest_mma_peak(kind, 100_000)
+        b.record()
+        b.synchronize()
+        rate[kind] = sms * 100_000 * 2.0 * 128 * 256 * k / (a.elapsed_time(b) / 1e3)
+    assert _loka.loka_device_status() == _loka.LOKA_OK
+    assert rate[0] > 1.5 * rate[1] > 0
+    with pytest.raises(_loka.LokaError):
+        _loka.loka_selftest_mma_peak(2, 1)
+    with pytest.raises(_loka.LokaError):
+        _loka.loka_selftest_mma_peak(0, 0)
+
+
 # -------------------------------------------------------------- MX 1x32
 @pytest.mark.parametrize("N", [64, 128, 192, 256])
 @pytest.mark.parametrize("norm", [W.NORM_NONE, W.NORM_LAYER, W.NORM_RMS])
