@@ -745,6 +745,15 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
       else
         return __ffma2_rn(__fmul2_rn(acc2(r, k, i), sx2), sw, b);
     };
+    // The statistics pass writes v back over the accumulator chunk it read
+    // (same lanes and columns), so the output pass reads v itself and
+    // neither recomputes it nor reloads the column scales and bias.
+    // v of pair (k, i) replaces the accumulator pair it came from (read
+    // once, so no extra registers hold the chunk)
+    auto put_v = [&](uint32_t (&r)[16], int k, int i, float2 v) {
+      r[4 * i + 2 * k] = __float_as_uint(v.x);
+      r[4 * i + 2 * k + 1] = __float_as_uint(v.y);
+    };
     int cur_group = -1;
     bool affine = false;
     float sx_next[2] = {1.f, 1.f};
@@ -857,7 +866,7 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
           // shifted sums: with K the mean of the row's first 8-value piece,
           // s1 += v - K and s2 += (v - K)^2; no division, little cancellation
           float shift[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};
-          for_chunks(t_base, [&](const uint32_t (&r)[16], int c) {
+          for_chunks(t_base, [&](uint32_t (&r)[16], int c) {
             const int c0 = c * 32;
             float2 sw[4], b[4];
 #pragma unroll
@@ -869,7 +878,10 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
             for (int k = 0; k < 2; ++k) {
               float2 v[4];
 #pragma unroll
-              for (int i = 0; i < 4; ++i) v[i] = vpair(r, k, i, sx2[k], sw[i], b[i]);
+              for (int i = 0; i < 4; ++i) {
+                v[i] = vpair(r, k, i, sx2[k], sw[i], b[i]);
+                put_v(r, k, i, v[i]);
+              }
               if constexpr (decltype(trk_tag)::value) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -892,6 +904,7 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
               s1[k] += a1.x + a1.y;
               m2[k] += a2.x + a2.y;
             }
+            tmem_st_16x256b_x4(t_base + static_cast<uint32_t>(c0), r);
           });
           // each lane holds 8 values of a row per valid chunk
           const float inv_me = nvc > 0 ? 1.0f / (8.0f * static_cast<float>(nvc)) : 0.0f;
@@ -902,7 +915,7 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
             m2[k] = fmaxf(m2[k] - s1[k] * d, 0.0f);
           }
         } else if (norm == kNormRms) {
-          for_chunks(t_base, [&](const uint32_t (&r)[16], int c) {
+          for_chunks(t_base, [&](uint32_t (&r)[16], int c) {
             const int c0 = c * 32;
             float2 sw[4], b[4];
 #pragma unroll
@@ -916,6 +929,7 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
                 const float2 v = vpair(r, k, i, sx2[k], sw[i], b[i]);
+                put_v(r, k, i, v);
                 if constexpr (decltype(trk_tag)::value) {
                   vhi[k] = max3f(vhi[k], v.x, v.y);
                   vlo[k] = min3f(vlo[k], v.x, v.y);
@@ -924,11 +938,12 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
               }
               m2[k] += q.x + q.y;
             }
+            tmem_st_16x256b_x4(t_base + static_cast<uint32_t>(c0), r);
           });
         } else if (norm == kNormBlockRms) {
           // BlockNorm: sums of squares per block of the row; the row's 4
           // lanes merge each chunk's sum, and lane (b % 4) keeps block b's
-          for_chunks(t_base, [&](const uint32_t (&r)[16], int c) {
+          for_chunks(t_base, [&](uint32_t (&r)[16], int c) {
             const int c0 = c * 32;
             float2 sw[4], b[4];
 #pragma unroll
@@ -943,6 +958,7 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
                 const float2 v = vpair(r, k, i, sx2[k], sw[i], b[i]);
+                put_v(r, k, i, v);
                 q = __ffma2_rn(v, v, q);
               }
               float qs = q.x + q.y;
@@ -953,6 +969,7 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
                 else bsq[k][0] += qs;
               }
             }
+            tmem_st_16x256b_x4(t_base + static_cast<uint32_t>(c0), r);
           });
         }
       };
@@ -965,6 +982,7 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
       } else {
         stats_pass(std::false_type{});
       }
+      tmem_st_wait();   // v is read back below
 
       float rstd[2] = {1.f, 1.f};
       // BlockNorm: 1/rms of the blocks this lane keeps
@@ -1066,8 +1084,12 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
       auto colv = [&](auto post_tag, int c0, int i, float2& sw, float2& b, float2& gm, float2& be) {
         gm = make_float2(1.f, 1.f);
         be = make_float2(0.f, 0.f);
-        sw = vec2(vec_sw, c0, i);
-        b = vec2(vec_b, c0, i);
+        sw = make_float2(1.f, 1.f);
+        b = make_float2(0.f, 0.f);
+        if constexpr ((decltype(post_tag)::value & 8) == 0) {
+          sw = vec2(vec_sw, c0, i);
+          b = vec2(vec_b, c0, i);
+        }
         if constexpr ((decltype(post_tag)::value & 1) != 0) {
           gm = vec2(vec_g, c0, i);
           be = vec2(vec_be, c0, i);
@@ -1078,7 +1100,8 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
       auto ypair = [&](auto post_tag, const uint32_t (&r)[16], int k, int i, float2 rs, float2 sw, float2 b,
                        float2 gm, float2 be) {
         constexpr int POST = decltype(post_tag)::value;
-        const float2 v = vpair(r, k, i, sx2[k], sw, b);
+        // bit 3: the chunk holds v already (written by the statistics pass)
+        const float2 v = (POST & 8) != 0 ? acc2(r, k, i) : vpair(r, k, i, sx2[k], sw, b);
         float2 y = __ffma2_rn(v, rs, nmr2[k]);
         if constexpr ((POST & 1) != 0) y = __ffma2_rn(y, gm, be);
         if constexpr ((POST & 2) != 0) {
@@ -1103,18 +1126,21 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
           rs[1] = rstd2[1];
         }
       };
-      // fn(post_tag) with the tag of this tile's group
+      // fn(post_tag) with the tag of this tile's group.  Without a norm there
+      // is no statistics pass (v not stored) and no gamma, beta or blocks.
       auto with_tags = [&](auto&& fn) {
-        const int post = (affine ? 1 : 0) | (act ? 2 : 0) | (norm == kNormBlockRms ? 4 : 0);
+        const int post = (affine ? 1 : 0) | (act ? 2 : 0) | (norm == kNormBlockRms ? 4 : 0) | (norm != kNormNone ? 8 : 0);
         switch (post) {
-          case 0: fn(std::integral_constant<int, 0>{}); break;
-          case 1: fn(std::integral_constant<int, 1>{}); break;
           case 2: fn(std::integral_constant<int, 2>{}); break;
-          case 3: fn(std::integral_constant<int, 3>{}); break;
-          case 4: fn(std::integral_constant<int, 4>{}); break;
-          case 5: fn(std::integral_constant<int, 5>{}); break;
-          case 6: fn(std::integral_constant<int, 6>{}); break;
-          default: fn(std::integral_constant<int, 7>{}); break;
+          case 8: fn(std::integral_constant<int, 8>{}); break;
+          case 9: fn(std::integral_constant<int, 9>{}); break;
+          case 10: fn(std::integral_constant<int, 10>{}); break;
+          case 11: fn(std::integral_constant<int, 11>{}); break;
+          case 12: fn(std::integral_constant<int, 12>{}); break;
+          case 13: fn(std::integral_constant<int, 13>{}); break;
+          case 14: fn(std::integral_constant<int, 14>{}); break;
+          case 15: fn(std::integral_constant<int, 15>{}); break;
+          default: fn(std::integral_constant<int, 0>{}); break;
         }
       };
 
