@@ -61,7 +61,13 @@ constexpr int kBM = 128;                 // rows per tile (= TMEM lanes)
 constexpr int kSliceBytes = 128;         // bytes of K per stage per row
 constexpr uint32_t kABytes = kBM * kSliceBytes;
 constexpr int kTmemCols = 512;
-constexpr int kThreads = 576;             // producer, MMA, 16 epilogue warps
+// producer, MMA, two idle warps (so the epilogue starts a warpgroup), 16
+// epilogue warps; setmaxnreg moves registers from the first warpgroup to the
+// epilogue (4 x 32 x kRegsLow + 16 x 32 x kRegsEpi <= 640 x 96, the launch's)
+constexpr int kThreads = 640;
+constexpr int kRegsLow = 56;
+constexpr int kRegsEpi = 104;
+static_assert(4 * 32 * kRegsLow + 16 * 32 * kRegsEpi <= kThreads * 96, "register shares exceed the launch's");
 constexpr int kEpiBar = 1;               // named barrier id for the epilogue warps
 constexpr int kQxBar = 3;                // named barrier id for the quantizer warps
 constexpr int kMaxStages = 8;            // TMA ring stages
@@ -83,6 +89,11 @@ constexpr size_t kResidentWLimit = 128 * 1024;
 // per sub-partition 40 + 3 x 48 + 4 x 80 = 504 of the 512 register slots.
 constexpr int kQxThreads = 1024;
 constexpr int kQxWarps = 12;             // quantizer warps
+// register shares of the in-kernel quantization kernel's warpgroups
+// (producer / MMA, quantizers, epilogue), within the launch's 1024 x 64
+constexpr int kQxRegsLow = 40;
+constexpr int kQxRegsQuant = 48;
+constexpr int kQxRegsEpi = 80;
 constexpr int kQxFirstWarp = 4;
 constexpr int kQxEpiWarp = 16;           // first epilogue warp
 constexpr uint32_t kQxSlotBytes = 1024;  // staging slot: one row of K = 512, two of K = 256
@@ -157,7 +168,7 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
   // in-kernel per-row quantization of bf16 X (one CTA per row, W resident)
   constexpr bool kQx = OP == static_cast<int>(OperandKind::kE4M3Qx);
   static_assert(!kQx || (CL == 1 && RESIDENT), "in-kernel quantization keeps W resident and rows within a CTA");
-  constexpr int EPI0 = kQx ? kQxEpiWarp : 2;       // first epilogue warp
+  constexpr int EPI0 = kQx ? kQxEpiWarp : 4;       // first epilogue warp
   constexpr int SF_COLS_MAX = OP == static_cast<int>(OperandKind::kMxE4M3) ? kMaxStages * (4 + 4 * sfb_blocks(N)) : 0;
   constexpr int NBUF = (2 * N + SF_COLS_MAX <= kTmemCols) ? 2 : 1;
   static_assert(N + SF_COLS_MAX <= kTmemCols, "accumulator and scale factors must fit in tensor memory");
@@ -1311,7 +1322,7 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
     // MMA warp waits for it (bounded) and frees tensor memory; everyone else
     // just leaves.
     if (warp < kQxFirstWarp) {
-      regs_dec<40>();
+      regs_dec<kQxRegsLow>();
       if (!misaligned) {
         if (warp == 0) run_producer();
         else if (warp == 1) run_mma();
@@ -1326,10 +1337,10 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
         tmem_dealloc(tmem_base, kTmemCols);
       }
     } else if (warp < kQxEpiWarp) {
-      regs_dec<48>();
+      regs_dec<kQxRegsQuant>();
       if (!misaligned) run_quantizer();
     } else {
-      regs_inc<80>();
+      regs_inc<kQxRegsEpi>();
       if (!misaligned) run_epilogue();
       tc_fence_before();
       __syncwarp();
@@ -1337,14 +1348,18 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
     }
     return;
   } else {
-    if (misaligned) {
-      // nothing to do: fall through to the teardown barriers
-    } else if (warp == 0) {
-      run_producer();
-    } else if (warp == 1) {
-      run_mma();
+    // every warpgroup takes its register share in its own branch (no
+    // barrier in between); a misaligned CTA skips all work but still meets
+    // the teardown barriers
+    if (warp < EPI0) {
+      regs_dec<kRegsLow>();
+      if (!misaligned) {
+        if (warp == 0) run_producer();
+        else if (warp == 1) run_mma();
+      }
     } else {
-      run_epilogue();
+      regs_inc<kRegsEpi>();
+      if (!misaligned) run_epilogue();
     }
   }
 
@@ -1398,6 +1413,16 @@ cudaError_t launch_one(const GemmParams& p, size_t smem, int sms, cudaStream_t s
   if (!(configured.load() & bit)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemLimit));
     if (e != cudaSuccess) return e;
+    // the warpgroups' setmaxnreg shares must fit in the registers the CTA
+    // is launched with, or an increase would wait forever: refuse instead
+    cudaFuncAttributes fa{};
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    const long launch_regs = static_cast<long>(fa.numRegs) * (OP == static_cast<int>(OperandKind::kE4M3Qx) ? kQxThreads : kThreads);
+    const long shares = OP == static_cast<int>(OperandKind::kE4M3Qx)
+                            ? 4L * 32 * kQxRegsLow + static_cast<long>(kQxWarps) * 32 * kQxRegsQuant + 16L * 32 * kQxRegsEpi
+                            : 4L * 32 * kRegsLow + 16L * 32 * kRegsEpi;
+    if (shares > launch_regs) return cudaErrorInvalidConfiguration;
     if (CL > 1) {
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
       if (e != cudaSuccess) return e;
