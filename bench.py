@@ -424,13 +424,21 @@ def measure(args, name, world, rank, local, dev, main):
     clocks = clk.summary()
 
     def timed(fn, n):
+        # n calls captured in one CUDA graph and replayed, so the host's cost
+        # per call (argument checks, descriptor encoding) is not in the time
         with torch.cuda.stream(stream):
             for i in range(3):
                 fn(i)
+            torch.cuda.synchronize()
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream, capture_error_mode="thread_local"):
+                for i in range(n):
+                    fn(i)
+            gr.replay()
+            torch.cuda.synchronize()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            for i in range(n):
-                fn(i)
+            gr.replay()
             b.record(stream)
             b.synchronize()
         return a.elapsed_time(b) / 1e3 / n
@@ -654,7 +662,7 @@ def measure(args, name, world, rank, local, dev, main):
         "config": {"workload": f"{name}: {len(layers)} x X[{l0.M},{l0.K}] W[{l0.N},{l0.K}], {desc}, bf16 out",
                    "l2": f"{nbuf} rotating X/Y buffer sets ({nbuf * (x_bytes + y_bytes) / 1e6:.0f} MB) > L2",
                    "parallelism": f"rows x{world}",
-                   "timing": "CUDA graph of K steps, CUDA events on the launching stream"},
+                   "timing": "CUDA graph of K steps (per-kernel figures: a CUDA graph of K launches each), CUDA events on the launching stream"},
         "roofline": roofline, "step_roofline": step_roofline, "kernels_us": {k: v * 1e6 for k, v in kern.items()},
         "compare": compare, "fp8_chained_layer": chained, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
         "gpu_launches": launches_per_step * args.steps,
