@@ -16,13 +16,15 @@ bool split_n_host(int N, int* local, int* cl) { return split_n(N, local, cl); }
 bool gemm_qx_supported(int N, int K, int norm, OutKind out) {
   const GemmRoute r = gemm_route(N, norm);
   if (out != OutKind::kBf16 || r.cl != 1 || r.slices != 1) return false;
-  // Chosen only where W stays resident beside two A tiles: with one A tile
-  // the quantizer warps wait for every tile's MMAs, and the measured step
-  // was slower than quantizer + GEMM (rec-MLP layer, K = 512, W streamed
-  // from L2: 48 vs 35 us); with two (K = 256, the ensemble layers) it
-  // matched it.
+  // Chosen only where it measured no slower than quantizer + GEMM: W
+  // resident beside two A tiles at 256 columns per CTA (K = 256, the
+  // ensemble layers: equal in the step, 2% faster with static W).  With one
+  // A tile (K = 512) the quantizer warps wait for every tile's MMAs (48 vs
+  // 35 us on the rec-MLP layer), and at 64 columns per CTA the quantizer
+  // warps outweigh the short epilogue (75.7 vs 63.3 us at M = 262144,
+  // K = 256, N = 64).
   const QxPlan q = plan_qx(r.local, K);
-  return q.stages > 0 && q.a_bufs == 2;
+  return r.local == 256 && q.stages > 0 && q.a_bufs == 2;
 }
 
 GemmRoute gemm_route(int N, int norm) {

@@ -81,6 +81,71 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const __grid_constant__
   }
 }
 
+// Rows of at most 128 columns: LPR lanes per row (one 16-byte vector each,
+// LPR * 8 columns), 32 / LPR rows per warp step, and U steps loaded before
+// any is processed, so a warp keeps U * 512 bytes in flight where one row
+// per half-warp would keep 128 to 256.  Reductions stay within a row's LPR
+// lanes.  Same arithmetic as quant_rows_kernel.
+template <int MODE, int LPR>
+__global__ void __launch_bounds__(256) quant_rows_narrow_kernel(const __grid_constant__ QuantJobs jobs) {
+  launch_dependents();   // the GEMM that follows may start its prologue
+  constexpr int RPW = 32 / LPR;   // rows per warp step
+  constexpr int U = 4;            // steps in flight
+  const int lane = threadIdx.x & 31;
+  const int hl = lane % LPR;      // lane within the row = its vector
+  const int sub = lane / LPR;     // row within the step
+  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  // every lane of a warp runs the loop the same number of times (base is
+  // per warp); rows past the last one are dummies that load nothing
+  for (int64_t base = warp0 * RPW * U; base < jobs.total_rows; base += nwarps * RPW * U) {
+    uint4 v[U];
+    const QuantJob* jb[U];
+    int64_t row[U];
+    bool live[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t gr = base + u * RPW + sub;
+      live[u] = gr < jobs.total_rows;
+      jb[u] = &jobs.j[find_job(jobs, live[u] ? gr : 0)];
+      row[u] = (live[u] ? gr : 0) - jb[u]->row_begin;
+      const int nvec = static_cast<int>(jb[u]->cols >> 3);
+      const uint4* src = reinterpret_cast<const uint4*>(jb[u]->x) + row[u] * (jb[u]->ld >> 3);
+      v[u] = (live[u] && hl < nvec) ? __ldcs(src + hl) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const QuantJob& job = *jb[u];
+      const int nvec = static_cast<int>(job.cols >> 3);
+      const bool act = live[u] && hl < nvec;
+      uint2* dst = reinterpret_cast<uint2*>(job.q + row[u] * job.cols);
+      if (MODE == kScaleRow) {
+        float m = abs_max8(v[u], 0.0f);
+#pragma unroll
+        for (int o = 1; o < LPR; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float inv, scale;
+        row_scales(m, inv, scale);
+        if (act) dst[hl] = cast8(v[u], inv);
+        if (live[u] && hl == 0) reinterpret_cast<float*>(job.scales)[row[u]] = scale;
+      } else {
+        float m = abs_max8(v[u], 0.0f);
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        const int e = mx_exponent(m);
+        if (act) {
+          dst[hl] = cast8(v[u], pow2_neg(e));
+          if ((hl & 3) == 0) {
+            uint8_t* sc = reinterpret_cast<uint8_t*>(job.scales) + row[u] * (job.cols >> 5);
+            sc[hl >> 2] = static_cast<uint8_t>(e + 127);
+            if (job.sf_tc != nullptr)
+              job.sf_tc[sf_tc_offset(row[u], hl >> 2, (job.cols + 127) >> 7)] = static_cast<uint8_t>(e + 127);
+          }
+        }
+      }
+    }
+  }
+}
+
 // Rows of at most 256 columns: one half-warp per row, two rows per warp.
 // Lane l of a half holds vectors l and l + 16 of its row (512 contiguous
 // bytes per row per load pair), so a warp keeps two rows' bytes in flight
@@ -340,12 +405,24 @@ __global__ void __launch_bounds__(256) quant_block32_kernel(const __grid_constan
 // One wave of the grid-stride kernel: as many 256-thread blocks as are
 // resident at once (the register count decides; asked once per kernel and
 // device), never more than one warp per row.  V = 0: the long-row kernel;
-// V = -1: half-warp rows (at most 256 columns).
+// V = -1: half-warp rows (at most 256 columns); V = -4, -8, -16: -V lanes per
+// row (at most 32, 64, 128 columns); V > 0: V vectors per lane.
+template <int MODE, int V>
+constexpr auto rows_kernel() {
+  if constexpr (V == 0)
+    return quant_rows_long_kernel<MODE>;
+  else if constexpr (V == -1)
+    return quant_rows_half_kernel<MODE>;
+  else if constexpr (V < -1)
+    return quant_rows_narrow_kernel<MODE, -V>;
+  else
+    return quant_rows_kernel<MODE, V>;
+}
+
 template <int MODE, int V>
 cudaError_t launch_one_wave(const QuantJobs& jobs, int sms, cudaStream_t stream) {
   const int threads = 256;
-  auto kern = V == 0 ? quant_rows_long_kernel<MODE>
-                     : (V == -1 ? quant_rows_half_kernel<MODE> : quant_rows_kernel<MODE, (V > 0 ? V : 1)>);
+  auto kern = rows_kernel<MODE, V>();
   static std::atomic<int> per_sm[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -357,7 +434,10 @@ cudaError_t launch_one_wave(const QuantJobs& jobs, int sms, cudaStream_t stream)
     if (occ < 1) occ = 1;
     per_sm[dev & 63].store(occ);
   }
-  int64_t blocks = (jobs.total_rows + (V == -1 ? 15 : 7)) / (V == -1 ? 16 : 8);
+  // rows one block takes per pass: 8 warps x rows per warp (x 4 steps for
+  // the narrow kernel)
+  constexpr int64_t kRowsPerBlock = V == -1 ? 16 : (V < -1 ? 8 * (32 / -V) * 4 : 8);
+  int64_t blocks = (jobs.total_rows + kRowsPerBlock - 1) / kRowsPerBlock;
   const int64_t cap = static_cast<int64_t>(sms) * occ;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
@@ -367,7 +447,10 @@ cudaError_t launch_one_wave(const QuantJobs& jobs, int sms, cudaStream_t stream)
 
 template <int MODE>
 cudaError_t launch_rows(const QuantJobs& jobs, int max_cols, int sms, cudaStream_t stream) {
-  if (max_cols <= 256) return launch_one_wave<MODE, -1>(jobs, sms, stream);   // half-warp rows
+  if (max_cols <= 32) return launch_one_wave<MODE, -4>(jobs, sms, stream);     // 4 lanes per row
+  if (max_cols <= 64) return launch_one_wave<MODE, -8>(jobs, sms, stream);     // 8 lanes per row
+  if (max_cols <= 128) return launch_one_wave<MODE, -16>(jobs, sms, stream);   // 16 lanes per row
+  if (max_cols <= 256) return launch_one_wave<MODE, -1>(jobs, sms, stream);    // half-warp rows
   if (max_cols <= 512) return launch_one_wave<MODE, 2>(jobs, sms, stream);
   if (max_cols <= 1024) return launch_one_wave<MODE, 4>(jobs, sms, stream);
   if (max_cols <= 2048) return launch_one_wave<MODE, 8>(jobs, sms, stream);

@@ -14,10 +14,11 @@ per-tensor, per-row, MX 1x32 and square 32x32-block E4M3 scaling, and the
 bf16 path.  For each
 problem (M, N, K, norm, outlier fraction) and variant:
 
-* time: CUDA events around repeated calls on one stream after warm-up, with
-  bf16 X quantized inside every call and W quantized once beforehand (model
-  weights are static); small problems stay in L2 between calls, which favours
-  every variant alike;
+* time: the device time of repeated calls (captured in a CUDA graph and
+  replayed under CUDA events on one stream after warm-up), with bf16 X
+  quantized inside every call and W quantized once beforehand (model weights
+  are static); small problems stay in L2 between calls, which favours every
+  variant alike;
 * error: ``loka_quant_error`` -- normwise relative error and MERE of the
   pre-norm FP8 output against the same layer on bf16 inputs with fp32
   accumulation, which is the bf16 variant itself (so its error is 0).
@@ -76,22 +77,31 @@ def synthetic_layer(M: int, N: int, K: int, outlier_frac: float, seed: int, devi
 
 
 def time_call(fn, stream, min_ms: float = 2.0, warmup: int = 3) -> float:
-    """Mean microseconds per call: CUDA events on `stream` around repeated
-    calls, enough of them to cover at least `min_ms`."""
+    """Mean microseconds per call of the device work: the calls are captured
+    in a CUDA graph (so the host's cost per call is not in the time) and the
+    graph replayed under CUDA events on `stream`, with enough calls in it to
+    cover at least `min_ms`."""
     import torch
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             fn()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
         reps = 1
         while True:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+                for _ in range(reps):
+                    fn()
+            g.replay()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            for _ in range(reps):
-                fn()
+            g.replay()
             b.record(stream)
             b.synchronize()
             ms = a.elapsed_time(b)
-            if ms >= min_ms or reps >= 4096:
+            del g
+            if ms >= min_ms or reps >= 1024:
                 return 1e3 * ms / reps
             reps *= 2
 

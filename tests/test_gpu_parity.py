@@ -79,7 +79,7 @@ def test_quantize_every_bf16_pattern_at_unit_scale(lib, mode):
 
 
 @pytest.mark.parametrize("mode", [W.SCALE_ROW, W.SCALE_MX32])
-@pytest.mark.parametrize("cols", [32, 96, 128, 256, 512, 1024, 2048, 2080, 4096])
+@pytest.mark.parametrize("cols", [32, 64, 96, 128, 160, 256, 512, 1024, 2048, 2080, 4096])
 def test_quantize_shapes_and_ragged_widths(lib, mode, cols):
     x = W.random_bf16((37, cols), seed=cols, dist="laplace", outlier_frac=0.01)
     _check_quant(x, mode)
