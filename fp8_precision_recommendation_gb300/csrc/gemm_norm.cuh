@@ -18,7 +18,7 @@
 // scales, exactly what the standalone quantizer makes of the bf16 output, so
 // the next layer takes them as pre-quantized activations.
 //
-// Design (one CTA per SM, persistent, warp-specialized, 576 threads):
+// Design (one CTA per SM, persistent, warp-specialized, 640 threads):
 //   warp 0       TMA producer: 128-byte K slices of A (and of B when W does
 //                not stay resident) into a shared-memory ring, 128B-swizzled,
 //                one mbarrier per stage.  When N x K of the weights fits in
@@ -28,7 +28,9 @@
 //                the fp32 accumulator of a 128 x N tile lives in TMEM, double
 //                buffered when 2N <= 512 columns so the epilogue of tile i
 //                overlaps the MMAs of tile i+1.
-//   warps 2..17  epilogue, two teams of 8 warps taking alternate tiles (and
+//   warps 2, 3   idle (they complete warpgroup 0, whose registers the
+//                epilogue takes with setmaxnreg).
+//   warps 4..19  epilogue, two teams of 8 warps taking alternate tiles (and
 //                accumulator buffers); each warp owns 16 whole rows of its
 //                team's tile.  tcgen05.ld.16x256b gives every thread 2 rows
 //                x 8 columns of a 32-column chunk, so a per-column value
@@ -38,7 +40,8 @@
 //                ahead.  Row statistics are fp32 shifted sums (LayerNorm) or
 //                sums of squares (RMSNorm), merged across the 4 lanes of a
 //                row (shuffles) and, for rows wider than one CTA, across the
-//                cluster's CTAs (distributed shared memory).  Normalized rows
+//                cluster's CTAs (distributed shared memory); the statistics
+//                pass writes v back to TMEM for the output pass.  Normalized rows
 //                are rounded, transposed across the 4 lanes and stored as
 //                contiguous 16-byte (bf16) or 8-byte (E4M3) pieces.
 // The output makes no extra HBM round trip: Y is written once.
@@ -78,12 +81,12 @@ constexpr size_t kSmemLimit = 227 * 1024;
 constexpr size_t kResidentWLimit = 128 * 1024;
 
 // In-kernel activation quantization (OperandKind::kE4M3Qx): 32 warps.
-//   warp 0        W: resident (once per group) or streamed through a ring
+//   warp 0        W, resident (once per group)
 //   warp 1        MMA;  warps 2-3 idle (they fill warpgroup 0)
 //   warps 4-15    quantizers: each loads its own rows of X (cp.async into a
 //                 private ring of 1 KB slots) and writes their codes into
 //                 the A tile
-//   warps 16-31   epilogue, as in the 576-thread kernel
+//   warps 16-31   epilogue, as in the 640-thread kernel
 // Registers: launched at 64 per thread (32 warps, 8 per sub-partition), then
 // warpgroup 0 drops to 40, the quantizers to 48 and the epilogue rises to 80:
 // per sub-partition 40 + 3 x 48 + 4 x 80 = 504 of the 512 register slots.

@@ -160,11 +160,17 @@ loka_status loka_quantize_fp8_block32(const void* x, int64_t rows, int64_t cols,
  * One descriptor per independent layer (group).  All groups of one call must
  * share N, K, mode, norm, norm_block, eps, act and the *_is_fp8 flags; M
  * may differ.
- *   M >= 0; K % 128 == 0; N in {64, 128, 192, 256, 512, 1024, 2048}.  Rows
- *   wider than 256 are split into 256-column slices: with LayerNorm or
- *   RMSNorm over a thread-block cluster of N/256 CTAs that merge their row
- *   statistics through distributed shared memory; with no norm or BlockNorm
- *   over N/256 independent CTAs (no statistic spans the row).
+ *   M >= 0; K >= 32 and a multiple of 32; N a multiple of 32 from 32 to
+ *   2048 (the pages' production shapes, LoKA section II-C, include widths
+ *   such as 768); anything else is LOKA_ERR_UNSUPPORTED.  A K that is not a
+ *   multiple of 128 is read as zero-padded to the next one (no effect on
+ *   the result).  Rows of up to 256 columns run on one CTA of 64, 128, 192
+ *   or 256 columns (the columns past N hold nothing); rows wider than 256
+ *   are split into 256-column slices, the last one partial: with LayerNorm
+ *   or RMSNorm over a thread-block cluster of 2, 4 or 8 CTAs that merge
+ *   their row statistics (weighted by the columns each holds) through
+ *   distributed shared memory; with no norm or BlockNorm over
+ *   ceil(N/256) independent CTAs (no statistic spans the row).
  *   x: bf16 [M,K] (x_is_fp8 = 0) or E4M3 [M,K] with x_scales as produced by
  *      loka_quantize_fp8 (x_is_fp8 = 1).  Same for w / w_scales / w_is_fp8.
  *   mode: LOKA_SCALE_* (LOKA_BF16 runs the bf16 GEMM; *_is_fp8 must be 0).
