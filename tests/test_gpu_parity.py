@@ -618,3 +618,48 @@ def test_odd_width_blocknorm_and_quantized_output(lib, N):
         torch.cuda.synchronize()
         assert torch.equal(layer.y_q, q), f"N{N} out{out_mode}"
         assert torch.equal(layer.y_q_scales.view(torch.uint8), s.view(torch.uint8)), f"N{N} out{out_mode}"
+
+
+# ------------------------------------------------ a partial last wave
+# Row counts that leave the persistent grid's last wave a quarter full, the
+# last tile ragged (both 64-row halves partly filled, the second half empty,
+# or full): every row against the oracle, for the per-row, MX, bf16 and
+# BlockNorm epilogues and the quantized outputs.
+def _tail_rows(tail):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tiles = sms + sms // 4
+    return (tiles - 1) * 128 + tail
+
+
+@pytest.mark.parametrize("tail", [111, 30, 128])
+@pytest.mark.parametrize("mode,norm", [(W.SCALE_ROW, W.NORM_LAYER), (W.SCALE_MX32, W.NORM_RMS),
+                                       (W.SCALE_ROW, W.NORM_BLOCK_RMS), (W.SCALE_BF16, W.NORM_LAYER)])
+def test_partial_last_wave(lib, tail, mode, norm):
+    M = _tail_rows(tail)
+    inp = W.make_layer(M, 512, 256, mode=mode, norm=norm, seed=tail + 3 * mode + norm, outlier_frac=0.01,
+                       bias_var=0.02, gamma_uniform=True)
+    if norm == W.NORM_BLOCK_RMS:
+        inp.norm_block = 64
+        layer = loka.Layer(x=_gpu(inp.x), w=_gpu(inp.w), bias=_gpu(inp.bias), gamma=_gpu(inp.gamma),
+                           mode=inp.mode, norm=inp.norm, eps=inp.eps, norm_block=64)
+        (y,) = loka.fp8_linear_norm([layer])
+        torch.cuda.synchronize()
+        y = y.cpu()
+    else:
+        (y,) = _run([inp])
+    _check_layer(inp, y, what=f"M{M} mode{mode} norm{norm} (every row)")
+
+
+def test_partial_last_wave_quantized_output(lib):
+    M = _tail_rows(77)
+    inp = W.make_layer(M, 512, 256, mode=W.SCALE_ROW, norm=W.NORM_LAYER, seed=77, outlier_frac=0.01, bias_var=0.02)
+    for out_mode in (W.SCALE_ROW, W.SCALE_MX32):
+        layer = loka.Layer(x=_gpu(inp.x), w=_gpu(inp.w), bias=_gpu(inp.bias), mode=inp.mode, norm=inp.norm,
+                           eps=inp.eps, y_q_mode=out_mode)
+        loka.fp8_linear_norm([layer])
+        torch.cuda.synchronize()
+        assert loka._loka.loka_device_status() == 0
+        _check_layer(inp, layer.y.cpu(), what=f"M{M} quantized out {out_mode}")
+        q, s = loka.quantize_fp8(layer.y, out_mode)
+        torch.cuda.synchronize()
+        assert torch.equal(layer.y_q, q) and torch.equal(layer.y_q_scales.view(torch.uint8), s.view(torch.uint8))
