@@ -350,7 +350,7 @@ def _two_step(inps):
     return [y.cpu() for y in ys]
 
 
-@pytest.mark.parametrize("K", [256, 512])
+@pytest.mark.parametrize("K", [32, 64, 128, 256, 512])
 @pytest.mark.parametrize("N", [64, 128, 192, 256])
 @pytest.mark.parametrize("norm", [W.NORM_NONE, W.NORM_LAYER, W.NORM_RMS])
 def test_bf16_inputs_match_caller_quantized_inputs(lib, K, N, norm):
