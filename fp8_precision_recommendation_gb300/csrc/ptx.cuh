@@ -396,6 +396,7 @@ __host__ __device__ constexpr uint32_t idesc_dense(uint32_t a_fmt, uint32_t b_fm
   return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
+// Predicated global stores (no branch around them).
 __device__ __forceinline__ void st_global_pred_v2f32(void* ptr, float2 v, uint32_t pred) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %3, 0;\n\t@p st.global.v2.f32 [%0], {%1, %2};\n\t}" ::"l"(ptr), "f"(v.x),
