@@ -23,10 +23,11 @@ def _layers(inp, dev):
     return mk
 
 
-@pytest.mark.parametrize("mode,norm", [(W.SCALE_ROW, W.NORM_LAYER), (W.SCALE_TENSOR, W.NORM_RMS)])
-def test_static_scratch_matches_workspace_entry_point_twice(lib, mode, norm):
+@pytest.mark.parametrize("mode,norm,K,N", [(W.SCALE_ROW, W.NORM_LAYER, 512, 256), (W.SCALE_TENSOR, W.NORM_RMS, 512, 256),
+                                           (W.SCALE_ROW, W.NORM_LAYER, 96, 160), (W.SCALE_MX32, W.NORM_RMS, 64, 320)])
+def test_static_scratch_matches_workspace_entry_point_twice(lib, mode, norm, K, N):
     dev = torch.device("cuda")
-    inp = W.make_layer(2000, 512, 256, mode=mode, norm=norm, seed=41, bias_var=0.02, outlier_frac=0.01,
+    inp = W.make_layer(2000, K, N, mode=mode, norm=norm, seed=41, bias_var=0.02, outlier_frac=0.01,
                        gamma_uniform=True)
     mk = _layers(inp, dev)
     ref = mk()
