@@ -165,7 +165,7 @@ def _weights(R, C, count, seed):
     return out
 
 
-@pytest.mark.parametrize("R,C", [(64, 96), (256, 512)])
+@pytest.mark.parametrize("R,C", [(64, 96), (256, 512), (1024, 2048)])
 def test_weight_model_update_against_oracle(lib, R, C):
     wm = loka.WeightModel(R, C, DEV)
     st = None
