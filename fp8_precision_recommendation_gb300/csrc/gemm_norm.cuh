@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(OP == static_cast<int>(OperandKind::kE4M3Qx) ?
   if (!x_early) wait_prerequisite_grids();
   const uint32_t tmem_base = *tmem_slot;
   const Watchdog wd{abort_flag, p.status, p.wait_limit_ns};
-  // one lane waits, the whole warp follows its verdict
+  // one lane waits, the whole warp follows its result
   auto warp_wait = [&](uint32_t bar, uint32_t parity, bool cluster_scope, unsigned code = kErrEpilogueWait) {
     int okw = 1;
     if (lane == 0)

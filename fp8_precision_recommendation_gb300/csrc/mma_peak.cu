@@ -1,6 +1,6 @@
 // Dense tensor-core throughput of this GPU, measured with the same tcgen05
 // instructions the GEMM issues: the FP8 peak (kind::f8f6f4, E4M3 x E4M3 ->
-// fp32) against which the contraction's tensor-pipe share is judged, and
+// fp32) against which the contraction's tensor-pipe share is measured, and
 // the bf16 peak (kind::f16) for a check against the library GEMM's number.
 //
 // One CTA per SM (its shared memory keeps a second one off the SM).  Thread

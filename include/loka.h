@@ -94,7 +94,7 @@ loka_status loka_selftest_watchdog(uint64_t limit_ns, void* stream);
 
 /* Diagnostic: the dense tensor-core peak of this GPU, for the tensor-pipe
  * share of the FP8 contraction (LoKA page, Table I lists the GB300's dense
- * FP8 rate; the pages judge FP8 GEMMs by their fraction of it).  Launches one
+ * FP8 rate; the pages rate FP8 GEMMs by their fraction of it).  Launches one
  * CTA per SM; each issues `mmas_per_sm` tcgen05 MMAs of M = 128, N = 256 and
  * one 32-byte K step (kind 0: E4M3 x E4M3, K = 32; kind 1: bf16 x bf16,
  * K = 16; fp32 accumulation in tensor memory) on zero-filled shared-memory
